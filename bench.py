@@ -1,0 +1,450 @@
+"""Benchmark of the paged split-KV decode path on GB300.
+
+One step = one decode pass of the whole path over one synthetic batch: host
+planning (shared-prefix detection, split-KV work list, cascade plan), the upload of
+the work lists, the split-KV partial kernel(s) and merge_states.  The headline
+workload is the flat paged-decode batch (32 requests, Hq=32, Hkv=8, D=128, page 16,
+lengths U[512,4096] with a partial last page, 16384-page pool, tile 512 tokens);
+the metric is unique KV bytes per second.  The cascade workload (64 requests, 16
+sharing an 8192-token prefix) is timed as a flat arm and a cascade arm on the same
+inputs, and the MLA workload (128 heads over an fp8 576-wide latent) is timed too.
+
+L2 is flushed (a 256 MB write) before every timed step, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+NOMINAL_HBM_GBS = 8000.0
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def unique_kv_bytes(w) -> int:
+    """Bytes of K and V a decode step must read at least once: every distinct
+    (page, slot) referenced by the page table, for all KV heads."""
+    seen = set()
+    tokens = 0
+    for b in range(w.batch):
+        ids = w.page_indices[w.page_indptr[b]:w.page_indptr[b + 1]]
+        for k, pid in enumerate(ids):
+            valid = w.page_size if k < len(ids) - 1 else int(w.last_page_len[b])
+            key = int(pid)
+            if key in seen:
+                continue
+            seen.add(key)
+            tokens += valid
+    return tokens * w.kv_bytes_per_token()
+
+
+def flat_kv_bytes(w) -> int:
+    return int(np.sum(w.lengths)) * w.kv_bytes_per_token()
+
+
+# ----------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.text = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.text, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.text or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our kernels
+class Arm:
+    """One workload on the device, run through the library's public API."""
+
+    def __init__(self, w, enable: int):
+        import paged_split_kv_decode_gb300 as psd
+        self.psd = psd
+        self.w = w
+        self.enable = enable
+        self.ctx = psd.Context(torch.cuda.current_device())
+        self.q = w.q.cuda()
+        self.k = w.k_pool.cuda()
+        self.v = self.k if w.v_pool is None else w.v_pool.cuda()
+        self.indices = torch.from_numpy(np.ascontiguousarray(w.page_indices, dtype=np.int32)).cuda()
+        self.table = psd.HostTable(w.page_indptr, w.page_indices, w.last_page_len, w.page_size)
+        self.args = psd.decode_args(self.q, self.k, self.v, self.indices, num_pages=w.num_pages,
+                                    page_size=w.page_size, Hkv=w.Hkv, Dv=w.Dv, sm_scale=w.sm_scale,
+                                    k_scale=w.k_scale, v_scale=w.v_scale)
+        self.plan = psd.plan_decode(self.table, w.tile_tokens, enable, w.min_shared_pages, w.min_members)
+        self.o = torch.empty((w.batch, w.Hq, w.Dv), dtype=torch.float32, device="cuda")
+        self.lse = torch.empty((w.batch, w.Hq), dtype=torch.float32, device="cuda")
+        # workspace sized for this page table's largest plan
+        cap_items = int(w.page_indptr[-1])
+        self.ws = torch.empty(psd.workspace_bytes(w.batch, cap_items, self.plan.num_rows + w.batch,
+                                                  w.Hq, w.Dv), dtype=torch.uint8, device="cuda")
+        self.stats = None
+
+    def step(self):
+        """Host planning + the device path, as a caller runs it each decode step."""
+        psd, w = self.psd, self.w
+        psd.plan_decode(self.table, w.tile_tokens, self.enable, w.min_shared_pages, w.min_members,
+                        plan=self.plan)
+        self.stats = psd.cascade_decode(self.ctx, self.args, self.plan, self.o, self.lse, self.ws)
+
+    def launches_per_step(self) -> int:
+        return (2 if self.plan.num_members > 0 else 1) + 1
+
+    def check(self):
+        assert self.psd.check_device_error(self.ctx, self.ws) == 0
+
+
+def time_steps(fn, steps: int, warmup: int, flush: torch.Tensor):
+    """Per-step CUDA-event times (ms) with an L2 flush before each step."""
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        fn()
+        e1.record(s)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+def partial_kernel_timing(arm: Arm, steps: int, warmup: int, flush):
+    """The split-KV partial kernel alone over the flat work list, launched through
+    paged_decode_partial on the current stream."""
+    psd, w = arm.psd, arm.w
+    items, o_indptr = psd.split_plan(arm.table, w.tile_tokens)
+    N = int(o_indptr[-1])
+    v = torch.empty((N, w.Hq, w.Dv), dtype=torch.float32, device="cuda")
+    l = torch.empty((N, w.Hq), dtype=torch.float32, device="cuda")
+    ws = torch.empty(psd.workspace_bytes(0, len(items), 0, w.Hq, w.Dv), dtype=torch.uint8, device="cuda")
+    times = time_steps(lambda: psd.paged_decode_partial(arm.ctx, arm.args, items, v, l, ws), steps, warmup, flush)
+    q_bytes = w.q.numel() * 2
+    out_bytes = N * w.Hq * (w.Dv + 1) * 4
+    algo = flat_kv_bytes(w) + q_bytes + out_bytes
+    return times, algo, N
+
+
+def e2e_timing(arm: Arm, steps: int, warmup: int, flush):
+    """Same decode step through the public API with host buffers: the step's query
+    rows and page table are copied from pinned host memory, the outputs read back."""
+    psd, w = arm.psd, arm.w
+    q_host = w.q.pin_memory()
+    idx_host = torch.from_numpy(np.ascontiguousarray(w.page_indices, dtype=np.int32)).pin_memory()
+    o_host = torch.empty(arm.o.shape, dtype=torch.float32).pin_memory()
+    l_host = torch.empty(arm.lse.shape, dtype=torch.float32).pin_memory()
+
+    def step():
+        arm.q.copy_(q_host, non_blocking=True)
+        arm.indices.copy_(idx_host, non_blocking=True)
+        arm.step()
+        o_host.copy_(arm.o, non_blocking=True)
+        l_host.copy_(arm.lse, non_blocking=True)
+
+    times = time_steps(step, steps, warmup, flush)
+    plan_bytes = (arm.plan.num_items * 16 + (w.batch * 3 + 1) * 4 + 256)
+    h2d = q_host.numel() * 2 + idx_host.numel() * 4 + plan_bytes
+    d2h = o_host.numel() * 4 + l_host.numel() * 4
+    return times, h2d, d2h
+
+
+# ----------------------------------------------------------------------- oracle
+def oracle_baseline(w, budget_s: float = 12.0):
+    """The float64 oracle (as it stands) on the host: gather + softmax attention per
+    request.  Requests are processed in order until the time budget is spent."""
+    from oracle import attention as A
+    a = A.workload_arrays(w)
+    q = A.bf16_bits_to_f64(a["q_raw"])
+    t0 = time.perf_counter()
+    done_tokens = 0
+    done = 0
+    while True:
+        for b in range(w.batch):
+            K, V = A.gather_kv(a, b)
+            A.attend(q[b], K, V, a["sm_scale"])
+            done_tokens += int(w.lengths[b])
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        if time.perf_counter() - t0 > budget_s or done >= 4 * w.batch:
+            break
+    dt = time.perf_counter() - t0
+    gbs = done_tokens * w.kv_bytes_per_token() / dt / 1e9
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} requests ({done_tokens} tokens) of the {w.name} batch in {dt:.1f} s, "
+                      "float64 numpy gather + softmax attention"}
+
+
+# ------------------------------------------------------------------- main paths
+def dist_setup(n):
+    if n <= 1 or "RANK" not in os.environ:
+        return 0, 1, int(os.environ.get("LOCAL_RANK", 0))
+    import torch.distributed as dist
+    dist.init_process_group("nccl")
+    return dist.get_rank(), dist.get_world_size(), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_max(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def run_ours(args):
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    hbm, bf16, bf16s, peak_src = measured_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    w = synth.flat_decode(seed=0, canary=False)
+    arm = Arm(w, enable=1)
+    arm.step()
+    arm.check()
+    kv_bytes = unique_kv_bytes(w)
+
+    barrier(world)
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        times = time_steps(arm.step, args.steps, args.warmup, flush)
+        barrier(world)
+        t_wall = time.perf_counter() - t_wall0
+        kt, algo, n_rows = partial_kernel_timing(arm, args.steps, args.warmup, flush)
+    arm.check()
+    ms = statistics.mean(times)
+    ms_max = dist_max(ms, world)
+    value = world * kv_bytes / (ms_max * 1e-3) / 1e9
+    k_ms = statistics.mean(kt)
+    achieved = algo / (k_ms * 1e-3) / 1e9
+
+    et, h2d, d2h = e2e_timing(arm, args.steps, args.warmup, flush)
+    e2e_ms = dist_max(statistics.mean(et), world)
+
+    extra = {}
+    if not args.quick:
+        # cascade workload: flat arm vs cascade arm on the same inputs
+        wc = synth.cascade_decode(seed=0, canary=False)
+        flat_arm, casc_arm = Arm(wc, enable=0), Arm(wc, enable=1)
+        casc_arm.step()
+        casc_arm.check()
+        st = casc_arm.stats
+        tf = statistics.mean(time_steps(flat_arm.step, args.steps, args.warmup, flush))
+        tc = statistics.mean(time_steps(casc_arm.step, args.steps, args.warmup, flush))
+        flat_b, uniq_b = flat_kv_bytes(wc), unique_kv_bytes(wc)
+        removed = (flat_b - uniq_b) / flat_b
+        reduction = (tf - tc) / tf
+        extra["flat_vs_cascade"] = {
+            "workload": "cascade decode: 64 requests, 16 share an 8192-token prefix (suffix U[64,1024]), "
+                        "48 independent U[512,4096]; Hq=32, Hkv=8, D=128, page 16, tile 512",
+            "flat_ms": round(tf, 4), "cascade_ms": round(tc, 4),
+            "flat_tokens_per_s": round(wc.batch / (tf * 1e-3), 1),
+            "cascade_tokens_per_s": round(wc.batch / (tc * 1e-3), 1),
+            "flat_unique_kv_gbs": round(uniq_b / (tf * 1e-3) / 1e9, 1),
+            "cascade_unique_kv_gbs": round(uniq_b / (tc * 1e-3) / 1e9, 1),
+            "removed_read_fraction": round(removed, 4), "wall_time_reduction": round(reduction, 4),
+            "criterion_reduction_ge_0.7x_removed": bool(reduction >= 0.7 * removed),
+            "stats": st,
+        }
+        del flat_arm, casc_arm
+        # MLA workload
+        wm = synth.mla_decode(seed=0, canary=False)
+        marm = Arm(wm, enable=1)
+        marm.step()
+        marm.check()
+        tm = statistics.mean(time_steps(marm.step, max(3, args.steps // 2), args.warmup, flush))
+        mb = unique_kv_bytes(wm)
+        flops = float(np.sum(wm.lengths)) * wm.Hq * (wm.Dqk + wm.Dv) * 2
+        extra["mla"] = {
+            "workload": "MLA decode: 128 requests U[4096,32768], 128 heads, latent 576 fp8-e4m3 "
+                        "(V = first 512), page 64, tile 2048",
+            "ms": round(tm, 4), "tokens_per_s": round(wm.batch / (tm * 1e-3), 1),
+            "unique_kv_gbs": round(mb / (tm * 1e-3) / 1e9, 1),
+            "tflops": round(flops / (tm * 1e-3) / 1e12, 1),
+            "tensor_frac_of_sustained_bf16": round(flops / (tm * 1e-3) / 1e12 / bf16s, 4) if bf16s else None,
+        }
+        del marm
+
+    if rank == 0:
+        line = {
+            "metric": "unique KV GB/s (flat paged decode; cascade and MLA arms alongside)",
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_max, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "flat paged decode: batch 32, Hq=32, Hkv=8, D=128, page 16, "
+                                   "lengths U[512,4096] partial last page, 16384-page pool, tile 512, "
+                                   "then merge_states",
+                       "batch": w.batch, "unique_kv_bytes": kv_bytes,
+                       "l2": "flushed (256 MB write) before every timed step",
+                       "parallelism": f"replicas x{world}"},
+            "decode_tokens_per_s": round(world * w.batch / (ms_max * 1e-3), 1),
+            "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+            "pct_of_measured_hbm": round(100 * value / world / hbm, 2),
+            "roofline": {"bound": "hbm", "kernel": "partial_cc_kernel<128,4> (split-KV partial, CUDA cores)",
+                         "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "peak_source": peak_src + " copy bandwidth",
+                         "traffic": None, "algorithmic_bytes_per_launch": algo,
+                         "launch_ms": round(k_ms, 5)},
+            "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": arm.launches_per_step() * args.steps,
+            "wall_s": round(t_wall, 3),
+            "clocks": clk.summary(),
+        }
+        line.update(extra)
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_baseline(w)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle timed on the host cores, on the flat workload (rank 0 only)."""
+    rank = int(os.environ.get("RANK", 0))
+    if rank != 0:
+        return
+    w = synth.flat_decode(seed=0, canary=False)
+    kv_bytes = unique_kv_bytes(w)
+    from oracle import attention as A
+    a = A.workload_arrays(w)
+    q = A.bf16_bits_to_f64(a["q_raw"])
+    reqs = list(range(min(8, w.batch)))           # bounded sample per step
+    sample_bytes = int(np.sum(w.lengths[reqs])) * w.kv_bytes_per_token()
+
+    def step():
+        for b in reqs:
+            K, V = A.gather_kv(a, b)
+            A.attend(q[b], K, V, a["sm_scale"])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = sample_bytes / dt / 1e9
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    print(json.dumps({
+        "impl": "reference", "metric": "unique KV GB/s (flat paged decode; cascade and MLA arms alongside)",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "flat paged decode: batch 32, Hq=32, Hkv=8, D=128, page 16, "
+                               "lengths U[512,4096] partial last page, 16384-page pool, tile 512",
+                   "sample": f"requests {reqs[0]}..{reqs[-1]} per step", "unique_kv_bytes": kv_bytes},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{len(reqs)} of {w.batch} requests per step, float64 numpy"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--quick", action="store_true", help="flat workload only")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

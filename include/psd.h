@@ -1,0 +1,268 @@
+/*
+ * psd.h - paged split-KV decode for one NVIDIA GB300 (sm_103a): the C ABI.
+ *
+ * Operations (mlxcel PR #1004, "compute shared prompt prefixes once per decode
+ * batch"; ROCm ATOM PR #1701 section 3.2 for fp8 latent KV):
+ *   paged_decode_partial  split-KV partial attention; one (V, LSE) row per work item
+ *                         and query head, LSE in log2 units (Merge contract section)
+ *   merge_states          log2-LSE merge of contiguous rows grouped by o_indptr
+ *                         (Merge contract section)
+ *   detect_shared_prefix  host: pick one subgroup sharing a whole-page prefix
+ *                         (Detection section, Task item 1)
+ *   build_cascade_plan    host: level-0 / level-1 work lists and merge groups
+ *                         (Task item 2)
+ *   cascade_decode        device: level 0 with KV-head-major stacked queries,
+ *                         level 1, and the exact merge (Decomposition section)
+ *
+ * Conventions shared by every entry point
+ *   - Every function returns psd_status; nothing throws or aborts across the ABI.
+ *     On failure psd_last_error() returns a thread-local message.
+ *   - "device" pointers are CUDA global memory on the context's device; "host"
+ *     pointers are ordinary CPU memory.  All buffers are owned by the caller.  The
+ *     library allocates no device memory on any call: scratch lives in a
+ *     caller-provided workspace sized by psd_workspace_bytes().
+ *   - Device work is enqueued asynchronously on the caller's stream (NULL = the
+ *     legacy default stream).  Host arrays passed in may be reused as soon as the
+ *     call returns.
+ *   - Host validation (shapes, page table, page ids < num_pages, alignment) runs
+ *     before any launch and returns PSD_ERR_INVALID_ARG.  Kernels re-check page
+ *     ids; a bad id or an expired bounded wait sets a flag in the workspace that
+ *     psd_check_device_error() reports as PSD_ERR_DEVICE_FAULT.  No kernel traps.
+ *
+ * Layouts (row-major, innermost last)
+ *   q        [B, Hq, Dqk]                 bf16
+ *   k_pool   [num_pages, page_size, Hkv, Dqk]  bf16 or fp8-e4m3 codes
+ *   v_pool   [num_pages, page_size, Hkv, Dv]   same dtype; or v_pool == k_pool with
+ *            Hkv == 1 and Dv <= Dqk: V is the first Dv columns of the K rows (an MLA
+ *            latent shared by K and V)
+ *   partial  v [N, Hq, Dv] f32 normalised per row, lse [N, Hq] f32 (log2)
+ *   page table (CSR): page_indptr [B+1], page_indices [nnz], last_page_len [B];
+ *            request b has n_b = page_indptr[b+1]-page_indptr[b] >= 1 pages and
+ *            L_b = (n_b - 1) * page_size + last_page_len[b] tokens,
+ *            1 <= last_page_len[b] <= page_size.
+ *   Query head h reads KV head h / (Hq / Hkv) (Decomposition section).
+ *   fp8-e4m3 elements decode to code * k_scale (K) and code * v_scale (V).
+ */
+#ifndef PSD_H
+#define PSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *psd_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  PSD_OK = 0,
+  PSD_ERR_INVALID_ARG = 1,
+  PSD_ERR_UNSUPPORTED = 2,
+  PSD_ERR_CUDA = 3,
+  PSD_ERR_DEVICE_FAULT = 4,
+  PSD_ERR_WORKSPACE_TOO_SMALL = 5
+} psd_status;
+
+typedef enum { PSD_BF16 = 0, PSD_FP8_E4M3 = 1 } psd_dtype;
+
+/* Why a cascade was not taken (Path attribution section: CascadeFailed(reason)). */
+typedef enum {
+  PSD_DECLINE_NONE = 0,                /* cascade taken */
+  PSD_DECLINE_DISABLED = 1,            /* switched off by argument or environment */
+  PSD_DECLINE_NO_SHARED_PAGES = 2,     /* no two multi-page requests share a first page */
+  PSD_DECLINE_MEMBERS_BELOW_THRESHOLD = 3,
+  PSD_DECLINE_SPAN_BELOW_THRESHOLD = 4 /* includes spans capped below the threshold */
+} psd_decline_reason;
+
+/* Device-fault flag bits written by kernels into the workspace. */
+enum {
+  PSD_FAULT_PAGE_ID = 1,      /* a page id outside [0, num_pages) was skipped */
+  PSD_FAULT_WAIT_TIMEOUT = 2  /* a bounded barrier wait gave up */
+};
+
+/* CSR page table (Detection section: PagedCsrView).  Host or device arrays. */
+typedef struct {
+  const int32_t *page_indptr;   /* [batch + 1] */
+  const int32_t *page_indices;  /* [page_indptr[batch]] */
+  const int32_t *last_page_len; /* [batch] */
+  int32_t batch;
+  int32_t page_size;
+} psd_page_table;
+
+/* One split-KV unit: a (request, page tile) pair (Decomposition section).
+ *   q_index  request whose query rows are used; -1 = the stacked level-0 request
+ *   page_off position in page_indices of the tile's first page
+ *   n_tokens tokens in the tile (1..tile_tokens)
+ *   out_row  partial row written (level 0: chunk index within the shared span) */
+typedef struct {
+  int32_t q_index;
+  int32_t page_off;
+  int32_t n_tokens;
+  int32_t out_row;
+} psd_work_item;
+
+/* Problem description shared by paged_decode_partial and cascade_decode. */
+typedef struct {
+  const void *q;                   /* device [batch, Hq, Dqk] bf16 */
+  const void *k_pool;              /* device [num_pages, page_size, Hkv, Dqk] */
+  const void *v_pool;              /* device [num_pages, page_size, Hkv, Dv], or k_pool */
+  const int32_t *page_indices_dev; /* device copy of the page table's page_indices */
+  int64_t num_page_indices;        /* length of page_indices_dev (nnz) */
+  int64_t num_pages;
+  int32_t batch, Hq, Hkv, Dqk, Dv, page_size;
+  int32_t kv_dtype;                /* psd_dtype */
+  float k_scale, v_scale;          /* fp8 dequant scales; ignored for bf16 */
+  float sm_scale;                  /* softmax scale, e.g. 1/sqrt(Dqk) */
+} psd_decode_args;
+
+/* A decode plan: flat (num_members == 0) or two-level cascade.  The caller owns
+ * every array and sets the capacities; psd_plan_capacity() gives them. */
+typedef struct {
+  /* capacities (in) */
+  int32_t batch_capacity;      /* >= batch */
+  int32_t item_capacity;       /* >= page_indptr[batch] (each item holds >= 1 page) */
+  int32_t *members;            /* [batch_capacity] member requests, increasing */
+  int32_t *member_row_base;    /* [batch_capacity] first merge row of each member */
+  psd_work_item *l0_items;     /* [item_capacity] level-0 chunks of the shared span */
+  psd_work_item *l1_items;     /* [item_capacity] level-1 (or flat) chunks */
+  int32_t *o_indptr;           /* [batch_capacity + 1] final merge groups */
+  /* results (out) */
+  int32_t batch, page_size, tile_tokens;
+  int32_t num_members, shared_pages, decline_reason;
+  int32_t l0_num_items, l1_num_items;
+  int32_t num_rows;            /* total partial rows = o_indptr[batch] */
+} psd_cascade_plan;
+
+/* Which path a cascade_decode call took (Path attribution section:
+ * PagedDecodeOutcome::FusedCascade / CascadeFailed). */
+typedef struct {
+  int32_t path; /* 0 flat, 1 cascade */
+  int32_t decline_reason;
+  int32_t batch, members, shared_pages, shared_tokens;
+  int32_t prefix_chunks, suffix_chunks;
+} psd_cascade_stats;
+
+/* In-context counters (Task item 5, without a metrics server). */
+typedef struct {
+  int64_t launches_flat, launches_cascade;
+  int64_t cascade_shared_tokens, cascade_member_sequences, cascade_failures;
+} psd_counters;
+
+typedef struct psd_ctx psd_ctx;
+
+/* ----------------------------------------------------------------- context */
+/* Create a context bound to CUDA device `device` (queries SM count, loads the
+ * driver's tensor-map encoder).  Host memory only.  Thread-compatible: one
+ * context per thread, or external locking. */
+psd_status psd_create(psd_ctx **ctx, int device);
+psd_status psd_destroy(psd_ctx *ctx);
+/* Thread-local message describing the last failure on this thread. */
+const char *psd_last_error(void);
+psd_status psd_get_counters(const psd_ctx *ctx, psd_counters *out);
+/* Kill switch (Task item 4): reads PSD_CASCADE_ATTENTION; 0/false/off/no -> 0,
+ * 1/true/on/yes -> 1, unset or anything else -> `fallback`. */
+int32_t psd_cascade_env_enabled(int32_t fallback);
+
+/* ------------------------------------------------------------ host planning */
+/* Flat split-KV work list (Decomposition: one unit per (request, page tile)).
+ * Request b gets ceil(L_b / tile_tokens) items; item c starts at page position
+ * page_indptr[b] + c*tile_tokens/page_size and writes row o_indptr[b] + c.
+ * host: host page table.  items: [item_capacity] host.  o_indptr: [batch+1] host.
+ * tile_tokens must be a positive multiple of page_size. */
+psd_status psd_split_plan(const psd_page_table *host, int32_t tile_tokens,
+                          psd_work_item *items, int32_t item_capacity,
+                          int32_t *num_items, int32_t *o_indptr);
+
+/* Shared-prefix detection (Detection section; Task items 1 and 4; Left out /
+ * unsure).  Requests with >= 2 pages are grouped by first page id; a group with
+ * >= max(2, min_members) requests gets span = longest positional common page
+ * prefix over all its members, capped at min(n_b) - 1 so no member's last page is
+ * shared; spans >= max(1, min_shared_pages) compete on span * (members - 1), ties
+ * to the group with the smallest first member.  Outputs (host): members [batch]
+ * in increasing order, *num_members (0 on decline), *shared_pages,
+ * *decline_reason (psd_decline_reason).  Deterministic and bit-exact. */
+psd_status detect_shared_prefix(const psd_page_table *host, int32_t min_shared_pages,
+                                int32_t min_members, int32_t *members,
+                                int32_t *num_members, int32_t *shared_pages,
+                                int32_t *decline_reason);
+
+/* Cascade plan (Task item 2).  Level 0: the first shared_pages pages of members[0]
+ * (identical pool pages for every member) split into tile_tokens chunks, items
+ * with q_index -1 and out_row = chunk index.  Level 1: every request, members
+ * starting after the span, non-members whole.  Merge group of request b: its
+ * level-0 rows (members only; row member_row_base[m] + chunk) then its level-1
+ * rows.  num_members == 0 gives the flat plan.  plan arrays are host memory. */
+psd_status build_cascade_plan(const psd_page_table *host, const int32_t *members,
+                              int32_t num_members, int32_t shared_pages,
+                              int32_t tile_tokens, psd_cascade_plan *plan);
+
+/* detect_shared_prefix + build_cascade_plan, or the flat plan with the decline
+ * reason.  enable: 1 on, 0 off, -1 = psd_cascade_env_enabled(0). */
+psd_status psd_plan_decode(const psd_page_table *host, int32_t tile_tokens, int32_t enable,
+                           int32_t min_shared_pages, int32_t min_members,
+                           psd_cascade_plan *plan);
+
+/* Capacities a plan for this page table needs. */
+psd_status psd_plan_capacity(const psd_page_table *host, int32_t *batch_capacity,
+                             int32_t *item_capacity);
+
+/* Workspace bytes for cascade_decode / paged_decode_partial: work lists and
+ * merge groups for up to `num_items` items and `batch` requests, plus partial
+ * rows `num_rows` x Hq x Dv (pass 0 rows for paged_decode_partial). */
+size_t psd_workspace_bytes(int32_t batch, int32_t num_items, int64_t num_rows, int32_t Hq,
+                           int32_t Dv);
+
+/* ---------------------------------------------------------------- device ops */
+/* Split-KV partial attention (Decomposition and Merge contract sections).
+ * For every item i and query head h, over the item's tokens j:
+ *   t_j = sm_scale * <q[item.q_index, h], k_j> * log2(e),  m = max_j t_j,
+ *   l = sum_j 2^(t_j - m),  v_out[item.out_row, h] = sum_j 2^(t_j - m) v_j / l,
+ *   lse_out[item.out_row, h] = m + log2(l).
+ * One CTA owns all G = Hq/Hkv query heads of one KV head for one item, so each
+ * K/V element is read from HBM once.  items: host [num_items] with q_index in
+ * [0, batch).  v_out: device [out_rows, Hq, Dv] f32.  lse_out: device
+ * [out_rows, Hq] f32.  workspace: device, >= psd_workspace_bytes(batch,
+ * num_items, 0, Hq, Dv) bytes, 16-byte aligned. */
+psd_status paged_decode_partial(psd_ctx *ctx, const psd_decode_args *args,
+                                const psd_work_item *items, int32_t num_items,
+                                float *v_out, float *lse_out, int64_t out_rows,
+                                void *workspace, size_t workspace_bytes,
+                                psd_stream_t stream);
+
+/* Log2-LSE merge (Merge contract section).  For output row r and head h over rows
+ * i in [o_indptr[r], o_indptr[r+1]):  M = max lse_i, w_i = 2^(lse_i - M),
+ *   v_out = sum w_i v_i / sum w_i,  lse_out = M + log2(sum w_i).
+ * A one-row group copies v and lse bit-exactly; an empty or all -inf group
+ * gives 0 and -inf.  v_in device [N, H, D] f32, lse_in device [N, H] f32,
+ * o_indptr_dev device [num_out + 1] int32 (non-decreasing), v_out device
+ * [num_out, H, D] f32, lse_out device [num_out, H] f32 or NULL.  D % 4 == 0,
+ * D <= 1024; all pointers 16-byte aligned. */
+psd_status merge_states(psd_ctx *ctx, const float *v_in, const float *lse_in,
+                        const int32_t *o_indptr_dev, int64_t num_out, int32_t H,
+                        int32_t D, float *v_out, float *lse_out, psd_stream_t stream);
+
+/* Two-level cascade decode (Decomposition section; Task item 2), or flat decode
+ * when plan->num_members == 0.  Level 0 attends the shared span once with the
+ * members' query heads stacked KV-head-major (h0 = kv*(M*G) + m*G + g); level 1
+ * attends every request's remaining tokens; merge_states combines each member's
+ * level-0 and level-1 rows (and passes a non-member's single chunk group through).
+ * o: device [batch, Hq, Dv] f32.  lse: device [batch, Hq] f32 (log2) or NULL.
+ * workspace: >= psd_workspace_bytes(batch, plan item total, plan->num_rows, Hq, Dv).
+ * stats (host, nullable) receives which path ran. */
+psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
+                          const psd_cascade_plan *plan, float *o, float *lse,
+                          void *workspace, size_t workspace_bytes,
+                          psd_cascade_stats *stats, psd_stream_t stream);
+
+/* Synchronises `stream` and reads the workspace's fault flag: PSD_OK, or
+ * PSD_ERR_DEVICE_FAULT with the PSD_FAULT_* bits in *fault_bits (nullable).
+ * Clears the flag. */
+psd_status psd_check_device_error(psd_ctx *ctx, void *workspace, psd_stream_t stream,
+                                  int32_t *fault_bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSD_H */

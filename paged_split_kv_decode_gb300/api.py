@@ -1,0 +1,274 @@
+"""Thin Python binding over the C ABI (include/psd.h).
+
+The functions keep the C names and only marshal arguments: torch tensors become
+device pointers, numpy int32 arrays become host pointers, the current torch stream
+becomes the CUDA stream.  Every step of the decode path (planning included) runs in
+``libpsd.so``; nothing here computes any part of it.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import _lib as L
+
+
+def _ptr_i32(a: np.ndarray):
+    return a.ctypes.data_as(L.P_i32)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev_ptr(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def kv_dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return L.PSD_BF16
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return L.PSD_FP8_E4M3
+    raise ValueError(f"unsupported KV dtype {t.dtype}")
+
+
+class Context:
+    """A psd_ctx bound to one CUDA device."""
+
+    def __init__(self, device=None):
+        lib = L.load()
+        dev = torch.cuda.current_device() if device is None else int(device)
+        self._h = C.c_void_p()
+        L.check(lib.psd_create(C.byref(self._h), dev))
+        self.device = dev
+
+    @property
+    def handle(self):
+        return self._h
+
+    def counters(self) -> dict:
+        c = L.Counters()
+        L.check(L.load().psd_get_counters(self._h, C.byref(c)))
+        return {k: getattr(c, k) for k, _ in L.Counters._fields_}
+
+    def close(self):
+        if self._h:
+            L.load().psd_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class HostTable:
+    """A host CSR page table kept alive for the C ABI."""
+
+    def __init__(self, page_indptr, page_indices, last_page_len, page_size: int):
+        self.indptr = _i32(page_indptr)
+        self.indices = _i32(page_indices)
+        self.last = _i32(last_page_len)
+        self.page_size = int(page_size)
+        self.c = L.PageTable(_ptr_i32(self.indptr), _ptr_i32(self.indices), _ptr_i32(self.last),
+                             int(self.indptr.shape[0] - 1), self.page_size)
+
+    @property
+    def batch(self):
+        return int(self.indptr.shape[0] - 1)
+
+    @property
+    def nnz(self):
+        return int(self.indptr[-1])
+
+
+def split_plan(table: HostTable, tile_tokens: int):
+    """psd_split_plan: flat work list -> (items [n, 4] int32, o_indptr [B+1])."""
+    lib = L.load()
+    cap = max(table.nnz, 1)
+    items = (L.WorkItem * cap)()
+    n = C.c_int32()
+    o_indptr = np.zeros(table.batch + 1, dtype=np.int32)
+    L.check(lib.psd_split_plan(C.byref(table.c), int(tile_tokens), items, cap, C.byref(n),
+                               _ptr_i32(o_indptr)))
+    arr = np.ctypeslib.as_array(C.cast(items, L.P_i32), shape=(cap * 4,)).reshape(cap, 4)
+    return arr[: n.value].copy(), o_indptr
+
+
+def detect_shared_prefix(table: HostTable, min_shared_pages: int = 16, min_members: int = 2):
+    """detect_shared_prefix -> (members list, shared_pages, decline_reason)."""
+    lib = L.load()
+    members = np.zeros(max(table.batch, 1), dtype=np.int32)
+    nm, sp, reason = C.c_int32(), C.c_int32(), C.c_int32()
+    L.check(lib.detect_shared_prefix(C.byref(table.c), int(min_shared_pages), int(min_members),
+                                     _ptr_i32(members), C.byref(nm), C.byref(sp), C.byref(reason)))
+    return [int(x) for x in members[: nm.value]], int(sp.value), int(reason.value)
+
+
+class Plan:
+    """A psd_cascade_plan with caller-owned (numpy) arrays."""
+
+    def __init__(self, table: HostTable):
+        self.table = table
+        bc, ic = C.c_int32(), C.c_int32()
+        L.check(L.load().psd_plan_capacity(C.byref(table.c), C.byref(bc), C.byref(ic)))
+        self.members_a = np.zeros(bc.value, dtype=np.int32)
+        self.row_base_a = np.zeros(bc.value, dtype=np.int32)
+        self.o_indptr_a = np.zeros(bc.value + 1, dtype=np.int32)
+        self.l0 = (L.WorkItem * ic.value)()
+        self.l1 = (L.WorkItem * ic.value)()
+        self.c = L.CascadePlan()
+        self.c.batch_capacity = bc.value
+        self.c.item_capacity = ic.value
+        self.c.members = _ptr_i32(self.members_a)
+        self.c.member_row_base = _ptr_i32(self.row_base_a)
+        self.c.l0_items = self.l0
+        self.c.l1_items = self.l1
+        self.c.o_indptr = _ptr_i32(self.o_indptr_a)
+
+    def _items(self, arr, n):
+        cap = self.c.item_capacity
+        a = np.ctypeslib.as_array(C.cast(arr, L.P_i32), shape=(cap * 4,)).reshape(cap, 4)
+        return a[:n].copy()
+
+    @property
+    def members(self):
+        return [int(x) for x in self.members_a[: self.c.num_members]]
+
+    @property
+    def member_row_base(self):
+        return [int(x) for x in self.row_base_a[: self.c.num_members]]
+
+    @property
+    def o_indptr(self):
+        return [int(x) for x in self.o_indptr_a[: self.c.batch + 1]]
+
+    @property
+    def l0_items(self):
+        return self._items(self.l0, self.c.l0_num_items)
+
+    @property
+    def l1_items(self):
+        return self._items(self.l1, self.c.l1_num_items)
+
+    @property
+    def num_items(self):
+        return self.c.l0_num_items + self.c.l1_num_items
+
+    def __getattr__(self, name):
+        if name in ("num_members", "shared_pages", "decline_reason", "num_rows", "tile_tokens",
+                    "batch", "page_size", "l0_num_items", "l1_num_items"):
+            return getattr(self.c, name)
+        raise AttributeError(name)
+
+
+def build_cascade_plan(table: HostTable, members, shared_pages: int, tile_tokens: int) -> Plan:
+    plan = Plan(table)
+    m = _i32(list(members) if len(members) else [0])
+    L.check(L.load().build_cascade_plan(C.byref(table.c), _ptr_i32(m), len(members),
+                                        int(shared_pages), int(tile_tokens), C.byref(plan.c)))
+    return plan
+
+
+def plan_decode(table: HostTable, tile_tokens: int, enable: int = 1, min_shared_pages: int = 16,
+                min_members: int = 2, plan: Plan = None) -> Plan:
+    """psd_plan_decode: detection + cascade plan, or the flat plan with a reason."""
+    plan = plan if plan is not None else Plan(table)
+    L.check(L.load().psd_plan_decode(C.byref(table.c), int(tile_tokens), int(enable),
+                                     int(min_shared_pages), int(min_members), C.byref(plan.c)))
+    return plan
+
+
+def cascade_env_enabled(fallback: int = 0) -> int:
+    return int(L.load().psd_cascade_env_enabled(int(fallback)))
+
+
+def workspace_bytes(batch: int, num_items: int, num_rows: int, Hq: int, Dv: int) -> int:
+    return int(L.load().psd_workspace_bytes(int(batch), int(num_items), int(num_rows), int(Hq), int(Dv)))
+
+
+def decode_args(q, k_pool, v_pool, page_indices_dev, *, num_pages: int, page_size: int,
+                Hkv: int, Dv: int, sm_scale: float, k_scale: float = 1.0,
+                v_scale: float = 1.0) -> L.DecodeArgs:
+    """psd_decode_args from device tensors (v_pool is k_pool for a shared latent)."""
+    a = L.DecodeArgs()
+    a.q = _dev_ptr(q, "q")
+    a.k_pool = _dev_ptr(k_pool, "k_pool")
+    a.v_pool = _dev_ptr(v_pool, "v_pool")
+    if page_indices_dev.dtype != torch.int32:
+        raise ValueError("page_indices must be int32")
+    a.page_indices_dev = _dev_ptr(page_indices_dev, "page_indices")
+    a.num_page_indices = int(page_indices_dev.numel())
+    a.num_pages = int(num_pages)
+    a.batch, a.Hq, a.Dqk = (int(x) for x in q.shape)
+    a.Hkv = int(Hkv)
+    a.Dv = int(Dv)
+    a.page_size = int(page_size)
+    a.kv_dtype = kv_dtype_code(k_pool)
+    a.k_scale, a.v_scale, a.sm_scale = float(k_scale), float(v_scale), float(sm_scale)
+    return a
+
+
+def paged_decode_partial(ctx: Context, args: L.DecodeArgs, items: np.ndarray, v_out: torch.Tensor,
+                         lse_out: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """paged_decode_partial over a host work list ([n, 4] int32 rows
+    (q_index, page_off, n_tokens, out_row))."""
+    it = _i32(items).reshape(-1, 4)
+    n = it.shape[0]
+    arr = (L.WorkItem * max(n, 1)).from_buffer_copy(it.tobytes() or bytes(16))
+    L.check(L.load().paged_decode_partial(
+        ctx.handle, C.byref(args), arr, n, _dev_ptr(v_out, "v_out"), _dev_ptr(lse_out, "lse_out"),
+        int(v_out.shape[0]), _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def merge_states(ctx: Context, v_in: torch.Tensor, lse_in: torch.Tensor, o_indptr_dev: torch.Tensor,
+                 v_out: torch.Tensor, lse_out: torch.Tensor = None, stream=None):
+    """merge_states: v_in [N, H, D] f32, lse_in [N, H] f32, o_indptr [M+1] int32 (device)."""
+    M = int(o_indptr_dev.numel()) - 1
+    H, D = int(v_in.shape[1]), int(v_in.shape[2])
+    L.check(L.load().merge_states(
+        ctx.handle, _dev_ptr(v_in, "v_in"), _dev_ptr(lse_in, "lse_in"),
+        _dev_ptr(o_indptr_dev, "o_indptr"), M, H, D, _dev_ptr(v_out, "v_out"),
+        None if lse_out is None else _dev_ptr(lse_out, "lse_out"), _stream(stream)))
+
+
+def cascade_decode(ctx: Context, args: L.DecodeArgs, plan: Plan, o: torch.Tensor,
+                   lse: torch.Tensor = None, workspace: torch.Tensor = None, stream=None) -> dict:
+    """cascade_decode (flat when the plan has no members); returns the path stats."""
+    stats = L.CascadeStats()
+    L.check(L.load().cascade_decode(
+        ctx.handle, C.byref(args), C.byref(plan.c), _dev_ptr(o, "o"),
+        None if lse is None else _dev_ptr(lse, "lse"), _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), C.byref(stats), _stream(stream)))
+    return {k: getattr(stats, k) for k, _ in L.CascadeStats._fields_}
+
+
+def check_device_error(ctx: Context, workspace: torch.Tensor, stream=None) -> int:
+    """psd_check_device_error: raises PsdError on a flagged device fault."""
+    bits = C.c_int32()
+    st = L.load().psd_check_device_error(ctx.handle, _dev_ptr(workspace, "workspace"), _stream(stream),
+                                         C.byref(bits))
+    if st != L.PSD_OK:
+        raise L.PsdError(st, L.load().psd_last_error().decode(errors="replace"))
+    return int(bits.value)
+
+
+def workspace_for(plan: Plan, Hq: int, Dv: int, device) -> torch.Tensor:
+    n = workspace_bytes(plan.batch, max(plan.num_items, 1), plan.num_rows, Hq, Dv)
+    return torch.empty(n, dtype=torch.uint8, device=device)

@@ -1,0 +1,416 @@
+// The C ABI: context, argument validation, work-list upload, kernel dispatch and
+// the cascade orchestration (mlxcel PR #1004, "compute shared prompt prefixes once
+// per decode batch": Decomposition, Merge contract, Task items 2-5, Path
+// attribution).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+#include "psd_internal.h"
+
+namespace psd {
+
+static thread_local std::string g_error;
+
+void clear_error() { g_error.clear(); }
+
+psd_status fail(psd_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_error = buf;
+  return st;
+}
+
+}  // namespace psd
+
+using namespace psd;
+
+struct psd_ctx {
+  DeviceInfo dev;
+  psd_counters counters;
+  // Two pinned staging buffers for the per-call H2D upload of work lists; an
+  // event per buffer tells when its previous copy has finished reading it.
+  void *staging[2] = {nullptr, nullptr};
+  size_t staging_cap[2] = {0, 0};
+  cudaEvent_t staging_done[2] = {nullptr, nullptr};
+  bool staging_pending[2] = {false, false};
+  int next = 0;
+};
+
+namespace {
+
+const float kLog2e = 1.4426950408889634f;
+
+struct DeviceGuard {  // make ctx->dev.device current for the call, restore after
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
+    else prev = -1;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+psd_status validate_args(const psd_decode_args *a) {
+  if (!a) return fail(PSD_ERR_INVALID_ARG, "args: NULL");
+  if (!a->q || !a->k_pool || !a->v_pool || !a->page_indices_dev)
+    return fail(PSD_ERR_INVALID_ARG, "args: NULL device pointer");
+  if (!aligned16(a->q) || !aligned16(a->k_pool) || !aligned16(a->v_pool))
+    return fail(PSD_ERR_INVALID_ARG, "args: q / k_pool / v_pool must be 16-byte aligned");
+  if (a->batch < 0 || a->Hq < 1 || a->Hkv < 1 || a->Hq % a->Hkv != 0)
+    return fail(PSD_ERR_INVALID_ARG, "args: need Hq %% Hkv == 0 (Hq %d, Hkv %d)", a->Hq, a->Hkv);
+  if (a->Dqk < 8 || a->Dv < 8 || a->Dqk % 8 || a->Dv % 8)
+    return fail(PSD_ERR_INVALID_ARG, "args: head dims must be positive multiples of 8");
+  if (a->page_size < 1 || a->num_pages < 1 || a->num_page_indices < 0)
+    return fail(PSD_ERR_INVALID_ARG, "args: page_size / num_pages / num_page_indices");
+  if (a->num_pages > 0x7fffffffLL) return fail(PSD_ERR_INVALID_ARG, "args: num_pages > 2^31-1");
+  if (a->kv_dtype != PSD_BF16 && a->kv_dtype != PSD_FP8_E4M3)
+    return fail(PSD_ERR_INVALID_ARG, "args: kv_dtype %d", a->kv_dtype);
+  if (!std::isfinite(a->sm_scale) || !std::isfinite(a->k_scale) || !std::isfinite(a->v_scale))
+    return fail(PSD_ERR_INVALID_ARG, "args: scales must be finite");
+  if (a->v_pool == a->k_pool && (a->Hkv != 1 || a->Dv > a->Dqk))
+    return fail(PSD_ERR_INVALID_ARG, "args: a shared latent (v_pool == k_pool) needs Hkv == 1, Dv <= Dqk");
+  return PSD_OK;
+}
+
+psd_status validate_items(const psd_decode_args *a, const psd_work_item *items, int32_t n,
+                          int64_t out_rows, bool stacked, int32_t num_members) {
+  const int P = a->page_size;
+  for (int32_t i = 0; i < n; ++i) {
+    const psd_work_item &it = items[i];
+    if (stacked ? it.q_index != -1 : (it.q_index < 0 || it.q_index >= a->batch))
+      return fail(PSD_ERR_INVALID_ARG, "item %d: q_index %d", i, it.q_index);
+    if (it.n_tokens < 1 || it.page_off < 0 ||
+        int64_t(it.page_off) + (it.n_tokens + P - 1) / P > a->num_page_indices)
+      return fail(PSD_ERR_INVALID_ARG, "item %d: page_off %d / n_tokens %d outside the page table", i,
+                  it.page_off, it.n_tokens);
+    if (it.out_row < 0 || (!stacked && it.out_row >= out_rows))
+      return fail(PSD_ERR_INVALID_ARG, "item %d: out_row %d outside [0, %lld)", i, it.out_row,
+                  (long long)out_rows);
+  }
+  (void)num_members;
+  return PSD_OK;
+}
+
+PartialLaunch base_launch(const psd_decode_args *a) {
+  PartialLaunch L;
+  L.q = a->q;
+  L.k_pool = a->k_pool;
+  L.v_pool = a->v_pool;
+  L.page_indices = a->page_indices_dev;
+  L.num_pages = a->num_pages;
+  L.Hq_req = a->Hq;
+  L.Hkv = a->Hkv;
+  L.Dqk = a->Dqk;
+  L.Dv = a->Dv;
+  L.page_size = a->page_size;
+  L.Gm = a->Hq / a->Hkv;
+  L.G_cta = L.Gm;
+  L.kv_dtype = a->kv_dtype;
+  L.latent_v = a->v_pool == a->k_pool;
+  const float ks = a->kv_dtype == PSD_FP8_E4M3 ? a->k_scale : 1.f;
+  L.q_scale = a->sm_scale * kLog2e * ks;
+  L.v_scale = a->kv_dtype == PSD_FP8_E4M3 ? a->v_scale : 1.f;
+  return L;
+}
+
+bool dispatchable(const PartialLaunch &L) { return partial_cc_supports(L) || partial_tc_supports(L); }
+
+psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
+  if (partial_cc_supports(L)) return launch_partial_cc(L, dev, s);
+  if (partial_tc_supports(L)) return launch_partial_tc(L, dev, s);
+  return fail(PSD_ERR_UNSUPPORTED, "no kernel for Dqk %d, Dv %d, rows/KV head %d, dtype %d, latent %d",
+              L.Dqk, L.Dv, L.G_cta, L.kv_dtype, int(L.latent_v));
+}
+
+// Copies `bytes` of host data into a pinned staging buffer and enqueues one H2D
+// copy to `dst` on `s`.
+psd_status upload(psd_ctx *ctx, void *dst, const void *src, size_t bytes, cudaStream_t s) {
+  const int i = ctx->next;
+  ctx->next ^= 1;
+  if (ctx->staging_pending[i]) {
+    cudaError_t e = cudaEventSynchronize(ctx->staging_done[i]);
+    if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "staging event: %s", cudaGetErrorString(e));
+    ctx->staging_pending[i] = false;
+  }
+  if (ctx->staging_cap[i] < bytes) {
+    if (ctx->staging[i]) cudaFreeHost(ctx->staging[i]);
+    ctx->staging[i] = nullptr;
+    size_t cap = bytes < 65536 ? 65536 : bytes * 2;
+    cudaError_t e = cudaHostAlloc(&ctx->staging[i], cap, cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+      ctx->staging_cap[i] = 0;
+      return fail(PSD_ERR_CUDA, "pinned staging buffer: %s", cudaGetErrorString(e));
+    }
+    ctx->staging_cap[i] = cap;
+  }
+  std::memcpy(ctx->staging[i], src, bytes);
+  cudaError_t e = cudaMemcpyAsync(dst, ctx->staging[i], bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "work-list upload: %s", cudaGetErrorString(e));
+  e = cudaEventRecord(ctx->staging_done[i], s);
+  if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "staging event record: %s", cudaGetErrorString(e));
+  ctx->staging_pending[i] = true;
+  return PSD_OK;
+}
+
+}  // namespace
+
+extern "C" const char *psd_last_error(void) { return g_error.c_str(); }
+
+extern "C" psd_status psd_create(psd_ctx **out, int device) {
+  clear_error();
+  if (!out) return fail(PSD_ERR_INVALID_ARG, "psd_create: NULL out");
+  *out = nullptr;
+  int n = 0;
+  cudaError_t e = cudaGetDeviceCount(&n);
+  if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cudaGetDeviceCount: %s", cudaGetErrorString(e));
+  if (device < 0 || device >= n) return fail(PSD_ERR_INVALID_ARG, "device %d of %d", device, n);
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+  if (major != 10 || minor != 3)
+    return fail(PSD_ERR_UNSUPPORTED, "built for sm_103a (GB300); device %d is sm_%d%d", device, major,
+                minor);
+  psd_ctx *c = new psd_ctx();
+  std::memset(&c->counters, 0, sizeof(c->counters));
+  c->dev.device = device;
+  cudaDeviceGetAttribute(&c->dev.num_sms, cudaDevAttrMultiProcessorCount, device);
+  cudaDeviceGetAttribute(&c->dev.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  DeviceGuard g(device);
+  cudaDriverEntryPointQueryResult q;
+  void *fn = nullptr;
+  e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+    delete c;
+    return fail(PSD_ERR_CUDA, "driver entry point cuTensorMapEncodeTiled unavailable");
+  }
+  c->dev.encode_tiled = fn;
+  for (int i = 0; i < 2; ++i) {
+    e = cudaEventCreateWithFlags(&c->staging_done[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      psd_destroy(c);
+      return fail(PSD_ERR_CUDA, "cudaEventCreate: %s", cudaGetErrorString(e));
+    }
+  }
+  *out = c;
+  return PSD_OK;
+}
+
+extern "C" psd_status psd_destroy(psd_ctx *c) {
+  clear_error();
+  if (!c) return PSD_OK;
+  DeviceGuard g(c->dev.device);
+  for (int i = 0; i < 2; ++i) {
+    if (c->staging_pending[i]) cudaEventSynchronize(c->staging_done[i]);
+    if (c->staging_done[i]) cudaEventDestroy(c->staging_done[i]);
+    if (c->staging[i]) cudaFreeHost(c->staging[i]);
+  }
+  delete c;
+  return PSD_OK;
+}
+
+extern "C" psd_status psd_get_counters(const psd_ctx *c, psd_counters *out) {
+  clear_error();
+  if (!c || !out) return fail(PSD_ERR_INVALID_ARG, "NULL");
+  *out = c->counters;
+  return PSD_OK;
+}
+
+extern "C" size_t psd_workspace_bytes(int32_t batch, int32_t num_items, int64_t num_rows, int32_t Hq,
+                                      int32_t Dv) {
+  if (batch < 0 || num_items < 0 || num_rows < 0 || Hq < 0 || Dv < 0) return 0;
+  return workspace_layout(batch, num_items, num_rows, Hq, Dv).total;
+}
+
+extern "C" psd_status paged_decode_partial(psd_ctx *ctx, const psd_decode_args *args,
+                                           const psd_work_item *items, int32_t num_items,
+                                           float *v_out, float *lse_out, int64_t out_rows,
+                                           void *workspace, size_t workspace_bytes,
+                                           psd_stream_t stream) {
+  clear_error();
+  if (!ctx) return fail(PSD_ERR_INVALID_ARG, "NULL context");
+  psd_status st = validate_args(args);
+  if (st != PSD_OK) return st;
+  if (num_items < 0 || (num_items > 0 && (!items || !v_out || !lse_out)) || !workspace)
+    return fail(PSD_ERR_INVALID_ARG, "paged_decode_partial: NULL items / outputs / workspace");
+  if (!aligned16(workspace) || !aligned16(v_out))
+    return fail(PSD_ERR_INVALID_ARG, "paged_decode_partial: workspace and v_out must be 16-byte aligned");
+  st = validate_items(args, items, num_items, out_rows, false, 0);
+  if (st != PSD_OK) return st;
+  const WorkspaceLayout lay = workspace_layout(0, num_items, 0, args->Hq, args->Dv);
+  if (workspace_bytes < lay.total)
+    return fail(PSD_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, lay.total);
+  PartialLaunch L = base_launch(args);
+  if (!dispatchable(L))
+    return launch_partial(L, ctx->dev, reinterpret_cast<cudaStream_t>(stream));
+  DeviceGuard g(ctx->dev.device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  std::vector<uint8_t> host(lay.lists_bytes, 0);
+  if (num_items) std::memcpy(host.data() + lay.items_off, items, sizeof(psd_work_item) * num_items);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  st = upload(ctx, ws, host.data(), host.size(), s);
+  if (st != PSD_OK) return st;
+  L.items = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
+  L.num_items = num_items;
+  L.v_out = v_out;
+  L.lse_out = lse_out;
+  L.fault = reinterpret_cast<int32_t *>(ws);
+  return launch_partial(L, ctx->dev, s);
+}
+
+extern "C" psd_status merge_states(psd_ctx *ctx, const float *v_in, const float *lse_in,
+                                   const int32_t *o_indptr_dev, int64_t num_out, int32_t H, int32_t D,
+                                   float *v_out, float *lse_out, psd_stream_t stream) {
+  clear_error();
+  if (!ctx) return fail(PSD_ERR_INVALID_ARG, "NULL context");
+  if (num_out < 0 || H < 0 || D < 4 || D % 4 || D > 1024)
+    return fail(PSD_ERR_INVALID_ARG, "merge_states: need num_out >= 0, H >= 0, D %% 4 == 0, D <= 1024");
+  if (num_out == 0 || H == 0) return PSD_OK;
+  if (!v_in || !lse_in || !o_indptr_dev || !v_out)
+    return fail(PSD_ERR_INVALID_ARG, "merge_states: NULL pointer");
+  if (!aligned16(v_in) || !aligned16(v_out))
+    return fail(PSD_ERR_INVALID_ARG, "merge_states: v_in / v_out must be 16-byte aligned");
+  DeviceGuard g(ctx->dev.device);
+  return launch_merge(v_in, lse_in, o_indptr_dev, num_out, H, D, v_out, lse_out, ctx->dev,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
+                                     const psd_cascade_plan *plan, float *o, float *lse,
+                                     void *workspace, size_t workspace_bytes,
+                                     psd_cascade_stats *stats, psd_stream_t stream) {
+  clear_error();
+  if (!ctx) return fail(PSD_ERR_INVALID_ARG, "NULL context");
+  psd_status st = validate_args(args);
+  if (st != PSD_OK) return st;
+  if (!plan || !o || !workspace) return fail(PSD_ERR_INVALID_ARG, "cascade_decode: NULL plan / o / workspace");
+  if (!aligned16(workspace) || !aligned16(o))
+    return fail(PSD_ERR_INVALID_ARG, "cascade_decode: workspace and o must be 16-byte aligned");
+  const int32_t B = args->batch;
+  if (plan->batch != B || plan->page_size != args->page_size)
+    return fail(PSD_ERR_INVALID_ARG, "cascade_decode: plan batch/page_size (%d/%d) != args (%d/%d)",
+                plan->batch, plan->page_size, B, args->page_size);
+  const int32_t M = plan->num_members, n0 = plan->l0_num_items, n1 = plan->l1_num_items;
+  if (M < 0 || M > B || n0 < 0 || n1 < 0 || (M == 0) != (n0 == 0) || plan->num_rows < 0 ||
+      plan->o_indptr[0] != 0 || plan->o_indptr[B] != plan->num_rows)
+    return fail(PSD_ERR_INVALID_ARG, "cascade_decode: inconsistent plan");
+  for (int32_t b = 0; b < B; ++b)
+    if (plan->o_indptr[b + 1] < plan->o_indptr[b])
+      return fail(PSD_ERR_INVALID_ARG, "cascade_decode: o_indptr decreasing at %d", b);
+  for (int32_t m = 0; m < M; ++m) {
+    if (plan->members[m] < 0 || plan->members[m] >= B ||
+        plan->member_row_base[m] != plan->o_indptr[plan->members[m]])
+      return fail(PSD_ERR_INVALID_ARG, "cascade_decode: member %d", m);
+    if (plan->o_indptr[plan->members[m] + 1] - plan->member_row_base[m] < n0)
+      return fail(PSD_ERR_INVALID_ARG, "cascade_decode: member %d has fewer rows than level 0", m);
+  }
+  st = validate_items(args, plan->l0_items, n0, plan->num_rows, true, M);
+  if (st == PSD_OK) st = validate_items(args, plan->l1_items, n1, plan->num_rows, false, M);
+  if (st != PSD_OK) return st;
+  for (int32_t i = 0; i < n0; ++i)
+    if (plan->l0_items[i].out_row >= n0) return fail(PSD_ERR_INVALID_ARG, "level-0 item %d: chunk index", i);
+
+  const WorkspaceLayout lay = workspace_layout(B, n0 + n1, plan->num_rows, args->Hq, args->Dv);
+  if (workspace_bytes < lay.total)
+    return fail(PSD_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, lay.total);
+
+  PartialLaunch L1 = base_launch(args);
+  PartialLaunch L0 = L1;
+  L0.G_cta = M * L1.Gm;
+  if (!dispatchable(L1)) return launch_partial(L1, ctx->dev, nullptr);
+  if (M > 0 && !dispatchable(L0)) return launch_partial(L0, ctx->dev, nullptr);
+
+  DeviceGuard g(ctx->dev.device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  std::vector<uint8_t> host(lay.lists_bytes, 0);
+  psd_work_item *hi = reinterpret_cast<psd_work_item *>(host.data() + lay.items_off);
+  if (n0) std::memcpy(hi, plan->l0_items, sizeof(psd_work_item) * n0);
+  if (n1) std::memcpy(hi + n0, plan->l1_items, sizeof(psd_work_item) * n1);
+  if (M) {
+    std::memcpy(host.data() + lay.members_off, plan->members, sizeof(int32_t) * M);
+    std::memcpy(host.data() + lay.row_base_off, plan->member_row_base, sizeof(int32_t) * M);
+  }
+  std::memcpy(host.data() + lay.indptr_off, plan->o_indptr, sizeof(int32_t) * (B + 1));
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  st = upload(ctx, ws, host.data(), host.size(), s);
+  if (st != PSD_OK) return st;
+
+  float *vpart = reinterpret_cast<float *>(ws + lay.vpart_off);
+  float *lpart = reinterpret_cast<float *>(ws + lay.lpart_off);
+  int32_t *fault = reinterpret_cast<int32_t *>(ws);
+  const psd_work_item *ditems = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
+  if (M > 0) {
+    L0.items = ditems;
+    L0.num_items = n0;
+    L0.members = reinterpret_cast<const int32_t *>(ws + lay.members_off);
+    L0.member_row_base = reinterpret_cast<const int32_t *>(ws + lay.row_base_off);
+    L0.v_out = vpart;
+    L0.lse_out = lpart;
+    L0.fault = fault;
+    st = launch_partial(L0, ctx->dev, s);
+    if (st != PSD_OK) return st;
+  }
+  L1.items = ditems + n0;
+  L1.num_items = n1;
+  L1.v_out = vpart;
+  L1.lse_out = lpart;
+  L1.fault = fault;
+  st = launch_partial(L1, ctx->dev, s);
+  if (st != PSD_OK) return st;
+  st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq,
+                    args->Dv, o, lse, ctx->dev, s);
+  if (st != PSD_OK) return st;
+
+  if (M > 0) {
+    ctx->counters.launches_cascade += 1;
+    ctx->counters.cascade_shared_tokens += int64_t(plan->shared_pages) * args->page_size;
+    ctx->counters.cascade_member_sequences += M;
+  } else {
+    ctx->counters.launches_flat += 1;
+    if (plan->decline_reason != PSD_DECLINE_NONE && plan->decline_reason != PSD_DECLINE_DISABLED)
+      ctx->counters.cascade_failures += 1;
+  }
+  if (stats) {
+    stats->path = M > 0 ? 1 : 0;
+    stats->decline_reason = plan->decline_reason;
+    stats->batch = B;
+    stats->members = M;
+    stats->shared_pages = plan->shared_pages;
+    stats->shared_tokens = plan->shared_pages * args->page_size;
+    stats->prefix_chunks = n0;
+    stats->suffix_chunks = n1;
+  }
+  return PSD_OK;
+}
+
+extern "C" psd_status psd_check_device_error(psd_ctx *ctx, void *workspace, psd_stream_t stream,
+                                             int32_t *fault_bits) {
+  clear_error();
+  if (!ctx || !workspace) return fail(PSD_ERR_INVALID_ARG, "NULL");
+  DeviceGuard g(ctx->dev.device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t flag = 0;
+  cudaError_t e = cudaMemcpyAsync(&flag, workspace, sizeof(flag), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "psd_check_device_error: %s", cudaGetErrorString(e));
+  if (fault_bits) *fault_bits = flag;
+  if (flag) {
+    e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return fail(PSD_ERR_DEVICE_FAULT, "kernel fault flag 0x%x (1 = page id out of range, 2 = wait timeout)", flag);
+  }
+  return PSD_OK;
+}

@@ -1,0 +1,55 @@
+// Host-side launch interfaces of the CUDA kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "psd_internal.h"
+
+namespace psd {
+
+struct DeviceInfo {
+  int device = 0;
+  int num_sms = 0;
+  int smem_optin = 0;
+  void *encode_tiled = nullptr;  // driver cuTensorMapEncodeTiled
+};
+
+// One partial-attention launch over a device work list.
+//   Items with q_index >= 0 use query rows q[q_index, kv*Gm + g] (g < Gm) and
+//   write rows out_row.  Items with q_index < 0 are the stacked level-0 request:
+//   CTA row j (< G_cta = M*Gm) is member m = j / Gm, head kv*Gm + j % Gm, reading
+//   q[members[m], .] and writing row member_row_base[m] + out_row.
+struct PartialLaunch {
+  const void *q = nullptr;
+  const void *k_pool = nullptr;
+  const void *v_pool = nullptr;  // == k_pool for a shared latent
+  const int32_t *page_indices = nullptr;
+  const psd_work_item *items = nullptr;  // device
+  int32_t num_items = 0;
+  const int32_t *members = nullptr;          // device, stacked items only
+  const int32_t *member_row_base = nullptr;  // device, stacked items only
+  float *v_out = nullptr;
+  float *lse_out = nullptr;
+  int32_t *fault = nullptr;
+  int64_t num_pages = 0;
+  int32_t Hq_req = 0;  // query heads per request in q and in the outputs
+  int32_t Hkv = 0, Dqk = 0, Dv = 0, page_size = 0;
+  int32_t Gm = 0;      // query heads per KV head of one request
+  int32_t G_cta = 0;   // query rows per CTA (Gm, or M*Gm when stacked)
+  int32_t kv_dtype = PSD_BF16;
+  bool latent_v = false;
+  int32_t max_item_tokens = 0;
+  float q_scale = 1.f;  // sm_scale * log2(e) * k_scale
+  float v_scale = 1.f;
+};
+
+bool partial_cc_supports(const PartialLaunch &p);
+psd_status launch_partial_cc(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
+bool partial_tc_supports(const PartialLaunch &p);
+psd_status launch_partial_tc(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
+
+psd_status launch_merge(const float *v_in, const float *lse_in, const int32_t *o_indptr,
+                        int64_t num_out, int32_t H, int32_t D, float *v_out, float *lse_out,
+                        const DeviceInfo &dev, cudaStream_t s);
+
+}  // namespace psd

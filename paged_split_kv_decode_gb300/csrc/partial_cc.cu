@@ -1,0 +1,358 @@
+// K1: split-KV partial attention on CUDA cores for G = Hq/Hkv <= 8.
+//
+// mlxcel PR #1004 ("compute shared prompt prefixes once per decode batch"),
+// Decomposition section: one CTA owns all G query heads of one KV head for one
+// (request, page tile), so every K/V element is read from HBM exactly once and
+// reused by the G heads; Merge contract section: each row leaves normalised by
+// its own denominator with LSE = m + log2(l) in log2 units.
+//
+// GB300 shape: grid = (work items, Hkv), 4 warps.  Warp w streams pages w, w+4,
+// ... of the tile through a private 3-stage ring: one TMA box per page for K and
+// one for V ({D, 1 head, page_size slots}), completing on an mbarrier, L2
+// evict-first.  A token row is D/8 lanes x 16 bytes (128-bit shared loads);
+// scores are reduced with a warp-shuffle butterfly, the online softmax runs per
+// sub-batch of tokens, and the four warp states are merged through shared memory.
+// Queries are pre-scaled by sm_scale*log2(e) so scores are already in log2 units.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "device.cuh"
+#include "kernels.h"
+
+namespace psd {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kStages = 3;
+
+struct CCParams {
+  const __nv_bfloat16 *q;
+  const int32_t *page_indices;
+  const psd_work_item *items;
+  const int32_t *members;
+  const int32_t *member_row_base;
+  float *v_out;
+  float *lse_out;
+  int32_t *fault;
+  int64_t num_pages;
+  int Hq_req, Dqk, Dv, page_size, Gm, G_cta;
+  float q_scale, v_scale;
+};
+
+__host__ __device__ constexpr int cc_unroll(int G) { return (32 / G) < 8 ? (32 / G) : 8; }
+
+template <int D, int G>
+__global__ void __launch_bounds__(kWarps * 32)
+    partial_cc_kernel(const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const CCParams p) {
+  constexpr int LPT = D / 8;     // lanes per token row (8 bf16 = 16 bytes per lane)
+  constexpr int TPS = 32 / LPT;  // tokens per warp step
+  constexpr int UNR = cc_unroll(G);
+  extern __shared__ __align__(1024) uint8_t smem[];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const psd_work_item it = p.items[blockIdx.x];
+  const int kv = blockIdx.y;
+  const int P = p.page_size;
+  const uint32_t page_bytes = uint32_t(P) * D * 2;
+  uint8_t *ring = smem + size_t(warp) * kStages * 2 * page_bytes;
+  const size_t stage_total = size_t(kWarps) * kStages * 2 * page_bytes;
+  const size_t red_total = size_t(kWarps) * G * (D + 2) * sizeof(float);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (stage_total > red_total ? stage_total : red_total)) +
+                   warp * kStages;
+
+  const int tslot = lane / LPT;
+  const int d0 = (lane % LPT) * 8;
+
+  // Query rows of this CTA, pre-scaled into log2 units.
+  float qf[G][8];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (g < p.G_cta) {
+      const int m = g / p.Gm;
+      const int qb = it.q_index >= 0 ? it.q_index : __ldg(p.members + m);
+      const int head = kv * p.Gm + (g - m * p.Gm);
+      const uint4 r = __ldg(reinterpret_cast<const uint4 *>(
+          p.q + (int64_t(qb) * p.Hq_req + head) * p.Dqk + d0));
+      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        qf[g][2 * e] = bf16_lo(w[e]) * p.q_scale;
+        qf[g][2 * e + 1] = bf16_hi(w[e]) * p.q_scale;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qf[g][e] = 0.f;
+    }
+  }
+
+  const int n_pages = (it.n_tokens + P - 1) / P;
+  const int my_pages = n_pages > warp ? (n_pages - warp + kWarps - 1) / kWarps : 0;
+  const uint64_t pol = l2_evict_first_policy();
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  auto issue = [&](int i) {  // lane 0 only
+    const int s = i % kStages;
+    const int pg = warp + i * kWarps;
+    const int id = __ldg(p.page_indices + it.page_off + pg);
+    const uint32_t bar = smem_u32(&bars[s]);
+    if (id < 0 || int64_t(id) >= p.num_pages) {
+      atomicOr(p.fault, PSD_FAULT_PAGE_ID);
+      mbar_arrive(bar);
+      return;
+    }
+    mbar_arrive_expect_tx(bar, 2 * page_bytes);
+    uint8_t *kb = ring + size_t(s) * 2 * page_bytes;
+    tma_load_4d(smem_u32(kb), &tmK, 0, kv, 0, id, bar, pol);
+    tma_load_4d(smem_u32(kb + page_bytes), &tmV, 0, kv, 0, id, bar, pol);
+  };
+  if (lane == 0) {
+    const int pre = my_pages < kStages ? my_pages : kStages;
+    for (int i = 0; i < pre; ++i) issue(i);
+  }
+
+  float m_run[G], l_run[G], acc[G][8];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m_run[g] = neg_inf();
+    l_run[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+  }
+
+  for (int i = 0; i < my_pages; ++i) {
+    const int s = i % kStages;
+    const int pg = warp + i * kWarps;
+    const int id = __ldg(p.page_indices + it.page_off + pg);
+    const bool page_ok = id >= 0 && int64_t(id) < p.num_pages;
+    const int valid = page_ok ? min(P, it.n_tokens - pg * P) : 0;
+    const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / kStages) & 1u, p.fault);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const uint8_t *kb = ring + size_t(s) * 2 * page_bytes;
+    const uint8_t *vb = kb + page_bytes;
+
+    for (int base = 0; base < valid; base += TPS * UNR) {
+      float sc[UNR][G];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int tok = base + u * TPS + tslot;
+        float part[G];
+        if (tok < valid) {
+          const uint4 r = *reinterpret_cast<const uint4 *>(kb + (size_t(tok) * D + d0) * 2);
+          const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+          float kf[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            kf[2 * e] = bf16_lo(w[e]);
+            kf[2 * e + 1] = bf16_hi(w[e]);
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float a = qf[g][0] * kf[0];
+#pragma unroll
+            for (int e = 1; e < 8; ++e) a = fmaf(qf[g][e], kf[e], a);
+            part[g] = a;
+          }
+        } else {
+#pragma unroll
+          for (int g = 0; g < G; ++g) part[g] = 0.f;
+        }
+#pragma unroll
+        for (int off = LPT / 2; off > 0; off >>= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) part[g] += __shfl_xor_sync(0xffffffffu, part[g], off);
+#pragma unroll
+        for (int g = 0; g < G; ++g) sc[u][g] = tok < valid ? part[g] : neg_inf();
+      }
+      // Online softmax update over this sub-batch.
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float mb = sc[0][g];
+#pragma unroll
+        for (int u = 1; u < UNR; ++u) mb = fmaxf(mb, sc[u][g]);
+#pragma unroll
+        for (int off = LPT; off < 32; off <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+        const float m_new = fmaxf(m_run[g], mb);
+        const float alpha = ex2(m_run[g] - m_new);  // 0 when m_run is -inf
+        m_run[g] = m_new;
+        l_run[g] *= alpha;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+      }
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int tok = base + u * TPS + tslot;
+        if (tok < valid) {
+          const uint4 r = *reinterpret_cast<const uint4 *>(vb + (size_t(tok) * D + d0) * 2);
+          const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+          float vf[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            vf[2 * e] = bf16_lo(w[e]);
+            vf[2 * e + 1] = bf16_hi(w[e]);
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float pr = ex2(sc[u][g] - m_run[g]);
+            l_run[g] += pr;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pr, vf[e], acc[g][e]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && i + kStages < my_pages) issue(i + kStages);
+  }
+
+  // Combine the token slots of the warp.
+#pragma unroll
+  for (int off = LPT; off < 32; off <<= 1) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      l_run[g] += __shfl_xor_sync(0xffffffffu, l_run[g], off);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], off);
+    }
+  }
+
+  // Merge the four warps through shared memory (the rings are no longer used).
+  __syncthreads();
+  float *red_acc = reinterpret_cast<float *>(smem);          // [kWarps][G][D]
+  float *red_m = red_acc + size_t(kWarps) * G * D;            // [kWarps][G]
+  float *red_l = red_m + kWarps * G;                          // [kWarps][G]
+  if (tslot == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float4 *dst = reinterpret_cast<float4 *>(red_acc + (size_t(warp) * G + g) * D + d0);
+      dst[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+      dst[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      red_m[warp * G + g] = m_run[g];
+      red_l[warp * G + g] = l_run[g];
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < p.G_cta * D; idx += kWarps * 32) {
+    const int g = idx / D, d = idx - g * D;
+    float M = neg_inf();
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * G + g]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float sc = ex2(red_m[w * G + g] - M);
+      L = fmaf(sc, red_l[w * G + g], L);
+      O = fmaf(sc, red_acc[(size_t(w) * G + g) * D + d], O);
+    }
+    const bool live = M != neg_inf();
+    const int m = g / p.Gm;
+    const int row = it.q_index >= 0 ? it.out_row : __ldg(p.member_row_base + m) + it.out_row;
+    const int head = kv * p.Gm + (g - m * p.Gm);
+    const int64_t o = int64_t(row) * p.Hq_req + head;
+    p.v_out[o * p.Dv + d] = live ? O / L * p.v_scale : 0.f;
+    if (d == 0) p.lse_out[o] = live ? M + log2f(L) : neg_inf();
+  }
+}
+
+template <int D, int G>
+size_t cc_smem_bytes(int page_size) {
+  const size_t stage = size_t(kWarps) * kStages * 2 * size_t(page_size) * D * 2;
+  const size_t red = size_t(kWarps) * G * (D + 2) * sizeof(float);
+  return std::max(stage, red) + size_t(kWarps) * kStages * sizeof(uint64_t);
+}
+
+bool encode_pool_map(CUtensorMap *map, const DeviceInfo &dev, const void *pool, int64_t num_pages,
+                     int page_size, int Hkv, int D) {
+  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(dev.encode_tiled);
+  if (!encode) return false;
+  cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(page_size), cuuint64_t(num_pages)};
+  cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(Hkv) * D * 2,
+                           cuuint64_t(page_size) * Hkv * D * 2};
+  cuuint32_t box[4] = {cuuint32_t(D), 1, cuuint32_t(page_size), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, int G>
+psd_status launch_cc(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
+  CUtensorMap tmK, tmV;
+  if (!encode_pool_map(&tmK, dev, L.k_pool, L.num_pages, L.page_size, L.Hkv, D) ||
+      !encode_pool_map(&tmV, dev, L.v_pool, L.num_pages, L.page_size, L.Hkv, D))
+    return fail(PSD_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
+  CCParams p;
+  p.q = reinterpret_cast<const __nv_bfloat16 *>(L.q);
+  p.page_indices = L.page_indices;
+  p.items = L.items;
+  p.members = L.members;
+  p.member_row_base = L.member_row_base;
+  p.v_out = L.v_out;
+  p.lse_out = L.lse_out;
+  p.fault = L.fault;
+  p.num_pages = L.num_pages;
+  p.Hq_req = L.Hq_req;
+  p.Dqk = L.Dqk;
+  p.Dv = L.Dv;
+  p.page_size = L.page_size;
+  p.Gm = L.Gm;
+  p.G_cta = L.G_cta;
+  p.q_scale = L.q_scale;
+  p.v_scale = L.v_scale;
+  const size_t smem = cc_smem_bytes<D, G>(L.page_size);
+  if (smem > size_t(dev.smem_optin))
+    return fail(PSD_ERR_UNSUPPORTED, "page_size %d needs %zu bytes of shared memory", L.page_size, smem);
+  auto kern = partial_cc_kernel<D, G>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  }
+  dim3 grid(unsigned(L.num_items), unsigned(L.Hkv)), block(kWarps * 32);
+  kern<<<grid, block, smem, s>>>(tmK, tmV, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "partial (CUDA cores) launch: %s", cudaGetErrorString(e));
+  return PSD_OK;
+}
+
+template <int D>
+psd_status launch_cc_d(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
+  if (L.G_cta <= 1) return launch_cc<D, 1>(L, dev, s);
+  if (L.G_cta <= 2) return launch_cc<D, 2>(L, dev, s);
+  if (L.G_cta <= 4) return launch_cc<D, 4>(L, dev, s);
+  return launch_cc<D, 8>(L, dev, s);
+}
+
+}  // namespace
+
+bool partial_cc_supports(const PartialLaunch &p) {
+  return p.kv_dtype == PSD_BF16 && !p.latent_v && p.Dqk == p.Dv &&
+         (p.Dqk == 64 || p.Dqk == 128 || p.Dqk == 256) && p.G_cta >= 1 && p.G_cta <= 8;
+}
+
+psd_status launch_partial_cc(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
+  if (L.num_items == 0) return PSD_OK;
+  switch (L.Dqk) {
+    case 64: return launch_cc_d<64>(L, dev, s);
+    case 128: return launch_cc_d<128>(L, dev, s);
+    case 256: return launch_cc_d<256>(L, dev, s);
+    default: return fail(PSD_ERR_UNSUPPORTED, "CUDA-core partial: head dim %d", L.Dqk);
+  }
+}
+
+}  // namespace psd

@@ -1,0 +1,168 @@
+"""Split-KV partials, flat decode and the two-level cascade on the GPU against the
+float64 oracle (mlxcel PR #1004: Decomposition, Merge contract, Task item 2,
+Correctness coverage)."""
+import numpy as np
+import pytest
+import torch
+
+import paged_split_kv_decode_gb300 as psd
+import synth
+from oracle import attention as A
+from oracle import cascade as OC
+from oracle import planner as PL
+from _gpu_util import Dev, assert_close, ctx, oracle_partials
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("maker,seed", [(synth.tiny_cascade, 0), (synth.tiny_cascade, 1),
+                                        (synth.flat_decode, 0)])
+def test_partials_match_oracle_chunk_by_chunk(maker, seed):
+    w = maker(seed=seed)
+    v, l, items, o_indptr = Dev(w).partials()
+    rv, rl, ro = oracle_partials(w)
+    assert o_indptr.tolist() == ro
+    assert_close(v, l, rv, rl, w.kv_dtype, "partials")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_flat_decode_full_size(seed):
+    """Flat config at full size (32 requests, 16384-page pool, tile 512), every output."""
+    w = synth.flat_decode(seed=seed)
+    d = Dev(w)
+    o, lse, stats, plan = d.decode(enable=1, with_stats=True)
+    assert stats["path"] == 0 and stats["decline_reason"] == PL.DECLINE_NO_SHARED_PAGES
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, w.kv_dtype, "flat")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_cascade_matches_oracle(seed):
+    w = synth.tiny_cascade(seed=seed)
+    d = Dev(w)
+    o, lse, stats, plan = d.decode(enable=1, with_stats=True)
+    assert stats["path"] == 1 and stats["members"] == 3 and stats["shared_pages"] == 4
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, w.kv_dtype, "tiny cascade")
+    fo, fl = d.decode(enable=0)
+    assert np.abs(o - fo).max() < 1e-3 and np.abs(lse - fl).max() < 1e-4
+
+
+def test_tiny_cascade_declines_at_default_thresholds():
+    w = synth.tiny_cascade(seed=0)
+    o, lse, stats, _ = Dev(w).decode(enable=1, min_shared_pages=16, min_members=2, with_stats=True)
+    assert stats["path"] == 0 and stats["decline_reason"] == PL.DECLINE_SPAN_BELOW_THRESHOLD
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, w.kv_dtype, "declined")
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_cascade_config_full_size(seed):
+    """Cascade config at full size: 64 requests, 16 members share 8192 tokens; the
+    cascade arm, the flat arm and the oracle agree."""
+    w = synth.cascade_decode(seed=seed)
+    d = Dev(w)
+    o, lse, stats, plan = d.decode(enable=1, with_stats=True)
+    assert stats["path"] == 1 and stats["members"] == 16 and stats["shared_pages"] == 512
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, w.kv_dtype, "cascade")
+    fo, fl = d.decode(enable=0)
+    assert_close(fo, fl, ro, rl, w.kv_dtype, "flat arm")
+    assert np.abs(o - fo).max() < 2e-3
+
+
+def test_cascade_with_small_group_uses_stacked_cuda_core_path():
+    """2 members x G=4 = 8 stacked rows per KV head: level 0 runs on the CUDA-core
+    kernel's stacked mode."""
+    w = synth.cascade_decode(seed=3, members=2, others=3, shared_tokens=512)
+    o, lse, stats, _ = Dev(w).decode(enable=1, with_stats=True)
+    assert stats["members"] == 2
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, w.kv_dtype, "2-member cascade")
+
+
+def test_cascade_level_partials_match_oracle_levels():
+    """The composite partial rows of a cascade equal the oracle's level-0 (unstacked)
+    and level-1 rows."""
+    w = synth.cascade_decode(seed=4, members=4, others=4, shared_tokens=1024)
+    a = A.workload_arrays(w)
+    plan = PL.plan_decode(w.page_indptr, w.page_indices, w.last_page_len, w.page_size,
+                          w.tile_tokens, True, 16, 2)
+    o, lse, vref, lref = OC.cascade_levels(a, plan, w.tile_tokens)
+    fo, fl = A.decode_attention(a)
+    assert np.abs(o - fo).max() < 1e-11
+    go, gl = Dev(w).decode(enable=1)
+    assert_close(go, gl, fo, fl, w.kv_dtype, "4-member cascade")
+
+
+def _stacked_level0(w, member_major):
+    members = [0, 1, 2]
+    M, G = len(members), w.Hq // w.Hkv
+    d = Dev(w)
+    qm = d.q[members]                                            # [M, Hq, D]
+    if member_major:
+        q0 = qm.reshape(1, M * w.Hq, w.Dqk).contiguous()
+    else:
+        q0 = qm.reshape(M, w.Hkv, G, w.Dqk).permute(1, 0, 2, 3).reshape(1, M * w.Hq, w.Dqk).contiguous()
+    span = 4
+    items = np.array([[0, int(w.page_indptr[0]), span * w.page_size, 0]], dtype=np.int32)
+    v = torch.empty((1, M * w.Hq, w.Dv), device="cuda")
+    l = torch.empty((1, M * w.Hq), device="cuda")
+    ws = torch.empty(psd.workspace_bytes(0, 1, 0, M * w.Hq, w.Dv), dtype=torch.uint8, device="cuda")
+    psd.paged_decode_partial(ctx(), d.args(q=q0), items, v, l, ws)
+    return v.cpu().double().numpy(), l.cpu().double().numpy()
+
+
+def test_kv_head_major_stacking_matches_and_member_major_reads_wrong_kv_head():
+    """Negative control named on the page: member-major stacking through the kernel's
+    h / (M*G) mapping reads the wrong KV head."""
+    w = synth.tiny_cascade(seed=2)
+    a = A.workload_arrays(w)
+    rv, rl = OC.level0_partials(a, [0, 1, 2], 4, 4 * w.page_size)
+    gv, gl = _stacked_level0(w, member_major=False)
+    assert_close(gv, gl, rv, rl, "bf16", "kv-major level 0")
+    bv, bl = _stacked_level0(w, member_major=True)
+    assert np.abs(bv - rv).max() > 0.1
+
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(256, 8, 1), (64, 6, 3), (128, 2, 2)])
+def test_other_head_dims_and_group_sizes(D, Hq, Hkv):
+    rng = np.random.default_rng(D + Hq)
+    lengths = synth.lengths_with_partial_last_page(rng, 5, 20, 700, 16)
+    w = synth._make("shape", rng, lengths, Hq=Hq, Hkv=Hkv, Dqk=D, Dv=D, page_size=16,
+                    num_pages=400, tile_tokens=64)
+    o, lse = Dev(w).decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "bf16", f"D={D} G={Hq // Hkv}")
+
+
+def test_fp8_pool_with_separate_k_and_v():
+    rng = np.random.default_rng(21)
+    lengths = synth.lengths_with_partial_last_page(rng, 6, 30, 900, 16)
+    w = synth._make("fp8gqa", rng, lengths, Hq=8, Hkv=2, Dqk=128, Dv=128, page_size=16,
+                    num_pages=512, tile_tokens=128, kv_dtype="fp8_e4m3")
+    o, lse = Dev(w).decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "fp8_e4m3", "fp8 GQA")
+
+
+def test_large_page_size_and_single_token_requests():
+    rng = np.random.default_rng(22)
+    lengths = [1, 2, 63, 64, 65, 300]
+    w = synth._make("edge", rng, lengths, Hq=8, Hkv=2, Dqk=128, Dv=128, page_size=64,
+                    num_pages=64, tile_tokens=128)
+    o, lse = Dev(w).decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "bf16", "page 64")
+    v, l, items, o_indptr = Dev(w).partials()
+    rv, rl2, _ = oracle_partials(w)
+    assert_close(v, l, rv, rl2, "bf16", "page 64 partials")
+
+
+def test_outputs_ignore_nan_canaries():
+    """Unused pool pages and slots past last_page_len are NaN; any stray read would
+    surface as NaN in the outputs."""
+    w = synth.flat_decode(seed=5, batch=8)
+    assert torch.isnan(w.k_pool.float()).any()
+    o, lse = Dev(w).decode(enable=0)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()

@@ -1,0 +1,103 @@
+"""Error behaviour through the C ABI on the GPU: host validation rejects bad
+arguments before any launch; an out-of-range page id in the device page table is
+caught by the kernels' bounds checks, skipped, and reported through the workspace
+fault flag (no trap)."""
+import numpy as np
+import pytest
+import torch
+
+import paged_split_kv_decode_gb300 as psd
+import synth
+from _gpu_util import Dev, ctx
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_partial(d, indices_dev):
+    w = d.w
+    items, o_indptr = psd.split_plan(d.table, w.tile_tokens)
+    N = int(o_indptr[-1])
+    v = torch.empty((N, w.Hq, w.Dv), device="cuda")
+    l = torch.empty((N, w.Hq), device="cuda")
+    ws = torch.empty(psd.workspace_bytes(0, len(items), 0, w.Hq, w.Dv), dtype=torch.uint8, device="cuda")
+    args = psd.decode_args(d.q, d.k, d.v, indices_dev, num_pages=w.num_pages, page_size=w.page_size,
+                           Hkv=w.Hkv, Dv=w.Dv, sm_scale=w.sm_scale)
+    psd.paged_decode_partial(ctx(), args, items, v, l, ws)
+    return ws
+
+
+@pytest.mark.parametrize("which", ["cuda_core", "tensor_core"])
+def test_out_of_range_page_id_sets_fault_flag(which):
+    w = synth.tiny_cascade(seed=0)
+    d = Dev(w)
+    bad = d.indices.clone()
+    bad[3] = w.num_pages + 7
+    if which == "cuda_core":
+        ws = _run_partial(d, bad)
+    else:
+        plan = psd.plan_decode(d.table, w.tile_tokens, 1, 4, 2)
+        assert plan.num_members == 3
+        o = torch.empty((w.batch, w.Hq, w.Dv), device="cuda")
+        ws = psd.workspace_for(plan, w.Hq, w.Dv, "cuda")
+        args = psd.decode_args(d.q, d.k, d.v, bad, num_pages=w.num_pages, page_size=w.page_size,
+                               Hkv=w.Hkv, Dv=w.Dv, sm_scale=w.sm_scale)
+        psd.cascade_decode(ctx(), args, plan, o, None, ws)
+    with pytest.raises(psd.PsdError) as e:
+        psd.check_device_error(ctx(), ws)
+    assert e.value.status == 4
+    # the flag is cleared by the check and the context stays usable
+    assert psd.check_device_error(ctx(), ws) == 0
+    ws2 = _run_partial(d, d.indices)
+    assert psd.check_device_error(ctx(), ws2) == 0
+
+
+def test_invalid_arguments_are_rejected_before_launch():
+    w = synth.tiny_cascade(seed=0)
+    d = Dev(w)
+    plan = psd.plan_decode(d.table, w.tile_tokens, 1, 4, 2)
+    o = torch.empty((w.batch, w.Hq, w.Dv), device="cuda")
+    ws = psd.workspace_for(plan, w.Hq, w.Dv, "cuda")
+    args = d.args()
+    args.Hkv = 3                                    # Hq % Hkv != 0
+    with pytest.raises(psd.PsdError) as e:
+        psd.cascade_decode(ctx(), args, plan, o, None, ws)
+    assert e.value.status == 1
+    small = ws[: ws.numel() // 2]
+    with pytest.raises(psd.PsdError) as e:
+        psd.cascade_decode(ctx(), d.args(), plan, o, None, small)
+    assert e.value.status == 5
+    mis = torch.empty(ws.numel() + 16, dtype=torch.uint8, device="cuda")[4:4 + ws.numel()]
+    with pytest.raises(psd.PsdError) as e:
+        psd.cascade_decode(ctx(), d.args(), plan, o, None, mis)
+    assert e.value.status == 1
+    items = np.array([[0, int(w.page_indptr[-1]) - 1, 10 * w.page_size, 0]], dtype=np.int32)
+    v = torch.empty((1, w.Hq, w.Dv), device="cuda")
+    l = torch.empty((1, w.Hq), device="cuda")
+    with pytest.raises(psd.PsdError) as e:                # item runs past the page table
+        psd.paged_decode_partial(ctx(), d.args(), items, v, l, ws)
+    assert e.value.status == 1
+    torch.cuda.synchronize()
+
+
+def test_unsupported_head_dim_is_reported():
+    rng = np.random.default_rng(0)
+    w = synth._make("d40", rng, [40, 50], Hq=2, Hkv=1, Dqk=40, Dv=40, page_size=16, num_pages=16,
+                    tile_tokens=32)
+    d = Dev(w)
+    plan = psd.plan_decode(d.table, w.tile_tokens, 0)
+    o = torch.empty((w.batch, w.Hq, w.Dv), device="cuda")
+    with pytest.raises(psd.PsdError) as e:
+        psd.cascade_decode(ctx(), d.args(), plan, o, None, psd.workspace_for(plan, w.Hq, w.Dv, "cuda"))
+    assert e.value.status == 2
+
+
+def test_counters_track_paths():
+    w = synth.tiny_cascade(seed=1)
+    d = Dev(w)
+    before = ctx().counters()
+    d.decode(enable=1)
+    d.decode(enable=0)
+    after = ctx().counters()
+    assert after["launches_cascade"] == before["launches_cascade"] + 1
+    assert after["launches_flat"] == before["launches_flat"] + 1
+    assert after["cascade_member_sequences"] == before["cascade_member_sequences"] + 3

@@ -1,0 +1,112 @@
+"""merge_states (K3) on the GPU against the float64 oracle merge (mlxcel PR #1004,
+Merge contract section)."""
+import numpy as np
+import pytest
+import torch
+
+import paged_split_kv_decode_gb300 as psd
+import synth
+from oracle import attention as A
+from _gpu_util import ctx
+
+pytestmark = pytest.mark.gpu
+
+TOL_O, TOL_L = 2e-5, 2e-5  # f32 arithmetic on f32 inputs
+
+
+def _gpu_merge(v_in, lse_in, o_indptr, lse_out=True):
+    M = len(o_indptr) - 1
+    H, D = v_in.shape[1], v_in.shape[2]
+    dv = v_in.cuda() if not v_in.is_cuda else v_in
+    dl = lse_in.cuda() if not lse_in.is_cuda else lse_in
+    ind = torch.from_numpy(np.asarray(o_indptr, dtype=np.int32)).cuda()
+    vo = torch.full((M, H, D), float("nan"), device="cuda")
+    lo = torch.full((M, H), float("nan"), device="cuda") if lse_out else None
+    psd.merge_states(ctx(), dv, dl, ind, vo, lo)
+    torch.cuda.synchronize()
+    return vo, lo
+
+
+@pytest.mark.parametrize("num_out,seed", [(1, 0), (1000, 1), (16384, 2)])
+def test_merge_parity_full_check(num_out, seed):
+    v_in, lse_in, o_indptr = synth.merge_inputs(seed, num_out)
+    ro, rl = A.merge_states(v_in.numpy(), lse_in.numpy(), o_indptr)
+    vo, lo = _gpu_merge(v_in, lse_in, o_indptr)
+    assert np.abs(vo.cpu().double().numpy() - ro).max() < TOL_O
+    assert np.abs(lo.cpu().double().numpy() - rl).max() < TOL_L
+
+
+@pytest.mark.parametrize("H,D", [(128, 512), (8, 64), (4, 1024), (3, 12)])
+def test_merge_parity_other_shapes(H, D):
+    rng = np.random.default_rng(H + D)
+    o_indptr = synth.merge_groups(rng, 300, 1, 40)
+    N = int(o_indptr[-1])
+    v_in = torch.from_numpy(rng.standard_normal((N, H, D), dtype=np.float32))
+    lse_in = torch.from_numpy(rng.uniform(-5, 20, size=(N, H)).astype(np.float32))
+    ro, rl = A.merge_states(v_in.numpy(), lse_in.numpy(), o_indptr)
+    vo, lo = _gpu_merge(v_in, lse_in, o_indptr)
+    assert np.abs(vo.cpu().double().numpy() - ro).max() < TOL_O
+    assert np.abs(lo.cpu().double().numpy() - rl).max() < TOL_L
+
+
+def test_group_of_one_is_bit_exact_identity():
+    v_in, lse_in, _ = synth.merge_inputs(3, 64)
+    N = v_in.shape[0]
+    vo, lo = _gpu_merge(v_in, lse_in, np.arange(N + 1))
+    assert torch.equal(vo.cpu(), v_in) and torch.equal(lo.cpu(), lse_in)
+
+
+def test_merge_is_associative_across_regroupings():
+    rng = np.random.default_rng(4)
+    v_in = torch.from_numpy(rng.standard_normal((9, 32, 128), dtype=np.float32))
+    lse_in = torch.from_numpy(rng.uniform(-5, 20, size=(9, 32)).astype(np.float32))
+    direct, dl = _gpu_merge(v_in, lse_in, [0, 9])
+    sub, sl = _gpu_merge(v_in, lse_in, [0, 2, 5, 9])
+    two, tl = _gpu_merge(sub, sl, [0, 3])
+    assert (two - direct).abs().max().item() < 1e-5 and (tl - dl).abs().max().item() < 1e-5
+
+
+def test_natural_log_lse_fails_parity():
+    """Negative control: LSEs in natural-log units fed to the log2 merge."""
+    v_in, lse_in, o_indptr = synth.merge_inputs(5, 500)
+    ro, _ = A.merge_states(v_in.numpy(), lse_in.numpy(), o_indptr)
+    vo, _ = _gpu_merge(v_in, lse_in * float(np.log(2.0)), o_indptr)
+    assert np.abs(vo.cpu().double().numpy() - ro).max() > 1e-2
+
+
+def test_empty_and_neg_inf_groups():
+    v_in = torch.ones((3, 2, 8))
+    lse_in = torch.tensor([[0.0, 1.0], [-float("inf"), -float("inf")], [-float("inf"), 2.0]])
+    vo, lo = _gpu_merge(v_in, lse_in, [0, 0, 1, 2, 3])
+    assert torch.equal(vo[0].cpu(), torch.zeros(2, 8)) and torch.all(lo[0].cpu() == -float("inf"))
+    assert torch.equal(vo[1].cpu(), v_in[0]) and torch.equal(lo[1].cpu(), lse_in[0])
+    assert torch.equal(vo[2].cpu(), torch.zeros(2, 8))           # one row, lse -inf
+    assert torch.equal(vo[3, 1].cpu(), v_in[2, 1]) and torch.equal(vo[3, 0].cpu(), torch.zeros(8))
+
+
+def test_lse_out_may_be_null():
+    v_in, lse_in, o_indptr = synth.merge_inputs(6, 100)
+    ro, _ = A.merge_states(v_in.numpy(), lse_in.numpy(), o_indptr)
+    vo, _ = _gpu_merge(v_in, lse_in, o_indptr, lse_out=False)
+    assert np.abs(vo.cpu().double().numpy() - ro).max() < TOL_O
+
+
+@pytest.mark.parametrize("num_out", [262144, 1048576])
+def test_merge_sweep_large_sampled(num_out):
+    """Large sweep points: inputs drawn on the device; 4096 seeded output rows are
+    checked against the oracle on their own input rows."""
+    v_in, lse_in, o_indptr = synth.merge_inputs_device(7, num_out)
+    vo, lo = _gpu_merge(v_in, lse_in, o_indptr)
+    rng = np.random.default_rng(8)
+    rows = np.sort(rng.choice(num_out, size=4096, replace=False))
+    rows[0] = 0  # includes the forced group of one
+    src = np.concatenate([np.arange(o_indptr[r], o_indptr[r + 1]) for r in rows])
+    sizes = o_indptr[rows + 1] - o_indptr[rows]
+    sub_indptr = np.concatenate([[0], np.cumsum(sizes)])
+    idx = torch.from_numpy(src).cuda()
+    ro, rl = A.merge_states(v_in[idx].cpu().numpy(), lse_in[idx].cpu().numpy(), sub_indptr)
+    ridx = torch.from_numpy(rows).cuda()
+    assert np.abs(vo[ridx].cpu().double().numpy() - ro).max() < TOL_O
+    assert np.abs(lo[ridx].cpu().double().numpy() - rl).max() < TOL_L
+    del v_in, lse_in, vo, lo
+    torch.cuda.empty_cache()
