@@ -6,9 +6,10 @@
 // reused by the G heads; Merge contract section: each row leaves normalised by
 // its own denominator with LSE = m + log2(l) in log2 units.
 //
-// GB300 shape: grid = (work items, Hkv), 4 warps.  Warp w streams pages w, w+4,
-// ... of the tile through a private 3-stage ring: one TMA box per page for K and
-// one for V ({D, 1 head, page_size slots}), completing on an mbarrier, L2
+// GB300 shape: grid = (work items, Hkv), 4 warps.  The item's tokens are cut into
+// ring tiles of gcd(page_size, 16) consecutive slots of one page; warp w streams
+// tiles w, w+4, ... through a private 3-stage ring: one TMA box per tile for K and
+// one for V ({D, 1 head, tile slots}), completing on an mbarrier, L2
 // evict-first.  A token row is D/8 lanes x 16 bytes (128-bit shared loads);
 // scores are reduced with a warp-shuffle butterfly, the online softmax runs per
 // sub-batch of tokens, and the four warp states are merged through shared memory.
@@ -39,7 +40,7 @@ struct CCParams {
   float *lse_out;
   int32_t *fault;
   int64_t num_pages;
-  int Hq_req, Dqk, Dv, page_size, Gm, G_cta;
+  int Hq_req, Dqk, Dv, page_size, sub, Gm, G_cta;  // sub = tokens per ring tile
   float q_scale, v_scale;
 };
 
@@ -58,7 +59,9 @@ __global__ void __launch_bounds__(kWarps * 32)
   const psd_work_item it = p.items[blockIdx.x];
   const int kv = blockIdx.y;
   const int P = p.page_size;
-  const uint32_t page_bytes = uint32_t(P) * D * 2;
+  const int SUB = p.sub;          // tile = SUB consecutive slots of one page
+  const int TPP = P / SUB;        // tiles per page
+  const uint32_t page_bytes = uint32_t(SUB) * D * 2;
   uint8_t *ring = smem + size_t(warp) * kStages * 2 * page_bytes;
   const size_t stage_total = size_t(kWarps) * kStages * 2 * page_bytes;
   const size_t red_total = size_t(kWarps) * G * (D + 2) * sizeof(float);
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
   }
 
-  const int n_pages = (it.n_tokens + P - 1) / P;
+  const int n_pages = (it.n_tokens + SUB - 1) / SUB;  // tiles of this item
   const int my_pages = n_pages > warp ? (n_pages - warp + kWarps - 1) / kWarps : 0;
   const uint64_t pol = l2_evict_first_policy();
 
@@ -104,7 +107,8 @@ __global__ void __launch_bounds__(kWarps * 32)
   auto issue = [&](int i) {  // lane 0 only
     const int s = i % kStages;
     const int pg = warp + i * kWarps;
-    const int id = __ldg(p.page_indices + it.page_off + pg);
+    const int id = __ldg(p.page_indices + it.page_off + pg / TPP);
+    const int slot0 = (pg % TPP) * SUB;
     const uint32_t bar = smem_u32(&bars[s]);
     if (id < 0 || int64_t(id) >= p.num_pages) {
       atomicOr(p.fault, PSD_FAULT_PAGE_ID);
@@ -113,8 +117,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
     mbar_arrive_expect_tx(bar, 2 * page_bytes);
     uint8_t *kb = ring + size_t(s) * 2 * page_bytes;
-    tma_load_4d(smem_u32(kb), &tmK, 0, kv, 0, id, bar, pol);
-    tma_load_4d(smem_u32(kb + page_bytes), &tmV, 0, kv, 0, id, bar, pol);
+    tma_load_4d(smem_u32(kb), &tmK, 0, kv, slot0, id, bar, pol);
+    tma_load_4d(smem_u32(kb + page_bytes), &tmV, 0, kv, slot0, id, bar, pol);
   };
   if (lane == 0) {
     const int pre = my_pages < kStages ? my_pages : kStages;
@@ -133,9 +137,9 @@ __global__ void __launch_bounds__(kWarps * 32)
   for (int i = 0; i < my_pages; ++i) {
     const int s = i % kStages;
     const int pg = warp + i * kWarps;
-    const int id = __ldg(p.page_indices + it.page_off + pg);
+    const int id = __ldg(p.page_indices + it.page_off + pg / TPP);
     const bool page_ok = id >= 0 && int64_t(id) < p.num_pages;
-    const int valid = page_ok ? min(P, it.n_tokens - pg * P) : 0;
+    const int valid = page_ok ? min(SUB, it.n_tokens - pg * SUB) : 0;
     const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / kStages) & 1u, p.fault);
     if (!__all_sync(0xffffffffu, ok)) break;
     const uint8_t *kb = ring + size_t(s) * 2 * page_bytes;
@@ -269,21 +273,31 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
+int ring_tile_tokens(int page_size) {  // gcd(page_size, 16)
+  int a = page_size, b = 16;
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
 template <int D, int G>
-size_t cc_smem_bytes(int page_size) {
-  const size_t stage = size_t(kWarps) * kStages * 2 * size_t(page_size) * D * 2;
+size_t cc_smem_bytes(int sub) {
+  const size_t stage = size_t(kWarps) * kStages * 2 * size_t(sub) * D * 2;
   const size_t red = size_t(kWarps) * G * (D + 2) * sizeof(float);
   return std::max(stage, red) + size_t(kWarps) * kStages * sizeof(uint64_t);
 }
 
 bool encode_pool_map(CUtensorMap *map, const DeviceInfo &dev, const void *pool, int64_t num_pages,
-                     int page_size, int Hkv, int D) {
+                     int page_size, int sub, int Hkv, int D) {
   auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(dev.encode_tiled);
   if (!encode) return false;
   cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(page_size), cuuint64_t(num_pages)};
   cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(Hkv) * D * 2,
                            cuuint64_t(page_size) * Hkv * D * 2};
-  cuuint32_t box[4] = {cuuint32_t(D), 1, cuuint32_t(page_size), 1};
+  cuuint32_t box[4] = {cuuint32_t(D), 1, cuuint32_t(sub), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims,
                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -293,9 +307,10 @@ bool encode_pool_map(CUtensorMap *map, const DeviceInfo &dev, const void *pool, 
 
 template <int D, int G>
 psd_status launch_cc(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
+  const int sub = ring_tile_tokens(L.page_size);
   CUtensorMap tmK, tmV;
-  if (!encode_pool_map(&tmK, dev, L.k_pool, L.num_pages, L.page_size, L.Hkv, D) ||
-      !encode_pool_map(&tmV, dev, L.v_pool, L.num_pages, L.page_size, L.Hkv, D))
+  if (!encode_pool_map(&tmK, dev, L.k_pool, L.num_pages, L.page_size, sub, L.Hkv, D) ||
+      !encode_pool_map(&tmV, dev, L.v_pool, L.num_pages, L.page_size, sub, L.Hkv, D))
     return fail(PSD_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
   CCParams p;
   p.q = reinterpret_cast<const __nv_bfloat16 *>(L.q);
@@ -311,11 +326,12 @@ psd_status launch_cc(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t
   p.Dqk = L.Dqk;
   p.Dv = L.Dv;
   p.page_size = L.page_size;
+  p.sub = sub;
   p.Gm = L.Gm;
   p.G_cta = L.G_cta;
   p.q_scale = L.q_scale;
   p.v_scale = L.v_scale;
-  const size_t smem = cc_smem_bytes<D, G>(L.page_size);
+  const size_t smem = cc_smem_bytes<D, G>(sub);
   if (smem > size_t(dev.smem_optin))
     return fail(PSD_ERR_UNSUPPORTED, "page_size %d needs %zu bytes of shared memory", L.page_size, smem);
   auto kern = partial_cc_kernel<D, G>;
