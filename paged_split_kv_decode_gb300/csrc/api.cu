@@ -8,6 +8,7 @@
 
 #include <cmath>
 #include <cstdarg>
+#include <algorithm>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -20,6 +21,12 @@ namespace psd {
 static thread_local std::string g_error;
 
 void clear_error() { g_error.clear(); }
+
+void longest_first(const psd_work_item *items, int32_t n, int32_t *order) {
+  for (int32_t i = 0; i < n; ++i) order[i] = i;
+  std::stable_sort(order, order + n,
+                   [items](int32_t a, int32_t b) { return items[a].n_tokens > items[b].n_tokens; });
+}
 
 psd_status fail(psd_status st, const char *fmt, ...) {
   char buf[512];
@@ -260,10 +267,12 @@ extern "C" psd_status paged_decode_partial(psd_ctx *ctx, const psd_decode_args *
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   std::vector<uint8_t> host(lay.lists_bytes, 0);
   if (num_items) std::memcpy(host.data() + lay.items_off, items, sizeof(psd_work_item) * num_items);
+  longest_first(items, num_items, reinterpret_cast<int32_t *>(host.data() + lay.order_off));
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   st = upload(ctx, ws, host.data(), host.size(), s);
   if (st != PSD_OK) return st;
   L.items = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
+  L.order = reinterpret_cast<const int32_t *>(ws + lay.order_off);
   L.num_items = num_items;
   L.v_out = v_out;
   L.lse_out = lse_out;
@@ -339,6 +348,9 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   psd_work_item *hi = reinterpret_cast<psd_work_item *>(host.data() + lay.items_off);
   if (n0) std::memcpy(hi, plan->l0_items, sizeof(psd_work_item) * n0);
   if (n1) std::memcpy(hi + n0, plan->l1_items, sizeof(psd_work_item) * n1);
+  int32_t *ho = reinterpret_cast<int32_t *>(host.data() + lay.order_off);
+  longest_first(plan->l0_items, n0, ho);
+  longest_first(plan->l1_items, n1, ho + n0);
   if (M) {
     std::memcpy(host.data() + lay.members_off, plan->members, sizeof(int32_t) * M);
     std::memcpy(host.data() + lay.row_base_off, plan->member_row_base, sizeof(int32_t) * M);
@@ -354,6 +366,7 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   const psd_work_item *ditems = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
   if (M > 0) {
     L0.items = ditems;
+    L0.order = reinterpret_cast<const int32_t *>(ws + lay.order_off);
     L0.num_items = n0;
     L0.members = reinterpret_cast<const int32_t *>(ws + lay.members_off);
     L0.member_row_base = reinterpret_cast<const int32_t *>(ws + lay.row_base_off);
@@ -364,6 +377,7 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
     if (st != PSD_OK) return st;
   }
   L1.items = ditems + n0;
+  L1.order = reinterpret_cast<const int32_t *>(ws + lay.order_off) + n0;
   L1.num_items = n1;
   L1.v_out = vpart;
   L1.lse_out = lpart;

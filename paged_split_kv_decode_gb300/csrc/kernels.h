@@ -25,6 +25,7 @@ struct PartialLaunch {
   const void *v_pool = nullptr;  // == k_pool for a shared latent
   const int32_t *page_indices = nullptr;
   const psd_work_item *items = nullptr;  // device
+  const int32_t *order = nullptr;        // device, CTA -> item index (longest first), or NULL
   int32_t num_items = 0;
   const int32_t *members = nullptr;          // device, stacked items only
   const int32_t *member_row_base = nullptr;  // device, stacked items only

@@ -6,14 +6,17 @@
 // reused by the G heads; Merge contract section: each row leaves normalised by
 // its own denominator with LSE = m + log2(l) in log2 units.
 //
-// GB300 shape: grid = (work items, Hkv), 4 warps.  The item's tokens are cut into
-// ring tiles of gcd(page_size, 16) consecutive slots of one page; warp w streams
-// tiles w, w+4, ... through a private 3-stage ring: one TMA box per tile for K and
-// one for V ({D, 1 head, tile slots}), completing on an mbarrier, L2
-// evict-first.  A token row is D/8 lanes x 16 bytes (128-bit shared loads);
-// scores are reduced with a warp-shuffle butterfly, the online softmax runs per
-// sub-batch of tokens, and the four warp states are merged through shared memory.
-// Queries are pre-scaled by sm_scale*log2(e) so scores are already in log2 units.
+// GB300 shape: grid = (work items, Hkv), 4 warps, 4 CTAs per SM (16 warps).  The
+// item's tokens are cut into ring tiles of gcd(page_size, 8) consecutive slots of
+// one page; warp w streams tiles w, w+4, ... through a private 3-stage ring: one
+// TMA box per tile for K and one for V ({D, 1 head, tile slots}), completing on an
+// mbarrier, L2 evict-first.  A token row is D/8 lanes x 16 bytes (128-bit shared
+// loads).  The G partial dot products of a lane are summed over the row's lanes by
+// a halving ("transpose") butterfly that leaves one full score per lane, so the
+// exponentials are computed once per (head, token); products use packed f32x2
+// FMAs.  The online softmax advances once per tile, and the four warp states are
+// merged through shared memory.  Queries are pre-scaled by sm_scale*log2(e) so
+// scores are already in log2 units.  CTAs visit items longest first.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -40,39 +43,68 @@ struct CCParams {
   float *lse_out;
   int32_t *fault;
   int64_t num_pages;
+  const int32_t *order;  // CTA -> item (longest items first), or NULL
   int Hq_req, Dqk, Dv, page_size, sub, Gm, G_cta;  // sub = tokens per ring tile
   float q_scale, v_scale;
 };
 
-__host__ __device__ constexpr int cc_unroll(int G) { return (32 / G) < 8 ? (32 / G) : 8; }
+// Sums G per-lane values over the LPT lanes of a token slot, halving the number
+// of values per lane at each butterfly step: afterwards lane l holds the full sum
+// of value (l % LPT) / (LPT / G).  log2(G) select/shuffle halvings plus
+// log2(LPT / G) plain steps instead of G * log2(LPT) shuffles.
+template <int G, int LPT>
+__device__ __forceinline__ float transpose_reduce(float (&v)[G], int lane) {
+  float cur[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) cur[g] = v[g];
+  int off = LPT / 2;
+#pragma unroll
+  for (int n = G; n > 1; n >>= 1, off >>= 1) {
+    const bool upper = (lane & off) != 0;  // this lane keeps the upper half
+#pragma unroll
+    for (int k = 0; k < n / 2; ++k) {
+      const float send = upper ? cur[k] : cur[k + n / 2];
+      const float keep = upper ? cur[k + n / 2] : cur[k];
+      cur[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  float r = cur[0];
+#pragma unroll
+  for (; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+  return r;
+}
 
 template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, G <= 4 ? 4 : 2)
     partial_cc_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const CCParams p) {
-  constexpr int LPT = D / 8;     // lanes per token row (8 bf16 = 16 bytes per lane)
-  constexpr int TPS = 32 / LPT;  // tokens per warp step
-  constexpr int UNR = cc_unroll(G);
+  constexpr int LPT = D / 8;         // lanes per token row (8 bf16 = 16 bytes per lane)
+  constexpr int TPS = 32 / LPT;      // tokens per warp step
+  constexpr int HL = LPT / G;        // lanes per head after the transpose reduce
+  static_assert(G <= LPT, "one score per lane needs G <= D / 8");
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const psd_work_item it = p.items[blockIdx.x];
+  const psd_work_item it = p.items[p.order ? __ldg(p.order + blockIdx.x) : blockIdx.x];
   const int kv = blockIdx.y;
   const int P = p.page_size;
-  const int SUB = p.sub;          // tile = SUB consecutive slots of one page
+  const int SUB = p.sub;          // ring tile = SUB consecutive slots of one page
   const int TPP = P / SUB;        // tiles per page
-  const uint32_t page_bytes = uint32_t(SUB) * D * 2;
-  uint8_t *ring = smem + size_t(warp) * kStages * 2 * page_bytes;
-  const size_t stage_total = size_t(kWarps) * kStages * 2 * page_bytes;
+  const int steps = SUB / TPS > 0 ? SUB / TPS : 1;
+  const uint32_t tile_bytes = uint32_t(SUB) * D * 2;
+  uint8_t *ring = smem + size_t(warp) * kStages * 2 * tile_bytes;
+  const size_t stage_total = size_t(kWarps) * kStages * 2 * tile_bytes;
   const size_t red_total = size_t(kWarps) * G * (D + 2) * sizeof(float);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (stage_total > red_total ? stage_total : red_total)) +
                    warp * kStages;
 
   const int tslot = lane / LPT;
-  const int d0 = (lane % LPT) * 8;
+  const int sl = lane % LPT;
+  const int d0 = sl * 8;
+  const int my_head = sl / HL;  // the head whose score this lane holds after a reduce
 
-  // Query rows of this CTA, pre-scaled into log2 units.
-  float qf[G][8];
+  // Query rows of this CTA, pre-scaled into log2 units, as float pairs.
+  float2 q2[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     if (g < p.G_cta) {
@@ -83,18 +115,16 @@ __global__ void __launch_bounds__(kWarps * 32)
           p.q + (int64_t(qb) * p.Hq_req + head) * p.Dqk + d0));
       const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        qf[g][2 * e] = bf16_lo(w[e]) * p.q_scale;
-        qf[g][2 * e + 1] = bf16_hi(w[e]) * p.q_scale;
-      }
+      for (int e = 0; e < 4; ++e)
+        q2[g][e] = make_float2(bf16_lo(w[e]) * p.q_scale, bf16_hi(w[e]) * p.q_scale);
     } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) qf[g][e] = 0.f;
+      for (int e = 0; e < 4; ++e) q2[g][e] = make_float2(0.f, 0.f);
     }
   }
 
-  const int n_pages = (it.n_tokens + SUB - 1) / SUB;  // tiles of this item
-  const int my_pages = n_pages > warp ? (n_pages - warp + kWarps - 1) / kWarps : 0;
+  const int n_tiles = (it.n_tokens + SUB - 1) / SUB;
+  const int my_tiles = n_tiles > warp ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
   const uint64_t pol = l2_evict_first_policy();
 
   if (lane == 0) {
@@ -106,128 +136,129 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   auto issue = [&](int i) {  // lane 0 only
     const int s = i % kStages;
-    const int pg = warp + i * kWarps;
-    const int id = __ldg(p.page_indices + it.page_off + pg / TPP);
-    const int slot0 = (pg % TPP) * SUB;
+    const int t = warp + i * kWarps;
+    const int id = __ldg(p.page_indices + it.page_off + t / TPP);
+    const int slot0 = (t % TPP) * SUB;
     const uint32_t bar = smem_u32(&bars[s]);
     if (id < 0 || int64_t(id) >= p.num_pages) {
       atomicOr(p.fault, PSD_FAULT_PAGE_ID);
       mbar_arrive(bar);
       return;
     }
-    mbar_arrive_expect_tx(bar, 2 * page_bytes);
-    uint8_t *kb = ring + size_t(s) * 2 * page_bytes;
+    mbar_arrive_expect_tx(bar, 2 * tile_bytes);
+    uint8_t *kb = ring + size_t(s) * 2 * tile_bytes;
     tma_load_4d(smem_u32(kb), &tmK, 0, kv, slot0, id, bar, pol);
-    tma_load_4d(smem_u32(kb + page_bytes), &tmV, 0, kv, slot0, id, bar, pol);
+    tma_load_4d(smem_u32(kb + tile_bytes), &tmV, 0, kv, slot0, id, bar, pol);
   };
   if (lane == 0) {
-    const int pre = my_pages < kStages ? my_pages : kStages;
+    const int pre = my_tiles < kStages ? my_tiles : kStages;
     for (int i = 0; i < pre; ++i) issue(i);
   }
 
-  float m_run[G], l_run[G], acc[G][8];
+  float m_run = neg_inf(), l_run = 0.f;  // for my_head, over this lane's token slot
+  float2 acc[G][4];
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m_run[g] = neg_inf();
-    l_run[g] = 0.f;
+  for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
-  }
+    for (int e = 0; e < 4; ++e) acc[g][e] = make_float2(0.f, 0.f);
 
-  for (int i = 0; i < my_pages; ++i) {
+  for (int i = 0; i < my_tiles; ++i) {
     const int s = i % kStages;
-    const int pg = warp + i * kWarps;
-    const int id = __ldg(p.page_indices + it.page_off + pg / TPP);
+    const int t = warp + i * kWarps;
+    const int id = __ldg(p.page_indices + it.page_off + t / TPP);
     const bool page_ok = id >= 0 && int64_t(id) < p.num_pages;
-    const int valid = page_ok ? min(SUB, it.n_tokens - pg * SUB) : 0;
+    const int valid = page_ok ? min(SUB, it.n_tokens - t * SUB) : 0;
     const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / kStages) & 1u, p.fault);
     if (!__all_sync(0xffffffffu, ok)) break;
-    const uint8_t *kb = ring + size_t(s) * 2 * page_bytes;
-    const uint8_t *vb = kb + page_bytes;
+    const uint8_t *kb = ring + size_t(s) * 2 * tile_bytes;
+    const uint8_t *vb = kb + tile_bytes;
 
-    for (int base = 0; base < valid; base += TPS * UNR) {
-      float sc[UNR][G];
+    if (valid > 0) {
+      // ---- scores of my_head for this lane's tokens
+      float sc[8];
+      float mt = neg_inf();
 #pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const int tok = base + u * TPS + tslot;
-        float part[G];
-        if (tok < valid) {
-          const uint4 r = *reinterpret_cast<const uint4 *>(kb + (size_t(tok) * D + d0) * 2);
-          const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-          float kf[8];
+      for (int u = 0; u < 8; ++u) {
+        if (u < steps) {
+          const int tok = u * TPS + tslot;
+          float part[G];
+          if (tok < valid) {
+            const uint4 r = *reinterpret_cast<const uint4 *>(kb + (size_t(tok) * D + d0) * 2);
+            const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+            float2 k2[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            kf[2 * e] = bf16_lo(w[e]);
-            kf[2 * e + 1] = bf16_hi(w[e]);
+            for (int e = 0; e < 4; ++e) k2[e] = make_float2(bf16_lo(w[e]), bf16_hi(w[e]));
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              float2 a = __fmul2_rn(q2[g][0], k2[0]);
+#pragma unroll
+              for (int e = 1; e < 4; ++e) a = __ffma2_rn(q2[g][e], k2[e], a);
+              part[g] = a.x + a.y;
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < G; ++g) part[g] = 0.f;
           }
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            float a = qf[g][0] * kf[0];
-#pragma unroll
-            for (int e = 1; e < 8; ++e) a = fmaf(qf[g][e], kf[e], a);
-            part[g] = a;
-          }
-        } else {
-#pragma unroll
-          for (int g = 0; g < G; ++g) part[g] = 0.f;
+          const float sv = transpose_reduce<G, LPT>(part, lane);
+          sc[u] = tok < valid ? sv : neg_inf();
+          mt = fmaxf(mt, sc[u]);
         }
-#pragma unroll
-        for (int off = LPT / 2; off > 0; off >>= 1)
-#pragma unroll
-          for (int g = 0; g < G; ++g) part[g] += __shfl_xor_sync(0xffffffffu, part[g], off);
-#pragma unroll
-        for (int g = 0; g < G; ++g) sc[u][g] = tok < valid ? part[g] : neg_inf();
       }
-      // Online softmax update over this sub-batch.
+#pragma unroll
+      for (int off = LPT; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+      // ---- online softmax: new running max, rescale of every head's accumulator
+      const float m_new = fmaxf(m_run, mt);
+      const float alpha = ex2(m_run - m_new);  // 0 while m_run is -inf
+      m_run = m_new;
+      l_run *= alpha;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float mb = sc[0][g];
+        const float ag = __shfl_sync(0xffffffffu, alpha, tslot * LPT + g * HL);
+        const float2 a2 = make_float2(ag, ag);
 #pragma unroll
-        for (int u = 1; u < UNR; ++u) mb = fmaxf(mb, sc[u][g]);
-#pragma unroll
-        for (int off = LPT; off < 32; off <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
-        const float m_new = fmaxf(m_run[g], mb);
-        const float alpha = ex2(m_run[g] - m_new);  // 0 when m_run is -inf
-        m_run[g] = m_new;
-        l_run[g] *= alpha;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+        for (int e = 0; e < 4; ++e) acc[g][e] = __fmul2_rn(acc[g][e], a2);
       }
+      // ---- probabilities and P V
 #pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const int tok = base + u * TPS + tslot;
-        if (tok < valid) {
-          const uint4 r = *reinterpret_cast<const uint4 *>(vb + (size_t(tok) * D + d0) * 2);
-          const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-          float vf[8];
+      for (int u = 0; u < 8; ++u) {
+        if (u < steps) {
+          const int tok = u * TPS + tslot;
+          const float pm = ex2(sc[u] - m_run);  // 0 for masked tokens
+          l_run += pm;
+          float pg[G];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            vf[2 * e] = bf16_lo(w[e]);
-            vf[2 * e + 1] = bf16_hi(w[e]);
-          }
+          for (int g = 0; g < G; ++g) pg[g] = __shfl_sync(0xffffffffu, pm, tslot * LPT + g * HL);
+          if (tok < valid) {
+            const uint4 r = *reinterpret_cast<const uint4 *>(vb + (size_t(tok) * D + d0) * 2);
+            const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+            float2 v2[4];
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float pr = ex2(sc[u][g] - m_run[g]);
-            l_run[g] += pr;
+            for (int e = 0; e < 4; ++e) v2[e] = make_float2(bf16_lo(w[e]), bf16_hi(w[e]));
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pr, vf[e], acc[g][e]);
+            for (int g = 0; g < G; ++g) {
+              const float2 p2 = make_float2(pg[g], pg[g]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[g][e] = __ffma2_rn(p2, v2[e], acc[g][e]);
+            }
           }
         }
       }
     }
     __syncwarp();
-    if (lane == 0 && i + kStages < my_pages) issue(i + kStages);
+    if (lane == 0 && i + kStages < my_tiles) issue(i + kStages);
   }
 
-  // Combine the token slots of the warp.
+  // Combine the token slots of the warp (all slots share m_run per head).
 #pragma unroll
   for (int off = LPT; off < 32; off <<= 1) {
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      l_run[g] += __shfl_xor_sync(0xffffffffu, l_run[g], off);
+    for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], off);
-    }
+      for (int e = 0; e < 4; ++e) {
+        acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, off);
+        acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, off);
+      }
   }
 
   // Merge the four warps through shared memory (the rings are no longer used).
@@ -239,15 +270,12 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       float4 *dst = reinterpret_cast<float4 *>(red_acc + (size_t(warp) * G + g) * D + d0);
-      dst[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-      dst[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+      dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+      dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
     }
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      red_m[warp * G + g] = m_run[g];
-      red_l[warp * G + g] = l_run[g];
+    if (sl % HL == 0) {
+      red_m[warp * G + my_head] = m_run;
+      red_l[warp * G + my_head] = l_run;
     }
   }
   __syncthreads();
@@ -273,8 +301,8 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-int ring_tile_tokens(int page_size) {  // gcd(page_size, 16)
-  int a = page_size, b = 16;
+int ring_tile_tokens(int page_size) {  // gcd(page_size, 8)
+  int a = page_size, b = 8;
   while (b) {
     const int t = a % b;
     a = b;
@@ -316,6 +344,7 @@ psd_status launch_cc(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t
   p.q = reinterpret_cast<const __nv_bfloat16 *>(L.q);
   p.page_indices = L.page_indices;
   p.items = L.items;
+  p.order = L.order;
   p.members = L.members;
   p.member_row_base = L.member_row_base;
   p.v_out = L.v_out;

@@ -9,6 +9,10 @@
 
 namespace psd {
 
+// Item visiting order for a launch: indices of items[0, n) by decreasing token
+// count (stable), so the longest tiles start first and short ones fill the tail.
+void longest_first(const psd_work_item *items, int32_t n, int32_t *order);
+
 // Thread-local error message (psd_last_error).
 void clear_error();
 psd_status fail(psd_status st, const char *fmt, ...);
@@ -17,12 +21,13 @@ psd_status validate_table(const psd_page_table *t, int64_t num_pages);
 
 // Workspace layout (all offsets 256-byte aligned):
 //   [0, 256)        header: int32 fault flag at offset 0
-//   lists           work items, members, member_row_base, o_indptr (one H2D copy)
+//   lists           work items, CTA order, members, member_row_base, o_indptr
+//                   (one H2D copy)
 //   v partials      [num_rows, Hq, Dv] f32
 //   lse partials    [num_rows, Hq] f32
 struct WorkspaceLayout {
   size_t lists_off, lists_bytes;
-  size_t items_off, members_off, row_base_off, indptr_off;
+  size_t items_off, order_off, members_off, row_base_off, indptr_off;
   size_t vpart_off, lpart_off;
   size_t total;
 };
@@ -34,7 +39,9 @@ inline WorkspaceLayout workspace_layout(int32_t batch, int32_t num_items, int64_
   WorkspaceLayout L;
   L.lists_off = 0;  // the header travels with the lists in the same copy
   L.items_off = 256;
-  L.members_off = L.items_off + sizeof(psd_work_item) * size_t(num_items > 0 ? num_items : 0);
+  const size_t n = size_t(num_items > 0 ? num_items : 0);
+  L.order_off = L.items_off + sizeof(psd_work_item) * n;
+  L.members_off = L.order_off + sizeof(int32_t) * n;
   L.row_base_off = L.members_off + sizeof(int32_t) * size_t(batch);
   L.indptr_off = L.row_base_off + sizeof(int32_t) * size_t(batch);
   L.lists_bytes = L.indptr_off + sizeof(int32_t) * size_t(batch + 1);
