@@ -255,6 +255,30 @@ psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
                           void *workspace, size_t workspace_bytes,
                           psd_cascade_stats *stats, psd_stream_t stream);
 
+/* cascade_decode for callers that cannot allocate device memory.  No counterpart
+ * on the source pages: it exists for callers that run inside another runtime's
+ * memory pool or a plugin sandbox and may not call cudaMalloc (or any allocator)
+ * when they decode, so they cannot hand cascade_decode a workspace.  This entry
+ * point takes the same inputs and outputs but keeps all scratch (work lists, the
+ * fault word, the partial rows) in one fixed 16 MiB array in the library's own
+ * device memory, present on every GPU that loads the library until the process
+ * exits.  It calls no allocating routine (no cudaMalloc/cudaFree, no pinned host
+ * buffer).
+ *   - Plans whose scratch (psd_workspace_bytes of the plan) exceeds 16 MiB are
+ *     rejected with PSD_ERR_WORKSPACE_TOO_SMALL and a message naming both sizes.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents; each call clears the fault word itself.  Calls whose device work
+ *     overlaps (other streams, unordered host threads) race on the array.
+ *   - fault_bits_dev (device int32, nullable) receives the call's PSD_FAULT_* bits.
+ * Results equal cascade_decode's on the same plan. */
+psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_args *args,
+                                   const psd_cascade_plan *plan, float *o, float *lse,
+                                   int32_t *fault_bits_dev, psd_cascade_stats *stats,
+                                   psd_stream_t stream);
+
 /* Synchronises `stream` and reads the workspace's fault flag: PSD_OK, or
  * PSD_ERR_DEVICE_FAULT with the PSD_FAULT_* bits in *fault_bits (nullable).
  * Clears the flag. */

@@ -20,7 +20,7 @@ EXPORTS = [
     "psd_create", "psd_destroy", "psd_last_error", "psd_get_counters", "psd_cascade_env_enabled",
     "psd_split_plan", "detect_shared_prefix", "build_cascade_plan", "psd_plan_decode",
     "psd_plan_capacity", "psd_workspace_bytes", "paged_decode_partial", "merge_states",
-    "cascade_decode", "psd_check_device_error",
+    "cascade_decode", "psd_check_device_error", "cascade_decode_no_alloc",
 ]
 
 
@@ -93,6 +93,8 @@ def _sig(lib):
     lib.cascade_decode.argtypes = [V, C.POINTER(DecodeArgs), C.POINTER(CascadePlan), V, V, V,
                                    C.c_size_t, C.POINTER(CascadeStats), V]
     lib.psd_check_device_error.argtypes = [V, V, V, P_i32]
+    lib.cascade_decode_no_alloc.argtypes = [V, C.POINTER(DecodeArgs), C.POINTER(CascadePlan), V, V, V,
+                                            C.POINTER(CascadeStats), V]
     for name in EXPORTS:
         f = getattr(lib, name)
         if f.restype is C.c_int or f.restype is None:

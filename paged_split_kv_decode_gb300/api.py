@@ -259,6 +259,21 @@ def cascade_decode(ctx: Context, args: L.DecodeArgs, plan: Plan, o: torch.Tensor
     return {k: getattr(stats, k) for k, _ in L.CascadeStats._fields_}
 
 
+def cascade_decode_no_alloc(ctx: Context, args: L.DecodeArgs, plan: Plan, o: torch.Tensor,
+                            lse: torch.Tensor = None, fault_bits: torch.Tensor = None,
+                            stream=None) -> dict:
+    """cascade_decode_no_alloc: cascade_decode without a workspace, for callers that
+    cannot allocate device memory (scratch lives in the library's fixed 16 MiB
+    device array; see include/psd.h).  fault_bits: optional device int32[1]."""
+    stats = L.CascadeStats()
+    L.check(L.load().cascade_decode_no_alloc(
+        ctx.handle, C.byref(args), C.byref(plan.c), _dev_ptr(o, "o"),
+        None if lse is None else _dev_ptr(lse, "lse"),
+        None if fault_bits is None else _dev_ptr(fault_bits, "fault_bits"),
+        C.byref(stats), _stream(stream)))
+    return {k: getattr(stats, k) for k, _ in L.CascadeStats._fields_}
+
+
 def check_device_error(ctx: Context, workspace: torch.Tensor, stream=None) -> int:
     """psd_check_device_error: raises PsdError on a flagged device fault."""
     bits = C.c_int32()

@@ -20,9 +20,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpsd.so")
 
-CU_SOURCES = ["api.cu", "merge.cu", "partial_cc.cu", "partial_tc.cu"]
+CU_SOURCES = ["api.cu", "merge.cu", "partial_cc.cu", "partial_tc.cu", "no_alloc.cu"]
 CPP_SOURCES = ["plan.cpp"]
-HEADERS = ["psd_internal.h", "kernels.h", "device.cuh"]
+HEADERS = ["psd_internal.h", "kernels.h", "device.cuh", "context.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",

@@ -13,8 +13,7 @@
 #include <string>
 #include <vector>
 
-#include "kernels.h"
-#include "psd_internal.h"
+#include "context.h"
 
 namespace psd {
 
@@ -42,32 +41,9 @@ psd_status fail(psd_status st, const char *fmt, ...) {
 
 using namespace psd;
 
-struct psd_ctx {
-  DeviceInfo dev;
-  psd_counters counters;
-  // Two pinned staging buffers for the per-call H2D upload of work lists; an
-  // event per buffer tells when its previous copy has finished reading it.
-  void *staging[2] = {nullptr, nullptr};
-  size_t staging_cap[2] = {0, 0};
-  cudaEvent_t staging_done[2] = {nullptr, nullptr};
-  bool staging_pending[2] = {false, false};
-  int next = 0;
-};
+namespace psd {
 
-namespace {
-
-const float kLog2e = 1.4426950408889634f;
-
-struct DeviceGuard {  // make ctx->dev.device current for the call, restore after
-  int prev = -1;
-  explicit DeviceGuard(int dev) {
-    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
-    else prev = -1;
-  }
-  ~DeviceGuard() {
-    if (prev >= 0) cudaSetDevice(prev);
-  }
-};
+static const float kLog2e = 1.4426950408889634f;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -142,6 +118,10 @@ psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStr
   return fail(PSD_ERR_UNSUPPORTED, "no kernel for Dqk %d, Dv %d, rows/KV head %d, dtype %d, latent %d",
               L.Dqk, L.Dv, L.G_cta, L.kv_dtype, int(L.latent_v));
 }
+
+}  // namespace psd
+
+namespace {
 
 // Copies `bytes` of host data into a pinned staging buffer and enqueues one H2D
 // copy to `dst` on `s`.

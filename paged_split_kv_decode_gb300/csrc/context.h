@@ -1,0 +1,42 @@
+// The context object and the host-side helpers shared by the entry points.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "psd_internal.h"
+
+struct psd_ctx {
+  psd::DeviceInfo dev;
+  psd_counters counters;
+  // Two pinned staging buffers for the per-call H2D upload of work lists; an
+  // event per buffer tells when its previous copy has finished reading it.
+  void *staging[2] = {nullptr, nullptr};
+  size_t staging_cap[2] = {0, 0};
+  cudaEvent_t staging_done[2] = {nullptr, nullptr};
+  bool staging_pending[2] = {false, false};
+  int next = 0;
+};
+
+namespace psd {
+
+struct DeviceGuard {  // make a device current for one call, restore the caller's after
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
+    else prev = -1;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+bool aligned16(const void *p);
+psd_status validate_args(const psd_decode_args *a);
+psd_status validate_items(const psd_decode_args *a, const psd_work_item *items, int32_t n,
+                          int64_t out_rows, bool stacked, int32_t num_members);
+PartialLaunch base_launch(const psd_decode_args *a);
+bool dispatchable(const PartialLaunch &L);
+psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s);
+
+}  // namespace psd

@@ -1,0 +1,185 @@
+// cascade_decode_no_alloc: cascade_decode for callers that cannot allocate
+// device memory.
+//
+// Some callers cannot call cudaMalloc (or any allocator) at the point where they
+// decode: code running inside another framework's memory pool that forbids
+// foreign allocations, plugins handed only the tensors they read and write, or
+// runtimes that reserve all device memory up front.  They cannot provide the
+// workspace cascade_decode needs, so this entry point keeps its scratch (work
+// lists, the fault word and the partial rows) in one fixed array in the library's
+// own device memory instead.  It calls no allocating routine.
+//
+// The array lives for the life of the process on every GPU that loads the
+// library and is shared by every call on that GPU: calls whose device work
+// overlaps (different streams, or host threads without ordering) race on it and
+// produce garbage.  Each call clears the part that must start at zero (the fault
+// word); the rest keeps the previous call's contents until overwritten.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "context.h"
+
+namespace {
+
+// 16 MiB: the flat and cascade decode batches need about 3 and 6 MiB.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+constexpr int kMaxDevices = 64;
+
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_no_alloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_setup_mutex;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The first call on a
+// device looks it up with cudaGetSymbolAddress (host code only sees a host-side
+// stand-in under the array's name, never a usable device address).
+psd_status scratch_address(int device, uint8_t **out) {
+  if (device < 0 || device >= kMaxDevices)
+    return psd::fail(PSD_ERR_UNSUPPORTED, "cascade_decode_no_alloc: device %d out of range", device);
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_scratch_addr[device]) {
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_no_alloc_scratch);
+    if (e != cudaSuccess || !p)
+      return psd::fail(PSD_ERR_CUDA, "cascade_decode_no_alloc: cudaGetSymbolAddress: %s",
+                       cudaGetErrorString(e));
+    g_scratch_addr[device] = p;
+  }
+  *out = static_cast<uint8_t *>(g_scratch_addr[device]);
+  return PSD_OK;
+}
+
+psd_status copy_in(void *dst, const void *src, size_t bytes, cudaStream_t s) {
+  if (!bytes) return PSD_OK;
+  cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess)
+    return psd::fail(PSD_ERR_CUDA, "cascade_decode_no_alloc: upload: %s", cudaGetErrorString(e));
+  return PSD_OK;
+}
+
+}  // namespace
+
+using namespace psd;
+
+extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_args *args,
+                                              const psd_cascade_plan *plan, float *o, float *lse,
+                                              int32_t *fault_bits_dev, psd_cascade_stats *stats,
+                                              psd_stream_t stream) {
+  clear_error();
+  if (!ctx) return fail(PSD_ERR_INVALID_ARG, "NULL context");
+  psd_status st = validate_args(args);
+  if (st != PSD_OK) return st;
+  if (!plan || !o) return fail(PSD_ERR_INVALID_ARG, "cascade_decode_no_alloc: NULL plan / o");
+  if (!aligned16(o)) return fail(PSD_ERR_INVALID_ARG, "cascade_decode_no_alloc: o must be 16-byte aligned");
+  const int32_t B = args->batch;
+  if (plan->batch != B || plan->page_size != args->page_size)
+    return fail(PSD_ERR_INVALID_ARG, "cascade_decode_no_alloc: plan batch/page_size (%d/%d) != args (%d/%d)",
+                plan->batch, plan->page_size, B, args->page_size);
+  const int32_t M = plan->num_members, n0 = plan->l0_num_items, n1 = plan->l1_num_items;
+  if (M < 0 || M > B || n0 < 0 || n1 < 0 || (M == 0) != (n0 == 0) || plan->num_rows < 0 ||
+      plan->o_indptr[0] != 0 || plan->o_indptr[B] != plan->num_rows)
+    return fail(PSD_ERR_INVALID_ARG, "cascade_decode_no_alloc: inconsistent plan");
+  for (int32_t b = 0; b < B; ++b)
+    if (plan->o_indptr[b + 1] < plan->o_indptr[b])
+      return fail(PSD_ERR_INVALID_ARG, "cascade_decode_no_alloc: o_indptr decreasing at %d", b);
+  for (int32_t m = 0; m < M; ++m) {
+    if (plan->members[m] < 0 || plan->members[m] >= B ||
+        plan->member_row_base[m] != plan->o_indptr[plan->members[m]] ||
+        plan->o_indptr[plan->members[m] + 1] - plan->member_row_base[m] < n0)
+      return fail(PSD_ERR_INVALID_ARG, "cascade_decode_no_alloc: member %d", m);
+  }
+  st = validate_items(args, plan->l0_items, n0, plan->num_rows, true, M);
+  if (st == PSD_OK) st = validate_items(args, plan->l1_items, n1, plan->num_rows, false, M);
+  if (st != PSD_OK) return st;
+  for (int32_t i = 0; i < n0; ++i)
+    if (plan->l0_items[i].out_row >= n0)
+      return fail(PSD_ERR_INVALID_ARG, "cascade_decode_no_alloc: level-0 item %d chunk index", i);
+
+  const WorkspaceLayout lay = workspace_layout(B, n0 + n1, plan->num_rows, args->Hq, args->Dv);
+  if (lay.total > kNoAllocScratchBytes)
+    return fail(PSD_ERR_WORKSPACE_TOO_SMALL,
+                "cascade_decode_no_alloc: this plan needs %zu bytes of scratch but the library's "
+                "static scratch holds %zu bytes; use cascade_decode with a workspace",
+                lay.total, kNoAllocScratchBytes);
+
+  PartialLaunch L1 = base_launch(args);
+  PartialLaunch L0 = L1;
+  L0.G_cta = M * L1.Gm;
+  if (!dispatchable(L1)) return launch_partial(L1, ctx->dev, nullptr);
+  if (M > 0 && !dispatchable(L0)) return launch_partial(L0, ctx->dev, nullptr);
+
+  DeviceGuard g(ctx->dev.device);
+  uint8_t *ws = nullptr;
+  st = scratch_address(ctx->dev.device, &ws);
+  if (st != PSD_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  // Work lists straight from the caller's host plan; the fault word starts at 0.
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, s);
+  if (e != cudaSuccess)
+    return fail(PSD_ERR_CUDA, "cascade_decode_no_alloc: clear: %s", cudaGetErrorString(e));
+  const size_t isz = sizeof(psd_work_item);
+  if ((st = copy_in(ws + lay.items_off, plan->l0_items, isz * n0, s)) != PSD_OK) return st;
+  if ((st = copy_in(ws + lay.items_off + isz * n0, plan->l1_items, isz * n1, s)) != PSD_OK) return st;
+  if ((st = copy_in(ws + lay.members_off, plan->members, sizeof(int32_t) * M, s)) != PSD_OK) return st;
+  if ((st = copy_in(ws + lay.row_base_off, plan->member_row_base, sizeof(int32_t) * M, s)) != PSD_OK)
+    return st;
+  if ((st = copy_in(ws + lay.indptr_off, plan->o_indptr, sizeof(int32_t) * (B + 1), s)) != PSD_OK)
+    return st;
+
+  float *vpart = reinterpret_cast<float *>(ws + lay.vpart_off);
+  float *lpart = reinterpret_cast<float *>(ws + lay.lpart_off);
+  int32_t *fault = reinterpret_cast<int32_t *>(ws);
+  const psd_work_item *ditems = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
+  if (M > 0) {
+    L0.items = ditems;
+    L0.num_items = n0;
+    L0.members = reinterpret_cast<const int32_t *>(ws + lay.members_off);
+    L0.member_row_base = reinterpret_cast<const int32_t *>(ws + lay.row_base_off);
+    L0.v_out = vpart;
+    L0.lse_out = lpart;
+    L0.fault = fault;
+    if ((st = launch_partial(L0, ctx->dev, s)) != PSD_OK) return st;
+  }
+  L1.items = ditems + n0;
+  L1.num_items = n1;
+  L1.v_out = vpart;
+  L1.lse_out = lpart;
+  L1.fault = fault;
+  if ((st = launch_partial(L1, ctx->dev, s)) != PSD_OK) return st;
+  st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq,
+                    args->Dv, o, lse, ctx->dev, s);
+  if (st != PSD_OK) return st;
+  if (fault_bits_dev) {
+    e = cudaMemcpyAsync(fault_bits_dev, fault, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess)
+      return fail(PSD_ERR_CUDA, "cascade_decode_no_alloc: fault word: %s", cudaGetErrorString(e));
+  }
+
+  if (M > 0) {
+    ctx->counters.launches_cascade += 1;
+    ctx->counters.cascade_shared_tokens += int64_t(plan->shared_pages) * args->page_size;
+    ctx->counters.cascade_member_sequences += M;
+  } else {
+    ctx->counters.launches_flat += 1;
+    if (plan->decline_reason != PSD_DECLINE_NONE && plan->decline_reason != PSD_DECLINE_DISABLED)
+      ctx->counters.cascade_failures += 1;
+  }
+  if (stats) {
+    stats->path = M > 0 ? 1 : 0;
+    stats->decline_reason = plan->decline_reason;
+    stats->batch = B;
+    stats->members = M;
+    stats->shared_pages = plan->shared_pages;
+    stats->shared_tokens = plan->shared_pages * args->page_size;
+    stats->prefix_chunks = n0;
+    stats->suffix_chunks = n1;
+  }
+  return PSD_OK;
+}
