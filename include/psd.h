@@ -157,6 +157,14 @@ typedef struct psd_ctx psd_ctx;
  * context per thread, or external locking. */
 psd_status psd_create(psd_ctx **ctx, int device);
 psd_status psd_destroy(psd_ctx *ctx);
+/* Which kernel computes partials when a KV head has few query rows (G <= 16,
+ * bf16 pools).  AUTO and TENSOR_CORE: the small-group tensor-core kernel (rows
+ * padded to 16, QK^T and PV as m16n8k16 MMAs).  CUDA_CORE: the CUDA-core kernel
+ * (G <= 8; warp-shuffle reductions and f32x2 FMAs).  Both compute the same
+ * partials; many-row launches (stacked level 0, MLA) and fp8 always use the
+ * 64-row tensor-core kernel. */
+typedef enum { PSD_KERNEL_AUTO = 0, PSD_KERNEL_CUDA_CORE = 1, PSD_KERNEL_TENSOR_CORE = 2 } psd_partial_kernel;
+psd_status psd_set_partial_kernel(psd_ctx *ctx, int32_t kind);
 /* Thread-local message describing the last failure on this thread. */
 const char *psd_last_error(void);
 psd_status psd_get_counters(const psd_ctx *ctx, psd_counters *out);

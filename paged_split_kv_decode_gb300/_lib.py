@@ -14,10 +14,12 @@ PSD_OK = 0
 STATUS_NAMES = {0: "PSD_OK", 1: "PSD_ERR_INVALID_ARG", 2: "PSD_ERR_UNSUPPORTED", 3: "PSD_ERR_CUDA",
                 4: "PSD_ERR_DEVICE_FAULT", 5: "PSD_ERR_WORKSPACE_TOO_SMALL"}
 PSD_BF16, PSD_FP8_E4M3 = 0, 1
+PSD_KERNEL_AUTO, PSD_KERNEL_CUDA_CORE, PSD_KERNEL_TENSOR_CORE = 0, 1, 2
 
 # Every symbol include/psd.h declares.
 EXPORTS = [
     "psd_create", "psd_destroy", "psd_last_error", "psd_get_counters", "psd_cascade_env_enabled",
+    "psd_set_partial_kernel",
     "psd_split_plan", "detect_shared_prefix", "build_cascade_plan", "psd_plan_decode",
     "psd_plan_capacity", "psd_workspace_bytes", "paged_decode_partial", "merge_states",
     "cascade_decode", "psd_check_device_error", "cascade_decode_no_alloc",
@@ -77,6 +79,7 @@ def _sig(lib):
     lib.psd_last_error.restype = C.c_char_p
     lib.psd_last_error.argtypes = []
     lib.psd_get_counters.argtypes = [V, C.POINTER(Counters)]
+    lib.psd_set_partial_kernel.argtypes = [V, i32]
     lib.psd_cascade_env_enabled.argtypes = [i32]
     lib.psd_cascade_env_enabled.restype = i32
     lib.psd_split_plan.argtypes = [C.POINTER(PageTable), i32, C.POINTER(WorkItem), i32, P_i32, P_i32]

@@ -60,6 +60,12 @@ class Context:
     def handle(self):
         return self._h
 
+    def set_partial_kernel(self, kind: str):
+        """psd_set_partial_kernel: 'auto', 'cuda_core' or 'tensor_core'."""
+        code = {"auto": L.PSD_KERNEL_AUTO, "cuda_core": L.PSD_KERNEL_CUDA_CORE,
+                "tensor_core": L.PSD_KERNEL_TENSOR_CORE}[kind]
+        L.check(L.load().psd_set_partial_kernel(self._h, code))
+
     def counters(self) -> dict:
         c = L.Counters()
         L.check(L.load().psd_get_counters(self._h, C.byref(c)))

@@ -110,9 +110,17 @@ PartialLaunch base_launch(const psd_decode_args *a) {
   return L;
 }
 
-bool dispatchable(const PartialLaunch &L) { return partial_cc_supports(L) || partial_tc_supports(L); }
+bool dispatchable(const PartialLaunch &L) {
+  return partial_tcs_supports(L) || partial_cc_supports(L) || partial_tc_supports(L);
+}
 
+// Few query rows per KV head (G <= 16, bf16): the small-group tensor-core kernel,
+// or the CUDA-core kernel when the context asks for it; many rows (stacked level
+// 0, MLA) or fp8: the 64-row tensor-core kernel.
 psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
+  if (dev.partial_kernel == PSD_KERNEL_CUDA_CORE && partial_cc_supports(L))
+    return launch_partial_cc(L, dev, s);
+  if (partial_tcs_supports(L)) return launch_partial_tcs(L, dev, s);
   if (partial_cc_supports(L)) return launch_partial_cc(L, dev, s);
   if (partial_tc_supports(L)) return launch_partial_tc(L, dev, s);
   return fail(PSD_ERR_UNSUPPORTED, "no kernel for Dqk %d, Dv %d, rows/KV head %d, dtype %d, latent %d",
@@ -206,6 +214,15 @@ extern "C" psd_status psd_destroy(psd_ctx *c) {
     if (c->staging[i]) cudaFreeHost(c->staging[i]);
   }
   delete c;
+  return PSD_OK;
+}
+
+extern "C" psd_status psd_set_partial_kernel(psd_ctx *c, int32_t kind) {
+  clear_error();
+  if (!c) return fail(PSD_ERR_INVALID_ARG, "NULL context");
+  if (kind != PSD_KERNEL_AUTO && kind != PSD_KERNEL_CUDA_CORE && kind != PSD_KERNEL_TENSOR_CORE)
+    return fail(PSD_ERR_INVALID_ARG, "partial kernel kind %d", kind);
+  c->dev.partial_kernel = kind;
   return PSD_OK;
 }
 

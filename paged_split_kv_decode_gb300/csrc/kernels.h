@@ -12,6 +12,7 @@ struct DeviceInfo {
   int num_sms = 0;
   int smem_optin = 0;
   void *encode_tiled = nullptr;  // driver cuTensorMapEncodeTiled
+  int partial_kernel = 0;        // psd_partial_kernel preference for G <= 16
 };
 
 // One partial-attention launch over a device work list.
@@ -46,6 +47,8 @@ struct PartialLaunch {
 
 bool partial_cc_supports(const PartialLaunch &p);
 psd_status launch_partial_cc(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
+bool partial_tcs_supports(const PartialLaunch &p);
+psd_status launch_partial_tcs(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
 bool partial_tc_supports(const PartialLaunch &p);
 psd_status launch_partial_tc(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
 

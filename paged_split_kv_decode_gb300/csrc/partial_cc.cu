@@ -22,6 +22,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "device.cuh"
 #include "kernels.h"
@@ -45,6 +46,7 @@ struct CCParams {
   int64_t num_pages;
   const int32_t *order;  // CTA -> item (longest items first), or NULL
   int Hq_req, Dqk, Dv, page_size, sub, Gm, G_cta;  // sub = tokens per ring tile
+  int tpp_log2;  // log2(page_size / sub), or -1 if not a power of two
   float q_scale, v_scale;
 };
 
@@ -125,7 +127,26 @@ __global__ void __launch_bounds__(kWarps * 32, G <= 4 ? 4 : 2)
 
   const int n_tiles = (it.n_tokens + SUB - 1) / SUB;
   const int my_tiles = n_tiles > warp ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
+  const int n_item_pages = (it.n_tokens + P - 1) / P;
   const uint64_t pol = l2_evict_first_policy();
+
+  // Tile t of the item sits in page position t / TPP at slot (t % TPP) * SUB.
+  auto tile_pos = [&](int t) { return p.tpp_log2 >= 0 ? t >> p.tpp_log2 : t / TPP; };
+  // Page ids of the item, 32 positions per window, one per lane; a window is
+  // reloaded (warp-uniformly) only when a position leaves it.
+  auto load_window = [&](int base) {
+    const int pos = base + lane;
+    return pos < n_item_pages ? __ldg(p.page_indices + it.page_off + pos) : -1;
+  };
+  int win_i = 0, pid_i = load_window(0);  // window used to issue loads
+  int win_c = 0, pid_c = pid_i;           // window used to consume tiles
+  auto page_id = [&](int pos, int &win, int &pid) {  // all lanes, warp-uniform pos
+    if (pos - win >= 32) {
+      win = pos & ~31;
+      pid = load_window(win);
+    }
+    return __shfl_sync(0xffffffffu, pid, pos - win);
+  };
 
   if (lane == 0) {
 #pragma unroll
@@ -134,23 +155,26 @@ __global__ void __launch_bounds__(kWarps * 32, G <= 4 ? 4 : 2)
   }
   __syncwarp();
 
-  auto issue = [&](int i) {  // lane 0 only
+  auto issue = [&](int i) {  // all lanes call; lane 0 issues
     const int s = i % kStages;
     const int t = warp + i * kWarps;
-    const int id = __ldg(p.page_indices + it.page_off + t / TPP);
-    const int slot0 = (t % TPP) * SUB;
-    const uint32_t bar = smem_u32(&bars[s]);
-    if (id < 0 || int64_t(id) >= p.num_pages) {
-      atomicOr(p.fault, PSD_FAULT_PAGE_ID);
-      mbar_arrive(bar);
-      return;
+    const int pos = tile_pos(t);
+    const int id = page_id(pos, win_i, pid_i);
+    if (lane == 0) {
+      const int slot0 = (t - pos * TPP) * SUB;
+      const uint32_t bar = smem_u32(&bars[s]);
+      if (id < 0 || int64_t(id) >= p.num_pages) {
+        atomicOr(p.fault, PSD_FAULT_PAGE_ID);
+        mbar_arrive(bar);
+      } else {
+        mbar_arrive_expect_tx(bar, 2 * tile_bytes);
+        uint8_t *kb = ring + size_t(s) * 2 * tile_bytes;
+        tma_load_4d(smem_u32(kb), &tmK, 0, kv, slot0, id, bar, pol);
+        tma_load_4d(smem_u32(kb + tile_bytes), &tmV, 0, kv, slot0, id, bar, pol);
+      }
     }
-    mbar_arrive_expect_tx(bar, 2 * tile_bytes);
-    uint8_t *kb = ring + size_t(s) * 2 * tile_bytes;
-    tma_load_4d(smem_u32(kb), &tmK, 0, kv, slot0, id, bar, pol);
-    tma_load_4d(smem_u32(kb + tile_bytes), &tmV, 0, kv, slot0, id, bar, pol);
   };
-  if (lane == 0) {
+  {
     const int pre = my_tiles < kStages ? my_tiles : kStages;
     for (int i = 0; i < pre; ++i) issue(i);
   }
@@ -162,54 +186,46 @@ __global__ void __launch_bounds__(kWarps * 32, G <= 4 ? 4 : 2)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[g][e] = make_float2(0.f, 0.f);
 
-  for (int i = 0; i < my_tiles; ++i) {
-    const int s = i % kStages;
-    const int t = warp + i * kWarps;
-    const int id = __ldg(p.page_indices + it.page_off + t / TPP);
-    const bool page_ok = id >= 0 && int64_t(id) < p.num_pages;
-    const int valid = page_ok ? min(SUB, it.n_tokens - t * SUB) : 0;
-    const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / kStages) & 1u, p.fault);
-    if (!__all_sync(0xffffffffu, ok)) break;
-    const uint8_t *kb = ring + size_t(s) * 2 * tile_bytes;
-    const uint8_t *vb = kb + tile_bytes;
-
-    if (valid > 0) {
-      // ---- scores of my_head for this lane's tokens
-      float sc[8];
-      float mt = neg_inf();
+  // One ring tile: scores, online-softmax update, P V.  MASKED handles a tile with
+  // fewer than SUB valid tokens (the item's last tile, or a skipped page).
+  auto tile = [&](auto masked_tag, const uint8_t *kb, const uint8_t *vb, int valid) {
+    constexpr bool MASKED = decltype(masked_tag)::value;
+    float sc[8];
+    float mt = neg_inf();
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (u < steps) {
-          const int tok = u * TPS + tslot;
-          float part[G];
-          if (tok < valid) {
-            const uint4 r = *reinterpret_cast<const uint4 *>(kb + (size_t(tok) * D + d0) * 2);
-            const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-            float2 k2[4];
+    for (int u = 0; u < 8; ++u) {
+      if (u < steps) {
+        const int tok = u * TPS + tslot;
+        const bool ok = !MASKED || tok < valid;
+        float part[G];
+        if (ok) {
+          const uint4 r = *reinterpret_cast<const uint4 *>(kb + (size_t(tok) * D + d0) * 2);
+          const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+          float2 k2[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) k2[e] = make_float2(bf16_lo(w[e]), bf16_hi(w[e]));
+          for (int e = 0; e < 4; ++e) k2[e] = make_float2(bf16_lo(w[e]), bf16_hi(w[e]));
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-              float2 a = __fmul2_rn(q2[g][0], k2[0]);
+          for (int g = 0; g < G; ++g) {
+            float2 a = __fmul2_rn(q2[g][0], k2[0]);
 #pragma unroll
-              for (int e = 1; e < 4; ++e) a = __ffma2_rn(q2[g][e], k2[e], a);
-              part[g] = a.x + a.y;
-            }
-          } else {
-#pragma unroll
-            for (int g = 0; g < G; ++g) part[g] = 0.f;
+            for (int e = 1; e < 4; ++e) a = __ffma2_rn(q2[g][e], k2[e], a);
+            part[g] = a.x + a.y;
           }
-          const float sv = transpose_reduce<G, LPT>(part, lane);
-          sc[u] = tok < valid ? sv : neg_inf();
-          mt = fmaxf(mt, sc[u]);
-        }
-      }
+        } else {
 #pragma unroll
-      for (int off = LPT; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-      // ---- online softmax: new running max, rescale of every head's accumulator
-      const float m_new = fmaxf(m_run, mt);
+          for (int g = 0; g < G; ++g) part[g] = 0.f;
+        }
+        const float sv = transpose_reduce<G, LPT>(part, lane);
+        sc[u] = ok ? sv : neg_inf();
+        mt = fmaxf(mt, sc[u]);
+      }
+    }
+#pragma unroll
+    for (int off = LPT; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+    // online softmax: rescale only when some head's running max moved
+    const float m_new = fmaxf(m_run, mt);
+    if (!__all_sync(0xffffffffu, m_new == m_run)) {
       const float alpha = ex2(m_run - m_new);  // 0 while m_run is -inf
-      m_run = m_new;
       l_run *= alpha;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -218,34 +234,51 @@ __global__ void __launch_bounds__(kWarps * 32, G <= 4 ? 4 : 2)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[g][e] = __fmul2_rn(acc[g][e], a2);
       }
-      // ---- probabilities and P V
+      m_run = m_new;
+    }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (u < steps) {
-          const int tok = u * TPS + tslot;
-          const float pm = ex2(sc[u] - m_run);  // 0 for masked tokens
-          l_run += pm;
-          float pg[G];
+    for (int u = 0; u < 8; ++u) {
+      if (u < steps) {
+        const int tok = u * TPS + tslot;
+        const float pm = ex2(sc[u] - m_run);  // 0 for masked tokens
+        l_run += pm;
+        float pg[G];
 #pragma unroll
-          for (int g = 0; g < G; ++g) pg[g] = __shfl_sync(0xffffffffu, pm, tslot * LPT + g * HL);
-          if (tok < valid) {
-            const uint4 r = *reinterpret_cast<const uint4 *>(vb + (size_t(tok) * D + d0) * 2);
-            const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-            float2 v2[4];
+        for (int g = 0; g < G; ++g) pg[g] = __shfl_sync(0xffffffffu, pm, tslot * LPT + g * HL);
+        if (!MASKED || tok < valid) {
+          const uint4 r = *reinterpret_cast<const uint4 *>(vb + (size_t(tok) * D + d0) * 2);
+          const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+          float2 v2[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v2[e] = make_float2(bf16_lo(w[e]), bf16_hi(w[e]));
+          for (int e = 0; e < 4; ++e) v2[e] = make_float2(bf16_lo(w[e]), bf16_hi(w[e]));
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const float2 p2 = make_float2(pg[g], pg[g]);
+          for (int g = 0; g < G; ++g) {
+            const float2 p2 = make_float2(pg[g], pg[g]);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) acc[g][e] = __ffma2_rn(p2, v2[e], acc[g][e]);
-            }
+            for (int e = 0; e < 4; ++e) acc[g][e] = __ffma2_rn(p2, v2[e], acc[g][e]);
           }
         }
       }
     }
+  };
+
+  const bool exact_steps = steps * TPS == SUB;
+  for (int i = 0; i < my_tiles; ++i) {
+    const int s = i % kStages;
+    const int t = warp + i * kWarps;
+    const int id = page_id(tile_pos(t), win_c, pid_c);
+    const bool page_ok = id >= 0 && int64_t(id) < p.num_pages;
+    const int valid = page_ok ? min(SUB, it.n_tokens - t * SUB) : 0;
+    const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / kStages) & 1u, p.fault);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const uint8_t *kb = ring + size_t(s) * 2 * tile_bytes;
+    const uint8_t *vb = kb + tile_bytes;
+    if (valid == SUB && exact_steps)
+      tile(std::integral_constant<bool, false>(), kb, vb, valid);
+    else if (valid > 0)
+      tile(std::integral_constant<bool, true>(), kb, vb, valid);
     __syncwarp();
-    if (lane == 0 && i + kStages < my_tiles) issue(i + kStages);
+    if (i + kStages < my_tiles) issue(i + kStages);
   }
 
   // Combine the token slots of the warp (all slots share m_run per head).
@@ -356,6 +389,10 @@ psd_status launch_cc(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t
   p.Dv = L.Dv;
   p.page_size = L.page_size;
   p.sub = sub;
+  {
+    const int tpp = L.page_size / sub;
+    p.tpp_log2 = (tpp & (tpp - 1)) == 0 ? __builtin_ctz(unsigned(tpp)) : -1;
+  }
   p.Gm = L.Gm;
   p.G_cta = L.G_cta;
   p.q_scale = L.q_scale;

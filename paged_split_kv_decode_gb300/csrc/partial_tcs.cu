@@ -1,0 +1,419 @@
+// K1t: split-KV partial attention for small query groups (G = Hq/Hkv <= 16 rows
+// per KV head) with QK^T and PV on the tensor cores.
+//
+// Same work unit as the CUDA-core kernel (mlxcel PR #1004, Decomposition section:
+// one CTA owns all query heads of one KV head for one (request, page tile), so
+// each K/V element is read from HBM once) and the same outputs (Merge contract
+// section: rows normalised by their own denominator, LSE = m + log2 l in log2
+// units).  The difference is where the arithmetic runs: at G = 4 the CUDA-core
+// kernel spends ~90 issue slots per (token, KV head) on unpacking, FMAs and
+// shuffles and cannot keep up with HBM, while one m16n8k16 MMA covers 16 tokens x
+// 16 dims for all G rows (padded to 16) in one issue slot.
+//
+// GB300 shape: grid = (work items, Hkv), 4 warps, 3 CTAs per SM.  Warp w streams
+// 16-token tiles w, w+4, ... of the item through a private 2-stage ring; each
+// stage is 16 slots of one page loaded by TMA in 64-column boxes with the 128-byte
+// swizzle, so ldmatrix reads are bank-conflict free.  Per tile and warp: S = Q K^T
+// (D/16 x 2 MMAs, Q fragments held in registers), online softmax on the
+// accumulator fragments, P re-packed as the A operand, O += P V (D/8 MMAs, V via
+// transposed ldmatrix).  The four warp states merge through shared memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "device.cuh"
+#include "kernels.h"
+
+namespace psd {
+
+namespace {
+
+constexpr int kWarpsS = 4;
+constexpr int kStagesS = 2;
+constexpr int kTileTok = 16;
+
+struct TCSParams {
+  const __nv_bfloat16 *q;
+  const int32_t *page_indices;
+  const psd_work_item *items;
+  const int32_t *order;
+  const int32_t *members;
+  const int32_t *member_row_base;
+  float *v_out;
+  float *lse_out;
+  int32_t *fault;
+  int64_t num_pages;
+  int Hq_req, Dqk, Dv, page_size, Gm, G_cta;
+  int tpp_log2;  // log2(page_size / 16), or -1
+  float q_scale, v_scale;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Byte offset of (row, 8-column chunk `col8`) in a tile stored as 64-column boxes
+// of 16 rows x 128 bytes with the 128-byte swizzle (16-byte chunk index XOR row%8).
+__device__ __forceinline__ uint32_t sw128(int row, int col8) {
+  return uint32_t((col8 >> 3) * (kTileTok * 128) + row * 128 + (((col8 & 7) ^ (row & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
+    partial_tcs_kernel(const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const TCSParams p) {
+  constexpr int KSTEPS = D / 16;
+  constexpr int NT = D / 8;                       // n8 tiles of the output
+  constexpr uint32_t TILE_BYTES = kTileTok * D * 2;
+  extern __shared__ __align__(1024) uint8_t smem[];
+
+  // 128-byte-swizzled TMA boxes need 1024-byte aligned destinations.
+  uint8_t *base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const psd_work_item it = p.items[p.order ? __ldg(p.order + blockIdx.x) : blockIdx.x];
+  const int kv = blockIdx.y;
+  const int P = p.page_size;
+  const int TPP = P / kTileTok;
+  const size_t ring_total = size_t(kWarpsS) * kStagesS * 2 * TILE_BYTES;
+  const size_t red_total = size_t(kWarpsS) * 16 * (D + 2) * sizeof(float);
+  uint8_t *ring = base + size_t(warp) * kStagesS * 2 * TILE_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(base + (ring_total > red_total ? ring_total : red_total)) +
+                   warp * kStagesS;
+
+  // ---- Q fragments (rows >= G_cta are zero), pre-scaling is applied to S
+  uint32_t qa[KSTEPS][4];
+  {
+    const int r0 = lane >> 2, c0 = (lane & 3) * 2;
+    const __nv_bfloat16 *qrow[2] = {nullptr, nullptr};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int g = r0 + 8 * h;
+      if (g < p.G_cta) {
+        const int m = g / p.Gm;
+        const int qb = it.q_index >= 0 ? it.q_index : __ldg(p.members + m);
+        const int head = kv * p.Gm + (g - m * p.Gm);
+        qrow[h] = p.q + (int64_t(qb) * p.Hq_req + head) * p.Dqk;
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      const int c = kk * 16 + c0;
+      qa[kk][0] = qrow[0] ? __ldg(reinterpret_cast<const uint32_t *>(qrow[0] + c)) : 0u;
+      qa[kk][1] = qrow[1] ? __ldg(reinterpret_cast<const uint32_t *>(qrow[1] + c)) : 0u;
+      qa[kk][2] = qrow[0] ? __ldg(reinterpret_cast<const uint32_t *>(qrow[0] + c + 8)) : 0u;
+      qa[kk][3] = qrow[1] ? __ldg(reinterpret_cast<const uint32_t *>(qrow[1] + c + 8)) : 0u;
+    }
+  }
+
+  const int n_tiles = (it.n_tokens + kTileTok - 1) / kTileTok;
+  const int my_tiles = n_tiles > warp ? (n_tiles - warp + kWarpsS - 1) / kWarpsS : 0;
+  const int n_item_pages = (it.n_tokens + P - 1) / P;
+  const uint64_t pol = l2_evict_first_policy();
+  auto tile_pos = [&](int t) { return p.tpp_log2 >= 0 ? t >> p.tpp_log2 : t / TPP; };
+  auto load_window = [&](int first) {
+    const int pos = first + lane;
+    return pos < n_item_pages ? __ldg(p.page_indices + it.page_off + pos) : -1;
+  };
+  int win_i = 0, pid_i = load_window(0);
+  int win_c = 0, pid_c = pid_i;
+  auto page_id = [&](int pos, int &win, int &pid) {
+    if (pos - win >= 32) {
+      win = pos & ~31;
+      pid = load_window(win);
+    }
+    return __shfl_sync(0xffffffffu, pid, pos - win);
+  };
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < kStagesS; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  auto issue = [&](int i) {  // all lanes call; lane 0 issues
+    const int s = i % kStagesS;
+    const int t = warp + i * kWarpsS;
+    const int pos = tile_pos(t);
+    const int id = page_id(pos, win_i, pid_i);
+    if (lane == 0) {
+      const int slot0 = (t - pos * TPP) * kTileTok;
+      const uint32_t bar = smem_u32(&bars[s]);
+      if (id < 0 || int64_t(id) >= p.num_pages) {
+        atomicOr(p.fault, PSD_FAULT_PAGE_ID);
+        mbar_arrive(bar);
+      } else {
+        mbar_arrive_expect_tx(bar, 2 * TILE_BYTES);
+        uint8_t *kb = ring + size_t(s) * 2 * TILE_BYTES;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(smem_u32(kb + c * kTileTok * 128), &tmK, c * 64, kv, slot0, id, bar, pol);
+          tma_load_4d(smem_u32(kb + TILE_BYTES + c * kTileTok * 128), &tmV, c * 64, kv, slot0, id,
+                      bar, pol);
+        }
+      }
+    }
+  };
+  {
+    const int pre = my_tiles < kStagesS ? my_tiles : kStagesS;
+    for (int i = 0; i < pre; ++i) issue(i);
+  }
+
+  float o[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m_run[2] = {neg_inf(), neg_inf()};
+  float l_run[2] = {0.f, 0.f};
+
+  // ldmatrix lane roles: QK^T B operand (K rows = tokens), PV B operand (V^T)
+  const int kb_tok = (lane & 7) + ((lane >> 4) << 3);
+  const int kb_c8 = (lane >> 3) & 1;
+  const int vb_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+  const int vb_c8 = lane >> 4;
+
+  for (int i = 0; i < my_tiles; ++i) {
+    const int s = i % kStagesS;
+    const int t = warp + i * kWarpsS;
+    const int id = page_id(tile_pos(t), win_c, pid_c);
+    const bool page_ok = id >= 0 && int64_t(id) < p.num_pages;
+    const int valid = page_ok ? min(kTileTok, it.n_tokens - t * kTileTok) : 0;
+    const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / kStagesS) & 1u, p.fault);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    if (valid > 0) {
+      uint8_t *stage = ring + size_t(s) * 2 * TILE_BYTES;
+      if (valid < kTileTok) {
+        // Tail tile: V rows past the last token hold other slots (or NaN canaries);
+        // P is 0 there, so make them 0 too before the MMA multiplies them.
+        constexpr int CH = (D / 64) * 8;  // 16-byte chunks per row
+        for (int idx = lane; idx < (kTileTok - valid) * CH; idx += 32) {
+          const int r = valid + idx / CH, c = idx % CH;
+          *reinterpret_cast<uint4 *>(stage + TILE_BYTES + (c >> 3) * (kTileTok * 128) + r * 128 +
+                                     (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async();  // these generic writes precede the next TMA into the slot
+        __syncwarp();
+      }
+      const uint32_t kbase = smem_u32(stage);
+      const uint32_t vbase = kbase + TILE_BYTES;
+      // S = Q K^T over this warp's 16 tokens
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + sw128(kb_tok, kk * 2 + kb_c8), b0, b1, b2, b3);
+        mma16816(sc[0], qa[kk], b0, b1);
+        mma16816(sc[1], qa[kk], b2, b3);
+      }
+      // scale, mask, online softmax (rows lane/4 and lane/4 + 8)
+      const int tok0 = (lane & 3) * 2;
+      float tmax[2] = {neg_inf(), neg_inf()};
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const bool live = n * 8 + tok0 + (j & 1) < valid;
+          sc[n][j] = live ? sc[n][j] * p.q_scale : neg_inf();
+          tmax[j >> 1] = fmaxf(tmax[j >> 1], sc[n][j]);
+        }
+      float m_new[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 1));
+        tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 2));
+        m_new[h] = fmaxf(m_run[h], tmax[h]);
+      }
+      if (!__all_sync(0xffffffffu, m_new[0] == m_run[0] && m_new[1] == m_run[1])) {
+        const float a0 = ex2(m_run[0] - m_new[0]), a1 = ex2(m_run[1] - m_new[1]);
+        l_run[0] *= a0;
+        l_run[1] *= a1;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          o[n][0] *= a0;
+          o[n][1] *= a0;
+          o[n][2] *= a1;
+          o[n][3] *= a1;
+        }
+        m_run[0] = m_new[0];
+        m_run[1] = m_new[1];
+      }
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          sc[n][j] = ex2(sc[n][j] - m_run[j >> 1]);
+          l_run[j >> 1] += sc[n][j];
+        }
+      // P as two bf16 terms, P = hi + lo with |lo| <= 2^-9 |P|: both go through the
+      // MMA so P V keeps ~16 mantissa bits (one bf16 P would cost up to 2^-10 |v|
+      // on short chunks).
+      uint32_t pa[4], pl[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float x0 = sc[k >> 1][(k & 1) * 2], x1 = sc[k >> 1][(k & 1) * 2 + 1];
+        pa[k] = pack_bf16x2(x0, x1);
+        pl[k] = pack_bf16x2(x0 - bf16_lo(pa[k]), x1 - bf16_hi(pa[k]));
+      }
+      // O += P V
+#pragma unroll
+      for (int n = 0; n < NT; n += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vbase + sw128(vb_tok, n + vb_c8), b0, b1, b2, b3);
+        mma16816(o[n], pa, b0, b1);
+        mma16816(o[n + 1], pa, b2, b3);
+        mma16816(o[n], pl, b0, b1);
+        mma16816(o[n + 1], pl, b2, b3);
+      }
+    }
+    __syncwarp();
+    if (i + kStagesS < my_tiles) issue(i + kStagesS);
+  }
+
+  // ---- merge the four warps through shared memory (rings no longer used)
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+  }
+  __syncthreads();
+  float *red_o = reinterpret_cast<float *>(base);               // [kWarpsS][16][D]
+  float *red_m = red_o + size_t(kWarpsS) * 16 * D;               // [kWarpsS][16]
+  float *red_l = red_m + kWarpsS * 16;                           // [kWarpsS][16]
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = (lane >> 2) + 8 * h;
+    float *dst = red_o + (size_t(warp) * 16 + r) * D + (lane & 3) * 2;
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+      *reinterpret_cast<float2 *>(dst + n * 8) = make_float2(o[n][2 * h], o[n][2 * h + 1]);
+    if ((lane & 3) == 0) {
+      red_m[warp * 16 + r] = m_run[h];
+      red_l[warp * 16 + r] = l_run[h];
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < p.G_cta * D; idx += kWarpsS * 32) {
+    const int g = idx / D, d = idx - g * D;
+    float M = neg_inf();
+#pragma unroll
+    for (int w = 0; w < kWarpsS; ++w) M = fmaxf(M, red_m[w * 16 + g]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarpsS; ++w) {
+      const float sc = ex2(red_m[w * 16 + g] - M);
+      L = fmaf(sc, red_l[w * 16 + g], L);
+      O = fmaf(sc, red_o[(size_t(w) * 16 + g) * D + d], O);
+    }
+    const bool live = M != neg_inf();
+    const int m = g / p.Gm;
+    const int row = it.q_index >= 0 ? it.out_row : __ldg(p.member_row_base + m) + it.out_row;
+    const int head = kv * p.Gm + (g - m * p.Gm);
+    const int64_t orow = int64_t(row) * p.Hq_req + head;
+    p.v_out[orow * p.Dv + d] = live ? O / L * p.v_scale : 0.f;
+    if (d == 0) p.lse_out[orow] = live ? M + log2f(L) : neg_inf();
+  }
+}
+
+bool encode_sw128_map(CUtensorMap *map, const DeviceInfo &dev, const void *pool, int64_t num_pages,
+                      int page_size, int Hkv, int D) {
+  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(dev.encode_tiled);
+  if (!encode) return false;
+  cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(page_size), cuuint64_t(num_pages)};
+  cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(Hkv) * D * 2,
+                           cuuint64_t(page_size) * Hkv * D * 2};
+  cuuint32_t box[4] = {64, 1, cuuint32_t(kTileTok), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+size_t tcs_smem_bytes() {
+  const size_t ring = size_t(kWarpsS) * kStagesS * 2 * kTileTok * D * 2;
+  const size_t red = size_t(kWarpsS) * 16 * (D + 2) * sizeof(float);
+  return std::max(ring, red) + 1024 /* base alignment */ + kWarpsS * kStagesS * sizeof(uint64_t);
+}
+
+template <int D>
+psd_status launch_tcs(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
+  CUtensorMap tmK, tmV;
+  if (!encode_sw128_map(&tmK, dev, L.k_pool, L.num_pages, L.page_size, L.Hkv, D) ||
+      !encode_sw128_map(&tmV, dev, L.v_pool, L.num_pages, L.page_size, L.Hkv, D))
+    return fail(PSD_ERR_CUDA, "cuTensorMapEncodeTiled (128B swizzle) failed for the KV pool");
+  TCSParams p;
+  p.q = reinterpret_cast<const __nv_bfloat16 *>(L.q);
+  p.page_indices = L.page_indices;
+  p.items = L.items;
+  p.order = L.order;
+  p.members = L.members;
+  p.member_row_base = L.member_row_base;
+  p.v_out = L.v_out;
+  p.lse_out = L.lse_out;
+  p.fault = L.fault;
+  p.num_pages = L.num_pages;
+  p.Hq_req = L.Hq_req;
+  p.Dqk = L.Dqk;
+  p.Dv = L.Dv;
+  p.page_size = L.page_size;
+  p.Gm = L.Gm;
+  p.G_cta = L.G_cta;
+  const int tpp = L.page_size / kTileTok;
+  p.tpp_log2 = (tpp & (tpp - 1)) == 0 ? __builtin_ctz(unsigned(tpp)) : -1;
+  p.q_scale = L.q_scale;
+  p.v_scale = L.v_scale;
+  const size_t smem = tcs_smem_bytes<D>();
+  auto kern = partial_tcs_kernel<D>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  }
+  const dim3 grid(static_cast<unsigned>(L.num_items), static_cast<unsigned>(L.Hkv));
+  kern<<<grid, kWarpsS * 32, smem, s>>>(tmK, tmV, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "partial (small-group tensor cores) launch: %s", cudaGetErrorString(e));
+  return PSD_OK;
+}
+
+}  // namespace
+
+bool partial_tcs_supports(const PartialLaunch &p) {
+  return p.kv_dtype == PSD_BF16 && !p.latent_v && p.Dqk == p.Dv &&
+         (p.Dqk == 64 || p.Dqk == 128 || p.Dqk == 256) && p.G_cta >= 1 && p.G_cta <= 16 &&
+         p.page_size % kTileTok == 0;
+}
+
+psd_status launch_partial_tcs(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
+  if (L.num_items == 0) return PSD_OK;
+  switch (L.Dqk) {
+    case 64: return launch_tcs<64>(L, dev, s);
+    case 128: return launch_tcs<128>(L, dev, s);
+    case 256: return launch_tcs<256>(L, dev, s);
+    default: return fail(PSD_ERR_UNSUPPORTED, "small-group tensor-core partial: head dim %d", L.Dqk);
+  }
+}
+
+}  // namespace psd

@@ -22,6 +22,21 @@ def ctx():
     return _CTX
 
 
+class use_kernel:
+    """Selects the partial kernel for few query rows per KV head ('auto' =
+    small-group tensor cores, 'cuda_core' = the CUDA-core kernel) for a block."""
+
+    def __init__(self, kind):
+        self.kind = kind
+
+    def __enter__(self):
+        ctx().set_partial_kernel(self.kind)
+
+    def __exit__(self, *exc):
+        ctx().set_partial_kernel("auto")
+        return False
+
+
 class Dev:
     """Device copies of a synth.Workload."""
 

@@ -10,27 +10,33 @@ import synth
 from oracle import attention as A
 from oracle import cascade as OC
 from oracle import planner as PL
-from _gpu_util import Dev, assert_close, ctx, oracle_partials
+from _gpu_util import Dev, assert_close, ctx, oracle_partials, use_kernel
 
 pytestmark = pytest.mark.gpu
 
+KERNELS = ["auto", "cuda_core"]
 
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("maker,seed", [(synth.tiny_cascade, 0), (synth.tiny_cascade, 1),
                                         (synth.flat_decode, 0)])
-def test_partials_match_oracle_chunk_by_chunk(maker, seed):
+def test_partials_match_oracle_chunk_by_chunk(maker, seed, kernel):
     w = maker(seed=seed)
-    v, l, items, o_indptr = Dev(w).partials()
+    with use_kernel(kernel):
+        v, l, items, o_indptr = Dev(w).partials()
     rv, rl, ro = oracle_partials(w)
     assert o_indptr.tolist() == ro
     assert_close(v, l, rv, rl, w.kv_dtype, "partials")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("seed", [0, 1, 2])
-def test_flat_decode_full_size(seed):
+def test_flat_decode_full_size(seed, kernel):
     """Flat config at full size (32 requests, 16384-page pool, tile 512), every output."""
     w = synth.flat_decode(seed=seed)
     d = Dev(w)
-    o, lse, stats, plan = d.decode(enable=1, with_stats=True)
+    with use_kernel(kernel):
+        o, lse, stats, plan = d.decode(enable=1, with_stats=True)
     assert stats["path"] == 0 and stats["decline_reason"] == PL.DECLINE_NO_SHARED_PAGES
     ro, rl = A.decode_attention(A.workload_arrays(w))
     assert_close(o, lse, ro, rl, w.kv_dtype, "flat")
@@ -56,13 +62,15 @@ def test_tiny_cascade_declines_at_default_thresholds():
     assert_close(o, lse, ro, rl, w.kv_dtype, "declined")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("seed", [0, 1])
-def test_cascade_config_full_size(seed):
+def test_cascade_config_full_size(seed, kernel):
     """Cascade config at full size: 64 requests, 16 members share 8192 tokens; the
     cascade arm, the flat arm and the oracle agree."""
     w = synth.cascade_decode(seed=seed)
     d = Dev(w)
-    o, lse, stats, plan = d.decode(enable=1, with_stats=True)
+    with use_kernel(kernel):
+        o, lse, stats, plan = d.decode(enable=1, with_stats=True)
     assert stats["path"] == 1 and stats["members"] == 16 and stats["shared_pages"] == 512
     ro, rl = A.decode_attention(A.workload_arrays(w))
     assert_close(o, lse, ro, rl, w.kv_dtype, "cascade")
@@ -71,14 +79,17 @@ def test_cascade_config_full_size(seed):
     assert np.abs(o - fo).max() < 2e-3
 
 
-def test_cascade_with_small_group_uses_stacked_cuda_core_path():
-    """2 members x G=4 = 8 stacked rows per KV head: level 0 runs on the CUDA-core
-    kernel's stacked mode."""
-    w = synth.cascade_decode(seed=3, members=2, others=3, shared_tokens=512)
-    o, lse, stats, _ = Dev(w).decode(enable=1, with_stats=True)
-    assert stats["members"] == 2
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("members", [2, 4])
+def test_cascade_with_small_group_uses_stacked_small_kernels(kernel, members):
+    """2 members x G=4 = 8 stacked rows per KV head (either small-group kernel's
+    stacked mode) and 4 x 4 = 16 rows (small-group tensor-core kernel)."""
+    w = synth.cascade_decode(seed=3, members=members, others=3, shared_tokens=512)
+    with use_kernel(kernel):
+        o, lse, stats, _ = Dev(w).decode(enable=1, with_stats=True)
+    assert stats["members"] == members
     ro, rl = A.decode_attention(A.workload_arrays(w))
-    assert_close(o, lse, ro, rl, w.kv_dtype, "2-member cascade")
+    assert_close(o, lse, ro, rl, w.kv_dtype, f"{members}-member cascade")
 
 
 def test_cascade_level_partials_match_oracle_levels():
@@ -125,13 +136,15 @@ def test_kv_head_major_stacking_matches_and_member_major_reads_wrong_kv_head():
     assert np.abs(bv - rv).max() > 0.1
 
 
-@pytest.mark.parametrize("D,Hq,Hkv", [(256, 8, 1), (64, 6, 3), (128, 2, 2)])
-def test_other_head_dims_and_group_sizes(D, Hq, Hkv):
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("D,Hq,Hkv", [(256, 8, 1), (64, 6, 3), (128, 2, 2), (128, 16, 1)])
+def test_other_head_dims_and_group_sizes(D, Hq, Hkv, kernel):
     rng = np.random.default_rng(D + Hq)
     lengths = synth.lengths_with_partial_last_page(rng, 5, 20, 700, 16)
     w = synth._make("shape", rng, lengths, Hq=Hq, Hkv=Hkv, Dqk=D, Dv=D, page_size=16,
                     num_pages=400, tile_tokens=64)
-    o, lse = Dev(w).decode(enable=0)
+    with use_kernel(kernel):
+        o, lse = Dev(w).decode(enable=0)
     ro, rl = A.decode_attention(A.workload_arrays(w))
     assert_close(o, lse, ro, rl, "bf16", f"D={D} G={Hq // Hkv}")
 
@@ -146,15 +159,18 @@ def test_fp8_pool_with_separate_k_and_v():
     assert_close(o, lse, ro, rl, "fp8_e4m3", "fp8 GQA")
 
 
-def test_large_page_size_and_single_token_requests():
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("P", [64, 8])
+def test_page_sizes_and_single_token_requests(kernel, P):
     rng = np.random.default_rng(22)
     lengths = [1, 2, 63, 64, 65, 300]
-    w = synth._make("edge", rng, lengths, Hq=8, Hkv=2, Dqk=128, Dv=128, page_size=64,
-                    num_pages=64, tile_tokens=128)
-    o, lse = Dev(w).decode(enable=0)
+    w = synth._make("edge", rng, lengths, Hq=8, Hkv=2, Dqk=128, Dv=128, page_size=P,
+                    num_pages=512 // P * 8, tile_tokens=128)
+    with use_kernel(kernel):
+        o, lse = Dev(w).decode(enable=0)
+        v, l, items, o_indptr = Dev(w).partials()
     ro, rl = A.decode_attention(A.workload_arrays(w))
-    assert_close(o, lse, ro, rl, "bf16", "page 64")
-    v, l, items, o_indptr = Dev(w).partials()
+    assert_close(o, lse, ro, rl, "bf16", f"page {P}")
     rv, rl2, _ = oracle_partials(w)
     assert_close(v, l, rv, rl2, "bf16", "page 64 partials")
 
