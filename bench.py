@@ -180,20 +180,38 @@ def time_steps(fn, steps: int, warmup: int, flush: torch.Tensor):
     return [a.elapsed_time(b) for a, b in times]
 
 
-def partial_kernel_timing(arm: Arm, steps: int, warmup: int, flush):
-    """The split-KV partial kernel alone over the flat work list, launched through
-    paged_decode_partial on the current stream."""
-    psd, w = arm.psd, arm.w
-    items, o_indptr = psd.split_plan(arm.table, w.tile_tokens)
-    N = int(o_indptr[-1])
-    v = torch.empty((N, w.Hq, w.Dv), dtype=torch.float32, device="cuda")
-    l = torch.empty((N, w.Hq), dtype=torch.float32, device="cuda")
-    ws = torch.empty(psd.workspace_bytes(0, len(items), 0, w.Hq, w.Dv), dtype=torch.uint8, device="cuda")
-    times = time_steps(lambda: psd.paged_decode_partial(arm.ctx, arm.args, items, v, l, ws), steps, warmup, flush)
-    q_bytes = w.q.numel() * 2
-    out_bytes = N * w.Hq * (w.Dv + 1) * 4
-    algo = flat_kv_bytes(w) + q_bytes + out_bytes
-    return times, algo, N
+def kernel_timing(arm: Arm, steps: int, warmup: int, flush, kind: str = "auto"):
+    """Per-kernel device times of the decode step, from the CUDA events the library
+    records around each kernel on the stream it launches on ('auto' = the
+    16-row-group tensor-core partial kernel, 'cuda_core' = the CUDA-core one)."""
+    arm.ctx.set_partial_kernel(kind)
+    arm.ctx.set_timing(True)
+    for _ in range(warmup):
+        flush.zero_()
+        arm.step()
+    torch.cuda.synchronize()
+    out = {"level0_ms": [], "partial_ms": [], "merge_ms": []}
+    for _ in range(steps):
+        flush.zero_()
+        arm.step()
+        for k, v in arm.ctx.kernel_times().items():
+            out[k].append(v)
+    arm.ctx.set_timing(False)
+    arm.ctx.set_partial_kernel("auto")
+    return {k: statistics.mean(v) for k, v in out.items()}
+
+
+def partial_algorithmic_bytes(arm: Arm) -> int:
+    """Bytes the split-KV partial kernel must move: every K/V token of every work item
+    (all KV heads), the query rows, and the partial rows it writes."""
+    w = arm.w
+    n_rows = arm.plan.num_rows
+    return flat_kv_bytes(w) + w.q.numel() * 2 + n_rows * w.Hq * (w.Dv + 1) * 4
+
+
+def merge_algorithmic_bytes(arm: Arm) -> int:
+    w = arm.w
+    return (arm.plan.num_rows + w.batch) * w.Hq * (w.Dv + 1) * 4
 
 
 def e2e_timing(arm: Arm, steps: int, warmup: int, flush):
@@ -222,7 +240,8 @@ def e2e_timing(arm: Arm, steps: int, warmup: int, flush):
 # ----------------------------------------------------------------------- oracle
 def oracle_baseline(w, budget_s: float = 12.0):
     """The float64 oracle (as it stands) on the host: gather + softmax attention per
-    request.  Requests are processed in order until the time budget is spent."""
+    request.  Requests are processed in order, cycling over the batch, until the
+    time budget is spent."""
     from oracle import attention as A
     a = A.workload_arrays(w)
     q = A.bf16_bits_to_f64(a["q_raw"])
@@ -237,7 +256,7 @@ def oracle_baseline(w, budget_s: float = 12.0):
             done += 1
             if time.perf_counter() - t0 > budget_s:
                 break
-        if time.perf_counter() - t0 > budget_s or done >= 4 * w.batch:
+        if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
     gbs = done_tokens * w.kv_bytes_per_token() / dt / 1e9
@@ -290,13 +309,19 @@ def run_ours(args):
         times = time_steps(arm.step, args.steps, args.warmup, flush)
         barrier(world)
         t_wall = time.perf_counter() - t_wall0
-        kt, algo, n_rows = partial_kernel_timing(arm, args.steps, args.warmup, flush)
+        kt = kernel_timing(arm, args.steps, args.warmup, flush)
+        kt_cc = kernel_timing(arm, args.steps, args.warmup, flush, "cuda_core")
     arm.check()
+    algo = partial_algorithmic_bytes(arm)
+    merge_bytes = merge_algorithmic_bytes(arm)
     ms = statistics.mean(times)
     ms_max = dist_max(ms, world)
     value = world * kv_bytes / (ms_max * 1e-3) / 1e9
-    k_ms = statistics.mean(kt)
+    k_ms = kt["partial_ms"]
     achieved = algo / (k_ms * 1e-3) / 1e9
+    k_ms_cc = kt_cc["partial_ms"]
+    achieved_cc = algo / (k_ms_cc * 1e-3) / 1e9
+    merge_gbs = merge_bytes / (kt["merge_ms"] * 1e-3) / 1e9
 
     et, h2d, d2h = e2e_timing(arm, args.steps, args.warmup, flush)
     e2e_ms = dist_max(statistics.mean(et), world)
@@ -311,6 +336,8 @@ def run_ours(args):
         st = casc_arm.stats
         tf = statistics.mean(time_steps(flat_arm.step, args.steps, args.warmup, flush))
         tc = statistics.mean(time_steps(casc_arm.step, args.steps, args.warmup, flush))
+        kf = kernel_timing(flat_arm, args.steps, args.warmup, flush)
+        kc = kernel_timing(casc_arm, args.steps, args.warmup, flush)
         flat_b, uniq_b = flat_kv_bytes(wc), unique_kv_bytes(wc)
         removed = (flat_b - uniq_b) / flat_b
         reduction = (tf - tc) / tf
@@ -324,6 +351,8 @@ def run_ours(args):
             "cascade_unique_kv_gbs": round(uniq_b / (tc * 1e-3) / 1e9, 1),
             "removed_read_fraction": round(removed, 4), "wall_time_reduction": round(reduction, 4),
             "criterion_reduction_ge_0.7x_removed": bool(reduction >= 0.7 * removed),
+            "flat_kernels_ms": {k: round(v, 5) for k, v in kf.items()},
+            "cascade_kernels_ms": {k: round(v, 5) for k, v in kc.items()},
             "stats": st,
         }
         del flat_arm, casc_arm
@@ -333,6 +362,7 @@ def run_ours(args):
         marm.step()
         marm.check()
         tm = statistics.mean(time_steps(marm.step, max(3, args.steps // 2), args.warmup, flush))
+        km = kernel_timing(marm, max(3, args.steps // 2), 1, flush)
         mb = unique_kv_bytes(wm)
         flops = float(np.sum(wm.lengths)) * wm.Hq * (wm.Dqk + wm.Dv) * 2
         extra["mla"] = {
@@ -342,6 +372,9 @@ def run_ours(args):
             "unique_kv_gbs": round(mb / (tm * 1e-3) / 1e9, 1),
             "tflops": round(flops / (tm * 1e-3) / 1e12, 1),
             "tensor_frac_of_sustained_bf16": round(flops / (tm * 1e-3) / 1e12 / bf16s, 4) if bf16s else None,
+            "kernels_ms": {k: round(v, 4) for k, v in km.items()},
+            "partial_kernel_tflops": round(flops / (km["partial_ms"] * 1e-3) / 1e12, 1),
+            "partial_kernel_frac_of_burst_bf16": round(flops / (km["partial_ms"] * 1e-3) / 1e12 / bf16, 4),
         }
         del marm
 
@@ -368,11 +401,18 @@ def run_ours(args):
             "decode_tokens_per_s": round(world * w.batch / (ms_max * 1e-3), 1),
             "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
             "pct_of_measured_hbm": round(100 * value / world / hbm, 2),
-            "roofline": {"bound": "hbm", "kernel": "partial_cc_kernel<128,4> (split-KV partial, CUDA cores)",
+            "roofline": {"bound": "hbm",
+                         "kernel": "partial_tcs_kernel<128> (split-KV partial, 16-row-group tensor cores)",
                          "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "peak_source": peak_src + " copy bandwidth",
                          "traffic": None, "algorithmic_bytes_per_launch": algo,
                          "launch_ms": round(k_ms, 5)},
+            "merge_kernel": {"kernel": "merge_states_kernel<1>", "achieved": round(merge_gbs, 1),
+                             "unit": "GB/s", "frac": round(merge_gbs / hbm, 4),
+                             "launch_ms": round(kt["merge_ms"], 5), "algorithmic_bytes": merge_bytes},
+            "partial_cuda_core": {"kernel": "partial_cc_kernel<128,4> (split-KV partial, CUDA cores)",
+                                  "achieved": round(achieved_cc, 1), "unit": "GB/s",
+                                  "frac": round(achieved_cc / hbm, 4), "launch_ms": round(k_ms_cc, 5)},
             "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h)},

@@ -157,14 +157,23 @@ typedef struct psd_ctx psd_ctx;
  * context per thread, or external locking. */
 psd_status psd_create(psd_ctx **ctx, int device);
 psd_status psd_destroy(psd_ctx *ctx);
-/* Which kernel computes partials when a KV head has few query rows (G <= 16,
- * bf16 pools).  AUTO and TENSOR_CORE: the small-group tensor-core kernel (rows
- * padded to 16, QK^T and PV as m16n8k16 MMAs).  CUDA_CORE: the CUDA-core kernel
- * (G <= 8; warp-shuffle reductions and f32x2 FMAs).  Both compute the same
- * partials; many-row launches (stacked level 0, MLA) and fp8 always use the
- * 64-row tensor-core kernel. */
+/* Which kernel computes partials on bf16 pools with separate K and V.  AUTO and
+ * TENSOR_CORE: the 16-row-group tensor-core kernel (QK^T and PV as m16n8k16
+ * MMAs; the stacked level-0 rows are split into groups of 16).  CUDA_CORE: the
+ * CUDA-core kernel wherever it applies (G <= 8 rows per KV head; warp-shuffle
+ * reductions and f32x2 FMAs).  Both compute the same partials.  fp8 pools and the
+ * shared MLA latent always use the 64-row tensor-core kernel. */
 typedef enum { PSD_KERNEL_AUTO = 0, PSD_KERNEL_CUDA_CORE = 1, PSD_KERNEL_TENSOR_CORE = 2 } psd_partial_kernel;
 psd_status psd_set_partial_kernel(psd_ctx *ctx, int32_t kind);
+/* Kernel timing, for measurement: when enabled, paged_decode_partial and
+ * cascade_decode record CUDA events around each kernel they launch, on the
+ * stream that kernel runs on.  psd_get_kernel_times waits for the most recent
+ * call's events and returns the level-0 partial, the level-1 (or flat) partial
+ * and the merge kernel durations in milliseconds (0 for a kernel the call did not
+ * launch; any pointer may be NULL).  Enabling creates the events (host-side CUDA
+ * objects, no device memory). */
+psd_status psd_set_timing(psd_ctx *ctx, int32_t enable);
+psd_status psd_get_kernel_times(psd_ctx *ctx, float *level0_ms, float *partial_ms, float *merge_ms);
 /* Thread-local message describing the last failure on this thread. */
 const char *psd_last_error(void);
 psd_status psd_get_counters(const psd_ctx *ctx, psd_counters *out);

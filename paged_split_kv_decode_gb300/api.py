@@ -66,6 +66,16 @@ class Context:
                 "tensor_core": L.PSD_KERNEL_TENSOR_CORE}[kind]
         L.check(L.load().psd_set_partial_kernel(self._h, code))
 
+    def set_timing(self, enable: bool = True):
+        """psd_set_timing: CUDA events around every kernel the library launches."""
+        L.check(L.load().psd_set_timing(self._h, int(bool(enable))))
+
+    def kernel_times(self) -> dict:
+        """psd_get_kernel_times of the most recent call, in milliseconds."""
+        a, b, c = C.c_float(), C.c_float(), C.c_float()
+        L.check(L.load().psd_get_kernel_times(self._h, C.byref(a), C.byref(b), C.byref(c)))
+        return {"level0_ms": a.value, "partial_ms": b.value, "merge_ms": c.value}
+
     def counters(self) -> dict:
         c = L.Counters()
         L.check(L.load().psd_get_counters(self._h, C.byref(c)))

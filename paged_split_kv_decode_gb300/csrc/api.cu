@@ -114,9 +114,9 @@ bool dispatchable(const PartialLaunch &L) {
   return partial_tcs_supports(L) || partial_cc_supports(L) || partial_tc_supports(L);
 }
 
-// Few query rows per KV head (G <= 16, bf16): the small-group tensor-core kernel,
-// or the CUDA-core kernel when the context asks for it; many rows (stacked level
-// 0, MLA) or fp8: the 64-row tensor-core kernel.
+// bf16 pools with separate K and V: the 16-row-group tensor-core kernel (or, for
+// G <= 8 when the context asks for it, the CUDA-core kernel); fp8 pools and the
+// shared MLA latent: the 64-row tensor-core kernel.
 psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
   if (dev.partial_kernel == PSD_KERNEL_CUDA_CORE && partial_cc_supports(L))
     return launch_partial_cc(L, dev, s);
@@ -130,6 +130,13 @@ psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStr
 }  // namespace psd
 
 namespace {
+
+// Both cascade levels can share one launch when the 16-row-group tensor-core
+// kernel serves both and level 1 fits one row group.
+bool dispatch_fused(const PartialLaunch &L0, const PartialLaunch &L1, const DeviceInfo &dev) {
+  if (dev.partial_kernel == PSD_KERNEL_CUDA_CORE) return false;
+  return partial_tcs_supports(L0) && partial_tcs_supports(L1) && L1.G_cta <= 16;
+}
 
 // Copies `bytes` of host data into a pinned staging buffer and enqueues one H2D
 // copy to `dst` on `s`.
@@ -200,6 +207,13 @@ extern "C" psd_status psd_create(psd_ctx **out, int device) {
       return fail(PSD_ERR_CUDA, "cudaEventCreate: %s", cudaGetErrorString(e));
     }
   }
+  e = cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    psd_destroy(c);
+    return fail(PSD_ERR_CUDA, "side stream / events: %s", cudaGetErrorString(e));
+  }
   *out = c;
   return PSD_OK;
 }
@@ -213,6 +227,14 @@ extern "C" psd_status psd_destroy(psd_ctx *c) {
     if (c->staging_done[i]) cudaEventDestroy(c->staging_done[i]);
     if (c->staging[i]) cudaFreeHost(c->staging[i]);
   }
+  if (c->side) {
+    cudaStreamSynchronize(c->side);
+    cudaStreamDestroy(c->side);
+  }
+  if (c->fork) cudaEventDestroy(c->fork);
+  if (c->join) cudaEventDestroy(c->join);
+  for (auto &ev : c->tev)
+    if (ev) cudaEventDestroy(ev);
   delete c;
   return PSD_OK;
 }
@@ -223,6 +245,39 @@ extern "C" psd_status psd_set_partial_kernel(psd_ctx *c, int32_t kind) {
   if (kind != PSD_KERNEL_AUTO && kind != PSD_KERNEL_CUDA_CORE && kind != PSD_KERNEL_TENSOR_CORE)
     return fail(PSD_ERR_INVALID_ARG, "partial kernel kind %d", kind);
   c->dev.partial_kernel = kind;
+  return PSD_OK;
+}
+
+extern "C" psd_status psd_set_timing(psd_ctx *c, int32_t enable) {
+  clear_error();
+  if (!c) return fail(PSD_ERR_INVALID_ARG, "NULL context");
+  if (enable) {
+    DeviceGuard g(c->dev.device);
+    for (auto &ev : c->tev)
+      if (!ev) {
+        cudaError_t e = cudaEventCreate(&ev);
+        if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "timing events: %s", cudaGetErrorString(e));
+      }
+  }
+  c->timing = enable != 0;
+  return PSD_OK;
+}
+
+extern "C" psd_status psd_get_kernel_times(psd_ctx *c, float *level0_ms, float *partial_ms,
+                                           float *merge_ms) {
+  clear_error();
+  if (!c) return fail(PSD_ERR_INVALID_ARG, "NULL context");
+  if (!c->timing) return fail(PSD_ERR_INVALID_ARG, "timing is off (psd_set_timing)");
+  DeviceGuard g(c->dev.device);
+  float *out[3] = {level0_ms, partial_ms, merge_ms};
+  for (int k = 0; k < 3; ++k) {
+    if (!out[k]) continue;
+    *out[k] = 0.f;
+    if (!c->tev_used[k]) continue;
+    cudaError_t e = cudaEventSynchronize(c->tev[2 * k + 1]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(out[k], c->tev[2 * k], c->tev[2 * k + 1]);
+    if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "kernel times: %s", cudaGetErrorString(e));
+  }
   return PSD_OK;
 }
 
@@ -274,7 +329,13 @@ extern "C" psd_status paged_decode_partial(psd_ctx *ctx, const psd_decode_args *
   L.v_out = v_out;
   L.lse_out = lse_out;
   L.fault = reinterpret_cast<int32_t *>(ws);
-  return launch_partial(L, ctx->dev, s);
+  ctx->tev_used[0] = false;
+  ctx->tev_used[1] = ctx->timing;
+  ctx->tev_used[2] = false;
+  time_mark(ctx, 2, s);
+  st = launch_partial(L, ctx->dev, s);
+  time_mark(ctx, 3, s);
+  return st;
 }
 
 extern "C" psd_status merge_states(psd_ctx *ctx, const float *v_in, const float *lse_in,
@@ -361,7 +422,16 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   float *lpart = reinterpret_cast<float *>(ws + lay.lpart_off);
   int32_t *fault = reinterpret_cast<int32_t *>(ws);
   const psd_work_item *ditems = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
-  if (M > 0) {
+  const bool fused = M > 0 && dispatch_fused(L0, L1, ctx->dev);
+  if (fused) {  // both levels in one launch of the 16-row-group tensor-core kernel
+    L1.items = ditems;
+    L1.order = reinterpret_cast<const int32_t *>(ws + lay.order_off) + n0;
+    L1.num_items = n1;
+    L1.members = reinterpret_cast<const int32_t *>(ws + lay.members_off);
+    L1.member_row_base = reinterpret_cast<const int32_t *>(ws + lay.row_base_off);
+    L1.fused_l0_items = n0;
+    L1.fused_l0_rows = L0.G_cta;
+  } else if (M > 0) {  // level 0 on the side stream, after the upload
     L0.items = ditems;
     L0.order = reinterpret_cast<const int32_t *>(ws + lay.order_off);
     L0.num_items = n0;
@@ -370,19 +440,39 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
     L0.v_out = vpart;
     L0.lse_out = lpart;
     L0.fault = fault;
-    st = launch_partial(L0, ctx->dev, s);
+    cudaError_t e = cudaEventRecord(ctx->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->fork, 0);
+    if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cascade fork: %s", cudaGetErrorString(e));
+    time_mark(ctx, 0, ctx->side);
+    st = launch_partial(L0, ctx->dev, ctx->side);
+    time_mark(ctx, 1, ctx->side);
     if (st != PSD_OK) return st;
+    e = cudaEventRecord(ctx->join, ctx->side);
+    if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cascade join: %s", cudaGetErrorString(e));
   }
-  L1.items = ditems + n0;
-  L1.order = reinterpret_cast<const int32_t *>(ws + lay.order_off) + n0;
-  L1.num_items = n1;
+  if (!fused) {
+    L1.items = ditems + n0;
+    L1.order = reinterpret_cast<const int32_t *>(ws + lay.order_off) + n0;
+    L1.num_items = n1;
+  }
   L1.v_out = vpart;
   L1.lse_out = lpart;
   L1.fault = fault;
+  time_mark(ctx, 2, s);
   st = launch_partial(L1, ctx->dev, s);
+  time_mark(ctx, 3, s);
   if (st != PSD_OK) return st;
+  if (M > 0 && !fused) {
+    cudaError_t e = cudaStreamWaitEvent(s, ctx->join, 0);
+    if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cascade join: %s", cudaGetErrorString(e));
+  }
+  time_mark(ctx, 4, s);
   st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq,
                     args->Dv, o, lse, ctx->dev, s);
+  time_mark(ctx, 5, s);
+  ctx->tev_used[0] = ctx->timing && M > 0 && !fused;
+  ctx->tev_used[1] = ctx->timing;
+  ctx->tev_used[2] = ctx->timing;
   if (st != PSD_OK) return st;
 
   if (M > 0) {

@@ -16,7 +16,22 @@ struct psd_ctx {
   cudaEvent_t staging_done[2] = {nullptr, nullptr};
   bool staging_pending[2] = {false, false};
   int next = 0;
+  // Level 0 of a cascade runs on `side`, concurrently with level 1 on the caller's
+  // stream: fork after the upload, join before the merge.
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  // Optional kernel timing: events around level 0, level 1 / flat, and merge.
+  bool timing = false;
+  cudaEvent_t tev[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  bool tev_used[3] = {false, false, false};
 };
+
+namespace psd {
+// Records timing event `i` (0..5) of the context on stream `s` when timing is on.
+inline void time_mark(psd_ctx *c, int i, cudaStream_t s) {
+  if (c->timing && c->tev[i]) cudaEventRecord(c->tev[i], s);
+}
+}  // namespace psd
 
 namespace psd {
 

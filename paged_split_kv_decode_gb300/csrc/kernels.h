@@ -43,6 +43,11 @@ struct PartialLaunch {
   int32_t max_item_tokens = 0;
   float q_scale = 1.f;  // sm_scale * log2(e) * k_scale
   float v_scale = 1.f;
+  // Fused cascade launch (16-row-group tensor-core kernel only): `items` starts
+  // with this many level-0 items of `fused_l0_rows` stacked rows, followed by the
+  // num_items level-1 items (order indexes those).
+  int32_t fused_l0_items = 0;
+  int32_t fused_l0_rows = 0;
 };
 
 bool partial_cc_supports(const PartialLaunch &p);

@@ -4,8 +4,8 @@
 //
 // HBM-bound stream: each input row of one head is D floats read once, each output
 // row D floats written once.  One warp owns one (output row, head); lanes hold
-// float4 slices of D; up to 4 input rows are loaded before they are accumulated
-// so every warp keeps 4 * D * 4 bytes in flight.
+// float4 slices of D; up to 8 input rows (4 when D > 128) are loaded before they
+// are accumulated so every warp keeps several rows of loads in flight.
 #include <cuda_runtime.h>
 
 #include "device.cuh"
@@ -68,11 +68,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     const float w_mine =
         lane < cnt ? ex2(__ldg(lse_in + int64_t(lo + i0 + lane) * H + h) - M) : 0.f;
     sw += w_mine;
-    for (int j = 0; j < cnt; j += 4) {
-      float4 v[4][NV];
-      float w[4];
+    constexpr int U = NV == 1 ? 8 : 4;  // input rows in flight per warp
+    for (int j = 0; j < cnt; j += U) {
+      float4 v[U][NV];
+      float w[U];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < U; ++u) {
         w[u] = __shfl_sync(0xffffffffu, w_mine, (j + u) & 31);
         const bool ok = j + u < cnt;
         const float4 *src =
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
         if (!ok) w[u] = 0.f;
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
           acc[k].x = fmaf(w[u], v[u][k].x, acc[k].x);

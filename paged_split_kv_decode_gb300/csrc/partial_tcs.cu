@@ -1,5 +1,6 @@
-// K1t: split-KV partial attention for small query groups (G = Hq/Hkv <= 16 rows
-// per KV head) with QK^T and PV on the tensor cores.
+// K1t: split-KV partial attention with QK^T and PV on the tensor cores, in 16-row
+// groups: small query groups (G = Hq/Hkv <= 16) in one CTA per (item, KV head),
+// and the stacked level-0 rows (M*G) split over grid.z groups of 16.
 //
 // Same work unit as the CUDA-core kernel (mlxcel PR #1004, Decomposition section:
 // one CTA owns all query heads of one KV head for one (request, page tile), so
@@ -10,7 +11,8 @@
 // shuffles and cannot keep up with HBM, while one m16n8k16 MMA covers 16 tokens x
 // 16 dims for all G rows (padded to 16) in one issue slot.
 //
-// GB300 shape: grid = (work items, Hkv), 4 warps, 3 CTAs per SM.  Warp w streams
+// GB300 shape: grid = (work items, Hkv, row groups of 16), 4 warps, 3 CTAs per
+// SM (row groups of one item re-read its K/V tiles from L2, not HBM).  Warp w streams
 // 16-token tiles w, w+4, ... of the item through a private 2-stage ring; each
 // stage is 16 slots of one page loaded by TMA in 64-column boxes with the 128-byte
 // swizzle, so ldmatrix reads are bank-conflict free.  Per tile and warp: S = Q K^T
@@ -47,6 +49,10 @@ struct TCSParams {
   int64_t num_pages;
   int Hq_req, Dqk, Dv, page_size, Gm, G_cta;
   int tpp_log2;  // log2(page_size / 16), or -1
+  // Fused cascade launch: CTAs [0, n_l0_tasks) take level-0 item blockIdx.x / rg0,
+  // row group blockIdx.x % rg0 (G_l0 stacked rows); the rest take level-1 items
+  // l1_base + order[...].  A plain launch has n_l0_tasks = 0 and l1_base = 0.
+  int n_l0_tasks, rg0, G_l0, l1_base;
   float q_scale, v_scale;
 };
 
@@ -93,8 +99,21 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
   // 128-byte-swizzled TMA boxes need 1024-byte aligned destinations.
   uint8_t *base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const psd_work_item it = p.items[p.order ? __ldg(p.order + blockIdx.x) : blockIdx.x];
+  int item_index, group, G_rows;
+  if (int(blockIdx.x) < p.n_l0_tasks) {
+    item_index = blockIdx.x / p.rg0;
+    group = blockIdx.x - item_index * p.rg0;
+    G_rows = p.G_l0;
+  } else {
+    const int j = blockIdx.x - p.n_l0_tasks;
+    item_index = p.l1_base + (p.order ? __ldg(p.order + j) : j);
+    group = blockIdx.z;
+    G_rows = p.G_cta;
+  }
+  const psd_work_item it = p.items[item_index];
   const int kv = blockIdx.y;
+  const int row0 = group * 16;  // this CTA's 16-row group of the KV head's rows
+  const int rows = min(16, G_rows - row0);
   const int P = p.page_size;
   const int TPP = P / kTileTok;
   const size_t ring_total = size_t(kWarpsS) * kStagesS * 2 * TILE_BYTES;
@@ -110,8 +129,8 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
     const __nv_bfloat16 *qrow[2] = {nullptr, nullptr};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int g = r0 + 8 * h;
-      if (g < p.G_cta) {
+      const int g = row0 + r0 + 8 * h;
+      if (g < G_rows) {
         const int m = g / p.Gm;
         const int qb = it.q_index >= 0 ? it.q_index : __ldg(p.members + m);
         const int head = kv * p.Gm + (g - m * p.Gm);
@@ -314,17 +333,18 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
     }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < p.G_cta * D; idx += kWarpsS * 32) {
-    const int g = idx / D, d = idx - g * D;
+  for (int idx = threadIdx.x; idx < rows * D; idx += kWarpsS * 32) {
+    const int r = idx / D, d = idx - r * D;
+    const int g = row0 + r;
     float M = neg_inf();
 #pragma unroll
-    for (int w = 0; w < kWarpsS; ++w) M = fmaxf(M, red_m[w * 16 + g]);
+    for (int w = 0; w < kWarpsS; ++w) M = fmaxf(M, red_m[w * 16 + r]);
     float L = 0.f, O = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarpsS; ++w) {
-      const float sc = ex2(red_m[w * 16 + g] - M);
-      L = fmaf(sc, red_l[w * 16 + g], L);
-      O = fmaf(sc, red_o[(size_t(w) * 16 + g) * D + d], O);
+      const float sc = ex2(red_m[w * 16 + r] - M);
+      L = fmaf(sc, red_l[w * 16 + r], L);
+      O = fmaf(sc, red_o[(size_t(w) * 16 + r) * D + d], O);
     }
     const bool live = M != neg_inf();
     const int m = g / p.Gm;
@@ -385,13 +405,26 @@ psd_status launch_tcs(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_
   p.tpp_log2 = (tpp & (tpp - 1)) == 0 ? __builtin_ctz(unsigned(tpp)) : -1;
   p.q_scale = L.q_scale;
   p.v_scale = L.v_scale;
+  p.n_l0_tasks = 0;
+  p.rg0 = 1;
+  p.G_l0 = 0;
+  p.l1_base = 0;
+  unsigned grid_x = static_cast<unsigned>(L.num_items), grid_z = static_cast<unsigned>((L.G_cta + 15) / 16);
+  if (L.fused_l0_items > 0) {  // level-0 items precede L.items' level-1 items
+    p.rg0 = (L.fused_l0_rows + 15) / 16;
+    p.n_l0_tasks = L.fused_l0_items * p.rg0;
+    p.G_l0 = L.fused_l0_rows;
+    p.l1_base = L.fused_l0_items;
+    grid_x = static_cast<unsigned>(p.n_l0_tasks + L.num_items);
+    grid_z = 1;  // level-1 items have G_cta <= 16 rows (checked by the caller)
+  }
   const size_t smem = tcs_smem_bytes<D>();
   auto kern = partial_tcs_kernel<D>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   }
-  const dim3 grid(static_cast<unsigned>(L.num_items), static_cast<unsigned>(L.Hkv));
+  const dim3 grid(grid_x, static_cast<unsigned>(L.Hkv), grid_z);
   kern<<<grid, kWarpsS * 32, smem, s>>>(tmK, tmV, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "partial (small-group tensor cores) launch: %s", cudaGetErrorString(e));
@@ -402,12 +435,12 @@ psd_status launch_tcs(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_
 
 bool partial_tcs_supports(const PartialLaunch &p) {
   return p.kv_dtype == PSD_BF16 && !p.latent_v && p.Dqk == p.Dv &&
-         (p.Dqk == 64 || p.Dqk == 128 || p.Dqk == 256) && p.G_cta >= 1 && p.G_cta <= 16 &&
+         (p.Dqk == 64 || p.Dqk == 128 || p.Dqk == 256) && p.G_cta >= 1 && p.G_cta <= 256 &&
          p.page_size % kTileTok == 0;
 }
 
 psd_status launch_partial_tcs(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
-  if (L.num_items == 0) return PSD_OK;
+  if (L.num_items == 0 && L.fused_l0_items == 0) return PSD_OK;
   switch (L.Dqk) {
     case 64: return launch_tcs<64>(L, dev, s);
     case 128: return launch_tcs<128>(L, dev, s);
