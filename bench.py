@@ -237,6 +237,30 @@ def e2e_timing(arm: Arm, steps: int, warmup: int, flush):
     return times, h2d, d2h
 
 
+def merge_sweep(ctx, steps: int, warmup: int, flush, hbm: float):
+    """merge_states alone over the sweep's sizes (H=32, D=128, log2 LSE ~ U(-5,20),
+    groups U[1,16] with a group of one), inputs drawn on the device."""
+    import paged_split_kv_decode_gb300 as psd
+    out = []
+    for M in (1024, 16384, 262144, 1048576):
+        v_in, lse_in, o_indptr = synth.merge_inputs_device(0, M)
+        ind = torch.from_numpy(o_indptr).cuda()
+        N = int(o_indptr[-1])
+        H, D = v_in.shape[1], v_in.shape[2]
+        v_out = torch.empty((M, H, D), dtype=torch.float32, device="cuda")
+        l_out = torch.empty((M, H), dtype=torch.float32, device="cuda")
+        n = max(3, steps // 4) if M >= 262144 else steps
+        t = statistics.mean(time_steps(lambda: psd.merge_states(ctx, v_in, lse_in, ind, v_out, l_out),
+                                       n, min(warmup, 3), flush))
+        nbytes = (N + M) * H * (D + 1) * 4 + (M + 1) * 4
+        gbs = nbytes / (t * 1e-3) / 1e9
+        out.append({"rows": M, "input_rows": N, "ms": round(t, 4), "gbs": round(gbs, 1),
+                    "frac_of_measured_hbm": round(gbs / hbm, 4)})
+        del v_in, lse_in, v_out, l_out, ind
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------- oracle
 def oracle_baseline(w, budget_s: float = 12.0):
     """The float64 oracle (as it stands) on the host: gather + softmax attention per
@@ -377,6 +401,7 @@ def run_ours(args):
             "partial_kernel_frac_of_burst_bf16": round(flops / (km["partial_ms"] * 1e-3) / 1e12 / bf16, 4),
         }
         del marm
+        extra["merge_sweep"] = merge_sweep(arm.ctx, args.steps, args.warmup, flush, hbm)
 
     if rank == 0:
         line = {

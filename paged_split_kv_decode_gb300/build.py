@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpsd.so")
 
-CU_SOURCES = ["api.cu", "merge.cu", "partial_cc.cu", "partial_tcs.cu", "partial_tc.cu", "no_alloc.cu"]
+CU_SOURCES = ["api.cu", "merge.cu", "partial_cc.cu", "partial_tcs.cu", "partial_tc.cu", "partial_mla.cu",
+              "no_alloc.cu"]
 CPP_SOURCES = ["plan.cpp"]
 HEADERS = ["psd_internal.h", "kernels.h", "device.cuh", "context.h"]
 

@@ -95,6 +95,7 @@ PartialLaunch base_launch(const psd_decode_args *a) {
   L.v_pool = a->v_pool;
   L.page_indices = a->page_indices_dev;
   L.num_pages = a->num_pages;
+  L.q_batch = a->batch;
   L.Hq_req = a->Hq;
   L.Hkv = a->Hkv;
   L.Dqk = a->Dqk;
@@ -111,17 +112,22 @@ PartialLaunch base_launch(const psd_decode_args *a) {
 }
 
 bool dispatchable(const PartialLaunch &L) {
-  return partial_tcs_supports(L) || partial_cc_supports(L) || partial_tc_supports(L);
+  return partial_tcs_supports(L) || partial_cc_supports(L) || partial_mla_supports(L) ||
+         partial_tc_supports(L);
 }
 
 // bf16 pools with separate K and V: the 16-row-group tensor-core kernel (or, for
-// G <= 8 when the context asks for it, the CUDA-core kernel); fp8 pools and the
-// shared MLA latent: the 64-row tensor-core kernel.
+// G <= 8 when the context asks for it, the CUDA-core kernel); the fp8 MLA latent
+// (128 heads, 576/512): the tcgen05 kernel; other fp8 or latent shapes: the
+// 64-row mma.sync kernel (also used for MLA when the context asks for CUDA_CORE,
+// as the legacy-tensor-path reference).
 psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
   if (dev.partial_kernel == PSD_KERNEL_CUDA_CORE && partial_cc_supports(L))
     return launch_partial_cc(L, dev, s);
   if (partial_tcs_supports(L)) return launch_partial_tcs(L, dev, s);
   if (partial_cc_supports(L)) return launch_partial_cc(L, dev, s);
+  if (partial_mla_supports(L) && dev.partial_kernel != PSD_KERNEL_CUDA_CORE)
+    return launch_partial_mla(L, dev, s);
   if (partial_tc_supports(L)) return launch_partial_tc(L, dev, s);
   return fail(PSD_ERR_UNSUPPORTED, "no kernel for Dqk %d, Dv %d, rows/KV head %d, dtype %d, latent %d",
               L.Dqk, L.Dv, L.G_cta, L.kv_dtype, int(L.latent_v));

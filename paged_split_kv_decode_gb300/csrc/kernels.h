@@ -34,6 +34,7 @@ struct PartialLaunch {
   float *lse_out = nullptr;
   int32_t *fault = nullptr;
   int64_t num_pages = 0;
+  int32_t q_batch = 0;  // requests in q
   int32_t Hq_req = 0;  // query heads per request in q and in the outputs
   int32_t Hkv = 0, Dqk = 0, Dv = 0, page_size = 0;
   int32_t Gm = 0;      // query heads per KV head of one request
@@ -54,6 +55,8 @@ bool partial_cc_supports(const PartialLaunch &p);
 psd_status launch_partial_cc(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
 bool partial_tcs_supports(const PartialLaunch &p);
 psd_status launch_partial_tcs(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
+bool partial_mla_supports(const PartialLaunch &p);
+psd_status launch_partial_mla(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
 bool partial_tc_supports(const PartialLaunch &p);
 psd_status launch_partial_tc(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
 
