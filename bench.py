@@ -351,7 +351,7 @@ def run_ours(args):
     e2e_ms = dist_max(statistics.mean(et), world)
 
     extra = {}
-    if not args.quick:
+    if not args.quick and args.workload in ("all", "cascade"):
         # cascade workload: flat arm vs cascade arm on the same inputs
         wc = synth.cascade_decode(seed=0, canary=False)
         flat_arm, casc_arm = Arm(wc, enable=0), Arm(wc, enable=1)
@@ -380,8 +380,8 @@ def run_ours(args):
             "stats": st,
         }
         del flat_arm, casc_arm
-        # MLA workload
-        wm = synth.mla_decode(seed=0, canary=False)
+    if not args.quick and args.workload in ("all", "mla"):
+        wm = synth.mla_decode(seed=0, canary=False, batch=args.mla_batch)
         marm = Arm(wm, enable=1)
         marm.step()
         marm.check()
@@ -390,7 +390,7 @@ def run_ours(args):
         mb = unique_kv_bytes(wm)
         flops = float(np.sum(wm.lengths)) * wm.Hq * (wm.Dqk + wm.Dv) * 2
         extra["mla"] = {
-            "workload": "MLA decode: 128 requests U[4096,32768], 128 heads, latent 576 fp8-e4m3 "
+            "workload": f"MLA decode: {wm.batch} requests U[4096,32768], 128 heads, latent 576 fp8-e4m3 "
                         "(V = first 512), page 64, tile 2048",
             "ms": round(tm, 4), "tokens_per_s": round(wm.batch / (tm * 1e-3), 1),
             "unique_kv_gbs": round(mb / (tm * 1e-3) / 1e9, 1),
@@ -401,6 +401,7 @@ def run_ours(args):
             "partial_kernel_frac_of_burst_bf16": round(flops / (km["partial_ms"] * 1e-3) / 1e12 / bf16, 4),
         }
         del marm
+    if not args.quick and args.workload in ("all", "merge"):
         extra["merge_sweep"] = merge_sweep(arm.ctx, args.steps, args.warmup, flush, hbm)
 
     if rank == 0:
@@ -501,6 +502,9 @@ def main():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--quick", action="store_true", help="flat workload only")
+    p.add_argument("--workload", choices=["all", "cascade", "mla", "merge"], default="all",
+                   help="which workloads run after the flat headline")
+    p.add_argument("--mla-batch", type=int, default=128, help="requests in the MLA workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
     args = p.parse_args()
     if args.warmup < 3:

@@ -78,7 +78,9 @@ typedef enum {
 /* Device-fault flag bits written by kernels into the workspace. */
 enum {
   PSD_FAULT_PAGE_ID = 1,      /* a page id outside [0, num_pages) was skipped */
-  PSD_FAULT_WAIT_TIMEOUT = 2  /* a bounded barrier wait gave up */
+  PSD_FAULT_WAIT_TIMEOUT = 2, /* a bounded barrier wait gave up */
+  PSD_FAULT_RANGE = 4         /* a query value outside the f16 range reached the
+                                 f16 MLA tensor-core path (|q| > 65504) */
 };
 
 /* CSR page table (Detection section: PagedCsrView).  Host or device arrays. */

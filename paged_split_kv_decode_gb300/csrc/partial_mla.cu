@@ -7,22 +7,29 @@
 // #1004, Decomposition and Merge contract sections for the split-KV partial and
 // its (V, LSE) outputs in log2 units).
 //
-// GB300 design.  One CTA per (work item, half of the 512 V columns): its O half
-// [128 x 256] f32 lives in TMEM (256 columns) beside two S buffers [128 x 32]
-// (64 columns), and Q [128 x 576] bf16 stays in shared memory for the whole item
-// (147 KB, 128-byte swizzle, loaded once by TMA).  Per 32-token tile:
-//   * the four row warps load the tile's fp8 latent rows with 128-bit loads,
-//     widen them exactly to bf16 (e4m3 -> f16 -> f32 -> bf16) into a 128B-swizzled
-//     K tile (double buffered), and arrive on an mbarrier;
-//   * one control thread issues S = Q K^T (36 MMAs of M=128, N=32, K=16) into TMEM
-//     and commits to an mbarrier, then O += P V (2 MMAs of M=128, N=256, K=16,
-//     V read MN-major straight from the same K tile);
-//   * each row thread (thread = head = TMEM lane) reads its 32 scores with
-//     tcgen05.ld, keeps a lazily-updated running max (O is rescaled in TMEM only
-//     when the max grows by more than 2^8), writes P as bf16 into a 64B-swizzled
-//     tile and sums the same rounded P into l.
-// The k_scale folds into the score scale and v_scale into the output.  Two CTAs
-// per item (one per V half) both compute S; the tile is read from HBM once and
+// GB300 design.  One CTA per (work item, half of the 512 V columns).  TMEM (512
+// columns) holds the O half [128 x 256] f32, two S buffers [128 x 32] f32, and the
+// first 384 of Q's 576 columns as the MMA's A operand (f16 pairs); the remaining
+// 192 Q columns stay in shared memory (128-byte swizzle).  Keeping most of Q in
+// TMEM is what makes 32-token tiles pay: with Q in shared memory every M=128,
+// N=32 MMA re-read a 4 KB slice of it and the QK^T steps were bound by
+// shared-memory bandwidth.  The MMAs run in f16: e4m3 codes widen exactly to f16
+// with one hardware conversion per pair, Q is converted from bf16 once per item
+// (exact for |q| in [2^-14, 65504]; overflow sets a fault bit), and P in f16
+// keeps 3 more mantissa bits than bf16.  Warp roles, per 32-token tile:
+//   * converter warps 4-7 load the tile's fp8 latent rows with 128-bit loads (two
+//     tiles ahead) and widen them into a 128B-swizzled f16 K tile (2 buffers,
+//     freed when S is done) and this CTA's V half (3 buffers, freed when PV is
+//     done);
+//   * the control thread (warp 8) issues S = Q K^T (24 MMAs with A in TMEM, 12
+//     from shared memory; M=128, N=32, K=16) and O += P V (2 MMAs of M=128, N=256,
+//     K=16, V MN-major), each group committed to an mbarrier;
+//   * row warps 0-3 (thread = head = TMEM lane) first move their Q row into TMEM,
+//     then per tile read 32 scores with tcgen05.ld, keep a lazily-updated running
+//     max (O is rescaled in TMEM only when the max grows by more than 2^8), write
+//     P as f16 into a 64B-swizzled tile and sum the same rounded P into l.
+// The k_scale folds into the score scale and v_scale into the output.  The two CTAs
+// of an item (one per V half) both compute S; the tile is read from HBM once and
 // from L2 by the second CTA.  Every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -40,22 +47,32 @@ namespace {
 constexpr int kTokM = 32;                       // tokens per tile
 constexpr int kDqkM = 576, kDvM = 512, kDvHalf = 256, kRowsM = 128;
 constexpr int kQBoxes = kDqkM / 64;             // 9 boxes of 64 columns
-constexpr uint32_t kQBytes = kRowsM * kDqkM * 2;        // 147456
+constexpr int kQHeadBoxes = 6;                  // Q[:, 0:384] moves to TMEM
+constexpr uint32_t kQBytes = kRowsM * kDqkM * 2;        // 147456 (TMA landing)
+constexpr uint32_t kQBoxBytes = kRowsM * 128;           // 16384
 constexpr uint32_t kKTileBytes = kTokM * kDqkM * 2;     // 36864
+constexpr uint32_t kVTileBytes = kTokM * kDvHalf * 2;   // 16384
 constexpr uint32_t kPBytes = kRowsM * kTokM * 2;        // 8192
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK0 = kOffQ + kQBytes;
+// Shared memory: Q tail (3 boxes) | K0 | K1 | V0 | V1 | V2 | P | barriers.  Q lands
+// by TMA with its 6 head boxes over K0..V1, which are free until the head has
+// moved to TMEM.
+constexpr uint32_t kOffQT = 0;
+constexpr uint32_t kOffK0 = kOffQT + 3 * kQBoxBytes;    // 49152
 constexpr uint32_t kOffK1 = kOffK0 + kKTileBytes;
-constexpr uint32_t kOffP = kOffK1 + kKTileBytes;
-constexpr uint32_t kOffBar = kOffP + kPBytes;          // 229376
-constexpr uint32_t kSmemMLA = kOffBar + 256 + 1024;    // barriers + alignment slack
-constexpr int kThreadsM = 160;                  // 4 row warps + 1 control warp
+constexpr uint32_t kOffV0 = kOffK1 + kKTileBytes;
+constexpr uint32_t kOffP = kOffV0 + 3 * kVTileBytes;
+constexpr uint32_t kOffQHead = kOffK0;                  // 6 landing boxes
+constexpr uint32_t kOffBar = kOffP + kPBytes;
+constexpr uint32_t kSmemMLA = kOffBar + 256 + 1024;     // barriers + alignment slack
+static_assert(kOffQHead + kQHeadBoxes * kQBoxBytes <= kOffP, "Q head landing overlaps P");
+constexpr int kThreadsM = 288;                  // 4 row + 4 converter + 1 control warp
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256;      // S buffer b at kColS + 32 b
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;  // S buffer b at kColS + 32 b
 constexpr float kLazyRescale = 8.f;             // log2 units
 
 // mbarrier slots (uint64 each) at kOffBar
-enum { BQ = 0, BK0 = 1, BK1 = 2, BS0 = 3, BS1 = 4, BP = 5, BPV0 = 6, BPV1 = 7, BSLOT = 8 };
+enum { BQ = 0, BQREADY = 1, BK0 = 2, BK1 = 3, BS0 = 4, BS1 = 5, BP = 6, BPV0 = 7, BPV1 = 8, BPV2 = 9,
+       BSLOT = 10 };
 
 struct MLAParams {
   const uint8_t *k_pool;
@@ -74,16 +91,33 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
          (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(swz & 7u) << 61);
 }
-// kind::f16 instruction descriptor: f32 accumulate, bf16 A and B.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
-         (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+// kind::f16 instruction descriptor: f32 accumulate, f16 A and B.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) | (uint32_t(N >> 3) << 17) |
+         (uint32_t(M >> 4) << 24);
 }
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// A operand in TMEM (f16 pairs per 32-bit column, row m in lane m), accumulating.
+__device__ __forceinline__ void umma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Accumulating form (enable-input-d always set).
+__device__ __forceinline__ void umma_acc(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -128,15 +162,34 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+__device__ __forceinline__ uint32_t pack2_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
 }
-// 8 e4m3 codes -> 8 bf16, exact.
+__device__ __forceinline__ float f16_lo(uint32_t w) { return __low2float(*reinterpret_cast<__half2 *>(&w)); }
+__device__ __forceinline__ float f16_hi(uint32_t w) { return __high2float(*reinterpret_cast<__half2 *>(&w)); }
+// Two e4m3 codes (low 16 bits) -> f16x2, exact (hardware conversion).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 lo;\n\tmov.b32 {lo, _}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(h2) : "r"(w));
+  return h2;
+}
+// 8 e4m3 codes -> 8 f16, exact.
 __device__ __forceinline__ uint4 cvt8(uint32_t w0, uint32_t w1) {
-  const float2 a = e4m3x2_to_float2(w0 & 0xffffu), b = e4m3x2_to_float2(w0 >> 16);
-  const float2 c = e4m3x2_to_float2(w1 & 0xffffu), d = e4m3x2_to_float2(w1 >> 16);
-  return make_uint4(pack2_bf16(a.x, a.y), pack2_bf16(b.x, b.y), pack2_bf16(c.x, c.y), pack2_bf16(d.x, d.y));
+  return make_uint4(e4m3x2_to_f16x2(w0 & 0xffffu), e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 & 0xffffu),
+                    e4m3x2_to_f16x2(w1 >> 16));
+}
+// 8 bf16 -> 8 f16 (exact inside the f16 range); *bad is set on overflow.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool *bad) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float a = bf16_lo(w[k]), b = bf16_hi(w[k]);
+    o[k] = pack2_f16(a, b);
+    *bad |= (fabsf(a) > 65504.f) | (fabsf(b) > 65504.f);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __global__ void __launch_bounds__(kThreadsM, 1)
@@ -155,6 +208,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 
   if (tid == 0) {
     mbar_init(bar(BQ), 1);
+    mbar_init(bar(BQREADY), 256);
     mbar_init(bar(BK0), 128);
     mbar_init(bar(BK1), 128);
     mbar_init(bar(BS0), 1);
@@ -162,9 +216,10 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     mbar_init(bar(BP), 128);
     mbar_init(bar(BPV0), 1);
     mbar_init(bar(BPV1), 1);
+    mbar_init(bar(BPV2), 1);
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == 8) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -174,55 +229,78 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ control thread
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(BQ), kQBytes);
 #pragma unroll 1
-      for (int b = 0; b < kQBoxes; ++b)
-        tma_load_3d(smem_u32(sm + kOffQ + b * (kRowsM * 128)), &tmQ, b * 64, 0, it.q_index, bar(BQ));
-      bool ok = mbar_wait(bar(BQ), 0, p.fault);
-      const uint32_t id_qk = idesc_bf16(128, kTokM, false, false);
-      const uint32_t id_pv = idesc_bf16(128, kDvHalf, false, true);
-      const uint32_t q_base = smem_u32(sm + kOffQ);
-      const uint32_t p_base = smem_u32(sm + kOffP);
+      for (int b = 0; b < kQBoxes; ++b) {
+        const uint32_t dst = b < kQHeadBoxes ? kOffQHead + b * kQBoxBytes : kOffQT + (b - kQHeadBoxes) * kQBoxBytes;
+        tma_load_3d(smem_u32(sm + dst), &tmQ, b * 64, 0, it.q_index, bar(BQ));
+      }
+      bool ok = mbar_wait(bar(BQREADY), 0, p.fault);  // head in TMEM, tail in f16
+      tc_fence_after();
+      const uint32_t id_qk = idesc_f16(128, kTokM, false, false);
+      const uint32_t id_pv = idesc_f16(128, kDvHalf, false, true);
+      // Base descriptors, built once; operand steps add compile-time offsets (>> 4)
+      // to the start-address field, which never carries out of it (< 256 KB).
+      const uint64_t qtd = smem_desc(smem_u32(sm + kOffQT), 16, 1024, 2);
+      const uint64_t kd0 = smem_desc(smem_u32(sm + kOffK0), 16, 1024, 2);
+      const uint64_t kd1 = smem_desc(smem_u32(sm + kOffK1), 16, 1024, 2);
+      const uint64_t pd = smem_desc(smem_u32(sm + kOffP), 16, 512, 4);
+      const uint64_t vd0 = smem_desc(smem_u32(sm + kOffV0), kTokM * 128, 1024, 2);
       for (int i = 0; ok && i <= n_tiles; ++i) {
-        if (i < n_tiles) {  // S(i) = Q K(i)^T
+        if (i < n_tiles) {  // S(i) = Q K(i)^T: 24 steps with A in TMEM, 12 from shared memory
           const int b = i & 1;
           ok = mbar_wait(bar(BK0 + b), uint32_t(i >> 1) & 1u, p.fault);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t k_base = smem_u32(sm + (b ? kOffK1 : kOffK0));
-#pragma unroll 4
-          for (int k16 = 0; k16 < kDqkM / 16; ++k16) {
-            const uint32_t ko = (k16 & 3) * 32u;  // 16 columns within the 64-column box
-            umma(tmem + kColS + 32 * b,
-                 smem_desc(q_base + (k16 >> 2) * (kRowsM * 128) + ko, 16, 1024, 2),
-                 smem_desc(k_base + (k16 >> 2) * (kTokM * 128) + ko, 16, 1024, 2), id_qk, k16 > 0);
-          }
+          const uint64_t kdb = b ? kd1 : kd0;
+          const uint32_t d_s = tmem + kColS + 32 * b;
+          umma_tmem_a(d_s, tmem + kColQ, kdb, id_qk, 0);
+#pragma unroll
+          for (int k16 = 1; k16 < 4 * kQHeadBoxes; ++k16)
+            umma_tmem_a(d_s, tmem + kColQ + 8 * k16, kdb + (((k16 >> 2) * (kTokM * 128) + (k16 & 3) * 32) >> 4),
+                        id_qk, 1);
+#pragma unroll
+          for (int k16 = 4 * kQHeadBoxes; k16 < kDqkM / 16; ++k16)
+            umma_acc(d_s, qtd + ((((k16 >> 2) - kQHeadBoxes) * kQBoxBytes + (k16 & 3) * 32) >> 4),
+                     kdb + (((k16 >> 2) * (kTokM * 128) + (k16 & 3) * 32) >> 4), id_qk);
           umma_commit(bar(BS0 + b));
         }
         if (i > 0) {  // O += P(i-1) V(i-1)
-          const int j = i - 1, b = j & 1;
+          const int j = i - 1, vb = j % 3;
           ok = mbar_wait(bar(BP), uint32_t(j) & 1u, p.fault);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t v_base = smem_u32(sm + (b ? kOffK1 : kOffK0)) + half * 4 * (kTokM * 128);
+          const uint64_t vdb = vd0 + ((vb * kVTileBytes) >> 4);
+          umma(tmem + kColO, pd, vdb, id_pv, j > 0);
 #pragma unroll
-          for (int k = 0; k < kTokM / 16; ++k)
-            umma(tmem + kColO, smem_desc(p_base + k * 32, 16, 512, 4),
-                 smem_desc(v_base + k * 16 * 128, kTokM * 128, 1024, 2), id_pv, (j > 0 || k > 0));
-          umma_commit(bar(BPV0 + b));
+          for (int k = 1; k < kTokM / 16; ++k)
+            umma_acc(tmem + kColO, pd + ((k * 32) >> 4), vdb + ((k * 16 * 128) >> 4), id_pv);
+          umma_commit(bar(BPV0 + vb));
         }
       }
     }
-  } else {
-    // ---------------------------------------------------- row / converter threads
-    const int row = tid;                          // head = TMEM lane
-    const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-    const int ct = tid >> 2, cq = tid & 3;        // converter: token ct, 144-column quarter cq
-    uint4 raw[9];
-    auto fetch = [&](int i) {                     // 144 fp8 of token ct of tile i
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ converter warps
+    const int ctid = tid - 128;
+    const int ct = ctid >> 2, cq = ctid & 3;      // token ct of a tile, 144-column quarter cq
+    // Q tail: bf16 -> f16 in place (same 2-byte swizzled layout)
+    bool ok = mbar_wait(bar(BQ), 0, p.fault);
+    bool bad = false;
+    if (ok) {
+      for (int c = ctid; c < 3 * int(kQBoxBytes) / 16; c += 128) {
+        uint4 *q16 = reinterpret_cast<uint4 *>(sm + kOffQT) + c;
+        *q16 = bf16x8_to_f16x8(*q16, &bad);
+      }
+    }
+    if (bad) atomicOr(p.fault, PSD_FAULT_RANGE);
+    fence_proxy_async();
+    mbar_arrive(bar(BQREADY));
+    // the K/V buffers hold the Q head until the row warps have moved it to TMEM
+    ok = ok && mbar_wait(bar(BQREADY), 0, p.fault);
+    auto fetch = [&](uint4 (&raw)[9], int i) {  // 144 fp8 of token ct of tile i
       const int tok = i * kTokM + ct;
       if (i < n_tiles && tok < it.n_tokens) {
         const int id = __ldg(p.page_indices + it.page_off + tok / P);
@@ -238,39 +316,73 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 #pragma unroll
       for (int k = 0; k < 9; ++k) raw[k] = make_uint4(0u, 0u, 0u, 0u);
     };
-    auto convert = [&](int i) {                   // raw -> bf16 K tile i (128B swizzle)
+    // Tile i is widened from `raw` into K buffer i%2 (all 576 columns, for QK) and
+    // V buffer i%3 (this CTA's 256 V columns, for PV); `raw` is then refilled with
+    // tile i + 2, so two tiles' loads are always in flight.
+    auto step = [&](uint4 (&raw)[9], int i) {
+      if (i >= 2) {  // QK(i-2) released the K buffer
+        ok = mbar_wait(bar(BS0 + (i & 1)), uint32_t((i - 2) >> 1) & 1u, p.fault);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+      }
+      if (i >= 3) {  // PV(i-3) released the V buffer
+        ok = mbar_wait(bar(BPV0 + i % 3), uint32_t((i - 3) / 3) & 1u, p.fault);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+      }
       uint8_t *kt = sm + ((i & 1) ? kOffK1 : kOffK0);
-      const uint32_t w[36] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w,
-                              raw[2].x, raw[2].y, raw[2].z, raw[2].w, raw[3].x, raw[3].y, raw[3].z, raw[3].w,
-                              raw[4].x, raw[4].y, raw[4].z, raw[4].w, raw[5].x, raw[5].y, raw[5].z, raw[5].w,
-                              raw[6].x, raw[6].y, raw[6].z, raw[6].w, raw[7].x, raw[7].y, raw[7].z, raw[7].w,
-                              raw[8].x, raw[8].y, raw[8].z, raw[8].w};
+      uint8_t *vt = sm + kOffV0 + (i % 3) * kVTileBytes;
 #pragma unroll
       for (int j = 0; j < 18; ++j) {
         const int c = cq * 18 + j;                // 8-column chunk of the 576
-        *reinterpret_cast<uint4 *>(kt + (c >> 3) * (kTokM * 128) + ct * 128 +
-                                   (((c & 7) ^ (ct & 7)) << 4)) = cvt8(w[2 * j], w[2 * j + 1]);
+        const uint4 r = raw[j >> 1];
+        const uint4 h = cvt8((j & 1) ? r.z : r.x, (j & 1) ? r.w : r.y);
+        const uint32_t sw = (((c & 7) ^ (ct & 7)) << 4) + ct * 128;
+        *reinterpret_cast<uint4 *>(kt + (c >> 3) * (kTokM * 128) + sw) = h;
+        const int cv = c - 32 * half;             // V column chunk of this CTA's half
+        if (cv >= 0 && cv < 32) *reinterpret_cast<uint4 *>(vt + (cv >> 3) * (kTokM * 128) + sw) = h;
       }
       fence_proxy_async();
       mbar_arrive(bar(BK0 + (i & 1)));
+      fetch(raw, i + 2);
+      return true;
     };
-
-    float m_ref = neg_inf(), l_sum = 0.f;
-    bool ok = true;
-    if (n_tiles > 0) {
-      fetch(0);
-      convert(0);
-      fetch(1);
+    uint4 rawA[9], rawB[9];
+    fetch(rawA, 0);
+    fetch(rawB, 1);
+    for (int i = 0; i < n_tiles && ok; i += 2) {
+      if (!step(rawA, i)) break;
+      if (i + 1 < n_tiles && !step(rawB, i + 1)) break;
     }
-    for (int i = 0; i < n_tiles && ok; ++i) {
-      // convert tile i+1 once PV(i-1) has released its buffer
-      if (i + 1 < n_tiles) {
-        if (i >= 1) ok = mbar_wait(bar(BPV0 + ((i - 1) & 1)), uint32_t((i - 1) >> 1) & 1u, p.fault);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        convert(i + 1);
-        fetch(i + 2);
+  } else {
+    // ------------------------------------------------------------------ row warps
+    const int row = tid;                          // head = TMEM lane
+    const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+    // Q head (columns 0..383) of this row: bf16 from the landing boxes -> f16 pairs
+    // -> TMEM columns kColQ + 32 b (box b), the layout the MMA reads A from.
+    bool ok = mbar_wait(bar(BQ), 0, p.fault);
+    if (__all_sync(0xffffffffu, ok)) {
+      bool bad = false;
+#pragma unroll 1
+      for (int b = 0; b < kQHeadBoxes; ++b) {
+        uint32_t qw[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(sm + kOffQHead + b * kQBoxBytes + row * 128 +
+                                                           ((c ^ (row & 7)) << 4));
+          const uint4 h = bf16x8_to_f16x8(v, &bad);
+          qw[4 * c] = h.x;
+          qw[4 * c + 1] = h.y;
+          qw[4 * c + 2] = h.z;
+          qw[4 * c + 3] = h.w;
+        }
+        PSD_TMEM_ST32(lane_base + kColQ + 32 * b, qw);
       }
-      // scores of tile i
+      tmem_st_wait();
+      if (bad) atomicOr(p.fault, PSD_FAULT_RANGE);
+    }
+    tc_fence_before();
+    mbar_arrive(bar(BQREADY));
+    float m_ref = neg_inf(), l_sum = 0.f;
+    for (int i = 0; i < n_tiles && ok; ++i) {
       ok = mbar_wait(bar(BS0 + (i & 1)), uint32_t(i >> 1) & 1u, p.fault);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -287,7 +399,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       }
       // PV(i-1) must be done before P is rewritten or O rescaled
       if (i >= 1) {
-        ok = mbar_wait(bar(BPV0 + ((i - 1) & 1)), uint32_t((i - 1) >> 1) & 1u, p.fault);
+        ok = mbar_wait(bar(BPV0 + (i - 1) % 3), uint32_t((i - 1) / 3) & 1u, p.fault);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
       }
@@ -310,12 +422,12 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         }
         m_ref = m_new;
       }
-      // P = 2^(s - m_ref) as bf16 (64B-swizzled [128 x 32]); l sums the rounded P
+      // P = 2^(s - m_ref) as f16 (64B-swizzled [128 x 32]); l sums the rounded P
       uint32_t pk[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        pk[c] = pack2_bf16(ex2(s[2 * c] - m_ref), ex2(s[2 * c + 1] - m_ref));
-        l_sum += bf16_lo(pk[c]) + bf16_hi(pk[c]);
+        pk[c] = pack2_f16(ex2(s[2 * c] - m_ref), ex2(s[2 * c + 1] - m_ref));
+        l_sum += f16_lo(pk[c]) + f16_hi(pk[c]);
       }
       uint8_t *prow = sm + kOffP;
 #pragma unroll
@@ -331,7 +443,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // epilogue: O / l for this row and V half
     if (ok && n_tiles > 0) {
       const int j = n_tiles - 1;
-      ok = mbar_wait(bar(BPV0 + (j & 1)), uint32_t(j >> 1) & 1u, p.fault);
+      ok = mbar_wait(bar(BPV0 + j % 3), uint32_t(j / 3) & 1u, p.fault);
     }
     if (__all_sync(0xffffffffu, ok) && n_tiles > 0) {
       tc_fence_after();
@@ -354,7 +466,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
   }
