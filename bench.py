@@ -35,6 +35,19 @@ import synth  # noqa: E402
 L2_FLUSH_BYTES = 256 << 20
 NOMINAL_HBM_GBS = 8000.0
 
+# DRAM bytes (read + write) of one flat-decode launch of the partial kernel, from the
+# ncu capture summarised in profiles/partial_tcs_flat_decode.md.  Reported only while
+# the kernel source is the one the counters were taken on.
+TRAFFIC_SOURCE = os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", "partial_tcs.cu")
+TRAFFIC_SHA256 = "1b7c34039b64ef428dd3b5c7c6c5b0d941645b2e745cf77d847d3fb28c5242ef"
+TRAFFIC_BYTES = 316107008 + 1255936
+
+
+def partial_traffic():
+    import hashlib
+    with open(TRAFFIC_SOURCE, "rb") as f:
+        return TRAFFIC_BYTES if hashlib.sha256(f.read()).hexdigest() == TRAFFIC_SHA256 else None
+
 
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -431,7 +444,7 @@ def run_ours(args):
                          "kernel": "partial_tcs_kernel<128> (split-KV partial, 16-row-group tensor cores)",
                          "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "peak_source": peak_src + " copy bandwidth",
-                         "traffic": None, "algorithmic_bytes_per_launch": algo,
+                         "traffic": partial_traffic(), "algorithmic_bytes_per_launch": algo,
                          "launch_ms": round(k_ms, 5)},
             "merge_kernel": {"kernel": "merge_states_kernel<1>", "achieved": round(merge_gbs, 1),
                              "unit": "GB/s", "frac": round(merge_gbs / hbm, 4),
