@@ -473,8 +473,9 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
     if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cascade join: %s", cudaGetErrorString(e));
   }
   time_mark(ctx, 4, s);
+  const bool merge_follows_partial = !(M > 0 && !fused) && !ctx->timing;
   st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq,
-                    args->Dv, o, lse, ctx->dev, s);
+                    args->Dv, o, lse, ctx->dev, s, merge_follows_partial);
   time_mark(ctx, 5, s);
   ctx->tev_used[0] = ctx->timing && M > 0 && !fused;
   ctx->tev_used[1] = ctx->timing;

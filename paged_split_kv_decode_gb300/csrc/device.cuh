@@ -67,6 +67,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
   return true;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start once every block of the kernel before it on the stream
+// has called dependents_may_launch(); it must call wait_for_prior_grid() before it
+// touches anything that kernel writes (the wait returns at once when there is no
+// such kernel).
+__device__ __forceinline__ void dependents_may_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void wait_for_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));

@@ -60,8 +60,10 @@ psd_status launch_partial_mla(const PartialLaunch &p, const DeviceInfo &dev, cud
 bool partial_tc_supports(const PartialLaunch &p);
 psd_status launch_partial_tc(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
 
+// after_partial: the launch directly follows a partial kernel on stream s (no event
+// or copy between them), so it may start early and wait for that grid on the device.
 psd_status launch_merge(const float *v_in, const float *lse_in, const int32_t *o_indptr,
                         int64_t num_out, int32_t H, int32_t D, float *v_out, float *lse_out,
-                        const DeviceInfo &dev, cudaStream_t s);
+                        const DeviceInfo &dev, cudaStream_t s, bool after_partial = false);
 
 }  // namespace psd

@@ -154,7 +154,7 @@ extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_arg
   L1.fault = fault;
   if ((st = launch_partial(L1, ctx->dev, s)) != PSD_OK) return st;
   st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq,
-                    args->Dv, o, lse, ctx->dev, s);
+                    args->Dv, o, lse, ctx->dev, s, true);
   if (st != PSD_OK) return st;
   if (fault_bits_dev) {
     e = cudaMemcpyAsync(fault_bits_dev, fault, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);

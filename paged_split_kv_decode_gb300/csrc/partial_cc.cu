@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(kWarps * 32, G <= 4 ? 4 : 2)
   constexpr int HL = LPT / G;        // lanes per head after the transpose reduce
   static_assert(G <= LPT, "one score per lane needs G <= D / 8");
   extern __shared__ __align__(1024) uint8_t smem[];
+  dependents_may_launch();  // the merge that follows only waits for this grid
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const psd_work_item it = p.items[p.order ? __ldg(p.order + blockIdx.x) : blockIdx.x];

@@ -195,6 +195,7 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool *bad) {
 __global__ void __launch_bounds__(kThreadsM, 1)
     partial_mla_kernel(const __grid_constant__ CUtensorMap tmQ, const MLAParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  dependents_may_launch();  // the merge that follows only waits for this grid
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + BSLOT);

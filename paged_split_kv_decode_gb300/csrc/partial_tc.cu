@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(TCShape<DQK, DV, FP8, LATENT>::THREADS)
     partial_tc_kernel(const TCParams p) {
   using S = TCShape<DQK, DV, FP8, LATENT>;
   extern __shared__ __align__(128) uint8_t smem[];
+  dependents_may_launch();  // the merge that follows only waits for this grid
   uint8_t *sQ = smem;
   uint8_t *sStage = smem + S::Q_BYTES;
   uint8_t *sCvt = sStage + kStagesTC * S::STAGE;

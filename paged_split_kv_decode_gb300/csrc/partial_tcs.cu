@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
   constexpr int NT = D / 8;                       // n8 tiles of the output
   constexpr uint32_t TILE_BYTES = kTileTok * D * 2;
   extern __shared__ __align__(1024) uint8_t smem[];
+  dependents_may_launch();  // the merge that follows only waits for this grid
 
   // 128-byte-swizzled TMA boxes need 1024-byte aligned destinations.
   uint8_t *base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
