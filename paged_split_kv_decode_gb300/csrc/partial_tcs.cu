@@ -311,7 +311,9 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
     if (i + kStagesS < my_tiles) issue(i + kStagesS);
   }
 
-  // ---- merge the four warps through shared memory (rings no longer used)
+  // ---- merge the four warps through shared memory (rings no longer used).  Only
+  // the live rows are staged; each row's 8-float blocks are XOR-rotated by row % 4
+  // so the fragment stores of four rows fall in four bank groups.
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
@@ -324,35 +326,47 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int r = (lane >> 2) + 8 * h;
-    float *dst = red_o + (size_t(warp) * 16 + r) * D + (lane & 3) * 2;
+    if (r < rows) {
+      float *dst = red_o + (size_t(warp) * 16 + r) * D;
+      const int rot = (r & 3) << 3;
 #pragma unroll
-    for (int n = 0; n < NT; ++n)
-      *reinterpret_cast<float2 *>(dst + n * 8) = make_float2(o[n][2 * h], o[n][2 * h + 1]);
-    if ((lane & 3) == 0) {
-      red_m[warp * 16 + r] = m_run[h];
-      red_l[warp * 16 + r] = l_run[h];
+      for (int n = 0; n < NT; ++n)
+        *reinterpret_cast<float2 *>(dst + ((n * 8 + (lane & 3) * 2) ^ rot)) =
+            make_float2(o[n][2 * h], o[n][2 * h + 1]);
+      if ((lane & 3) == 0) {
+        red_m[warp * 16 + r] = m_run[h];
+        red_l[warp * 16 + r] = l_run[h];
+      }
     }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < rows * D; idx += kWarpsS * 32) {
-    const int r = idx / D, d = idx - r * D;
+  constexpr int D4 = D / 4;
+  for (int idx = threadIdx.x; idx < rows * D4; idx += kWarpsS * 32) {
+    const int r = idx / D4, d = (idx - r * D4) * 4;
     const int g = row0 + r;
     float M = neg_inf();
 #pragma unroll
     for (int w = 0; w < kWarpsS; ++w) M = fmaxf(M, red_m[w * 16 + r]);
-    float L = 0.f, O = 0.f;
+    float L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kWarpsS; ++w) {
       const float sc = ex2(red_m[w * 16 + r] - M);
       L = fmaf(sc, red_l[w * 16 + r], L);
-      O = fmaf(sc, red_o[(size_t(w) * 16 + r) * D + d], O);
+      const float4 v = *reinterpret_cast<const float4 *>(red_o + (size_t(w) * 16 + r) * D +
+                                                         (d ^ ((r & 3) << 3)));
+      O.x = fmaf(sc, v.x, O.x);
+      O.y = fmaf(sc, v.y, O.y);
+      O.z = fmaf(sc, v.z, O.z);
+      O.w = fmaf(sc, v.w, O.w);
     }
     const bool live = M != neg_inf();
+    const float f = live ? p.v_scale / L : 0.f;
     const int m = g / p.Gm;
     const int row = it.q_index >= 0 ? it.out_row : __ldg(p.member_row_base + m) + it.out_row;
     const int head = kv * p.Gm + (g - m * p.Gm);
     const int64_t orow = int64_t(row) * p.Hq_req + head;
-    p.v_out[orow * p.Dv + d] = live ? O / L * p.v_scale : 0.f;
+    *reinterpret_cast<float4 *>(p.v_out + orow * p.Dv + d) = make_float4(O.x * f, O.y * f, O.z * f, O.w * f);
     if (d == 0) p.lse_out[orow] = live ? M + log2f(L) : neg_inf();
   }
 }
