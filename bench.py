@@ -39,8 +39,8 @@ NOMINAL_HBM_GBS = 8000.0
 # ncu capture summarised in profiles/partial_tcs_flat_decode.md.  Reported only while
 # the kernel source is the one the counters were taken on.
 TRAFFIC_SOURCE = os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", "partial_tcs.cu")
-TRAFFIC_SHA256 = "1b7c34039b64ef428dd3b5c7c6c5b0d941645b2e745cf77d847d3fb28c5242ef"
-TRAFFIC_BYTES = 316107008 + 1255936
+TRAFFIC_SHA256 = "1b7f365523ca4dd3a85bb4a7eb725cf35520dc07f91f6c19d02f00ed1d98dbc7"
+TRAFFIC_BYTES = 316073728 + 1193984
 
 
 def partial_traffic():
