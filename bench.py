@@ -328,6 +328,32 @@ def barrier(world):
     torch.cuda.synchronize()
 
 
+def host_plan_us(w, reps=200):
+    """Host detection + cascade planning per call: from scratch (psd_plan_decode) and
+    as a plan-cache hit (the same table on the next layer)."""
+    import paged_split_kv_decode_gb300 as psd
+    t = psd.HostTable(w.page_indptr, w.page_indices, w.last_page_len, w.page_size)
+    plan = psd.plan_decode(t, w.tile_tokens, 1, w.min_shared_pages, w.min_members)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        psd.plan_decode(t, w.tile_tokens, 1, w.min_shared_pages, w.min_members, plan)
+    scratch = (time.perf_counter() - t0) / reps
+    cache = psd.PlanCache(4)
+    cache.lookup(t, w.tile_tokens, 1, w.min_shared_pages, w.min_members)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        cache.lookup(t, w.tile_tokens, 1, w.min_shared_pages, w.min_members)
+    hit = (time.perf_counter() - t0) / reps
+    cache.lookup(t, w.tile_tokens, 1, w.min_shared_pages, w.min_members, generation=1)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        cache.lookup(t, w.tile_tokens, 1, w.min_shared_pages, w.min_members, generation=1)
+    gen_hit = (time.perf_counter() - t0) / reps
+    return {"plan_decode": round(scratch * 1e6, 1), "plan_cache_hit": round(hit * 1e6, 1),
+            "plan_cache_generation_hit": round(gen_hit * 1e6, 1), "page_ids": int(w.page_indptr[-1]),
+            "note": "per call, through the Python binding"}
+
+
 def run_ours(args):
     rank, world, local = dist_setup(args.gpus)
     torch.cuda.set_device(local)
@@ -391,6 +417,7 @@ def run_ours(args):
             "flat_kernels_ms": {k: round(v, 5) for k, v in kf.items()},
             "cascade_kernels_ms": {k: round(v, 5) for k, v in kc.items()},
             "stats": st,
+            "host_plan_us": host_plan_us(wc),
         }
         del flat_arm, casc_arm
     if not args.quick and args.workload in ("all", "mla"):

@@ -226,6 +226,44 @@ psd_status psd_plan_decode(const psd_page_table *host, int32_t tile_tokens, int3
 psd_status psd_plan_capacity(const psd_page_table *host, int32_t *batch_capacity,
                              int32_t *item_capacity);
 
+/* Plan cache (mlxcel PR #1004, Left out / unsure: detection re-runs per layer and
+ * per step; a CascadePlan slot in the plan cache is the named follow-up).  The key
+ * is everything psd_plan_decode reads: the resolved enable switch, both thresholds,
+ * tile_tokens, page_size, batch and the full contents of page_indptr, page_indices
+ * and last_page_len, since a split-KV plan depends on KV lengths as well as on the
+ * page rows (FreeToken issue #750, Layer-major prefill for offloaded MoE, Attention
+ * batching section: a cache keyed by rows alone was a bug).  A hit returns exactly
+ * the plan psd_plan_decode would compute.
+ *
+ * The cache owns its plans: `capacity` entries in [1, 1024], least recently used
+ * evicted.  It is host-only, allocates host memory only, and is not thread-safe (one
+ * cache per thread).  psd_plan_cache_destroy(NULL) is a no-op. */
+typedef struct psd_plan_cache psd_plan_cache;
+psd_status psd_plan_cache_create(psd_plan_cache **cache, int32_t capacity);
+psd_status psd_plan_cache_destroy(psd_plan_cache *cache);
+/* Looks `host` up, planning it on a miss (same arguments and errors as
+ * psd_plan_decode; an invalid table is rejected before its arrays are read).
+ * *plan points into the cache and stays valid until the next lookup on this cache or
+ * its destruction; *hit (nullable) is 1 when no planning ran. */
+psd_status psd_plan_cache_lookup(psd_plan_cache *cache, const psd_page_table *host,
+                                 int32_t tile_tokens, int32_t enable, int32_t min_shared_pages,
+                                 int32_t min_members, const psd_cascade_plan **plan, int32_t *hit);
+/* As psd_plan_cache_lookup, with a caller-kept generation number for the page table
+ * (e.g. one per decode step, shared by every layer).  When generation >= 0 and an
+ * entry was stored or last matched under the same generation with the same
+ * tile_tokens, resolved enable, thresholds and batch, that entry is returned without
+ * reading the table's arrays: O(1) instead of O(page ids).  The caller must change
+ * the generation whenever any array of the table changes; reusing a generation for a
+ * different table returns that generation's plan.  generation < 0 is
+ * psd_plan_cache_lookup. */
+psd_status psd_plan_cache_lookup_gen(psd_plan_cache *cache, int64_t generation,
+                                     const psd_page_table *host, int32_t tile_tokens,
+                                     int32_t enable, int32_t min_shared_pages, int32_t min_members,
+                                     const psd_cascade_plan **plan, int32_t *hit);
+/* Lookups answered from the cache, lookups that planned, and live entries (all nullable). */
+psd_status psd_plan_cache_stats(const psd_plan_cache *cache, int64_t *hits, int64_t *misses,
+                                int32_t *entries);
+
 /* Workspace bytes for cascade_decode / paged_decode_partial: work lists and
  * merge groups for up to `num_items` items and `batch` requests, plus partial
  * rows `num_rows` x Hq x Dv (pass 0 rows for paged_decode_partial). */

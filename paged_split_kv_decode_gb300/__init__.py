@@ -3,7 +3,8 @@
 The compute lives in ``libpsd.so`` (hand-written CUDA behind the C ABI declared in
 ``include/psd.h``); ``api`` is a thin ctypes binding with the same names.
 """
-from .api import (Context, HostTable, Plan, build_cascade_plan, cascade_decode,  # noqa: F401
+from .api import (CachedPlan, Context, HostTable, Plan, PlanCache, build_cascade_plan,  # noqa: F401
+                  cascade_decode,
                   cascade_decode_no_alloc,
                   cascade_env_enabled, check_device_error, decode_args, detect_shared_prefix,
                   merge_states, paged_decode_partial, plan_decode, split_plan, workspace_bytes,

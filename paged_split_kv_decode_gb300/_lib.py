@@ -23,6 +23,8 @@ EXPORTS = [
     "psd_split_plan", "detect_shared_prefix", "build_cascade_plan", "psd_plan_decode",
     "psd_plan_capacity", "psd_workspace_bytes", "paged_decode_partial", "merge_states",
     "cascade_decode", "psd_check_device_error", "cascade_decode_no_alloc",
+    "psd_plan_cache_create", "psd_plan_cache_destroy", "psd_plan_cache_lookup", "psd_plan_cache_lookup_gen",
+    "psd_plan_cache_stats",
 ]
 
 
@@ -91,6 +93,13 @@ def _sig(lib):
                                        C.POINTER(CascadePlan)]
     lib.psd_plan_decode.argtypes = [C.POINTER(PageTable), i32, i32, i32, i32, C.POINTER(CascadePlan)]
     lib.psd_plan_capacity.argtypes = [C.POINTER(PageTable), P_i32, P_i32]
+    lib.psd_plan_cache_create.argtypes = [C.POINTER(V), i32]
+    lib.psd_plan_cache_destroy.argtypes = [V]
+    lib.psd_plan_cache_lookup.argtypes = [V, C.POINTER(PageTable), i32, i32, i32, i32,
+                                          C.POINTER(C.POINTER(CascadePlan)), P_i32]
+    lib.psd_plan_cache_lookup_gen.argtypes = [V, i64, C.POINTER(PageTable), i32, i32, i32, i32,
+                                              C.POINTER(C.POINTER(CascadePlan)), P_i32]
+    lib.psd_plan_cache_stats.argtypes = [V, C.POINTER(i64), C.POINTER(i64), P_i32]
     lib.psd_workspace_bytes.argtypes = [i32, i32, i64, i32, i32]
     lib.psd_workspace_bytes.restype = C.c_size_t
     lib.paged_decode_partial.argtypes = [V, C.POINTER(DecodeArgs), C.POINTER(WorkItem), i32, V, V,

@@ -193,6 +193,87 @@ class Plan:
         raise AttributeError(name)
 
 
+class CachedPlan:
+    """A plan owned by a PlanCache (a view of its psd_cascade_plan); valid until the
+    next lookup on that cache.  Same read accessors as Plan."""
+
+    def __init__(self, ptr, hit: bool):
+        self.c = ptr.contents
+        self.hit = hit
+
+    def _i32(self, p, n):
+        return [int(x) for x in np.ctypeslib.as_array(C.cast(p, L.P_i32), shape=(max(n, 1),))[:n]]
+
+    @property
+    def members(self):
+        return self._i32(self.c.members, self.c.num_members)
+
+    @property
+    def member_row_base(self):
+        return self._i32(self.c.member_row_base, self.c.num_members)
+
+    @property
+    def o_indptr(self):
+        return self._i32(self.c.o_indptr, self.c.batch + 1)
+
+    def _items(self, arr, n):
+        if n == 0:
+            return np.zeros((0, 4), dtype=np.int32)
+        return np.ctypeslib.as_array(C.cast(arr, L.P_i32), shape=(n * 4,)).reshape(n, 4).copy()
+
+    @property
+    def l0_items(self):
+        return self._items(self.c.l0_items, self.c.l0_num_items)
+
+    @property
+    def l1_items(self):
+        return self._items(self.c.l1_items, self.c.l1_num_items)
+
+    @property
+    def num_items(self):
+        return self.c.l0_num_items + self.c.l1_num_items
+
+    def __getattr__(self, name):
+        if name in ("num_members", "shared_pages", "decline_reason", "num_rows", "tile_tokens",
+                    "batch", "page_size", "l0_num_items", "l1_num_items"):
+            return getattr(self.c, name)
+        raise AttributeError(name)
+
+
+class PlanCache:
+    """psd_plan_cache: plans memoised by page-table contents and KV lengths."""
+
+    def __init__(self, capacity: int = 8):
+        self._h = C.c_void_p()
+        L.check(L.load().psd_plan_cache_create(C.byref(self._h), int(capacity)))
+
+    def lookup(self, table: HostTable, tile_tokens: int, enable: int = 1, min_shared_pages: int = 16,
+               min_members: int = 2, generation: int = -1) -> CachedPlan:
+        """psd_plan_cache_lookup, or psd_plan_cache_lookup_gen when generation >= 0."""
+        ptr = C.POINTER(L.CascadePlan)()
+        hit = C.c_int32()
+        L.check(L.load().psd_plan_cache_lookup_gen(self._h, int(generation), C.byref(table.c),
+                                                   int(tile_tokens), int(enable), int(min_shared_pages),
+                                                   int(min_members), C.byref(ptr), C.byref(hit)))
+        return CachedPlan(ptr, bool(hit.value))
+
+    def stats(self) -> dict:
+        h, m, n = C.c_int64(), C.c_int64(), C.c_int32()
+        L.check(L.load().psd_plan_cache_stats(self._h, C.byref(h), C.byref(m), C.byref(n)))
+        return {"hits": h.value, "misses": m.value, "entries": n.value}
+
+    def close(self):
+        if self._h:
+            L.load().psd_plan_cache_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def build_cascade_plan(table: HostTable, members, shared_pages: int, tile_tokens: int) -> Plan:
     plan = Plan(table)
     m = _i32(list(members) if len(members) else [0])

@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libpsd.so")
 
 CU_SOURCES = ["api.cu", "merge.cu", "partial_cc.cu", "partial_tcs.cu", "partial_tc.cu", "partial_mla.cu",
               "no_alloc.cu"]
-CPP_SOURCES = ["plan.cpp"]
+CPP_SOURCES = ["plan.cpp", "plan_cache.cpp"]
 HEADERS = ["psd_internal.h", "kernels.h", "device.cuh", "context.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
