@@ -312,3 +312,89 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
 
 def u8_codes(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.uint8).numpy()
+
+
+# ------------------------------------------------------------- RoPE + KV append
+def rope_cos_sin_table(max_position: int, rot_dim: int, base: float = 10000.0) -> np.ndarray:
+    """Caller data for the append step: cos_sin[p] = [cos p*theta_i .. , sin p*theta_i ..]
+    with theta_i = base^(-2i/rot_dim), i < rot_dim/2 (the common rotary schedule; the
+    append step itself only reads the table), float32 [max_position, rot_dim]."""
+    i = np.arange(rot_dim // 2, dtype=np.float64)
+    theta = base ** (-2.0 * i / rot_dim)
+    ang = np.arange(max_position, dtype=np.float64)[:, None] * theta[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+@dataclasses.dataclass
+class AppendStep:
+    """The new tokens of one decode step and the pool they are appended to.
+
+    q [T, Hq, Dq] bf16; k_nope [T, Hkv, Dn] bf16 or None; k_rope [T, Hkv, Dr] bf16;
+    v [T, Hkv, Dv] bf16 or None (latent: V lives in the K row); positions [T] int32;
+    slot_mapping [T] int32 (page * page_size + slot, negative = skip); pools as in
+    Workload (bf16, or uint8 fp8-e4m3 codes), filled with NaN canaries."""
+
+    name: str
+    q: torch.Tensor
+    k_nope: Optional[torch.Tensor]
+    k_rope: torch.Tensor
+    v: Optional[torch.Tensor]
+    positions: np.ndarray
+    slot_mapping: np.ndarray
+    cos_sin: np.ndarray
+    rot_dim: int
+    neox: bool
+    q_rope_col: int
+    k_pool: torch.Tensor
+    v_pool: Optional[torch.Tensor]
+    page_size: int
+    kv_dtype: str
+    k_scale: float
+    v_scale: float
+
+
+def append_step(seed: int = 0, kind: str = "gqa", T: int = 32, kv_dtype: str = "bf16", neox: bool = True,
+                skip_every: int = 0, num_pages: int = 512, max_position: int = 32768) -> AppendStep:
+    """One decode step's append for T requests.
+
+    gqa: Hq=32, Hkv=8, D=128, full rotary (rot_dim 128), separate K and V pools,
+         page 16 (the flat-decode shape).
+    mla: 128 query heads of 576 whose last 64 columns are roped; the K row is the
+         512-column latent followed by a 64-column roped part; no V pool, page 64
+         (the MLA-decode shape).
+    Each request appends one token at a random position at its own page slot (a
+    permutation of the pool's slots); with skip_every > 0 every skip_every-th token
+    has slot -1 (owned by another rank)."""
+    rng = np.random.default_rng(seed)
+    if kind == "gqa":
+        Hq, Hkv, Dq, Dn, Dr, Dv, P, rot, qcol = 32, 8, 128, 0, 128, 128, 16, 128, 0
+    elif kind == "mla":
+        Hq, Hkv, Dq, Dn, Dr, Dv, P, rot, qcol = 128, 1, 576, 512, 64, 0, 64, 64, 512
+    else:
+        raise ValueError(kind)
+    q = _bf16(rng.standard_normal((T, Hq, Dq)))
+    k_nope = _bf16(rng.standard_normal((T, Hkv, Dn))) if Dn else None
+    k_rope = _bf16(rng.standard_normal((T, Hkv, Dr)))
+    v = _bf16(rng.standard_normal((T, Hkv, Dv))) if Dv else None
+    positions = rng.integers(0, max_position, size=T).astype(np.int32)
+    slots = rng.choice(num_pages * P, size=T, replace=False).astype(np.int32)
+    if skip_every:
+        slots[::skip_every] = -1
+    Dk = Dn + Dr
+    if kv_dtype == "bf16":
+        k_pool = torch.full((num_pages, P, Hkv, Dk), 0, dtype=torch.int16).view(torch.bfloat16)
+        k_pool.view(torch.int16).fill_(np.int16(BF16_NAN_BITS))
+        v_pool = None
+        if Dv:
+            v_pool = torch.empty((num_pages, P, Hkv, Dv), dtype=torch.bfloat16)
+            v_pool.view(torch.int16).fill_(np.int16(BF16_NAN_BITS))
+    else:
+        k_pool = torch.full((num_pages, P, Hkv, Dk), FP8_E4M3_NAN_CODE, dtype=torch.uint8)
+        v_pool = torch.full((num_pages, P, Hkv, Dv), FP8_E4M3_NAN_CODE, dtype=torch.uint8) if Dv else None
+    # per-tensor scales in the usual amax / 448 form over the new values
+    ks = float(max(np.abs(k_rope.float().numpy()).max(),
+                   np.abs(k_nope.float().numpy()).max() if k_nope is not None else 0.0) / 448.0 * 1.25)
+    vs = float(np.abs(v.float().numpy()).max() / 448.0 * 1.25) if v is not None else 1.0
+    return AppendStep(f"append_{kind}_{kv_dtype}", q, k_nope, k_rope, v, positions, slots,
+                      rope_cos_sin_table(max_position, rot), rot, neox, qcol, k_pool, v_pool, P, kv_dtype,
+                      ks if kv_dtype != "bf16" else 1.0, vs if kv_dtype != "bf16" else 1.0)
