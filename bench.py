@@ -328,6 +328,38 @@ def barrier(world):
     torch.cuda.synchronize()
 
 
+def rope_append_timing(ctx, steps, warmup, flush):
+    """The RoPE + KV-append step before decode: one launch per step, CUDA events."""
+    import paged_split_kv_decode_gb300 as psd
+    out = {}
+    for kind, T, kv in (("gqa", 32, "bf16"), ("mla", 128, "fp8_e4m3"), ("gqa", 4096, "bf16")):
+        st = synth.append_step(seed=0, kind=kind, T=T, kv_dtype=kv, num_pages=max(1024, T // 8))
+        dev = lambda t: None if t is None else t.cuda().contiguous()
+        q, kn, kr, v, kp, vp = dev(st.q), dev(st.k_nope), dev(st.k_rope), dev(st.v), dev(st.k_pool), dev(st.v_pool)
+        cs = torch.from_numpy(st.cos_sin).cuda()
+        pos, slots = torch.from_numpy(st.positions).cuda(), torch.from_numpy(st.slot_mapping).cuda()
+        fault = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+        def step():
+            psd.rope_append_kv(ctx, q, kn, kr, v, cs, pos, slots, kp, vp, rot_dim=st.rot_dim, neox=st.neox,
+                               q_rope_col=st.q_rope_col, page_size=st.page_size, k_scale=st.k_scale,
+                               v_scale=st.v_scale, fault=fault)
+        ms = statistics.mean(time_steps(step, steps, warmup, flush))
+        assert int(fault.item()) == 0
+        esz = 1 if kv == "fp8_e4m3" else 2
+        Hq, Dq = st.q.shape[1], st.q.shape[2]
+        Hkv = st.k_rope.shape[1]
+        Dk = st.k_rope.shape[2] + (st.k_nope.shape[2] if st.k_nope is not None else 0)
+        Dv = st.v.shape[2] if st.v is not None else 0
+        # algorithmic bytes: q rope columns read + written, new K/V read, pool rows written,
+        # cos/sin rows and the two int32 per token
+        b = T * (2 * Hq * st.rot_dim * 2 + Hkv * (Dk + Dv) * 2 + Hkv * (Dk + Dv) * esz
+                 + st.rot_dim * 4 + 8)
+        out[f"{kind}_{kv}_T{T}"] = {"us": round(ms * 1e3, 2), "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                                    "algorithmic_bytes": int(b)}
+    return out
+
+
 def host_plan_us(w, reps=200):
     """Host detection + cascade planning per call: from scratch (psd_plan_decode) and
     as a plan-cache hit (the same table on the next layer)."""
@@ -443,6 +475,8 @@ def run_ours(args):
         del marm
     if not args.quick and args.workload in ("all", "merge"):
         extra["merge_sweep"] = merge_sweep(arm.ctx, args.steps, args.warmup, flush, hbm)
+    if not args.quick and args.workload in ("all", "append"):
+        extra["rope_append"] = rope_append_timing(arm.ctx, args.steps, args.warmup, flush)
 
     if rank == 0:
         line = {
@@ -542,7 +576,7 @@ def main():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--quick", action="store_true", help="flat workload only")
-    p.add_argument("--workload", choices=["all", "cascade", "mla", "merge"], default="all",
+    p.add_argument("--workload", choices=["all", "cascade", "mla", "merge", "append"], default="all",
                    help="which workloads run after the flat headline")
     p.add_argument("--mla-batch", type=int, default=128, help="requests in the MLA workload")
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -336,6 +336,52 @@ psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_args *args,
                                    int32_t *fault_bits_dev, psd_cascade_stats *stats,
                                    psd_stream_t stream);
 
+/* ---------------------------------------------------------------- RoPE + append
+ * The step before decode: the new token of each request is roped and appended to
+ * the paged pool (ROCm ATOM PR #1701, section 1 and 3.3: one fused kernel ropes
+ * every query and the new token's rope part of K, concatenates the non-rope latent
+ * with it, and writes the KV row only for the slots this rank owns; 3.2: fp8 KV
+ * dequantises as code * scale).
+ *
+ * Per token t (pos = positions[t], r = rot_dim, frequencies i < r/2 with
+ * c_i = cos_sin[pos][i], s_i = cos_sin[pos][r/2 + i]):
+ *   q[t, h, q_rope_col + a_i], q[t, h, q_rope_col + b_i] are rotated in place for
+ *   every head h, where (a_i, b_i) = (i, i + r/2) when neox, else (2i, 2i + 1):
+ *   x' = x c_i - y s_i, y' = y c_i + x s_i in f32, each product rounded, then bf16;
+ *   if slot_mapping[t] >= 0 (slot = page * page_size + position in page), for every
+ *   KV head: k_pool[slot] = [k_nope[t] | rope(k_rope[t]) on its first r columns]
+ *   and v_pool[slot] = v[t], stored as bf16, or for PSD_FP8_E4M3 as the saturating
+ *   round-to-nearest-even E4M3 code of value / scale (k_scale for K, v_scale for V).
+ * A position outside [0, max_position) leaves token t untouched and sets
+ * PSD_FAULT_RANGE; a slot >= num_pages * page_size skips its KV write and sets
+ * PSD_FAULT_PAGE_ID, both in *fault_dev (device int32, caller-owned, OR-ed).
+ * num_tokens == 0 is a no-op (the pointers are not checked). */
+typedef struct {
+  void *q;                     /* device [T, Hq, Dq] bf16, roped in place (NULL iff Hq == 0) */
+  int32_t Hq, Dq, q_rope_col;
+  const void *k_nope;          /* device [T, Hkv, Dk_nope] bf16 (NULL iff Dk_nope == 0) */
+  const void *k_rope;          /* device [T, Hkv, Dk_rope] bf16 */
+  int32_t Hkv, Dk_nope, Dk_rope;
+  const void *v;               /* device [T, Hkv, Dv] bf16 (NULL iff Dv == 0: V is in the K row) */
+  int32_t Dv;
+  int32_t rot_dim;             /* even, >= 2, <= Dk_rope, q_rope_col + rot_dim <= Dq */
+  int32_t neox;                /* 1: pairs (i, i + r/2); 0: pairs (2i, 2i + 1) */
+  const float *cos_sin;        /* device [max_position, rot_dim] f32 */
+  int32_t max_position;
+  const int32_t *positions;    /* device [T] */
+  const int32_t *slot_mapping; /* device [T]; negative = not this rank's slot (no KV write) */
+  int32_t num_tokens;          /* T */
+  void *k_pool;                /* device [num_pages, page_size, Hkv, Dk_nope + Dk_rope] */
+  void *v_pool;                /* device [num_pages, page_size, Hkv, Dv] (NULL iff Dv == 0) */
+  int64_t num_pages;
+  int32_t page_size;
+  int32_t kv_dtype;            /* PSD_BF16 or PSD_FP8_E4M3 (both pools) */
+  float k_scale, v_scale;      /* fp8 only: finite and > 0 */
+  int32_t *fault_dev;          /* device int32 fault word */
+} psd_rope_append_args;
+
+psd_status rope_append_kv(psd_ctx *ctx, const psd_rope_append_args *args, psd_stream_t stream);
+
 /* Synchronises `stream` and reads the workspace's fault flag: PSD_OK, or
  * PSD_ERR_DEVICE_FAULT with the PSD_FAULT_* bits in *fault_bits (nullable).
  * Clears the flag. */

@@ -7,6 +7,6 @@ from .api import (CachedPlan, Context, HostTable, Plan, PlanCache, build_cascade
                   cascade_decode,
                   cascade_decode_no_alloc,
                   cascade_env_enabled, check_device_error, decode_args, detect_shared_prefix,
-                  merge_states, paged_decode_partial, plan_decode, split_plan, workspace_bytes,
-                  workspace_for)
+                  merge_states, paged_decode_partial, plan_decode, rope_append_kv, split_plan,
+                  workspace_bytes, workspace_for)
 from ._lib import PsdError, load  # noqa: F401

@@ -24,13 +24,23 @@ EXPORTS = [
     "psd_plan_capacity", "psd_workspace_bytes", "paged_decode_partial", "merge_states",
     "cascade_decode", "psd_check_device_error", "cascade_decode_no_alloc",
     "psd_plan_cache_create", "psd_plan_cache_destroy", "psd_plan_cache_lookup", "psd_plan_cache_lookup_gen",
-    "psd_plan_cache_stats",
+    "psd_plan_cache_stats", "rope_append_kv",
 ]
 
 
 class PageTable(C.Structure):
     _fields_ = [("page_indptr", P_i32), ("page_indices", P_i32), ("last_page_len", P_i32),
                 ("batch", i32), ("page_size", i32)]
+
+
+class RopeAppendArgs(C.Structure):
+    _fields_ = [("q", C.c_void_p), ("Hq", i32), ("Dq", i32), ("q_rope_col", i32),
+                ("k_nope", C.c_void_p), ("k_rope", C.c_void_p), ("Hkv", i32), ("Dk_nope", i32),
+                ("Dk_rope", i32), ("v", C.c_void_p), ("Dv", i32), ("rot_dim", i32), ("neox", i32),
+                ("cos_sin", C.c_void_p), ("max_position", i32), ("positions", C.c_void_p),
+                ("slot_mapping", C.c_void_p), ("num_tokens", i32), ("k_pool", C.c_void_p),
+                ("v_pool", C.c_void_p), ("num_pages", i64), ("page_size", i32), ("kv_dtype", i32),
+                ("k_scale", C.c_float), ("v_scale", C.c_float), ("fault_dev", C.c_void_p)]
 
 
 class WorkItem(C.Structure):
@@ -100,6 +110,7 @@ def _sig(lib):
     lib.psd_plan_cache_lookup_gen.argtypes = [V, i64, C.POINTER(PageTable), i32, i32, i32, i32,
                                               C.POINTER(C.POINTER(CascadePlan)), P_i32]
     lib.psd_plan_cache_stats.argtypes = [V, C.POINTER(i64), C.POINTER(i64), P_i32]
+    lib.rope_append_kv.argtypes = [V, C.POINTER(RopeAppendArgs), V]
     lib.psd_workspace_bytes.argtypes = [i32, i32, i64, i32, i32]
     lib.psd_workspace_bytes.restype = C.c_size_t
     lib.paged_decode_partial.argtypes = [V, C.POINTER(DecodeArgs), C.POINTER(WorkItem), i32, V, V,

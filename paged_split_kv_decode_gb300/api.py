@@ -274,6 +274,49 @@ class PlanCache:
             pass
 
 
+def rope_append_kv(ctx: Context, q, k_nope, k_rope, v, cos_sin, positions, slot_mapping, k_pool, v_pool, *,
+                   rot_dim: int, neox: bool, q_rope_col: int, page_size: int, k_scale: float = 1.0,
+                   v_scale: float = 1.0, fault=None, stream=None):
+    """rope_append_kv: rope q in place and write the new tokens' K/V rows into the pools.
+
+    q [T, Hq, Dq] bf16, k_nope [T, Hkv, Dn] bf16 or None, k_rope [T, Hkv, Dr] bf16,
+    v [T, Hkv, Dv] bf16 or None, cos_sin [max_position, rot_dim] f32, positions and
+    slot_mapping [T] int32, pools bf16 (or uint8 fp8-e4m3 codes) [pages, page_size,
+    Hkv, D].  Returns the int32 fault word tensor (the one given, or a new zero one)."""
+    T = int(positions.numel())
+    if fault is None:
+        fault = torch.zeros(1, dtype=torch.int32, device=k_pool.device)
+    for name, t in (("positions", positions), ("slot_mapping", slot_mapping)):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{name} must be int32")
+    if cos_sin.dtype != torch.float32:
+        raise TypeError("cos_sin must be float32")
+    a = L.RopeAppendArgs()
+    Hq = int(q.shape[1]) if q is not None else 0
+    a.q = _dev_ptr(q, "q") if q is not None else None
+    a.Hq, a.Dq, a.q_rope_col = Hq, (int(q.shape[2]) if q is not None else 0), int(q_rope_col)
+    a.k_nope = _dev_ptr(k_nope, "k_nope") if k_nope is not None else None
+    a.k_rope = _dev_ptr(k_rope, "k_rope")
+    a.Hkv, a.Dk_nope, a.Dk_rope = int(k_rope.shape[1]), (int(k_nope.shape[2]) if k_nope is not None else 0), \
+        int(k_rope.shape[2])
+    a.v = _dev_ptr(v, "v") if v is not None else None
+    a.Dv = int(v.shape[2]) if v is not None else 0
+    a.rot_dim, a.neox = int(rot_dim), int(bool(neox))
+    a.cos_sin = _dev_ptr(cos_sin, "cos_sin")
+    a.max_position = int(cos_sin.shape[0])
+    a.positions = _dev_ptr(positions, "positions")
+    a.slot_mapping = _dev_ptr(slot_mapping, "slot_mapping")
+    a.num_tokens = T
+    a.k_pool = _dev_ptr(k_pool, "k_pool")
+    a.v_pool = _dev_ptr(v_pool, "v_pool") if v_pool is not None else None
+    a.num_pages, a.page_size = int(k_pool.shape[0]), int(page_size)
+    a.kv_dtype = kv_dtype_code(k_pool)
+    a.k_scale, a.v_scale = float(k_scale), float(v_scale)
+    a.fault_dev = _dev_ptr(fault, "fault")
+    L.check(L.load().rope_append_kv(ctx.handle, C.byref(a), _stream(stream)))
+    return fault
+
+
 def build_cascade_plan(table: HostTable, members, shared_pages: int, tile_tokens: int) -> Plan:
     plan = Plan(table)
     m = _i32(list(members) if len(members) else [0])

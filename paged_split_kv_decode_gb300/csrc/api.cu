@@ -504,6 +504,33 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   return PSD_OK;
 }
 
+extern "C" psd_status rope_append_kv(psd_ctx *ctx, const psd_rope_append_args *a, psd_stream_t stream) {
+  clear_error();
+  if (!ctx || !a) return fail(PSD_ERR_INVALID_ARG, "rope_append_kv: NULL");
+  if (a->num_tokens < 0 || a->Hq < 0 || a->Hkv < 1 || a->Dk_nope < 0 || a->Dk_rope < 1 || a->Dv < 0)
+    return fail(PSD_ERR_INVALID_ARG, "rope_append_kv: bad sizes");
+  if (a->num_tokens == 0) return PSD_OK;  // nothing is read or written (pointers may be NULL)
+  if (a->rot_dim < 2 || a->rot_dim % 2 || a->rot_dim > a->Dk_rope)
+    return fail(PSD_ERR_INVALID_ARG, "rope_append_kv: rot_dim %d must be even, >= 2 and <= Dk_rope %d",
+                a->rot_dim, a->Dk_rope);
+  if (a->Hq > 0 && (!a->q || a->q_rope_col < 0 || a->q_rope_col + a->rot_dim > a->Dq))
+    return fail(PSD_ERR_INVALID_ARG, "rope_append_kv: q rope columns outside Dq");
+  if ((a->Dk_nope > 0) != (a->k_nope != nullptr) || (a->Dv > 0) != (a->v != nullptr) ||
+      (a->Dv > 0) != (a->v_pool != nullptr))
+    return fail(PSD_ERR_INVALID_ARG, "rope_append_kv: k_nope / v / v_pool must be given exactly when their width > 0");
+  if (!a->k_rope || !a->cos_sin || !a->positions || !a->slot_mapping || !a->k_pool || !a->fault_dev)
+    return fail(PSD_ERR_INVALID_ARG, "rope_append_kv: NULL pointer");
+  if (a->max_position < 1 || a->page_size < 1 || a->num_pages < 0)
+    return fail(PSD_ERR_INVALID_ARG, "rope_append_kv: bad pool or table sizes");
+  if (a->kv_dtype != PSD_BF16 && a->kv_dtype != PSD_FP8_E4M3)
+    return fail(PSD_ERR_INVALID_ARG, "rope_append_kv: kv_dtype %d", a->kv_dtype);
+  if (a->kv_dtype == PSD_FP8_E4M3 && !(std::isfinite(a->k_scale) && a->k_scale > 0.f &&
+                                       std::isfinite(a->v_scale) && a->v_scale > 0.f))
+    return fail(PSD_ERR_INVALID_ARG, "rope_append_kv: fp8 scales must be finite and > 0");
+  DeviceGuard g(ctx->dev.device);
+  return launch_rope_append(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" psd_status psd_check_device_error(psd_ctx *ctx, void *workspace, psd_stream_t stream,
                                              int32_t *fault_bits) {
   clear_error();

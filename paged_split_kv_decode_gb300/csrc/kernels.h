@@ -60,6 +60,8 @@ psd_status launch_partial_mla(const PartialLaunch &p, const DeviceInfo &dev, cud
 bool partial_tc_supports(const PartialLaunch &p);
 psd_status launch_partial_tc(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
 
+psd_status launch_rope_append(const psd_rope_append_args *a, cudaStream_t s);
+
 // after_partial: the launch directly follows a partial kernel on stream s (no event
 // or copy between them), so it may start early and wait for that grid on the device.
 psd_status launch_merge(const float *v_in, const float *lse_in, const int32_t *o_indptr,
