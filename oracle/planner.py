@@ -196,3 +196,105 @@ def env_switch(value, default: bool) -> bool:
     if v in ("1", "true", "on", "yes"):
         return True
     return default
+
+
+# ------------------------------------------------ several and nested shared spans
+# An extension the pages scope out (Task item 1: "One shared level only, as scoped";
+# Left out / unsure: "Not attempted: nested sharing.  A common system prompt plus a
+# per-tenant sub-prefix would need a third level").  Readings, each pinned by a
+# hand-made case:
+#   N1  every first-page group that passes the thresholds becomes a segment (the
+#       groups are disjoint), not only the one with the most saved reads;
+#   N2  inside a segment [start, start + span), the members are grouped again by
+#       their page at start + span, and each group gets the same rules from there
+#       (span over all its members, capped so no member's last page is shared, both
+#       thresholds), up to max_levels levels in all;
+#   N3  segments are listed depth first, groups in order of their lowest batch index;
+#   N4  a request's final merge group holds the chunk rows of its segments in that
+#       order, then its level-1 rows, which start after its deepest segment.
+# With max_levels = 1 and one qualifying group the result is the two-level plan.
+
+def detect_segments(page_indptr, page_indices, min_shared_pages=DEFAULT_MIN_SHARED_PAGES,
+                    min_members=DEFAULT_MIN_MEMBERS, max_levels=2):
+    """Shared spans as (members, start_page, shared_pages), readings N1-N3."""
+    B = len(page_indptr) - 1
+    need, msp = max(2, int(min_members)), max(1, int(min_shared_pages))
+
+    def page(b, pos):
+        return int(page_indices[int(page_indptr[b]) + pos])
+
+    segs = []
+
+    def recurse(cands, start, level):
+        groups = {}
+        for b in cands:
+            if num_pages(page_indptr, b) - 1 - start >= 1:
+                groups.setdefault(page(b, start), []).append(b)
+        for g in groups.values():
+            if len(g) < need:
+                continue
+            cap = min(num_pages(page_indptr, b) for b in g) - 1 - start
+            span = 0
+            while span < cap and all(page(b, start + span) == page(g[0], start + span) for b in g[1:]):
+                span += 1
+            if span < msp:
+                continue
+            segs.append((list(g), start, span))
+            if level < max_levels:
+                recurse(g, start + span, level + 1)
+
+    recurse(list(range(B)), 0, 1)
+    return segs
+
+
+def build_nested_plan(page_indptr, last_page_len, page_size, segments, tile_tokens):
+    """Level-0 items per segment, level-1 items and the final merge groups (N4).
+
+    Returns dict(segments=[(first_member, num_members, start_page, shared_pages,
+    first_item, num_items)], members, member_row_base (one entry per (segment,
+    member)), l0_items (out_row = chunk index within the segment), l1_items, o_indptr,
+    num_rows)."""
+    ppt = tile_tokens // page_size
+    B = len(page_indptr) - 1
+    seg_chunks = [chunks_of(span * page_size, tile_tokens) for _, _, span in segments]
+    l0, seg_rows, members = [], [], []
+    for (g, start, span), ch in zip(segments, seg_chunks):
+        first_item = len(l0)
+        for c, (t0, t1) in enumerate(ch):
+            l0.append((-1, int(page_indptr[g[0]]) + start + c * ppt, t1 - t0, c))
+        seg_rows.append((len(members), len(g), start, span, first_item, len(ch)))
+        members.extend(g)
+    # rows of each request: its segments' chunks (segment order), then level 1
+    row_base = [0] * len(members)
+    l1, o_indptr = [], [0]
+    for b in range(B):
+        r = o_indptr[-1]
+        deepest = 0
+        for s, (g, start, span) in enumerate(segments):
+            if b in g:
+                row_base[seg_rows[s][0] + g.index(b)] = r
+                r += len(seg_chunks[s])
+                deepest = max(deepest, start + span)
+        L = request_length(page_indptr, last_page_len, page_size, b)
+        ch = chunks_of(L - deepest * page_size, tile_tokens)
+        for c, (t0, t1) in enumerate(ch):
+            l1.append((b, int(page_indptr[b]) + deepest + c * ppt, t1 - t0, r + c))
+        o_indptr.append(r + len(ch))
+    return dict(segments=seg_rows, members=members, member_row_base=row_base, l0_items=l0,
+                l1_items=l1, o_indptr=o_indptr, num_rows=o_indptr[-1])
+
+
+def plan_nested(page_indptr, page_indices, last_page_len, page_size, tile_tokens, enable=True,
+                min_shared_pages=DEFAULT_MIN_SHARED_PAGES, min_members=DEFAULT_MIN_MEMBERS,
+                max_levels=2):
+    """Nested plan when any segment qualifies, else the flat plan with the
+    two-level planner's decline reason (the top level applies the same tests)."""
+    segs = detect_segments(page_indptr, page_indices, min_shared_pages, min_members,
+                           max_levels) if enable else []
+    if enable and not segs:
+        reason = detect_shared_prefix(page_indptr, page_indices, min_shared_pages, min_members)[2]
+    else:
+        reason = DECLINE_NONE if segs else DECLINE_DISABLED
+    plan = build_nested_plan(page_indptr, last_page_len, page_size, segs, tile_tokens)
+    plan.update(decline_reason=reason)
+    return plan
