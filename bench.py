@@ -328,6 +328,40 @@ def barrier(world):
     torch.cuda.synchronize()
 
 
+def nested_timing(steps, warmup, flush):
+    """System prompt + two tenant sub-prefixes: flat arm, two-level cascade (the
+    system prompt once) and nested cascade (the tenant sub-prefixes once as well)."""
+    import paged_split_kv_decode_gb300 as psd
+    w = synth.nested_decode(seed=0, canary=False)
+    flat_arm, casc_arm = Arm(w, enable=0), Arm(w, enable=1)
+    nest = Arm(w, enable=1)
+    plan = psd.plan_nested(nest.table, w.tile_tokens, 1, w.min_shared_pages, w.min_members, 2)
+    ws = psd.nested_workspace_for(plan, w.Hq, w.Dv, "cuda")
+
+    def nested_step():
+        psd.cascade_decode_nested(nest.ctx, nest.args, plan, nest.o, nest.lse, ws)
+    nested_step()
+    torch.cuda.synchronize()
+    err = np.abs(nest.o.cpu().double().numpy() - flat_arm_outputs(flat_arm)).max()
+    tf = statistics.mean(time_steps(flat_arm.step, steps, warmup, flush))
+    tc = statistics.mean(time_steps(casc_arm.step, steps, warmup, flush))
+    tn = statistics.mean(time_steps(nested_step, steps, warmup, flush))
+    uniq = unique_kv_bytes(w)
+    return {"workload": "nested decode: 32 requests; a 4096-token system prompt for two tenants of 8, "
+                        "each with a 2048-token sub-prefix and suffixes U[64,1024]; 16 independent "
+                        "U[512,4096]; Hq=32, Hkv=8, D=128, page 16, tile 512",
+            "flat_ms": round(tf, 4), "two_level_ms": round(tc, 4), "nested_ms": round(tn, 4),
+            "segments": [list(x) for x in plan.segments], "flat_bytes": int(flat_kv_bytes(w)),
+            "unique_bytes": int(uniq), "nested_unique_kv_gbs": round(uniq / (tn * 1e-3) / 1e9, 1),
+            "max_abs_diff_vs_flat": float(err)}
+
+
+def flat_arm_outputs(arm):
+    arm.step()
+    torch.cuda.synchronize()
+    return arm.o.cpu().double().numpy()
+
+
 def rope_append_timing(ctx, steps, warmup, flush):
     """The RoPE + KV-append step before decode: one launch per step, CUDA events."""
     import paged_split_kv_decode_gb300 as psd
@@ -475,6 +509,8 @@ def run_ours(args):
         del marm
     if not args.quick and args.workload in ("all", "merge"):
         extra["merge_sweep"] = merge_sweep(arm.ctx, args.steps, args.warmup, flush, hbm)
+    if not args.quick and args.workload in ("all", "cascade", "nested"):
+        extra["nested"] = nested_timing(args.steps, args.warmup, flush)
     if not args.quick and args.workload in ("all", "append"):
         extra["rope_append"] = rope_append_timing(arm.ctx, args.steps, args.warmup, flush)
 
@@ -576,7 +612,7 @@ def main():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--quick", action="store_true", help="flat workload only")
-    p.add_argument("--workload", choices=["all", "cascade", "mla", "merge", "append"], default="all",
+    p.add_argument("--workload", choices=["all", "cascade", "mla", "merge", "append", "nested"], default="all",
                    help="which workloads run after the flat headline")
     p.add_argument("--mla-batch", type=int, default=128, help="requests in the MLA workload")
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -336,6 +336,66 @@ psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_args *args,
                                    int32_t *fault_bits_dev, psd_cascade_stats *stats,
                                    psd_stream_t stream);
 
+/* ------------------------------------------------- several and nested shared spans
+ * An extension the pages scope out (mlxcel PR #1004, Task item 1: "One shared level
+ * only, as scoped"; Left out / unsure: nested sharing, a common system prompt plus a
+ * per-tenant sub-prefix, "would need a third level").  Planning rules:
+ *   every first-page group that passes the thresholds becomes a segment (not only
+ *   the one with the most saved reads); inside a segment [start, start + span) its
+ *   members are grouped again by their page at start + span and each group gets the
+ *   same rules from there (span over all its members, capped so no member's last
+ *   page is shared, min_shared_pages, min_members), up to max_levels levels;
+ *   segments are listed depth first, groups in order of their lowest batch index.
+ * Each segment is one stacked level-0 request (M_s * G rows per KV head, KV-head
+ * major); request b's final merge group holds its segments' chunk rows in segment
+ * order, then its level-1 rows, which start after its deepest segment.  With
+ * max_levels = 1 and one qualifying group the plan equals psd_plan_decode's. */
+typedef struct {
+  int32_t first_member; /* into members[] and member_row_base[] */
+  int32_t num_members;
+  int32_t start_page;   /* page position of the span in every member's page list */
+  int32_t shared_pages;
+  int32_t first_item;   /* into l0_items[] */
+  int32_t num_items;
+} psd_segment;
+
+typedef struct {
+  /* capacities (in): psd_plan_nested_capacity gives them */
+  int32_t batch_capacity;   /* >= batch */
+  int32_t entry_capacity;   /* >= batch * max_levels ((segment, member) entries) */
+  int32_t segment_capacity; /* >= batch * max_levels */
+  int32_t item_capacity;    /* >= page_indptr[batch] */
+  psd_segment *segments;
+  int32_t *members;         /* [entry_capacity] each segment's members, increasing */
+  int32_t *member_row_base; /* [entry_capacity] first partial row of each entry */
+  psd_work_item *l0_items;  /* [item_capacity] span chunks, by segment; out_row = chunk */
+  psd_work_item *l1_items;  /* [item_capacity] */
+  int32_t *o_indptr;        /* [batch_capacity + 1] */
+  /* results (out) */
+  int32_t batch, page_size, tile_tokens, max_levels;
+  int32_t num_segments, num_entries, decline_reason;
+  int32_t l0_num_items, l1_num_items;
+  int32_t num_rows;
+} psd_nested_plan;
+
+psd_status psd_plan_nested_capacity(const psd_page_table *host, int32_t max_levels,
+                                    int32_t *batch_capacity, int32_t *entry_capacity,
+                                    int32_t *segment_capacity, int32_t *item_capacity);
+/* max_levels in [1, 8]; enable as in psd_plan_decode.  No segment: the flat plan
+ * with psd_plan_decode's decline reason. */
+psd_status psd_plan_nested(const psd_page_table *host, int32_t tile_tokens, int32_t enable,
+                           int32_t min_shared_pages, int32_t min_members, int32_t max_levels,
+                           psd_nested_plan *plan);
+/* Workspace bytes cascade_decode_nested needs for this plan. */
+size_t psd_nested_workspace_bytes(const psd_nested_plan *plan, int32_t Hq, int32_t Dv);
+/* Decode with a nested plan: one stacked level-0 launch per segment, level 1, one
+ * merge (stats->members counts (segment, member) entries and shared_pages sums the
+ * spans).  Same arguments, errors and fault word as cascade_decode. */
+psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args *args,
+                                 const psd_nested_plan *plan, float *o, float *lse,
+                                 void *workspace, size_t workspace_bytes,
+                                 psd_cascade_stats *stats, psd_stream_t stream);
+
 /* ---------------------------------------------------------------- RoPE + append
  * The step before decode: the new token of each request is roped and appended to
  * the paged pool (ROCm ATOM PR #1701, section 1 and 3.3: one fused kernel ropes

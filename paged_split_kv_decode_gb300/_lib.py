@@ -24,7 +24,8 @@ EXPORTS = [
     "psd_plan_capacity", "psd_workspace_bytes", "paged_decode_partial", "merge_states",
     "cascade_decode", "psd_check_device_error", "cascade_decode_no_alloc",
     "psd_plan_cache_create", "psd_plan_cache_destroy", "psd_plan_cache_lookup", "psd_plan_cache_lookup_gen",
-    "psd_plan_cache_stats", "rope_append_kv",
+    "psd_plan_cache_stats", "rope_append_kv", "psd_plan_nested_capacity", "psd_plan_nested",
+    "psd_nested_workspace_bytes", "cascade_decode_nested",
 ]
 
 
@@ -62,6 +63,20 @@ class CascadePlan(C.Structure):
                 ("page_size", i32), ("tile_tokens", i32), ("num_members", i32),
                 ("shared_pages", i32), ("decline_reason", i32), ("l0_num_items", i32),
                 ("l1_num_items", i32), ("num_rows", i32)]
+
+
+class Segment(C.Structure):
+    _fields_ = [("first_member", i32), ("num_members", i32), ("start_page", i32), ("shared_pages", i32),
+                ("first_item", i32), ("num_items", i32)]
+
+
+class NestedPlan(C.Structure):
+    _fields_ = [("batch_capacity", i32), ("entry_capacity", i32), ("segment_capacity", i32),
+                ("item_capacity", i32), ("segments", C.POINTER(Segment)), ("members", P_i32),
+                ("member_row_base", P_i32), ("l0_items", C.POINTER(WorkItem)),
+                ("l1_items", C.POINTER(WorkItem)), ("o_indptr", P_i32), ("batch", i32), ("page_size", i32),
+                ("tile_tokens", i32), ("max_levels", i32), ("num_segments", i32), ("num_entries", i32),
+                ("decline_reason", i32), ("l0_num_items", i32), ("l1_num_items", i32), ("num_rows", i32)]
 
 
 class CascadeStats(C.Structure):
@@ -111,6 +126,12 @@ def _sig(lib):
                                               C.POINTER(C.POINTER(CascadePlan)), P_i32]
     lib.psd_plan_cache_stats.argtypes = [V, C.POINTER(i64), C.POINTER(i64), P_i32]
     lib.rope_append_kv.argtypes = [V, C.POINTER(RopeAppendArgs), V]
+    lib.psd_plan_nested_capacity.argtypes = [C.POINTER(PageTable), i32, P_i32, P_i32, P_i32, P_i32]
+    lib.psd_plan_nested.argtypes = [C.POINTER(PageTable), i32, i32, i32, i32, i32, C.POINTER(NestedPlan)]
+    lib.psd_nested_workspace_bytes.argtypes = [C.POINTER(NestedPlan), i32, i32]
+    lib.psd_nested_workspace_bytes.restype = C.c_size_t
+    lib.cascade_decode_nested.argtypes = [V, C.POINTER(DecodeArgs), C.POINTER(NestedPlan), V, V, V, C.c_size_t,
+                                          C.POINTER(CascadeStats), V]
     lib.psd_workspace_bytes.argtypes = [i32, i32, i64, i32, i32]
     lib.psd_workspace_bytes.restype = C.c_size_t
     lib.paged_decode_partial.argtypes = [V, C.POINTER(DecodeArgs), C.POINTER(WorkItem), i32, V, V,
@@ -124,7 +145,8 @@ def _sig(lib):
     for name in EXPORTS:
         f = getattr(lib, name)
         if f.restype is C.c_int or f.restype is None:
-            if name not in ("psd_last_error", "psd_cascade_env_enabled", "psd_workspace_bytes"):
+            if name not in ("psd_last_error", "psd_cascade_env_enabled", "psd_workspace_bytes",
+                            "psd_nested_workspace_bytes"):
                 f.restype = C.c_int
 
 

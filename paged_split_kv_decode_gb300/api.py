@@ -424,6 +424,96 @@ def check_device_error(ctx: Context, workspace: torch.Tensor, stream=None) -> in
     return int(bits.value)
 
 
+class NestedPlan:
+    """A psd_nested_plan with caller-owned (numpy) arrays."""
+
+    def __init__(self, table: HostTable, max_levels: int):
+        self.table = table
+        bc, ec, sc, ic = C.c_int32(), C.c_int32(), C.c_int32(), C.c_int32()
+        L.check(L.load().psd_plan_nested_capacity(C.byref(table.c), int(max_levels), C.byref(bc), C.byref(ec),
+                                                  C.byref(sc), C.byref(ic)))
+        self.segments_a = (L.Segment * sc.value)()
+        self.members_a = np.zeros(ec.value, dtype=np.int32)
+        self.row_base_a = np.zeros(ec.value, dtype=np.int32)
+        self.o_indptr_a = np.zeros(bc.value + 1, dtype=np.int32)
+        self.l0 = (L.WorkItem * ic.value)()
+        self.l1 = (L.WorkItem * ic.value)()
+        self.c = L.NestedPlan()
+        self.c.batch_capacity, self.c.entry_capacity = bc.value, ec.value
+        self.c.segment_capacity, self.c.item_capacity = sc.value, ic.value
+        self.c.segments = self.segments_a
+        self.c.members = _ptr_i32(self.members_a)
+        self.c.member_row_base = _ptr_i32(self.row_base_a)
+        self.c.l0_items = self.l0
+        self.c.l1_items = self.l1
+        self.c.o_indptr = _ptr_i32(self.o_indptr_a)
+
+    def _items(self, arr, n):
+        cap = self.c.item_capacity
+        a = np.ctypeslib.as_array(C.cast(arr, L.P_i32), shape=(cap * 4,)).reshape(cap, 4)
+        return a[:n].copy()
+
+    @property
+    def segments(self):
+        return [(s.first_member, s.num_members, s.start_page, s.shared_pages, s.first_item, s.num_items)
+                for s in self.segments_a[: self.c.num_segments]]
+
+    @property
+    def members(self):
+        return [int(x) for x in self.members_a[: self.c.num_entries]]
+
+    @property
+    def member_row_base(self):
+        return [int(x) for x in self.row_base_a[: self.c.num_entries]]
+
+    @property
+    def o_indptr(self):
+        return [int(x) for x in self.o_indptr_a[: self.c.batch + 1]]
+
+    @property
+    def l0_items(self):
+        return self._items(self.l0, self.c.l0_num_items)
+
+    @property
+    def l1_items(self):
+        return self._items(self.l1, self.c.l1_num_items)
+
+    @property
+    def num_items(self):
+        return self.c.l0_num_items + self.c.l1_num_items
+
+    def __getattr__(self, name):
+        if name in ("num_segments", "num_entries", "decline_reason", "num_rows", "tile_tokens", "batch",
+                    "page_size", "max_levels", "l0_num_items", "l1_num_items"):
+            return getattr(self.c, name)
+        raise AttributeError(name)
+
+
+def plan_nested(table: HostTable, tile_tokens: int, enable: int = 1, min_shared_pages: int = 16,
+                min_members: int = 2, max_levels: int = 2) -> NestedPlan:
+    """psd_plan_nested: several disjoint and nested shared spans (see include/psd.h)."""
+    plan = NestedPlan(table, max_levels)
+    L.check(L.load().psd_plan_nested(C.byref(table.c), int(tile_tokens), int(enable), int(min_shared_pages),
+                                     int(min_members), int(max_levels), C.byref(plan.c)))
+    return plan
+
+
+def nested_workspace_for(plan: NestedPlan, Hq: int, Dv: int, device) -> torch.Tensor:
+    n = int(L.load().psd_nested_workspace_bytes(C.byref(plan.c), int(Hq), int(Dv)))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def cascade_decode_nested(ctx: Context, args: L.DecodeArgs, plan: NestedPlan, o: torch.Tensor,
+                          lse: torch.Tensor = None, workspace: torch.Tensor = None, stream=None) -> dict:
+    """cascade_decode_nested: one stacked level-0 launch per segment, level 1, one merge."""
+    stats = L.CascadeStats()
+    L.check(L.load().cascade_decode_nested(
+        ctx.handle, C.byref(args), C.byref(plan.c), _dev_ptr(o, "o"),
+        None if lse is None else _dev_ptr(lse, "lse"), _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), C.byref(stats), _stream(stream)))
+    return {k: getattr(stats, k) for k, _ in L.CascadeStats._fields_}
+
+
 def workspace_for(plan: Plan, Hq: int, Dv: int, device) -> torch.Tensor:
     n = workspace_bytes(plan.batch, max(plan.num_items, 1), plan.num_rows, Hq, Dv)
     return torch.empty(n, dtype=torch.uint8, device=device)

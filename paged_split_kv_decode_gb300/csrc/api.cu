@@ -435,8 +435,11 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
     L1.num_items = n1;
     L1.members = reinterpret_cast<const int32_t *>(ws + lay.members_off);
     L1.member_row_base = reinterpret_cast<const int32_t *>(ws + lay.row_base_off);
+    L1.fused_segments = 1;
     L1.fused_l0_items = n0;
-    L1.fused_l0_rows = L0.G_cta;
+    L1.seg_items[0] = n0;
+    L1.seg_rows[0] = L0.G_cta;
+    L1.seg_member0[0] = 0;
   } else if (M > 0) {  // level 0 on the side stream, after the upload
     L0.items = ditems;
     L0.order = reinterpret_cast<const int32_t *>(ws + lay.order_off);
@@ -498,6 +501,182 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
     stats->members = M;
     stats->shared_pages = plan->shared_pages;
     stats->shared_tokens = plan->shared_pages * args->page_size;
+    stats->prefix_chunks = n0;
+    stats->suffix_chunks = n1;
+  }
+  return PSD_OK;
+}
+
+extern "C" size_t psd_nested_workspace_bytes(const psd_nested_plan *plan, int32_t Hq, int32_t Dv) {
+  if (!plan) return 0;
+  return workspace_layout(plan->batch, plan->l0_num_items + plan->l1_num_items, plan->num_rows, Hq, Dv,
+                          plan->num_entries)
+      .total;
+}
+
+extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args *args,
+                                            const psd_nested_plan *plan, float *o, float *lse,
+                                            void *workspace, size_t workspace_bytes,
+                                            psd_cascade_stats *stats, psd_stream_t stream) {
+  clear_error();
+  if (!ctx || !plan || !o || !lse || !workspace) return fail(PSD_ERR_INVALID_ARG, "cascade_decode_nested: NULL");
+  psd_status st = validate_args(args);
+  if (st != PSD_OK) return st;
+  if (!aligned16(workspace)) return fail(PSD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  const int32_t B = plan->batch, S = plan->num_segments, E = plan->num_entries;
+  const int32_t n0 = plan->l0_num_items, n1 = plan->l1_num_items;
+  if (B != args->batch) return fail(PSD_ERR_INVALID_ARG, "cascade_decode_nested: plan batch %d != %d", B, args->batch);
+  if (S < 0 || E < 0 || n0 < 0 || n1 < 0 || (S == 0) != (n0 == 0) || plan->o_indptr[0] != 0 ||
+      plan->o_indptr[B] != plan->num_rows)
+    return fail(PSD_ERR_INVALID_ARG, "cascade_decode_nested: inconsistent plan");
+  for (int32_t b = 0; b < B; ++b)
+    if (plan->o_indptr[b + 1] < plan->o_indptr[b])
+      return fail(PSD_ERR_INVALID_ARG, "cascade_decode_nested: o_indptr decreasing at %d", b);
+  int32_t covered_entries = 0, covered_items = 0;
+  for (int32_t s = 0; s < S; ++s) {
+    const psd_segment &g = plan->segments[s];
+    if (g.first_member != covered_entries || g.num_members < 1 || g.first_item != covered_items ||
+        g.num_items < 1 || g.start_page < 0 || g.shared_pages < 1)
+      return fail(PSD_ERR_INVALID_ARG, "cascade_decode_nested: segment %d", s);
+    covered_entries += g.num_members;
+    covered_items += g.num_items;
+    for (int32_t k = 0; k < g.num_members; ++k) {
+      const int32_t e = g.first_member + k, b = plan->members[e];
+      if (b < 0 || b >= B || (k > 0 && b <= plan->members[e - 1]))
+        return fail(PSD_ERR_INVALID_ARG, "cascade_decode_nested: segment %d members", s);
+      if (plan->member_row_base[e] < plan->o_indptr[b] ||
+          int64_t(plan->member_row_base[e]) + g.num_items > plan->o_indptr[b + 1])
+        return fail(PSD_ERR_INVALID_ARG, "cascade_decode_nested: segment %d rows of request %d", s, b);
+    }
+    for (int32_t i = g.first_item; i < g.first_item + g.num_items; ++i)
+      if (plan->l0_items[i].out_row != i - g.first_item)
+        return fail(PSD_ERR_INVALID_ARG, "cascade_decode_nested: level-0 item %d: chunk index", i);
+  }
+  if (covered_entries != E || covered_items != n0)
+    return fail(PSD_ERR_INVALID_ARG, "cascade_decode_nested: segments do not cover the lists");
+  st = validate_items(args, plan->l0_items, n0, plan->num_rows, true, E);
+  if (st == PSD_OK) st = validate_items(args, plan->l1_items, n1, plan->num_rows, false, E);
+  if (st != PSD_OK) return st;
+
+  const WorkspaceLayout lay = workspace_layout(B, n0 + n1, plan->num_rows, args->Hq, args->Dv, E);
+  if (workspace_bytes < lay.total)
+    return fail(PSD_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, lay.total);
+  PartialLaunch L1 = base_launch(args);
+  if (!dispatchable(L1)) return launch_partial(L1, ctx->dev, nullptr);
+  for (int32_t s = 0; s < S; ++s) {
+    PartialLaunch L0 = L1;
+    L0.G_cta = plan->segments[s].num_members * L1.Gm;
+    if (!dispatchable(L0)) return launch_partial(L0, ctx->dev, nullptr);
+  }
+
+  DeviceGuard g(ctx->dev.device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  std::vector<uint8_t> host(lay.lists_bytes, 0);
+  psd_work_item *hi = reinterpret_cast<psd_work_item *>(host.data() + lay.items_off);
+  if (n0) std::memcpy(hi, plan->l0_items, sizeof(psd_work_item) * n0);
+  if (n1) std::memcpy(hi + n0, plan->l1_items, sizeof(psd_work_item) * n1);
+  int32_t *ho = reinterpret_cast<int32_t *>(host.data() + lay.order_off);
+  for (int32_t i = 0; i < n0; ++i) ho[i] = i;  // level 0: one launch per segment, in item order
+  longest_first(plan->l1_items, n1, ho + n0);
+  if (E) {
+    std::memcpy(host.data() + lay.members_off, plan->members, sizeof(int32_t) * E);
+    std::memcpy(host.data() + lay.row_base_off, plan->member_row_base, sizeof(int32_t) * E);
+  }
+  std::memcpy(host.data() + lay.indptr_off, plan->o_indptr, sizeof(int32_t) * (B + 1));
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  st = upload(ctx, ws, host.data(), host.size(), s);
+  if (st != PSD_OK) return st;
+
+  float *vpart = reinterpret_cast<float *>(ws + lay.vpart_off);
+  float *lpart = reinterpret_cast<float *>(ws + lay.lpart_off);
+  int32_t *fault = reinterpret_cast<int32_t *>(ws);
+  const psd_work_item *ditems = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
+  const int32_t *dmembers = reinterpret_cast<const int32_t *>(ws + lay.members_off);
+  const int32_t *drow_base = reinterpret_cast<const int32_t *>(ws + lay.row_base_off);
+  // Every segment's level 0 and level 1 in one launch when the 16-row-group
+  // tensor-core kernel serves all of them.
+  bool fused = S > 0 && S <= PartialLaunch::kMaxFusedSegments;
+  for (int32_t k = 0; fused && k < S; ++k) {
+    PartialLaunch L0 = L1;
+    L0.G_cta = plan->segments[k].num_members * L1.Gm;
+    fused = dispatch_fused(L0, L1, ctx->dev);
+  }
+  if (fused) {
+    L1.fused_segments = S;
+    L1.fused_l0_items = n0;
+    for (int32_t k = 0; k < S; ++k) {
+      L1.seg_items[k] = plan->segments[k].num_items;
+      L1.seg_rows[k] = plan->segments[k].num_members * L1.Gm;
+      L1.seg_member0[k] = plan->segments[k].first_member;
+    }
+    L1.members = dmembers;
+    L1.member_row_base = drow_base;
+  } else if (S > 0) {  // every segment's level 0 on the side stream, after the upload
+    cudaError_t e = cudaEventRecord(ctx->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->fork, 0);
+    if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "nested fork: %s", cudaGetErrorString(e));
+    time_mark(ctx, 0, ctx->side);
+    for (int32_t k = 0; k < S; ++k) {
+      const psd_segment &gk = plan->segments[k];
+      PartialLaunch L0 = L1;
+      L0.G_cta = gk.num_members * L1.Gm;
+      L0.items = ditems + gk.first_item;
+      L0.order = nullptr;
+      L0.num_items = gk.num_items;
+      L0.members = dmembers + gk.first_member;
+      L0.member_row_base = drow_base + gk.first_member;
+      L0.v_out = vpart;
+      L0.lse_out = lpart;
+      L0.fault = fault;
+      st = launch_partial(L0, ctx->dev, ctx->side);
+      if (st != PSD_OK) return st;
+    }
+    time_mark(ctx, 1, ctx->side);
+    e = cudaEventRecord(ctx->join, ctx->side);
+    if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "nested join: %s", cudaGetErrorString(e));
+  }
+  L1.items = fused ? ditems : ditems + n0;
+  L1.order = reinterpret_cast<const int32_t *>(ws + lay.order_off) + n0;
+  L1.num_items = n1;
+  L1.v_out = vpart;
+  L1.lse_out = lpart;
+  L1.fault = fault;
+  time_mark(ctx, 2, s);
+  st = launch_partial(L1, ctx->dev, s);
+  time_mark(ctx, 3, s);
+  if (st != PSD_OK) return st;
+  const bool joined = S > 0 && !fused;
+  if (joined) {
+    cudaError_t e = cudaStreamWaitEvent(s, ctx->join, 0);
+    if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "nested join: %s", cudaGetErrorString(e));
+  }
+  time_mark(ctx, 4, s);
+  st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq, args->Dv, o,
+                    lse, ctx->dev, s, !joined && !ctx->timing);
+  time_mark(ctx, 5, s);
+  ctx->tev_used[0] = ctx->timing && joined;
+  ctx->tev_used[1] = ctx->timing;
+  ctx->tev_used[2] = ctx->timing;
+  if (st != PSD_OK) return st;
+
+  int64_t shared_pages = 0;
+  for (int32_t k = 0; k < S; ++k) shared_pages += plan->segments[k].shared_pages;
+  if (S > 0) {
+    ctx->counters.launches_cascade += 1;
+    ctx->counters.cascade_shared_tokens += shared_pages * args->page_size;
+    ctx->counters.cascade_member_sequences += E;
+  } else {
+    ctx->counters.launches_flat += 1;
+    if (plan->decline_reason != PSD_DECLINE_NONE && plan->decline_reason != PSD_DECLINE_DISABLED)
+      ctx->counters.cascade_failures += 1;
+  }
+  if (stats) {
+    stats->path = S > 0 ? 1 : 0;
+    stats->decline_reason = plan->decline_reason;
+    stats->batch = B;
+    stats->members = E;
+    stats->shared_pages = int32_t(shared_pages);
+    stats->shared_tokens = int32_t(shared_pages * args->page_size);
     stats->prefix_chunks = n0;
     stats->suffix_chunks = n1;
   }

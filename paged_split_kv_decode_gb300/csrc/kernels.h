@@ -45,10 +45,14 @@ struct PartialLaunch {
   float q_scale = 1.f;  // sm_scale * log2(e) * k_scale
   float v_scale = 1.f;
   // Fused cascade launch (16-row-group tensor-core kernel only): `items` starts
-  // with this many level-0 items of `fused_l0_rows` stacked rows, followed by the
+  // with the level-0 items of `fused_segments` segments, in segment order (segment s:
+  // seg_items[s] items of seg_rows[s] stacked rows whose members are the entries
+  // from seg_member0[s] of `members` / `member_row_base`), followed by the
   // num_items level-1 items (order indexes those).
-  int32_t fused_l0_items = 0;
-  int32_t fused_l0_rows = 0;
+  static constexpr int kMaxFusedSegments = 8;
+  int32_t fused_segments = 0;
+  int32_t fused_l0_items = 0;  // sum of seg_items
+  int32_t seg_items[kMaxFusedSegments] = {}, seg_rows[kMaxFusedSegments] = {}, seg_member0[kMaxFusedSegments] = {};
 };
 
 bool partial_cc_supports(const PartialLaunch &p);

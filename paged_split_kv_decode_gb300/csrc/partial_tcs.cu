@@ -49,10 +49,14 @@ struct TCSParams {
   int64_t num_pages;
   int Hq_req, Dqk, Dv, page_size, Gm, G_cta;
   int tpp_log2;  // log2(page_size / 16), or -1
-  // Fused cascade launch: CTAs [0, n_l0_tasks) take level-0 item blockIdx.x / rg0,
-  // row group blockIdx.x % rg0 (G_l0 stacked rows); the rest take level-1 items
-  // l1_base + order[...].  A plain launch has n_l0_tasks = 0 and l1_base = 0.
-  int n_l0_tasks, rg0, G_l0, l1_base;
+  // Fused cascade launch: CTAs [0, n_l0_tasks) are level-0 tasks of nseg segments;
+  // segment s owns tasks [seg_task_end[s-1], seg_task_end[s]) = its items from
+  // seg_item0[s] times its ceil(seg_rows[s] / 16) row groups, with member entries
+  // from seg_member0[s].  The rest take level-1 items l1_base + order[...].  A plain
+  // launch has n_l0_tasks = 0 and l1_base = 0.
+  int n_l0_tasks, l1_base, nseg;
+  int seg_task_end[PartialLaunch::kMaxFusedSegments], seg_item0[PartialLaunch::kMaxFusedSegments];
+  int seg_rows[PartialLaunch::kMaxFusedSegments], seg_member0[PartialLaunch::kMaxFusedSegments];
   float q_scale, v_scale;
 };
 
@@ -100,11 +104,17 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
   // 128-byte-swizzled TMA boxes need 1024-byte aligned destinations.
   uint8_t *base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int item_index, group, G_rows;
+  int item_index, group, G_rows, member0 = 0;
   if (int(blockIdx.x) < p.n_l0_tasks) {
-    item_index = blockIdx.x / p.rg0;
-    group = blockIdx.x - item_index * p.rg0;
-    G_rows = p.G_l0;
+    const int task = int(blockIdx.x);
+    int sg = 0;
+    while (sg + 1 < p.nseg && task >= p.seg_task_end[sg]) ++sg;
+    const int local = task - (sg ? p.seg_task_end[sg - 1] : 0);
+    const int rg = (p.seg_rows[sg] + 15) >> 4;
+    item_index = p.seg_item0[sg] + local / rg;
+    group = local - (local / rg) * rg;
+    G_rows = p.seg_rows[sg];
+    member0 = p.seg_member0[sg];
   } else {
     const int j = blockIdx.x - p.n_l0_tasks;
     item_index = p.l1_base + (p.order ? __ldg(p.order + j) : j);
@@ -133,7 +143,7 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
       const int g = row0 + r0 + 8 * h;
       if (g < G_rows) {
         const int m = g / p.Gm;
-        const int qb = it.q_index >= 0 ? it.q_index : __ldg(p.members + m);
+        const int qb = it.q_index >= 0 ? it.q_index : __ldg(p.members + member0 + m);
         const int head = kv * p.Gm + (g - m * p.Gm);
         qrow[h] = p.q + (int64_t(qb) * p.Hq_req + head) * p.Dqk;
       }
@@ -363,7 +373,7 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
     const bool live = M != neg_inf();
     const float f = live ? p.v_scale / L : 0.f;
     const int m = g / p.Gm;
-    const int row = it.q_index >= 0 ? it.out_row : __ldg(p.member_row_base + m) + it.out_row;
+    const int row = it.q_index >= 0 ? it.out_row : __ldg(p.member_row_base + member0 + m) + it.out_row;
     const int head = kv * p.Gm + (g - m * p.Gm);
     const int64_t orow = int64_t(row) * p.Hq_req + head;
     *reinterpret_cast<float4 *>(p.v_out + orow * p.Dv + d) = make_float4(O.x * f, O.y * f, O.z * f, O.w * f);
@@ -421,15 +431,27 @@ psd_status launch_tcs(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_
   p.q_scale = L.q_scale;
   p.v_scale = L.v_scale;
   p.n_l0_tasks = 0;
-  p.rg0 = 1;
-  p.G_l0 = 0;
   p.l1_base = 0;
+  p.nseg = 0;
   unsigned grid_x = static_cast<unsigned>(L.num_items), grid_z = static_cast<unsigned>((L.G_cta + 15) / 16);
-  if (L.fused_l0_items > 0) {  // level-0 items precede L.items' level-1 items
-    p.rg0 = (L.fused_l0_rows + 15) / 16;
-    p.n_l0_tasks = L.fused_l0_items * p.rg0;
-    p.G_l0 = L.fused_l0_rows;
-    p.l1_base = L.fused_l0_items;
+  if (L.fused_segments > 0) {  // level-0 items of every segment precede L.items' level-1 items
+    if (L.fused_segments > PartialLaunch::kMaxFusedSegments)
+      return fail(PSD_ERR_UNSUPPORTED, "fused cascade launch: %d segments > %d", L.fused_segments,
+                  PartialLaunch::kMaxFusedSegments);
+    int64_t tasks = 0;
+    int item0 = 0;
+    for (int sg = 0; sg < L.fused_segments; ++sg) {
+      tasks += int64_t(L.seg_items[sg]) * ((L.seg_rows[sg] + 15) / 16);
+      if (tasks > 0x7fffffffLL) return fail(PSD_ERR_UNSUPPORTED, "fused cascade launch: too many tasks");
+      p.seg_task_end[sg] = int(tasks);
+      p.seg_item0[sg] = item0;
+      p.seg_rows[sg] = L.seg_rows[sg];
+      p.seg_member0[sg] = L.seg_member0[sg];
+      item0 += L.seg_items[sg];
+    }
+    p.nseg = L.fused_segments;
+    p.n_l0_tasks = int(tasks);
+    p.l1_base = item0;
     grid_x = static_cast<unsigned>(p.n_l0_tasks + L.num_items);
     grid_z = 1;  // level-1 items have G_cta <= 16 rows (checked by the caller)
   }

@@ -279,3 +279,158 @@ extern "C" psd_status psd_plan_capacity(const psd_page_table *host, int32_t *bat
   if (item_capacity) *item_capacity = std::max(host->page_indptr[host->batch], 1);
   return PSD_OK;
 }
+
+// ------------------------------------------------ several and nested shared spans
+// (An extension the pages scope out: mlxcel PR #1004, Task item 1 "One shared level
+// only, as scoped"; Left out / unsure, nested sharing of a system prompt plus a
+// per-tenant sub-prefix.)  Every first-page group passing the thresholds becomes a
+// segment; inside a segment the members regroup by their page at its end and the
+// same rules apply from there, up to max_levels; segments depth first, groups in
+// order of their lowest batch index.
+namespace psd {
+namespace {
+
+struct Seg {
+  std::vector<int32_t> members;
+  int32_t start, span;
+};
+
+void find_segments(const psd_page_table *t, const std::vector<int32_t> &cands, int32_t start,
+                   int32_t level, int32_t max_levels, size_t need, int32_t min_span, std::vector<Seg> &out) {
+  const int32_t *ip = t->page_indptr, *ix = t->page_indices;
+  std::unordered_map<int32_t, int32_t> slot;
+  std::vector<std::vector<int32_t>> groups;
+  for (int32_t b : cands) {
+    if (pages_of(t, b) - 1 - start < 1) continue;  // no shareable page at `start`
+    auto ins = slot.emplace(ix[ip[b] + start], int32_t(groups.size()));
+    if (ins.second) groups.emplace_back();
+    groups[ins.first->second].push_back(b);
+  }
+  for (auto &g : groups) {
+    if (g.size() < need) continue;
+    int32_t cap = pages_of(t, g[0]);
+    for (int32_t b : g) cap = std::min(cap, pages_of(t, b));
+    cap -= 1 + start;
+    int32_t span = 0;
+    const int32_t *lead = ix + ip[g[0]];
+    for (; span < cap; ++span) {
+      bool same = true;
+      for (size_t k = 1; k < g.size() && same; ++k) same = ix[ip[g[k]] + start + span] == lead[start + span];
+      if (!same) break;
+    }
+    if (span < min_span) continue;
+    out.push_back(Seg{g, start, span});
+    if (level < max_levels) find_segments(t, g, start + span, level + 1, max_levels, need, min_span, out);
+  }
+}
+
+}  // namespace
+}  // namespace psd
+
+using psd::clear_error;
+using psd::fail;
+
+extern "C" psd_status psd_plan_nested_capacity(const psd_page_table *host, int32_t max_levels,
+                                               int32_t *batch_capacity, int32_t *entry_capacity,
+                                               int32_t *segment_capacity, int32_t *item_capacity) {
+  clear_error();
+  psd_status st = psd::validate_table(host, -1);
+  if (st != PSD_OK) return st;
+  if (max_levels < 1 || max_levels > 8) return fail(PSD_ERR_INVALID_ARG, "max_levels %d outside [1, 8]", max_levels);
+  const int32_t B = std::max(host->batch, 1);
+  if (batch_capacity) *batch_capacity = B;
+  if (entry_capacity) *entry_capacity = B * max_levels;
+  if (segment_capacity) *segment_capacity = B * max_levels;
+  if (item_capacity) *item_capacity = std::max(host->page_indptr[host->batch], 1);
+  return PSD_OK;
+}
+
+extern "C" psd_status psd_plan_nested(const psd_page_table *host, int32_t tile_tokens, int32_t enable,
+                                      int32_t min_shared_pages, int32_t min_members, int32_t max_levels,
+                                      psd_nested_plan *plan) {
+  clear_error();
+  psd_status st = psd::validate_table(host, -1);
+  if (st != PSD_OK) return st;
+  if (!plan || !plan->segments || !plan->members || !plan->member_row_base || !plan->l0_items ||
+      !plan->l1_items || !plan->o_indptr)
+    return fail(PSD_ERR_INVALID_ARG, "nested plan: NULL array");
+  if (max_levels < 1 || max_levels > 8) return fail(PSD_ERR_INVALID_ARG, "max_levels %d outside [1, 8]", max_levels);
+  const int32_t B = host->batch, P = host->page_size;
+  if (tile_tokens < 1 || tile_tokens % P != 0)
+    return fail(PSD_ERR_INVALID_ARG, "tile_tokens %d is not a positive multiple of page_size %d", tile_tokens, P);
+  if (plan->batch_capacity < B) return fail(PSD_ERR_INVALID_ARG, "nested plan: batch_capacity < batch");
+  if (enable < 0) enable = psd_cascade_env_enabled(0);
+
+  std::vector<psd::Seg> segs;
+  if (enable) {
+    std::vector<int32_t> all(static_cast<size_t>(B));
+    for (int32_t b = 0; b < B; ++b) all[size_t(b)] = b;
+    psd::find_segments(host, all, 0, 1, max_levels, size_t(std::max(2, min_members)),
+                       std::max(1, min_shared_pages), segs);
+  }
+  int32_t reason = PSD_DECLINE_NONE;
+  if (!enable) {
+    reason = PSD_DECLINE_DISABLED;
+  } else if (segs.empty()) {  // the top level applies the two-level tests: same reason
+    std::vector<int32_t> tmp(static_cast<size_t>(std::max(B, 1)));
+    int32_t nm = 0, span = 0;
+    st = detect_shared_prefix(host, min_shared_pages, min_members, tmp.data(), &nm, &span, &reason);
+    if (st != PSD_OK) return st;
+  }
+  if (int32_t(segs.size()) > plan->segment_capacity)
+    return fail(PSD_ERR_INVALID_ARG, "nested plan: segment_capacity too small");
+
+  // level-0 items and member lists by segment
+  int32_t n0 = 0, entries = 0;
+  std::vector<int32_t> seg_chunks(static_cast<size_t>(segs.size()));
+  for (size_t s = 0; s < segs.size(); ++s) {
+    const psd::Seg &g = segs[s];
+    psd_segment &d = plan->segments[s];
+    d.first_member = entries;
+    d.num_members = int32_t(g.members.size());
+    d.start_page = g.start;
+    d.shared_pages = g.span;
+    d.first_item = n0;
+    const int32_t c = psd::emit_chunks(-1, host->page_indptr[g.members[0]] + g.start, int64_t(g.span) * P,
+                                       tile_tokens, P, 0, plan->l0_items, plan->item_capacity, &n0);
+    if (c < 0) return fail(PSD_ERR_INVALID_ARG, "nested plan: item_capacity too small");
+    d.num_items = c;
+    seg_chunks[s] = c;
+    if (entries + d.num_members > plan->entry_capacity)
+      return fail(PSD_ERR_INVALID_ARG, "nested plan: entry_capacity too small");
+    for (int32_t b : g.members) plan->members[entries++] = b;
+  }
+  // rows: each request's segments in segment order, then its level-1 chunks
+  std::vector<std::vector<std::pair<int32_t, int32_t>>> of_request(static_cast<size_t>(B));  // (segment, entry)
+  for (size_t s = 0; s < segs.size(); ++s)
+    for (int32_t k = 0; k < plan->segments[s].num_members; ++k) {
+      const int32_t e = plan->segments[s].first_member + k;
+      of_request[size_t(plan->members[e])].push_back({int32_t(s), e});
+    }
+  int32_t n1 = 0;
+  plan->o_indptr[0] = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    int32_t r = plan->o_indptr[b], deepest = 0;
+    for (auto &se : of_request[size_t(b)]) {
+      plan->member_row_base[se.second] = r;
+      r += seg_chunks[size_t(se.first)];
+      deepest = std::max(deepest, segs[size_t(se.first)].start + segs[size_t(se.first)].span);
+    }
+    const int32_t c = psd::emit_chunks(b, host->page_indptr[b] + deepest,
+                                       psd::tokens_of(host, b) - int64_t(deepest) * P, tile_tokens, P, r,
+                                       plan->l1_items, plan->item_capacity, &n1);
+    if (c < 0) return fail(PSD_ERR_INVALID_ARG, "nested plan: item_capacity too small");
+    plan->o_indptr[b + 1] = r + c;
+  }
+  plan->batch = B;
+  plan->page_size = P;
+  plan->tile_tokens = tile_tokens;
+  plan->max_levels = max_levels;
+  plan->num_segments = int32_t(segs.size());
+  plan->num_entries = entries;
+  plan->decline_reason = reason;
+  plan->l0_num_items = n0;
+  plan->l1_num_items = n1;
+  plan->num_rows = plan->o_indptr[B];
+  return PSD_OK;
+}

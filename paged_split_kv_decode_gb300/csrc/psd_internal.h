@@ -34,16 +34,19 @@ struct WorkspaceLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// member_entries: length of the members / member_row_base lists (the batch for a
+// two-level plan, the (segment, member) entries for a nested one).
 inline WorkspaceLayout workspace_layout(int32_t batch, int32_t num_items, int64_t num_rows,
-                                        int32_t Hq, int32_t Dv) {
+                                        int32_t Hq, int32_t Dv, int32_t member_entries = -1) {
+  if (member_entries < 0) member_entries = batch;
   WorkspaceLayout L;
   L.lists_off = 0;  // the header travels with the lists in the same copy
   L.items_off = 256;
   const size_t n = size_t(num_items > 0 ? num_items : 0);
   L.order_off = L.items_off + sizeof(psd_work_item) * n;
   L.members_off = L.order_off + sizeof(int32_t) * n;
-  L.row_base_off = L.members_off + sizeof(int32_t) * size_t(batch);
-  L.indptr_off = L.row_base_off + sizeof(int32_t) * size_t(batch);
+  L.row_base_off = L.members_off + sizeof(int32_t) * size_t(member_entries);
+  L.indptr_off = L.row_base_off + sizeof(int32_t) * size_t(member_entries);
   L.lists_bytes = L.indptr_off + sizeof(int32_t) * size_t(batch + 1);
   L.vpart_off = align256(L.lists_bytes);
   L.lpart_off = L.vpart_off + align256(sizeof(float) * size_t(num_rows) * size_t(Hq) * size_t(Dv));

@@ -146,6 +146,35 @@ def page_table(lengths: Sequence[int], page_size: int, num_pages: int, rng,
             np.asarray(last, dtype=np.int32))
 
 
+def page_table_prefixes(lengths: Sequence[int], page_size: int, num_pages: int, rng, prefixes):
+    """CSR page table where ``prefixes`` = [(members, n_pages), ...] are shared page
+    blocks allocated once each: a request's page list is the blocks of every prefix
+    it belongs to, in list order, then its own pages (a system prompt followed by a
+    per-tenant sub-prefix, as refcounted prompt blocks would be)."""
+    lengths = [int(x) for x in lengths]
+    perm = rng.permutation(num_pages).astype(np.int64)
+    cursor = 0
+    blocks = []
+    for members, n in prefixes:
+        blocks.append((set(int(m) for m in members), perm[cursor:cursor + int(n)]))
+        cursor += int(n)
+    indptr, indices, last = [0], [], []
+    for b, L in enumerate(lengths):
+        n = (L + page_size - 1) // page_size
+        pre = [ids for mem, ids in blocks if b in mem]
+        pre = np.concatenate(pre) if pre else np.empty(0, dtype=np.int64)
+        assert n > pre.shape[0]
+        own = perm[cursor:cursor + (n - pre.shape[0])]
+        cursor += n - pre.shape[0]
+        ids = np.concatenate([pre, own])
+        assert ids.shape[0] == n, "pool too small"
+        indices.append(ids)
+        indptr.append(indptr[-1] + n)
+        last.append(L - (n - 1) * page_size)
+    return (np.asarray(indptr, dtype=np.int32), np.concatenate(indices).astype(np.int32),
+            np.asarray(last, dtype=np.int32))
+
+
 def _valid_slots(indptr, indices, last, num_pages, page_size) -> np.ndarray:
     """Per pool page: number of leading slots that hold a token (0 if unreferenced)."""
     valid = np.zeros(num_pages, dtype=np.int64)
@@ -188,8 +217,11 @@ def fill_pool_fp8(rng, num_pages, page_size, Hkv, D, valid, canary: bool):
 
 def _make(name, rng, lengths, *, Hq, Hkv, Dqk, Dv, page_size, num_pages, tile_tokens,
           kv_dtype="bf16", latent_v=False, shared=None, canary=True,
-          min_shared_pages=16, min_members=2, sm_scale=None) -> Workload:
-    indptr, indices, last = page_table(lengths, page_size, num_pages, rng, shared)
+          min_shared_pages=16, min_members=2, sm_scale=None, prefixes=None) -> Workload:
+    if prefixes is not None:
+        indptr, indices, last = page_table_prefixes(lengths, page_size, num_pages, rng, prefixes)
+    else:
+        indptr, indices, last = page_table(lengths, page_size, num_pages, rng, shared)
     valid = _valid_slots(indptr, indices, last, num_pages, page_size)
     B = len(lengths)
     if kv_dtype == "bf16":
@@ -254,6 +286,31 @@ def cascade_decode(seed: int = 0, canary: bool = True, members: int = 16,
     return _make("cascade_decode", rng, lengths, Hq=32, Hkv=8, Dqk=128, Dv=128,
                  page_size=P, num_pages=16384, tile_tokens=512,
                  shared=(member_ids, shared_pages), canary=canary)
+
+
+def nested_decode(seed: int = 0, canary: bool = True, tenants: Sequence[int] = (8, 8),
+                  system_tokens: int = 4096, tenant_tokens: int = 2048, others: int = 16,
+                  page_size: int = 16, num_pages: int = 16384) -> Workload:
+    """A system prompt shared by every tenant's requests, one sub-prefix per tenant,
+    private suffixes U[64,1024]; plus independent requests U[512,4096].  Hq=32,
+    Hkv=8, D=128, tile 512 (the flat-decode heads).  Batch positions are shuffled."""
+    rng = np.random.default_rng(seed)
+    P = page_size
+    n_mem = int(sum(tenants))
+    suffix = rng.integers(64, 1025, size=n_mem)
+    own = rng.integers(512, 4097, size=others)
+    lengths = [system_tokens + tenant_tokens + int(x) for x in suffix] + [int(x) for x in own]
+    order = rng.permutation(len(lengths))
+    lengths = [lengths[i] for i in order]
+    pos = {int(order[j]): j for j in range(len(order))}           # original index -> batch slot
+    members = [pos[i] for i in range(n_mem)]
+    groups, k = [], 0
+    for t in tenants:
+        groups.append(members[k:k + int(t)])
+        k += int(t)
+    prefixes = [(members, system_tokens // P)] + [(g, tenant_tokens // P) for g in groups]
+    return _make("nested_decode", rng, lengths, Hq=32, Hkv=8, Dqk=128, Dv=128, page_size=P,
+                 num_pages=num_pages, tile_tokens=512, canary=canary, prefixes=prefixes)
 
 
 def mla_decode(seed: int = 0, canary: bool = True, batch: int = 128,
