@@ -328,6 +328,21 @@ def barrier(world):
     torch.cuda.synchronize()
 
 
+def autotune_report(arm, reps):
+    """psd_autotune_tile on the flat batch: cold-L2 step time per candidate tile (the
+    headline keeps the configured 512-token tile)."""
+    import paged_split_kv_decode_gb300 as psd
+    w = arm.w
+    tiles = [256, 384, 512, 768, 1024, 2048]
+    items, o_indptr = psd.split_plan(arm.table, min(tiles))
+    ws = torch.empty(psd.workspace_bytes(w.batch, max(len(items), 1), int(o_indptr[-1]), w.Hq, w.Dv),
+                     dtype=torch.uint8, device="cuda")
+    best, ms = arm.ctx.autotune_tile(arm.args, arm.table, tiles, arm.o, arm.lse, ws, 1, w.min_shared_pages,
+                                     w.min_members, reps=reps)
+    return {"tiles": tiles, "step_ms": [round(x, 5) for x in ms], "best_tile": best,
+            "method": "psd_autotune_tile: cascade_decode per tile, 256 MB flush before each timed call"}
+
+
 def nested_timing(steps, warmup, flush):
     """System prompt + two tenant sub-prefixes: flat arm, two-level cascade (the
     system prompt once) and nested cascade (the tenant sub-prefixes once as well)."""
@@ -511,6 +526,8 @@ def run_ours(args):
         extra["merge_sweep"] = merge_sweep(arm.ctx, args.steps, args.warmup, flush, hbm)
     if not args.quick and args.workload in ("all", "cascade", "nested"):
         extra["nested"] = nested_timing(args.steps, args.warmup, flush)
+    if not args.quick and args.workload in ("all", "tune"):
+        extra["autotune"] = autotune_report(arm, max(3, args.steps // 4))
     if not args.quick and args.workload in ("all", "append"):
         extra["rope_append"] = rope_append_timing(arm.ctx, args.steps, args.warmup, flush)
 
@@ -612,7 +629,8 @@ def main():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--quick", action="store_true", help="flat workload only")
-    p.add_argument("--workload", choices=["all", "cascade", "mla", "merge", "append", "nested"], default="all",
+    p.add_argument("--workload", choices=["all", "cascade", "mla", "merge", "append", "nested", "tune"],
+                   default="all",
                    help="which workloads run after the flat headline")
     p.add_argument("--mla-batch", type=int, default=128, help="requests in the MLA workload")
     p.add_argument("--no-cpu-baseline", action="store_true")

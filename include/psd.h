@@ -396,6 +396,32 @@ psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args *args,
                                  void *workspace, size_t workspace_bytes,
                                  psd_cascade_stats *stats, psd_stream_t stream);
 
+/* ------------------------------------------------------------ chunk-size tuning
+ * mlxcel PR #1004, Left out / unsure: the shape-bucketed kernel autotuner with the
+ * cold-L2 benchmark methodology is not wired to either cascade geometry; both plans
+ * use the heuristic chunk size.  psd_autotune_tile times cascade_decode for each
+ * candidate tile_tokens on the caller's batch (psd_plan_decode with `enable` and the
+ * thresholds): one untimed call, then `reps` timed calls, each preceded by a write
+ * of a 256 MB device buffer the context allocates once (cold L2), timed with CUDA
+ * events on `stream`; the call is synchronous.  The candidate with the lowest mean
+ * is recorded under the batch's shape bucket: (Hq, Hkv, Dqk, Dv, kv_dtype,
+ * page_size, batch and total tokens each rounded up to a power of two, whether the
+ * plan cascades).  Candidates must be positive multiples of page_size; o, lse and
+ * the workspace are as for cascade_decode and must fit every candidate (the
+ * smallest tile has the most partial rows).  ms_out (nullable, [n_tiles]) receives
+ * the means.  Unlike the decode entry points this call allocates (the flush
+ * buffer, once per context). */
+psd_status psd_autotune_tile(psd_ctx *ctx, const psd_decode_args *args, const psd_page_table *host,
+                             const int32_t *tiles, int32_t n_tiles, int32_t enable,
+                             int32_t min_shared_pages, int32_t min_members, int32_t reps, float *o,
+                             float *lse, void *workspace, size_t workspace_bytes, psd_stream_t stream,
+                             int32_t *best_tile, float *ms_out);
+/* The tile recorded for this batch's shape bucket by psd_autotune_tile on this
+ * context, or default_tile when none was (or the arguments are invalid). */
+int32_t psd_tuned_tile(psd_ctx *ctx, const psd_decode_args *args, const psd_page_table *host,
+                       int32_t enable, int32_t min_shared_pages, int32_t min_members,
+                       int32_t default_tile);
+
 /* ---------------------------------------------------------------- RoPE + append
  * The step before decode: the new token of each request is roped and appended to
  * the paged pool (ROCm ATOM PR #1701, section 1 and 3.3: one fused kernel ropes

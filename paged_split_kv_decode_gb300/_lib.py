@@ -25,7 +25,7 @@ EXPORTS = [
     "cascade_decode", "psd_check_device_error", "cascade_decode_no_alloc",
     "psd_plan_cache_create", "psd_plan_cache_destroy", "psd_plan_cache_lookup", "psd_plan_cache_lookup_gen",
     "psd_plan_cache_stats", "rope_append_kv", "psd_plan_nested_capacity", "psd_plan_nested",
-    "psd_nested_workspace_bytes", "cascade_decode_nested",
+    "psd_nested_workspace_bytes", "cascade_decode_nested", "psd_autotune_tile", "psd_tuned_tile",
 ]
 
 
@@ -126,6 +126,10 @@ def _sig(lib):
                                               C.POINTER(C.POINTER(CascadePlan)), P_i32]
     lib.psd_plan_cache_stats.argtypes = [V, C.POINTER(i64), C.POINTER(i64), P_i32]
     lib.rope_append_kv.argtypes = [V, C.POINTER(RopeAppendArgs), V]
+    lib.psd_autotune_tile.argtypes = [V, C.POINTER(DecodeArgs), C.POINTER(PageTable), P_i32, i32, i32, i32, i32,
+                                      i32, V, V, V, C.c_size_t, V, P_i32, C.POINTER(C.c_float)]
+    lib.psd_tuned_tile.argtypes = [V, C.POINTER(DecodeArgs), C.POINTER(PageTable), i32, i32, i32, i32]
+    lib.psd_tuned_tile.restype = i32
     lib.psd_plan_nested_capacity.argtypes = [C.POINTER(PageTable), i32, P_i32, P_i32, P_i32, P_i32]
     lib.psd_plan_nested.argtypes = [C.POINTER(PageTable), i32, i32, i32, i32, i32, C.POINTER(NestedPlan)]
     lib.psd_nested_workspace_bytes.argtypes = [C.POINTER(NestedPlan), i32, i32]
@@ -146,7 +150,7 @@ def _sig(lib):
         f = getattr(lib, name)
         if f.restype is C.c_int or f.restype is None:
             if name not in ("psd_last_error", "psd_cascade_env_enabled", "psd_workspace_bytes",
-                            "psd_nested_workspace_bytes"):
+                            "psd_nested_workspace_bytes", "psd_tuned_tile"):
                 f.restype = C.c_int
 
 

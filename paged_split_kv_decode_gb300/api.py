@@ -76,6 +76,27 @@ class Context:
         L.check(L.load().psd_get_kernel_times(self._h, C.byref(a), C.byref(b), C.byref(c)))
         return {"level0_ms": a.value, "partial_ms": b.value, "merge_ms": c.value}
 
+    def autotune_tile(self, args: L.DecodeArgs, table: "HostTable", tiles, o: torch.Tensor, lse: torch.Tensor,
+                      workspace: torch.Tensor, enable: int = 1, min_shared_pages: int = 16, min_members: int = 2,
+                      reps: int = 5, stream=None):
+        """psd_autotune_tile: times cascade_decode per candidate tile (cold L2) and
+        records the fastest for this shape bucket.  Returns (best_tile, [mean ms])."""
+        t = np.ascontiguousarray(tiles, dtype=np.int32)
+        ms = (C.c_float * len(t))()
+        best = C.c_int32()
+        L.check(L.load().psd_autotune_tile(
+            self._h, C.byref(args), C.byref(table.c), t.ctypes.data_as(L.P_i32), len(t), int(enable),
+            int(min_shared_pages), int(min_members), int(reps), _dev_ptr(o, "o"), _dev_ptr(lse, "lse"),
+            _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream),
+            C.byref(best), ms))
+        return best.value, [float(x) for x in ms]
+
+    def tuned_tile(self, args: L.DecodeArgs, table: "HostTable", default_tile: int, enable: int = 1,
+                   min_shared_pages: int = 16, min_members: int = 2) -> int:
+        """psd_tuned_tile: the tile recorded for this batch's shape bucket, else default_tile."""
+        return int(L.load().psd_tuned_tile(self._h, C.byref(args), C.byref(table.c), int(enable),
+                                           int(min_shared_pages), int(min_members), int(default_tile)))
+
     def counters(self) -> dict:
         c = L.Counters()
         L.check(L.load().psd_get_counters(self._h, C.byref(c)))

@@ -241,6 +241,7 @@ extern "C" psd_status psd_destroy(psd_ctx *c) {
   if (c->join) cudaEventDestroy(c->join);
   for (auto &ev : c->tev)
     if (ev) cudaEventDestroy(ev);
+  if (c->flush) cudaFree(c->flush);
   delete c;
   return PSD_OK;
 }

@@ -1,0 +1,146 @@
+// Chunk-size autotuning per shape bucket, timed cold (mlxcel PR #1004, Left out /
+// unsure: the shape-bucketed autotuner with cold-L2 methodology is not wired to
+// either cascade geometry; both plans use the heuristic chunk size).  Host code
+// only: every timed call is the public cascade_decode on the caller's batch.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "context.h"
+
+namespace psd {
+namespace {
+
+constexpr size_t kFlushBytes = size_t(256) << 20;  // about twice the 129 MB L2
+
+int64_t pow2_ceil(int64_t x) {
+  int64_t p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// The shape bucket of a batch; `ok` is false for an invalid table.
+std::array<int64_t, 9> bucket(const psd_decode_args *a, const psd_page_table *h, int32_t enable,
+                              int32_t min_shared_pages, int32_t min_members, bool *ok) {
+  std::array<int64_t, 9> k{};
+  *ok = validate_table(h, -1) == PSD_OK && a != nullptr;
+  if (!*ok) return k;
+  int64_t tokens = 0;
+  for (int32_t b = 0; b < h->batch; ++b)
+    tokens += int64_t(h->page_indptr[b + 1] - h->page_indptr[b] - 1) * h->page_size + h->last_page_len[b];
+  bool cascades = false;
+  if (enable < 0) enable = psd_cascade_env_enabled(0);
+  if (enable) {
+    std::vector<int32_t> m(static_cast<size_t>(std::max(h->batch, 1)));
+    int32_t nm = 0, span = 0, reason = 0;
+    cascades = detect_shared_prefix(h, min_shared_pages, min_members, m.data(), &nm, &span, &reason) == PSD_OK &&
+               nm > 0;
+  }
+  k = {a->Hq, a->Hkv, a->Dqk, a->Dv, a->kv_dtype, h->page_size, pow2_ceil(std::max(h->batch, 1)),
+       pow2_ceil(std::max<int64_t>(tokens, 1)), cascades ? 1 : 0};
+  return k;
+}
+
+}  // namespace
+}  // namespace psd
+
+using psd::fail;
+
+extern "C" psd_status psd_autotune_tile(psd_ctx *ctx, const psd_decode_args *args, const psd_page_table *host,
+                                        const int32_t *tiles, int32_t n_tiles, int32_t enable,
+                                        int32_t min_shared_pages, int32_t min_members, int32_t reps, float *o,
+                                        float *lse, void *workspace, size_t workspace_bytes, psd_stream_t stream,
+                                        int32_t *best_tile, float *ms_out) {
+  psd::clear_error();
+  if (!ctx || !args || !host || !tiles || n_tiles < 1 || reps < 1 || !best_tile)
+    return fail(PSD_ERR_INVALID_ARG, "psd_autotune_tile: NULL or empty arguments");
+  bool ok = false;
+  const auto key = psd::bucket(args, host, enable, min_shared_pages, min_members, &ok);
+  if (!ok) return fail(PSD_ERR_INVALID_ARG, "psd_autotune_tile: invalid page table");
+  for (int32_t i = 0; i < n_tiles; ++i)
+    if (tiles[i] < host->page_size || tiles[i] % host->page_size)
+      return fail(PSD_ERR_INVALID_ARG, "psd_autotune_tile: tile %d is not a positive multiple of page_size %d",
+                  tiles[i], host->page_size);
+  psd::DeviceGuard g(ctx->dev.device);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!ctx->flush) {
+    cudaError_t e = cudaMalloc(&ctx->flush, psd::kFlushBytes);
+    if (e != cudaSuccess) {
+      ctx->flush = nullptr;
+      return fail(PSD_ERR_CUDA, "psd_autotune_tile: flush buffer: %s", cudaGetErrorString(e));
+    }
+    ctx->flush_bytes = psd::kFlushBytes;
+  }
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  cudaError_t ce = cudaEventCreate(&e0);
+  if (ce == cudaSuccess) ce = cudaEventCreate(&e1);
+  if (ce != cudaSuccess) {
+    if (e0) cudaEventDestroy(e0);
+    return fail(PSD_ERR_CUDA, "psd_autotune_tile: events: %s", cudaGetErrorString(ce));
+  }
+  int32_t bc = 0, ic = 0;
+  psd_status st = psd_plan_capacity(host, &bc, &ic);
+  std::vector<int32_t> mem(static_cast<size_t>(bc)), rb(static_cast<size_t>(bc)), oi(static_cast<size_t>(bc) + 1);
+  std::vector<psd_work_item> l0(static_cast<size_t>(ic)), l1(static_cast<size_t>(ic));
+  float best_ms = 0.f;
+  int32_t best = -1;
+  for (int32_t i = 0; st == PSD_OK && i < n_tiles; ++i) {
+    psd_cascade_plan plan{};
+    plan.batch_capacity = bc;
+    plan.item_capacity = ic;
+    plan.members = mem.data();
+    plan.member_row_base = rb.data();
+    plan.l0_items = l0.data();
+    plan.l1_items = l1.data();
+    plan.o_indptr = oi.data();
+    st = psd_plan_decode(host, tiles[i], enable, min_shared_pages, min_members, &plan);
+    if (st != PSD_OK) break;
+    st = cascade_decode(ctx, args, &plan, o, lse, workspace, workspace_bytes, nullptr, stream);  // untimed
+    double total = 0.0;
+    for (int32_t r = 0; st == PSD_OK && r < reps; ++r) {
+      ce = cudaMemsetAsync(ctx->flush, r & 0xFF, ctx->flush_bytes, s);
+      if (ce == cudaSuccess) ce = cudaEventRecord(e0, s);
+      if (ce != cudaSuccess) {
+        st = fail(PSD_ERR_CUDA, "psd_autotune_tile: %s", cudaGetErrorString(ce));
+        break;
+      }
+      st = cascade_decode(ctx, args, &plan, o, lse, workspace, workspace_bytes, nullptr, stream);
+      if (st != PSD_OK) break;
+      float ms = 0.f;
+      ce = cudaEventRecord(e1, s);
+      if (ce == cudaSuccess) ce = cudaEventSynchronize(e1);
+      if (ce == cudaSuccess) ce = cudaEventElapsedTime(&ms, e0, e1);
+      if (ce != cudaSuccess) {
+        st = fail(PSD_ERR_CUDA, "psd_autotune_tile: timing: %s", cudaGetErrorString(ce));
+        break;
+      }
+      total += ms;
+    }
+    if (st != PSD_OK) break;
+    const float mean = float(total / reps);
+    if (ms_out) ms_out[i] = mean;
+    if (best < 0 || mean < best_ms) {
+      best = tiles[i];
+      best_ms = mean;
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (st != PSD_OK) return st;
+  ctx->tuned[key] = best;
+  *best_tile = best;
+  return PSD_OK;
+}
+
+extern "C" int32_t psd_tuned_tile(psd_ctx *ctx, const psd_decode_args *args, const psd_page_table *host,
+                                  int32_t enable, int32_t min_shared_pages, int32_t min_members,
+                                  int32_t default_tile) {
+  psd::clear_error();
+  if (!ctx) return default_tile;
+  bool ok = false;
+  const auto key = psd::bucket(args, host, enable, min_shared_pages, min_members, &ok);
+  if (!ok) return default_tile;
+  auto it = ctx->tuned.find(key);
+  return it == ctx->tuned.end() ? default_tile : it->second;
+}

@@ -3,6 +3,9 @@
 
 #include <cuda_runtime.h>
 
+#include <array>
+#include <map>
+
 #include "kernels.h"
 #include "psd_internal.h"
 
@@ -24,6 +27,11 @@ struct psd_ctx {
   bool timing = false;
   cudaEvent_t tev[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   bool tev_used[3] = {false, false, false};
+  // Chunk sizes chosen by psd_autotune_tile, by shape bucket, and the cold-L2 flush
+  // buffer it writes between timed calls (allocated on its first use).
+  std::map<std::array<int64_t, 9>, int32_t> tuned;
+  void *flush = nullptr;
+  size_t flush_bytes = 0;
 };
 
 namespace psd {
