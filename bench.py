@@ -305,18 +305,22 @@ def oracle_baseline(w, budget_s: float = 12.0):
 
 # ------------------------------------------------------------------- main paths
 def dist_setup(n):
+    """Replicas under torchrun: one process per GPU over NCCL (gloo without a GPU, as
+    in the CPU tests).  Returns (rank, world, local_rank)."""
     if n <= 1 or "RANK" not in os.environ:
         return 0, 1, int(os.environ.get("LOCAL_RANK", 0))
     import torch.distributed as dist
-    dist.init_process_group("nccl")
+    dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return dist.get_rank(), dist.get_world_size(), int(os.environ.get("LOCAL_RANK", 0))
 
 
 def dist_max(x: float, world: int) -> float:
+    """The maximum of x over the ranks (the slowest replica sets the job's time)."""
     if world <= 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], device=dev, dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -325,7 +329,15 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
+
+
+def replica_throughput(bytes_per_rank: int, ms_local: float, world: int) -> tuple:
+    """Whole-job GB/s of `world` replicas that each process bytes_per_rank per step:
+    all ranks' bytes over the slowest rank's step time.  Returns (GB/s, max ms)."""
+    ms_max = dist_max(ms_local, world)
+    return world * bytes_per_rank / (ms_max * 1e-3) / 1e9, ms_max
 
 
 def autotune_report(arm, reps):
@@ -459,8 +471,7 @@ def run_ours(args):
     algo = partial_algorithmic_bytes(arm)
     merge_bytes = merge_algorithmic_bytes(arm)
     ms = statistics.mean(times)
-    ms_max = dist_max(ms, world)
-    value = world * kv_bytes / (ms_max * 1e-3) / 1e9
+    value, ms_max = replica_throughput(kv_bytes, ms, world)
     k_ms = kt["partial_ms"]
     achieved = algo / (k_ms * 1e-3) / 1e9
     k_ms_cc = kt_cc["partial_ms"]
