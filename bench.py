@@ -39,8 +39,8 @@ NOMINAL_HBM_GBS = 8000.0
 # ncu capture summarised in profiles/partial_tcs_flat_decode.md.  Reported only while
 # the kernel source is the one the counters were taken on.
 TRAFFIC_SOURCE = os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", "partial_tcs.cu")
-TRAFFIC_SHA256 = "1b7f365523ca4dd3a85bb4a7eb725cf35520dc07f91f6c19d02f00ed1d98dbc7"
-TRAFFIC_BYTES = 316073728 + 1193984
+TRAFFIC_SHA256 = "bdf00e09fac468e2d0a0a015ca0724da4f4f1508a8fed112c43a4c3c0effa93f"
+TRAFFIC_BYTES = 316077568 + 1174272
 
 
 def partial_traffic():
