@@ -79,8 +79,8 @@ typedef enum {
 enum {
   PSD_FAULT_PAGE_ID = 1,      /* a page id outside [0, num_pages) was skipped */
   PSD_FAULT_WAIT_TIMEOUT = 2, /* a bounded barrier wait gave up */
-  PSD_FAULT_RANGE = 4         /* a query value outside the f16 range reached the
-                                 f16 MLA tensor-core path (|q| > 65504) */
+  PSD_FAULT_RANGE = 4         /* an index outside the range an operation accepts
+                                 (a RoPE position past the cos/sin table) */
 };
 
 /* CSR page table (Detection section: PagedCsrView).  Host or device arrays. */

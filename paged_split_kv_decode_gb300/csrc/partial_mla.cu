@@ -1,5 +1,6 @@
 // K2t: split-KV partial attention for the MLA latent shape on the 5th-generation
-// tensor cores (tcgen05.mma with TMEM accumulators).
+// tensor cores, computed straight on the fp8-e4m3 latent (tcgen05.mma
+// kind::f8f6f4, TMEM accumulators).
 //
 // Shape: 128 query heads over one 576-wide latent KV head stored as fp8-e4m3 with
 // a per-tensor scale; V is the first 512 columns of the same latent rows (ROCm
@@ -8,30 +9,31 @@
 // its (V, LSE) outputs in log2 units).
 //
 // GB300 design.  One CTA per (work item, half of the 512 V columns), 64-token
-// tiles.  TMEM (512 columns) holds the O half [128 x 256] f32, S [128 x 64] f32 and
-// the first 384 of Q's 576 columns as the MMA's A operand (f16 pairs); the other
-// 192 Q columns stay in shared memory (128-byte swizzle).  An M=128, K=16 MMA costs
-// about the same issue time at N=32 and N=64, so 64-token tiles halve the QK^T
-// instruction count per token; to fit them, the f16 K tile is never whole in
-// shared memory: it streams through a ring of 64-column blocks [64 tokens x 64],
-// each released by the commit of the four MMAs that read it.  The MMAs run in
-// f16: e4m3 codes widen exactly to f16 with one hardware conversion per pair, Q is
-// converted from bf16 once per item (exact for |q| in [2^-14, 65504]; overflow
-// sets a fault bit), and P in f16 keeps 3 more mantissa bits than bf16.  Roles:
-//   * eight converter warps, in two groups taking alternate tiles, hold a tile of
-//     fp8 latent rows in registers (128-bit loads issued two tiles ahead) and
-//     widen them block by block into the K ring and into this CTA's V half (3
-//     tile buffers, freed when PV is done);
-//   * the control warp issues S = Q K^T block by block (24 MMAs with
-//     A in TMEM, 12 from shared memory; M=128, N=64, K=16) and O += P V (4 MMAs of
-//     M=128, N=256, K=16, V MN-major), each group committed to an mbarrier;
-//   * row warps 0-3 (thread = head = TMEM lane) first move their Q row into TMEM,
-//     then per tile read 64 scores with tcgen05.ld, free S, keep a lazily-updated
-//     running max (O is rescaled in TMEM only when the max grows by more than 2^8),
-//     write P as f16 into a 128B-swizzled tile and sum P (in f32) into l.
-// The k_scale folds into the score scale and v_scale into the output.  The two CTAs
-// of an item (one per V half) both compute S; the tile is read from HBM once and
-// from L2 by the second CTA.  Every mbarrier wait is bounded.
+// tiles, one tile per 64-row page block.
+//   * Operands.  The latent tile is loaded by TMA as nine [64 tokens x 64 B] boxes
+//     with the 64-byte swizzle and used as it lands: K-major for S = Q K^T and,
+//     for this CTA's four V boxes, MN-major for O += P V.  No widening, no copy.
+//   * Precision.  Q and P enter the e4m3 MMAs as two terms each, hi = e4m3(x) and
+//     lo = e4m3(x - hi), which keeps 8 significant bits: a bf16 query row scaled
+//     by a power of two (its largest element to [128, 256)) splits exactly down
+//     to about 2^-10 of that element, and P carries a 2^-8 relative error.  The
+//     two-term S costs 36 MMAs of M=128, N=64, K=32 per tile, the same count and
+//     issue time as the K=16 f16 form; PV is 4 MMAs of N=256.
+//   * TMEM (512 columns): O's half [128 x 256] f32, two S buffers [128 x 64] f32,
+//     Q_hi[:, 0:512] as the A operand (4 e4m3 per column).  The row warps write P
+//     (hi and lo, 32 columns) over the S buffer it came from and the PV MMAs read
+//     A from there.  Q_hi[:, 512:576] and Q_lo stay in shared memory.
+//   * Roles: row warps 0-3 (thread = head = TMEM lane) convert Q once per item and
+//     run a lazily rescaled online softmax (O is rescaled in TMEM only when the
+//     running max grows by more than 2^4, so P <= 2^8 fits e4m3); control warp 4
+//     issues the MMAs (converged warp, one elected lane); producer warp 5 issues
+//     the TMA loads of four tile buffers and zeroes the rows past the end of a
+//     ragged last tile.
+//   * Per tile the control warp waits twice (tile landed, P written) and commits
+//     twice (S ready, tile and P consumed).
+// The k_scale and the query row's power of two fold into the score scale, v_scale
+// into the output.  The two CTAs of an item both compute S; the tile is read from
+// HBM once and from L2 by the second CTA.  Every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -47,47 +49,44 @@ namespace {
 
 constexpr int kTokM = 64;                       // tokens per tile
 constexpr int kDqkM = 576, kDvM = 512, kDvHalf = 256, kRowsM = 128;
-constexpr int kQBoxes = kDqkM / 64;             // 9 boxes of 64 columns
-constexpr int kKBlocks = kDqkM / 64;            // 9 K blocks of 64 columns per tile
-constexpr int kQHeadBoxes = 6;                  // Q[:, 0:384] moves to TMEM
-constexpr int kGroupSlots = 4;                  // K ring slots of each converter group
-constexpr int kRing = 2 * kGroupSlots;          // K ring slots
-constexpr int kVBufs = 3;                       // V tile buffers
-constexpr uint32_t kQBytes = kRowsM * kDqkM * 2;        // 147456 (TMA landing)
-constexpr uint32_t kQBoxBytes = kRowsM * 128;           // 16384
-constexpr uint32_t kKBlockBytes = kTokM * 128;          // 8192: 64 tokens x 64 f16
-constexpr uint32_t kVTileBytes = kTokM * kDvHalf * 2;   // 32768
-constexpr uint32_t kPBytes = kRowsM * kTokM * 2;        // 16384
-// Shared memory: Q tail (3 boxes) | K ring | V0 | V1 | V2 | P | barriers.  Q lands by
-// TMA with its 6 head boxes over the K ring and V, free until the head is in TMEM.
-constexpr uint32_t kOffQT = 0;
-constexpr uint32_t kOffK = kOffQT + 3 * kQBoxBytes;     // 49152
-constexpr uint32_t kOffV0 = kOffK + kRing * kKBlockBytes;
-constexpr uint32_t kOffP = kOffV0 + kVBufs * kVTileBytes;
-constexpr uint32_t kOffQHead = kOffK;                   // 6 landing boxes
-constexpr uint32_t kOffBar = kOffP + kPBytes;
-constexpr uint32_t kSmemMLA = kOffBar + 512 + 1024;     // barriers + alignment slack
-static_assert(kOffQHead + kQHeadBoxes * kQBoxBytes <= kOffP, "Q head landing overlaps P");
-// Warp w runs on sub-partition w % 4.  Row warps 0-3 (one per TMEM lane quadrant);
-// the control warp 4 shares sub-partition 0 only with row warp 0, since issue
-// slots taken by busy warps there slow its MMA issue several-fold; the converter
-// warps are 5-7, 9-11, 13, 14 (sub-partitions 1-3); warps 8 and 12 stay idle.
-constexpr int kConvWarps = 8;
-constexpr int kCtrlWarp = 4;
-constexpr int kThreadsM = 32 * 15;
-__host__ __device__ constexpr bool is_converter_warp(int w) { return w >= 5 && w <= 14 && (w & 3) != 0; }
-__host__ __device__ constexpr int converter_index(int w) { return (w - 5) - (w - 4) / 4; }  // 0..7
+constexpr int kBoxes = kDqkM / 64;              // 9 column boxes of 64 e4m3
+constexpr int kNB = 4;                          // tile buffers
+constexpr uint32_t kBoxBytes = kTokM * 64;              // 4096: [64 tokens x 64 B]
+constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;     // 36864
+constexpr uint32_t kQBoxBytes = kRowsM * 64;            // 8192: [128 rows x 64 e4m3]
+constexpr uint32_t kQLandBytes = kRowsM * 128;          // 16384: [128 rows x 64 bf16]
+constexpr uint32_t kQBytes = kBoxes * kQLandBytes;      // 147456 bf16 query rows
+// Shared memory: 4 tile buffers | Q in e4m3 (Q_hi box 8, Q_lo boxes 0..8) | barriers.
+constexpr uint32_t kOffK = 0;
+constexpr uint32_t kOffQS = kOffK + kNB * kTileBytes;           // 147456
+constexpr uint32_t kOffQHiTail = kOffQS;
+constexpr uint32_t kOffQLo = kOffQS + kQBoxBytes;
+constexpr uint32_t kOffBar = kOffQS + (1 + kBoxes) * kQBoxBytes;  // 229376
+constexpr uint32_t kSmemMLA = kOffBar + 256 + 1024;              // barriers + alignment slack
+// The bf16 query lands (before the e4m3 split) in the Q area (5 boxes) and tile
+// buffers 3 and 2 (2 boxes each); tiles 0 and 1 load meanwhile.
+__host__ __device__ constexpr uint32_t q_land(int b) {
+  return b < 5 ? kOffQS + uint32_t(b) * kQLandBytes
+               : b < 7 ? kOffK + 3 * kTileBytes + uint32_t(b - 5) * kQLandBytes
+                       : kOffK + 2 * kTileBytes + uint32_t(b - 7) * kQLandBytes;
+}
+static_assert(q_land(4) + kQLandBytes <= kOffBar, "Q landing overruns the Q area");
+static_assert(2 * kQLandBytes <= kTileBytes, "two landing boxes per tile buffer");
+static_assert(kOffQS % 1024 == 0 && (2 * kTileBytes) % 1024 == 0 && (3 * kTileBytes) % 1024 == 0,
+              "128B-swizzled landing boxes need 1024-byte alignment");
+constexpr int kRowWarps = 4, kCtrlWarp = 4, kProdWarp = 5;
+constexpr int kThreadsM = 32 * 6;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
-constexpr float kLazyRescale = 8.f;             // log2 units
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;   // S buffer b at kColS + 64 b
+constexpr float kLazyRescale = 4.f;             // log2 units
+constexpr float kPBias = 4.f;                   // P = 2^(score - m + 4) <= 2^8
 
 // mbarrier slots (uint64 each) at kOffBar
-enum { BQ = 0, BQREADY, BSFULL, BSFREE, BPFULL, BDRAIN, BPV0, BKFULL0 = BPV0 + kVBufs,
-       BKEMPTY0 = BKFULL0 + kRing, BSLOT = BKEMPTY0 + kRing };
-static_assert(BSLOT * 8 + 4 <= 512, "barrier area");
+enum { BQ = 0, BQREADY, BTAIL, BDRAIN, BSFULL0, BPFULL0 = BSFULL0 + 2, BKFULL0 = BPFULL0 + 2,
+       BKEMPTY0 = BKFULL0 + kNB, BSLOT = BKEMPTY0 + kNB };
+static_assert(BSLOT * 8 + 4 <= 256, "barrier area");
 
 struct MLAParams {
-  const uint8_t *k_pool;
   const int32_t *page_indices;
   const psd_work_item *items;
   const int32_t *order;
@@ -99,37 +98,29 @@ struct MLAParams {
   float q_scale, v_scale;
 };
 
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  // 64-byte swizzle (layout code 4), descriptor version 1
   return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
-         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(swz & 7u) << 61);
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(4) << 61);
 }
-// kind::f16 instruction descriptor: f32 accumulate, f16 A and B.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) | (uint32_t(N >> 3) << 17) |
-         (uint32_t(M >> 4) << 24);
+// kind::f8f6f4 instruction descriptor: f32 accumulate, e4m3 A and B (format 0).
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool b_mn) {
+  return (1u << 4) | (uint32_t(b_mn) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
-// A operand in TMEM (f16 pairs per 32-bit column, row m in lane m), accumulating.
-__device__ __forceinline__ void umma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                            uint32_t acc) {
+// A operand in TMEM (row m in lane m, 4 e4m3 per 32-bit column in K order).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-// Accumulating form (enable-input-d always set).
-__device__ __forceinline__ void umma_acc(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -147,6 +138,10 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Barrier among the row warps only.
+__device__ __forceinline__ void row_warps_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kRowWarps) : "memory");
 }
 #define PSD_TMEM_LD32(taddr, r)                                                                        \
   asm volatile(                                                                                        \
@@ -194,38 +189,26 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-__device__ __forceinline__ uint32_t pack2_f16(float lo, float hi) {
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&v);
+// Two floats -> two e4m3 codes (round to nearest even, saturating), `lo` in byte 0.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t v;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(v) : "f"(hi), "f"(lo));
+  return v;
 }
-__device__ __forceinline__ float f16_lo(uint32_t w) { return __low2float(*reinterpret_cast<__half2 *>(&w)); }
-__device__ __forceinline__ float f16_hi(uint32_t w) { return __high2float(*reinterpret_cast<__half2 *>(&w)); }
-// Two e4m3 codes (low 16 bits) -> f16x2, exact (hardware conversion).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
-  uint32_t h2;
-  asm("{\n\t.reg .b16 lo;\n\tmov.b32 {lo, _}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(h2) : "r"(w));
-  return h2;
+// Four floats -> hi and lo e4m3 words (element k in byte k): hi = e4m3(x),
+// lo = e4m3(x - hi); the subtraction is exact in f32.
+__device__ __forceinline__ void split4(float x0, float x1, float x2, float x3, uint32_t &hi, uint32_t &lo) {
+  const uint32_t h01 = e4m3x2(x0, x1), h23 = e4m3x2(x2, x3);
+  const float2 d01 = e4m3x2_to_float2(h01), d23 = e4m3x2_to_float2(h23);
+  hi = h01 | (h23 << 16);
+  lo = e4m3x2(x0 - d01.x, x1 - d01.y) | (e4m3x2(x2 - d23.x, x3 - d23.y) << 16);
 }
-// 8 e4m3 codes -> 8 f16, exact.
-__device__ __forceinline__ uint4 cvt8(uint32_t w0, uint32_t w1) {
-  return make_uint4(e4m3x2_to_f16x2(w0 & 0xffffu), e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 & 0xffffu),
-                    e4m3x2_to_f16x2(w1 >> 16));
-}
-// 8 bf16 -> 8 f16 (exact inside the f16 range); *bad is set on overflow.
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool *bad) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float a = bf16_lo(w[k]), b = bf16_hi(w[k]);
-    o[k] = pack2_f16(a, b);
-    *bad |= (fabsf(a) > 65504.f) | (fabsf(b) > 65504.f);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
+// Byte offset of 16-byte chunk c of row r in a 64-byte-swizzled box of 64-byte rows.
+__device__ __forceinline__ uint32_t sw64(int r, int c) { return uint32_t(r) * 64 + (uint32_t(c ^ ((r >> 1) & 3)) << 4); }
 
 __global__ void __launch_bounds__(kThreadsM, 1)
-    partial_mla_kernel(const __grid_constant__ CUtensorMap tmQ, const MLAParams p) {
+    partial_mla_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const MLAParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   dependents_may_launch();  // the merge that follows only waits for this grid
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -238,18 +221,20 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   const int half = blockIdx.z;                    // which 256 V columns
   const int P = p.page_size;
   const int n_tiles = (it.n_tokens + kTokM - 1) / kTokM;
+  const int tail = it.n_tokens - (n_tiles - 1) * kTokM;   // valid tokens of the last tile
 
   if (tid == 0) {
     mbar_init(bar(BQ), 1);
-    mbar_init(bar(BQREADY), 32 * kConvWarps + 128);
-    mbar_init(bar(BSFULL), 1);
-    mbar_init(bar(BSFREE), 4);   // one arrival per row warp
-    mbar_init(bar(BPFULL), 4);
+    mbar_init(bar(BQREADY), kRowWarps);
+    mbar_init(bar(BTAIL), 1);
     mbar_init(bar(BDRAIN), 1);
-    for (int b = 0; b < kVBufs; ++b) mbar_init(bar(BPV0 + b), 1);
-    for (int r = 0; r < kRing; ++r) {
-      mbar_init(bar(BKFULL0 + r), kConvWarps / 2);  // one arrival per warp of a group
-      mbar_init(bar(BKEMPTY0 + r), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(BSFULL0 + b), 1);
+      mbar_init(bar(BPFULL0 + b), kRowWarps);
+    }
+    for (int b = 0; b < kNB; ++b) {
+      mbar_init(bar(BKFULL0 + b), 1);
+      mbar_init(bar(BKEMPTY0 + b), 1);
     }
     fence_mbar_init();
   }
@@ -263,81 +248,115 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  if (warp == kCtrlWarp) {
-    // ------------------------------------------------------------- control warp
-    // The whole warp runs the loop and waits; one elected lane issues the MMAs.
-    // A wait on the issuing thread alone stalls the MMAs it has queued much
-    // longer, and each wait costs tensor-pipe time, so the loop waits for K
-    // blocks three at a time (a group's warps arrive on blocks in order, so the
-    // third block's barrier covers the first two) and never for V (the same
-    // warps store V before they arrive for the tile's last K block).
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------ producer warp
+    bool ok = true;
+    int issued = 0;  // tiles whose loads were issued
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(BQ), kQBytes);
 #pragma unroll 1
-      for (int b = 0; b < kQBoxes; ++b) {
-        const uint32_t dst = b < kQHeadBoxes ? kOffQHead + b * kQBoxBytes : kOffQT + (b - kQHeadBoxes) * kQBoxBytes;
-        tma_load_3d(smem_u32(sm + dst), &tmQ, b * 64, 0, it.q_index, bar(BQ));
+      for (int b = 0; b < kBoxes; ++b) tma_load_3d(smem_u32(sm + q_land(b)), &tmQ, b * 64, 0, it.q_index, bar(BQ));
+    }
+#pragma unroll 1
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int buf = j % kNB;
+      if (j >= kNB)  // PV(j - 4) has read the buffer
+        ok = mbar_wait(bar(BKEMPTY0 + buf), uint32_t(j / kNB - 1) & 1u, p.fault);
+      else if (j >= 2)  // buffers 2 and 3 hold query landing boxes until the split
+        ok = mbar_wait(bar(BQREADY), 0, p.fault);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const int tok = j * kTokM;
+      if (lane == 0) {
+        int page = __ldg(p.page_indices + it.page_off + tok / P);
+        if (page < 0 || int64_t(page) >= p.num_pages) {  // out of range: load the zero fill
+          atomicOr(p.fault, PSD_FAULT_PAGE_ID);
+          page = -1;
+        }
+        mbar_arrive_expect_tx(bar(BKFULL0 + buf), kTileBytes);
+        const uint32_t dst = smem_u32(sm + kOffK + buf * kTileBytes);
+#pragma unroll 1
+        for (int b = 0; b < kBoxes; ++b) tma_load_3d(dst + b * kBoxBytes, &tmK, b * 64, tok % P, page, bar(BKFULL0 + buf));
+      }
+      __syncwarp();
+      issued = j + 1;
+      if (j == n_tiles - 1 && tail < kTokM) {
+        // Rows past the item's last token (still inside its page) may hold anything:
+        // zero this CTA's four V boxes there, so that P = 0 never meets a NaN.
+        ok = mbar_wait(bar(BKFULL0 + buf), uint32_t(j / kNB) & 1u, p.fault);
+        if (__all_sync(0xffffffffu, ok)) {
+          uint8_t *vt = sm + kOffK + buf * kTileBytes + 4 * half * kBoxBytes;
+          const int n16 = (kTokM - tail) * 4;        // 16-byte chunks per box
+#pragma unroll 1
+          for (int c = lane; c < 4 * n16; c += 32)
+            *reinterpret_cast<uint4 *>(vt + (c / n16) * kBoxBytes + tail * 64 + (c % n16) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BTAIL));
       }
     }
-    __syncwarp();
-    bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BQREADY), 0, p.fault));  // head in TMEM, tail in f16
+    // No copy of this CTA may still be in flight when it exits.
+    mbar_wait(bar(BQ), 0, p.fault);
+    for (int j = max(0, issued - kNB); j < issued; ++j)   // the last tile of each buffer
+      mbar_wait(bar(BKFULL0 + j % kNB), uint32_t(j / kNB) & 1u, p.fault);
+  } else if (warp == kCtrlWarp) {
+    // ------------------------------------------------------------- control warp
+    // The whole warp waits; one elected lane issues.  (A wait on the issuing thread
+    // alone stalls the MMAs it has queued far longer.)
+    bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BQREADY), 0, p.fault));
     tc_fence_after();
-    const uint32_t id_qk = idesc_f16(128, kTokM, false, false);
-    const uint32_t id_pv = idesc_f16(128, kDvHalf, false, true);
+    const uint32_t id_qk = idesc_e4m3(128, kTokM, false);
+    const uint32_t id_pv = idesc_e4m3(128, kDvHalf, true);
     // Base descriptors, built once; operand steps add offsets (>> 4) to the
     // start-address field, which never carries out of it (< 256 KB).
-    const uint64_t qtd = smem_desc(smem_u32(sm + kOffQT), 16, 1024, 2);
-    const uint64_t kd = smem_desc(smem_u32(sm + kOffK), 16, 1024, 2);
-    const uint64_t pd = smem_desc(smem_u32(sm + kOffP), 16, 1024, 2);
-    const uint64_t vd = smem_desc(smem_u32(sm + kOffV0), kTokM * 128, 1024, 2);
-    const uint32_t d_s = tmem + kColS;
+    const uint64_t kd = smem_desc(smem_u32(sm + kOffK), 16, 512);
+    const uint64_t qhd = smem_desc(smem_u32(sm + kOffQHiTail), 16, 512);
+    const uint64_t qld = smem_desc(smem_u32(sm + kOffQLo), 16, 512);
+    // V (MN-major): 64-column atoms one box apart, 8-token groups 512 bytes apart
+    const uint64_t vd = smem_desc(smem_u32(sm + kOffK + 4 * half * kBoxBytes), kBoxBytes, 512);
     for (int i = 0; ok && i <= n_tiles; ++i) {
-      if (i < n_tiles) {  // S(i) = Q K(i)^T, block by block
-        if (i > 0) {      // the row warps have read S(i-1)
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(BSFREE), uint32_t(i - 1) & 1u, p.fault));
-          if (!ok) break;
-        }
-        // block b of tile i is block c of converter group i % 2, in that group's slots
-        const int c0 = (i >> 1) * kKBlocks, sbase = (i & 1) * kGroupSlots;
-#pragma unroll 1
-        for (int b = 0; b < kKBlocks; ++b) {
-          const int c = c0 + b, slot = sbase + c % kGroupSlots;
-          if (b % 3 == 0) {  // blocks b .. b+2 are in place once block b+2 is
-            const int cw = c + 2;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BKFULL0 + sbase + cw % kGroupSlots),
-                                                   uint32_t(cw / kGroupSlots) & 1u, p.fault));
-            if (!ok) break;
-            tc_fence_after();
-          }
-          if (elect_one()) {
-            const uint64_t kb = kd + ((slot * kKBlockBytes) >> 4);
-            if (b < kQHeadBoxes) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                umma_tmem_a(d_s, tmem + kColQ + 8 * (4 * b + j), kb + ((j * 32) >> 4), id_qk, (b | j) != 0);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                umma_acc(d_s, qtd + (((b - kQHeadBoxes) * kQBoxBytes + j * 32) >> 4), kb + ((j * 32) >> 4), id_qk);
-            }
-            umma_commit(bar(BKEMPTY0 + slot));
-            if (b == kKBlocks - 1) umma_commit(bar(BSFULL));
-          }
-          __syncwarp();
-        }
-        if (!ok) break;
-      }
-      if (i > 0) {  // O += P(i-1) V(i-1)
-        const int j = i - 1, vb = j % kVBufs;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(BPFULL), uint32_t(j) & 1u, p.fault));
+      if (i < n_tiles) {  // S(i) = Q K(i)^T into S buffer i % 2
+        const int buf = i % kNB;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(BKFULL0 + buf), uint32_t(i / kNB) & 1u, p.fault));
+        if (ok && i == n_tiles - 1 && tail < kTokM)
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(BTAIL), 0, p.fault));
         if (!ok) break;
         tc_fence_after();
         if (elect_one()) {
-          const uint64_t vdb = vd + ((vb * kVTileBytes) >> 4);
+          const uint32_t d_s = tmem + kColS + 64 * (i & 1);
+          const uint64_t kb = kd + ((buf * kTileBytes) >> 4);
 #pragma unroll
-          for (int k = 0; k < kTokM / 16; ++k)
-            umma(tmem + kColO, pd + ((k * 32) >> 4), vdb + ((k * 16 * 128) >> 4), id_pv, (j | k) != 0);
-          umma_commit(bar(BPV0 + vb));
+          for (int b = 0; b < kBoxes; ++b) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const uint64_t kbj = kb + ((b * kBoxBytes + j * 32) >> 4);
+              if (b < kBoxes - 1)
+                mma_ts(d_s, tmem + kColQ + 16 * b + 8 * j, kbj, id_qk, (b | j) != 0);
+              else
+                mma_ss(d_s, qhd + ((j * 32) >> 4), kbj, id_qk, 1u);
+              mma_ss(d_s, qld + ((b * kQBoxBytes + j * 32) >> 4), kbj, id_qk, 1u);
+            }
+          }
+          umma_commit(bar(BSFULL0 + (i & 1)));
+        }
+        __syncwarp();
+      }
+      if (i > 0) {  // O += P(i-1) V(i-1), P (hi | lo) in S buffer (i-1) % 2
+        const int j = i - 1, buf = j % kNB;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(BPFULL0 + (j & 1)), uint32_t(j >> 1) & 1u, p.fault));
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t a_p = tmem + kColS + 64 * (j & 1);
+          const uint64_t vb = vd + ((buf * kTileBytes) >> 4);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {  // tokens 32 k .. 32 k + 31
+            const uint64_t vbk = vb + ((k * 32 * 64) >> 4);
+            mma_ts(tmem + kColO, a_p + 8 * k, vbk, id_pv, (j | k) != 0);
+            mma_ts(tmem + kColO, a_p + 16 + 8 * k, vbk, id_pv, 1u);
+          }
+          umma_commit(bar(BKEMPTY0 + buf));
         }
         __syncwarp();
       }
@@ -346,142 +365,90 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     if (elect_one()) umma_commit(bar(BDRAIN));
     __syncwarp();
     mbar_wait(bar(BDRAIN), 0, p.fault);
-  } else if (is_converter_warp(warp)) {
-    // ------------------------------------------------------------ converter warps
-    const int cwi = converter_index(warp);
-    const int ctid = cwi * 32 + lane;
-    // Q tail: bf16 -> f16 in place (same 2-byte swizzled layout)
-    bool ok = mbar_wait(bar(BQ), 0, p.fault);
-    bool bad = false;
-    if (ok) {
-      for (int c = ctid; c < 3 * int(kQBoxBytes) / 16; c += 32 * kConvWarps) {
-        uint4 *q16 = reinterpret_cast<uint4 *>(sm + kOffQT) + c;
-        *q16 = bf16x8_to_f16x8(*q16, &bad);
-      }
-    }
-    if (bad) atomicOr(p.fault, PSD_FAULT_RANGE);
-    fence_proxy_async();
-    mbar_arrive(bar(BQREADY));
-    // Two groups of four warps take alternate tiles.  A thread of a group owns
-    // token ct of its tiles and slices 2 cw, 2 cw + 1 (32 bytes) of each 64-column
-    // block.  The proxy fence that publishes a block also waits for the thread's
-    // global loads in flight, so a group loads its next tile (i + 2) only after
-    // the last fence of tile i; the other group's tile gives those loads time to
-    // land before this group's next fence.
-    const int grp = cwi >> 2;
-    const int gtid = ctid & 127;
-    const int ct = gtid >> 1, cw = gtid & 1;
-    auto source = [&](int i) -> const uint4 * {  // token ct of tile i, or nullptr
-      const int tok = i * kTokM + ct;
-      if (i < n_tiles && tok < it.n_tokens) {
-        const int id = __ldg(p.page_indices + it.page_off + tok / P);
-        if (id >= 0 && int64_t(id) < p.num_pages)
-          return reinterpret_cast<const uint4 *>(p.k_pool + (int64_t(id) * P + tok % P) * kDqkM) + 2 * cw;
-        atomicOr(p.fault, PSD_FAULT_PAGE_ID);
-      }
-      return nullptr;
-    };
-    uint4 raw[2 * kKBlocks];
-    auto load = [&](int i) {
-      const uint4 *src = source(i);
-#pragma unroll
-      for (int b = 0; b < kKBlocks; ++b) {
-        raw[2 * b] = src ? __ldg(src + 4 * b) : make_uint4(0u, 0u, 0u, 0u);
-        raw[2 * b + 1] = src ? __ldg(src + 4 * b + 1) : make_uint4(0u, 0u, 0u, 0u);
-      }
-    };
-    const uint32_t row_off = uint32_t(ct) * 128;
-    uint32_t cpos[4];  // swizzled 16-byte chunk offsets of this thread's 4 chunks
-#pragma unroll
-    for (int k = 0; k < 4; ++k) cpos[k] = uint32_t((4 * cw + k) ^ (ct & 7)) << 4;
-    load(grp);
-    // the K ring and V buffers hold the Q head until the row warps have moved it
-    ok = ok && mbar_wait(bar(BQREADY), 0, p.fault);
-    // Tile i is widened block by block into the K ring (all 576 columns, for QK)
-    // and V buffer i%3 (this CTA's 256 V columns, for PV).
-    for (int i = grp; i < n_tiles && ok; i += 2) {
-      uint8_t *vt = sm + kOffV0 + (i % kVBufs) * kVTileBytes;
-#pragma unroll
-      for (int b = 0; b < kKBlocks; ++b) {
-        // this group's block c goes to its own slot c % kGroupSlots, so a slot's uses
-        // come from one group in order and no wait runs more than a phase ahead
-        const int c = (i >> 1) * kKBlocks + b, slot = grp * kGroupSlots + c % kGroupSlots;
-        if (c >= kGroupSlots) {  // the QK MMAs of the slot's previous block are done
-          ok = mbar_wait(bar(BKEMPTY0 + slot), uint32_t(c / kGroupSlots - 1) & 1u, p.fault);
-          if (!__all_sync(0xffffffffu, ok)) break;
-        }
-        const int vblk = b - 4 * half;  // V block of this CTA's half, or outside [0, 4)
-        if (vblk == 0 && i >= kVBufs) {  // PV(i-3) released V buffer i%3
-          ok = mbar_wait(bar(BPV0 + i % kVBufs), uint32_t(i / kVBufs - 1) & 1u, p.fault);
-          if (!__all_sync(0xffffffffu, ok)) break;
-        }
-        const uint4 h[4] = {cvt8(raw[2 * b].x, raw[2 * b].y), cvt8(raw[2 * b].z, raw[2 * b].w),
-                            cvt8(raw[2 * b + 1].x, raw[2 * b + 1].y), cvt8(raw[2 * b + 1].z, raw[2 * b + 1].w)};
-        uint8_t *kt = sm + kOffK + slot * kKBlockBytes + row_off;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(kt + cpos[k]) = h[k];
-        if (vblk >= 0 && vblk < 4) {
-          uint8_t *vrow = vt + vblk * kKBlockBytes + row_off;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4 *>(vrow + cpos[k]) = h[k];
-        }
-        fence_proxy_async();  // each thread's stores, then one arrival per warp
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BKFULL0 + slot));
-      }
-      load(i + 2);
-    }
-  } else if (warp < 4) {
+  } else if (warp < kRowWarps) {
     // ------------------------------------------------------------------ row warps
     const int row = tid;                          // head = TMEM lane
     const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-    // Q head (columns 0..383) of this row: bf16 from the landing boxes -> f16 pairs
-    // -> TMEM columns kColQ + 32 b (box b), the layout the MMA reads A from.
-    bool ok = mbar_wait(bar(BQ), 0, p.fault);
-    if (__all_sync(0xffffffffu, ok)) {
-      bool bad = false;
+    // Query split.  Pass 1 moves the bf16 row from the landing boxes to TMEM
+    // columns 0..287 (free until the first PV) and takes its largest magnitude;
+    // pass 2 scales the row by 2^k (largest element to [128, 256)) and writes
+    // hi = e4m3(x), lo = e4m3(x - hi): Q_hi[0:512] to TMEM, the rest to shared memory.
+    bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BQ), 0, p.fault));
+    float amax = 0.f;
+    if (ok) {
 #pragma unroll 1
-      for (int b = 0; b < kQHeadBoxes; ++b) {
-        uint32_t qw[32];
+      for (int b = 0; b < kBoxes; ++b) {
+        uint32_t w[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(sm + kOffQHead + b * kQBoxBytes + row * 128 +
-                                                           ((c ^ (row & 7)) << 4));
-          const uint4 h = bf16x8_to_f16x8(v, &bad);
-          qw[4 * c] = h.x;
-          qw[4 * c + 1] = h.y;
-          qw[4 * c + 2] = h.z;
-          qw[4 * c + 3] = h.w;
+          const uint4 v = *reinterpret_cast<const uint4 *>(sm + q_land(b) + row * 128 + ((c ^ (row & 7)) << 4));
+          w[4 * c] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
         }
-        PSD_TMEM_ST32(lane_base + kColQ + 32 * b, qw);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[c])), fabsf(bf16_hi(w[c]))));
+        PSD_TMEM_ST32(lane_base + 32 * b, w);
       }
       tmem_st_wait();
-      if (bad) atomicOr(p.fault, PSD_FAULT_RANGE);
     }
+    row_warps_sync();  // every landing row is read before pass 2 overwrites the Q area
+    // power of two: amax * 2^k in [128, 256); zero and subnormal rows keep k = 0
+    const int ex = int((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+    const int kq = ex > -127 ? max(-120, min(120, 7 - ex)) : 0;
+    const float qmul = __uint_as_float(uint32_t(127 + kq) << 23);
+    const float qs = p.q_scale * __uint_as_float(uint32_t(127 - kq) << 23);  // score scale of this row
+    if (ok) {
+#pragma unroll 1
+      for (int b = 0; b < kBoxes; ++b) {
+        uint32_t w[32], hi[16], lo[16];
+        PSD_TMEM_LD32(lane_base + 32 * b, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          split4(bf16_lo(w[2 * c]) * qmul, bf16_hi(w[2 * c]) * qmul, bf16_lo(w[2 * c + 1]) * qmul,
+                 bf16_hi(w[2 * c + 1]) * qmul, hi[c], lo[c]);
+        if (b < kBoxes - 1) {
+          PSD_TMEM_ST16(lane_base + kColQ + 16 * b, hi);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4 *>(sm + kOffQHiTail + sw64(row, c)) =
+                make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4 *>(sm + kOffQLo + b * kQBoxBytes + sw64(row, c)) =
+              make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+      }
+      tmem_st_wait();
+    }
+    fence_proxy_async();
     tc_fence_before();
-    mbar_arrive(bar(BQREADY));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(BQREADY));
+
     float m_ref = neg_inf(), l_sum = 0.f;
-    const bool qpos = p.q_scale >= 0.f;
+    const bool qpos = qs >= 0.f;
     for (int i = 0; i < n_tiles && ok; ++i) {
-      ok = mbar_wait(bar(BSFULL), uint32_t(i) & 1u, p.fault);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(BSFULL0 + (i & 1)), uint32_t(i >> 1) & 1u, p.fault));
+      if (!ok) break;
       tc_fence_after();
+      const uint32_t s_col = lane_base + kColS + 64 * (i & 1);
       uint32_t r0[32], r1[32];
-      PSD_TMEM_LD32(lane_base + kColS, r0);
-      PSD_TMEM_LD32(lane_base + kColS + 32, r1);
+      PSD_TMEM_LD32(s_col, r0);
+      PSD_TMEM_LD32(s_col + 32, r1);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BSFREE));    // QK(i+1) may overwrite S
-      const int valid = min(kTokM, it.n_tokens - i * kTokM);
+      const int valid = i == n_tiles - 1 ? tail : kTokM;
       const bool partial = valid < kTokM;
-      float s[64];  // raw scores q.k (scaled below)
+      float s[64];  // raw scores (q 2^k) . k_codes
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         s[c] = __uint_as_float(r0[c]);
         s[c + 32] = __uint_as_float(r1[c]);
       }
-      // max of the scaled valid scores = q_scale times the raw max (min if q_scale < 0)
+      // max of the scaled valid scores = qs times the raw max (min if qs < 0)
       float mr = qpos ? neg_inf() : -neg_inf();
       if (!partial) {
 #pragma unroll
@@ -491,17 +458,15 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         for (int c = 0; c < 64; ++c)
           if (c < valid) mr = qpos ? fmaxf(mr, s[c]) : fminf(mr, s[c]);
       }
-      const float mt = mr * p.q_scale;
-      // PV(i-1) must be done before P is rewritten or O rescaled
-      if (i >= 1) {
-        ok = mbar_wait(bar(BPV0 + (i - 1) % kVBufs), uint32_t((i - 1) / kVBufs) & 1u, p.fault);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-      }
+      const float mt = mr * qs;
       const bool grow = mt > m_ref + kLazyRescale;
       if (__any_sync(0xffffffffu, grow)) {
         const float m_new = grow ? mt : m_ref;
-        if (i >= 1) {  // rescale this warp's O rows in TMEM
+        if (i >= 1) {  // PV(i-1) must be done; then rescale this warp's O rows in TMEM
+          const int j = i - 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(BKEMPTY0 + j % kNB), uint32_t(j / kNB) & 1u, p.fault));
+          if (!ok) break;
+          tc_fence_after();
           const float alpha = ex2(m_ref - m_new);
 #pragma unroll 1
           for (int cb = 0; cb < kDvHalf / 16; ++cb) {  // 16 columns at a time: 64 scores stay live
@@ -512,43 +477,42 @@ __global__ void __launch_bounds__(kThreadsM, 1)
             for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
             PSD_TMEM_ST16(lane_base + kColO + cb * 16, o);
           }
-          tmem_st_wait();
           l_sum *= alpha;
         }
         m_ref = m_new;
       }
-      // P = 2^(q_scale s - m_ref) as f16 ([128 x 64], 128B-swizzled rows).  l sums P in
-      // f32 before the f16 rounding the PV MMA sees: at most 2^-11 relative per term.
-      uint8_t *prow = sm + kOffP + row * 128;
-      const float2 qs2 = make_float2(p.q_scale, p.q_scale), nm2 = make_float2(-m_ref, -m_ref);
+      // P = 2^(qs s - m_ref + 4) <= 2^8, split into e4m3 hi and lo words (4 tokens
+      // each) and written over the first 32 columns of this S buffer.  l sums the
+      // unsplit P in f32.
+      const float2 qs2 = make_float2(qs, qs), nb2 = make_float2(kPBias - m_ref, kPBias - m_ref);
       float2 lacc = make_float2(0.f, 0.f);
+      uint32_t pw[32];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int t = 8 * ch + 2 * c;
-          const float2 x = __ffma2_rn(make_float2(s[t], s[t + 1]), qs2, nm2);
-          float a = ex2(x.x), b = ex2(x.y);
-          if (partial) {
-            a = t < valid ? a : 0.f;
-            b = t + 1 < valid ? b : 0.f;
-          }
-          lacc = __fadd2_rn(lacc, make_float2(a, b));
-          pk[c] = pack2_f16(a, b);
+      for (int c = 0; c < 16; ++c) {
+        const int t = 4 * c;
+        const float2 x01 = __ffma2_rn(make_float2(s[t], s[t + 1]), qs2, nb2);
+        const float2 x23 = __ffma2_rn(make_float2(s[t + 2], s[t + 3]), qs2, nb2);
+        float a0 = ex2(x01.x), a1 = ex2(x01.y), a2 = ex2(x23.x), a3 = ex2(x23.y);
+        if (partial) {
+          a0 = t < valid ? a0 : 0.f;
+          a1 = t + 1 < valid ? a1 : 0.f;
+          a2 = t + 2 < valid ? a2 : 0.f;
+          a3 = t + 3 < valid ? a3 : 0.f;
         }
-        *reinterpret_cast<uint4 *>(prow + ((ch ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        lacc = __fadd2_rn(lacc, __fadd2_rn(make_float2(a0, a1), make_float2(a2, a3)));
+        split4(a0, a1, a2, a3, pw[c], pw[16 + c]);
       }
       l_sum += lacc.x + lacc.y;
-      fence_proxy_async();
+      PSD_TMEM_ST32(s_col, pw);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BPFULL));
+      if (lane == 0) mbar_arrive(bar(BPFULL0 + (i & 1)));
     }
     // epilogue: O / l for this row and V half
     if (ok && n_tiles > 0) {
       const int j = n_tiles - 1;
-      ok = mbar_wait(bar(BPV0 + j % kVBufs), uint32_t(j / kVBufs) & 1u, p.fault);
+      ok = mbar_wait(bar(BKEMPTY0 + j % kNB), uint32_t(j / kNB) & 1u, p.fault);
     }
     if (__all_sync(0xffffffffu, ok) && n_tiles > 0) {
       tc_fence_after();
@@ -566,7 +530,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
               make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
                           __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
       }
-      if (half == 0) p.lse_out[orow] = m_ref + log2f(l_sum);
+      if (half == 0) p.lse_out[orow] = m_ref - kPBias + log2f(l_sum);
     }
   }
   tc_fence_before();
@@ -589,22 +553,39 @@ bool encode_q_map(CUtensorMap *map, const DeviceInfo &dev, const void *q, int ba
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Latent pool [num_pages][page_size][576] e4m3 as a 3-D map; a box is 64 columns of
+// 64 consecutive token rows of one page, landing with the 64-byte swizzle.
+bool encode_latent_map(CUtensorMap *map, const DeviceInfo &dev, const void *pool, int64_t num_pages,
+                       int page_size) {
+  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(dev.encode_tiled);
+  if (!encode) return false;
+  cuuint64_t dims[3] = {cuuint64_t(kDqkM), cuuint64_t(page_size), cuuint64_t(num_pages)};
+  cuuint64_t strides[2] = {cuuint64_t(kDqkM), cuuint64_t(page_size) * kDqkM};
+  cuuint32_t box[3] = {64, cuuint32_t(kTokM), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(pool), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool partial_mla_supports(const PartialLaunch &L) {
   return L.latent_v && L.kv_dtype == PSD_FP8_E4M3 && L.Dqk == kDqkM && L.Dv == kDvM &&
-         L.G_cta == kRowsM && L.Hq_req == kRowsM && L.Hkv == 1 && L.page_size % kTokM == 0;
+         L.G_cta == kRowsM && L.Hq_req == kRowsM && L.Hkv == 1 && L.page_size % kTokM == 0 &&
+         reinterpret_cast<uintptr_t>(L.k_pool) % 16 == 0 && reinterpret_cast<uintptr_t>(L.q) % 16 == 0;
 }
 
 psd_status launch_partial_mla(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
   if (L.num_items == 0) return PSD_OK;
   if (size_t(dev.smem_optin) < kSmemMLA)
     return fail(PSD_ERR_UNSUPPORTED, "MLA tcgen05 partial needs %u bytes of shared memory", kSmemMLA);
-  CUtensorMap tmQ;
+  CUtensorMap tmQ, tmK;
   if (!encode_q_map(&tmQ, dev, L.q, L.q_batch, L.Hq_req))
     return fail(PSD_ERR_CUDA, "cuTensorMapEncodeTiled failed for q");
+  if (!encode_latent_map(&tmK, dev, L.k_pool, L.num_pages, L.page_size))
+    return fail(PSD_ERR_CUDA, "cuTensorMapEncodeTiled failed for the latent pool");
   MLAParams p;
-  p.k_pool = reinterpret_cast<const uint8_t *>(L.k_pool);
   p.page_indices = L.page_indices;
   p.items = L.items;
   p.order = L.order;
@@ -620,7 +601,7 @@ psd_status launch_partial_mla(const PartialLaunch &L, const DeviceInfo &dev, cud
                                        int(kSmemMLA));
   if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   const dim3 grid(static_cast<unsigned>(L.num_items), 1, 2);
-  partial_mla_kernel<<<grid, kThreadsM, kSmemMLA, s>>>(tmQ, p);
+  partial_mla_kernel<<<grid, kThreadsM, kSmemMLA, s>>>(tmQ, tmK, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "partial (MLA tcgen05) launch: %s", cudaGetErrorString(e));
   return PSD_OK;

@@ -4,6 +4,7 @@ first 512 columns) on the tensor-core partial kernel, against the float64 oracle
 for the split-KV merge)."""
 import numpy as np
 import pytest
+import torch
 
 import synth
 from oracle import attention as A
@@ -48,3 +49,47 @@ def test_mla_full_size_sampled_requests():
     ro, rl = A.decode_attention(A.workload_arrays(w), requests=req)
     assert_close(o[req], lse[req], ro[req], rl[req], "fp8_e4m3", "MLA full")
     assert np.isfinite(o).all()
+
+
+def _mla_small(seed, lengths, page_size=64, num_pages=512, tile=2048):
+    rng = np.random.default_rng(seed)
+    return synth._make("mla_small", rng, lengths, Hq=128, Hkv=1, Dqk=576, Dv=512, page_size=page_size,
+                       num_pages=num_pages, tile_tokens=tile, kv_dtype="fp8_e4m3", latent_v=True)
+
+
+@pytest.mark.parametrize("page_size", [64, 128])
+def test_mla_ragged_tails_and_short_items(page_size):
+    """Items of 1 to 2049 tokens: single-token and one-short tiles, whole pages, an
+    item that ends one token into a tile; NaN canaries fill every unused slot."""
+    w = _mla_small(4, [1, 63, 64, 65, 127, 128, 700, 2049], page_size=page_size)
+    o, lse = Dev(w).decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "fp8_e4m3", f"MLA ragged, page {page_size}")
+
+
+def test_mla_query_rows_far_outside_the_f16_range():
+    """A query row is split into two e4m3 terms after scaling by a power of two, so
+    any finite bf16 magnitude works: q * 2^40 with sm_scale * 2^-40 and q * 2^-60 with
+    sm_scale * 2^60 give the same scores and the same outputs as q itself."""
+    w = _mla_small(5, [900, 1500, 64])
+    d = Dev(w)
+    o0, l0 = d.decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o0, l0, ro, rl, "fp8_e4m3", "MLA q")
+    base_scale = w.sm_scale
+    for e in (40, -60):
+        d.q = (w.q.float() * 2.0 ** e).to(torch.bfloat16).to("cuda")
+        w.sm_scale = base_scale * 2.0 ** -e
+        o, l = d.decode(enable=0)
+        assert np.abs(o - o0).max() <= 1e-6 and np.abs(l - l0).max() <= 1e-6, f"2^{e}"
+    w.sm_scale = base_scale
+
+
+def test_mla_heads_of_different_magnitude():
+    """Head h scaled by 2^((h % 9) - 4): rows from flat to sharp softmax in one CTA."""
+    w = _mla_small(6, [3000, 777])
+    scale = torch.tensor([2.0 ** ((h % 9) - 4) for h in range(128)], dtype=torch.float32)
+    w.q = (w.q.float() * scale[None, :, None]).to(torch.bfloat16)
+    o, lse = Dev(w).decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "fp8_e4m3", "MLA mixed head magnitudes")
