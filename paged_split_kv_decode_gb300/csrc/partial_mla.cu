@@ -63,17 +63,18 @@ constexpr uint32_t kOffQHiTail = kOffQS;
 constexpr uint32_t kOffQLo = kOffQS + kQBoxBytes;
 constexpr uint32_t kOffBar = kOffQS + (1 + kBoxes) * kQBoxBytes;  // 229376
 constexpr uint32_t kSmemMLA = kOffBar + 256 + 1024;              // barriers + alignment slack
-// The bf16 query lands (before the e4m3 split) in the Q area (5 boxes) and tile
-// buffers 3 and 2 (2 boxes each); tiles 0 and 1 load meanwhile.
-__host__ __device__ constexpr uint32_t q_land(int b) {
+// A query lands in bf16 (before the e4m3 split) when the tiles issued so far are
+// consumed: boxes 0-4 over the Q area, boxes 5-6 and 7-8 in the tile buffers of the
+// third and fourth tiles to come (g = tiles issued so far).
+__host__ __device__ constexpr uint32_t q_land_at(int b, int g) {
   return b < 5 ? kOffQS + uint32_t(b) * kQLandBytes
-               : b < 7 ? kOffK + 3 * kTileBytes + uint32_t(b - 5) * kQLandBytes
-                       : kOffK + 2 * kTileBytes + uint32_t(b - 7) * kQLandBytes;
+               : b < 7 ? kOffK + uint32_t((g + 3) % kNB) * kTileBytes + uint32_t(b - 5) * kQLandBytes
+                       : kOffK + uint32_t((g + 2) % kNB) * kTileBytes + uint32_t(b - 7) * kQLandBytes;
 }
-static_assert(q_land(4) + kQLandBytes <= kOffBar, "Q landing overruns the Q area");
+static_assert(5 * kQLandBytes <= (1 + kBoxes) * kQBoxBytes, "Q landing overruns the Q area");
 static_assert(2 * kQLandBytes <= kTileBytes, "two landing boxes per tile buffer");
-static_assert(kOffQS % 1024 == 0 && (2 * kTileBytes) % 1024 == 0 && (3 * kTileBytes) % 1024 == 0,
-              "128B-swizzled landing boxes need 1024-byte alignment");
+static_assert(kOffQS % 1024 == 0 && kTileBytes % 1024 == 0, "128B-swizzled landing boxes need 1024-byte alignment");
+static_assert(8 * (256 + 1) <= (1 + kBoxes) * kQBoxBytes, "range scan scratch");
 constexpr int kRowWarps = 4, kCtrlWarp = 4, kProdWarp = 5;
 constexpr int kThreadsM = 32 * 6;
 constexpr uint32_t kTmemCols = 512;
@@ -82,14 +83,14 @@ constexpr float kLazyRescale = 4.f;             // log2 units
 constexpr float kPBias = 4.f;                   // P = 2^(score - m + 4) <= 2^8
 
 // mbarrier slots (uint64 each) at kOffBar
-enum { BQ = 0, BQREADY, BTAIL, BDRAIN, BSFULL0, BPFULL0 = BSFULL0 + 2, BKFULL0 = BPFULL0 + 2,
+enum { BQ = 0, BQSEEN, BQREADY, BORDY, BDRAIN, BSFULL0, BPFULL0 = BSFULL0 + 2, BKFULL0 = BPFULL0 + 2,
        BKEMPTY0 = BKFULL0 + kNB, BSLOT = BKEMPTY0 + kNB };
-static_assert(BSLOT * 8 + 4 <= 256, "barrier area");
+static_assert(BSLOT * 8 + 12 <= 256, "barrier area");
 
 struct MLAParams {
   const int32_t *page_indices;
   const psd_work_item *items;
-  const int32_t *order;
+  int num_items;
   float *v_out;
   float *lse_out;
   int32_t *fault;
@@ -138,10 +139,6 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// Barrier among the row warps only.
-__device__ __forceinline__ void row_warps_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(32 * kRowWarps) : "memory");
 }
 #define PSD_TMEM_LD32(taddr, r)                                                                        \
   asm volatile(                                                                                        \
@@ -203,6 +200,12 @@ __device__ __forceinline__ void split4(float x0, float x1, float x2, float x3, u
   hi = h01 | (h23 << 16);
   lo = e4m3x2(x0 - d01.x, x1 - d01.y) | (e4m3x2(x2 - d23.x, x3 - d23.y) << 16);
 }
+__device__ __forceinline__ void st_global_v8(float *dst, float a, float b, float c, float d, float e, float f,
+                                             float g, float h) {
+  asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d),
+               "f"(e), "f"(f), "f"(g), "f"(h)
+               : "memory");
+}
 // Byte offset of 16-byte chunk c of row r in a 64-byte-swizzled box of 64-byte rows.
 __device__ __forceinline__ uint32_t sw64(int r, int c) { return uint32_t(r) * 64 + (uint32_t(c ^ ((r >> 1) & 3)) << 4); }
 
@@ -214,19 +217,19 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + BSLOT);
+  int *srange = reinterpret_cast<int *>(tslot + 1);                // this pair's items [begin, end)
+  long long *sscan = reinterpret_cast<long long *>(sm + kOffQS);   // scratch until a query lands
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const psd_work_item it = p.items[p.order ? __ldg(p.order + blockIdx.x) : blockIdx.x];
   const int half = blockIdx.z;                    // which 256 V columns
   const int P = p.page_size;
-  const int n_tiles = (it.n_tokens + kTokM - 1) / kTokM;
-  const int tail = it.n_tokens - (n_tiles - 1) * kTokM;   // valid tokens of the last tile
 
   if (tid == 0) {
     mbar_init(bar(BQ), 1);
+    mbar_init(bar(BQSEEN), kRowWarps);
     mbar_init(bar(BQREADY), kRowWarps);
-    mbar_init(bar(BTAIL), 1);
+    mbar_init(bar(BORDY), kRowWarps);
     mbar_init(bar(BDRAIN), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(BSFULL0 + b), 1);
@@ -237,75 +240,114 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       mbar_init(bar(BKEMPTY0 + b), 1);
     }
     fence_mbar_init();
+    srange[0] = srange[1] = 0;
   }
   if (warp == kCtrlWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  // This CTA pair's items: the contiguous run of the (request-major) item list whose
+  // first tokens fall in its 1/gridDim.x share of all tokens.  Items stay whole, and
+  // consecutive items mostly belong to one request and reuse its split query.
+  {
+    const int n = p.num_items;
+    const int per = (n + kThreadsM - 1) / kThreadsM;
+    const int a0 = min(n, tid * per), a1 = min(n, a0 + per);
+    long long part = 0;
+    for (int i = a0; i < a1; ++i) part += __ldg(&p.items[i].n_tokens);
+    sscan[tid] = part;
+    __syncthreads();
+    if (tid == 0) {  // exclusive scan of the per-thread sums; the total at the end
+      long long acc = 0;
+      for (int t = 0; t < kThreadsM; ++t) {
+        const long long v = sscan[t];
+        sscan[t] = acc;
+        acc += v;
+      }
+      sscan[kThreadsM] = acc;
+    }
+    __syncthreads();
+    const long long total = sscan[kThreadsM];
+    const long long lo_t = total * blockIdx.x / gridDim.x, hi_t = total * (blockIdx.x + 1) / gridDim.x;
+    long long start = sscan[tid];
+    int c_lo = 0, c_hi = 0;  // items starting before lo_t / hi_t
+    for (int i = a0; i < a1; ++i) {
+      c_lo += start < lo_t;
+      c_hi += start < hi_t;
+      start += __ldg(&p.items[i].n_tokens);
+    }
+    if (c_lo) atomicAdd(srange, c_lo);
+    if (c_hi) atomicAdd(srange + 1, c_hi);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  const int begin = srange[0], end = srange[1];
 
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer warp
+    // Loads run ahead across item boundaries.  A query switch waits until every
+    // tile issued so far is consumed (the query lands over the Q area and two tile
+    // buffers), and the two tiles that follow go into those buffers only once the
+    // row warps have split the query.
     bool ok = true;
-    int issued = 0;  // tiles whose loads were issued
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(BQ), kQBytes);
+    int g = 0, issued = 0, nq = 0, cur_q = -1, gate = -kNB;
+    for (int m = begin; m < end && ok; ++m) {
+      const psd_work_item it = p.items[m];
+      const int nt = (it.n_tokens + kTokM - 1) / kTokM;
+      if (nt <= 0) continue;  // (the planner emits no empty items)
+      if (it.q_index != cur_q) {
+        if (g > 0)
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault));
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(BQ), kQBytes);
 #pragma unroll 1
-      for (int b = 0; b < kBoxes; ++b) tma_load_3d(smem_u32(sm + q_land(b)), &tmQ, b * 64, 0, it.q_index, bar(BQ));
-    }
-#pragma unroll 1
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int buf = j % kNB;
-      if (j >= kNB)  // PV(j - 4) has read the buffer
-        ok = mbar_wait(bar(BKEMPTY0 + buf), uint32_t(j / kNB - 1) & 1u, p.fault);
-      else if (j >= 2)  // buffers 2 and 3 hold query landing boxes until the split
-        ok = mbar_wait(bar(BQREADY), 0, p.fault);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      const int tok = j * kTokM;
-      if (lane == 0) {
-        int page = __ldg(p.page_indices + it.page_off + tok / P);
-        if (page < 0 || int64_t(page) >= p.num_pages) {  // out of range: load the zero fill
-          atomicOr(p.fault, PSD_FAULT_PAGE_ID);
-          page = -1;
-        }
-        mbar_arrive_expect_tx(bar(BKFULL0 + buf), kTileBytes);
-        const uint32_t dst = smem_u32(sm + kOffK + buf * kTileBytes);
-#pragma unroll 1
-        for (int b = 0; b < kBoxes; ++b) tma_load_3d(dst + b * kBoxBytes, &tmK, b * 64, tok % P, page, bar(BKFULL0 + buf));
-      }
-      __syncwarp();
-      issued = j + 1;
-      if (j == n_tiles - 1 && tail < kTokM) {
-        // Rows past the item's last token (still inside its page) may hold anything:
-        // zero this CTA's four V boxes there, so that P = 0 never meets a NaN.
-        ok = mbar_wait(bar(BKFULL0 + buf), uint32_t(j / kNB) & 1u, p.fault);
-        if (__all_sync(0xffffffffu, ok)) {
-          uint8_t *vt = sm + kOffK + buf * kTileBytes + 4 * half * kBoxBytes;
-          const int n16 = (kTokM - tail) * 4;        // 16-byte chunks per box
-#pragma unroll 1
-          for (int c = lane; c < 4 * n16; c += 32)
-            *reinterpret_cast<uint4 *>(vt + (c / n16) * kBoxBytes + tail * 64 + (c % n16) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-          fence_proxy_async();
+          for (int b = 0; b < kBoxes; ++b)
+            tma_load_3d(smem_u32(sm + q_land_at(b, g)), &tmQ, b * 64, 0, it.q_index, bar(BQ));
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BTAIL));
+        cur_q = it.q_index;
+        gate = g + 2;
+        ++nq;
+      }
+#pragma unroll 1
+      for (int j = 0; j < nt; ++j) {
+        const int buf = g % kNB;
+        if (g >= kNB)  // PV(g - 4) has read the buffer
+          ok = mbar_wait(bar(BKEMPTY0 + buf), uint32_t(g / kNB - 1) & 1u, p.fault);
+        if (ok && g >= gate && g < gate + 2)  // a query landing box sits in this buffer
+          ok = mbar_wait(bar(BQREADY), uint32_t(nq - 1) & 1u, p.fault);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const int tok = j * kTokM;
+        if (lane == 0) {
+          int page = __ldg(p.page_indices + it.page_off + tok / P);
+          if (page < 0 || int64_t(page) >= p.num_pages) {  // out of range: load the zero fill
+            atomicOr(p.fault, PSD_FAULT_PAGE_ID);
+            page = -1;
+          }
+          mbar_arrive_expect_tx(bar(BKFULL0 + buf), kTileBytes);
+          const uint32_t dst = smem_u32(sm + kOffK + buf * kTileBytes);
+#pragma unroll 1
+          for (int b = 0; b < kBoxes; ++b)
+            tma_load_3d(dst + b * kBoxBytes, &tmK, b * 64, tok % P, page, bar(BKFULL0 + buf));
+        }
+        __syncwarp();
+        issued = ++g;
       }
     }
     // No copy of this CTA may still be in flight when it exits.
-    mbar_wait(bar(BQ), 0, p.fault);
-    for (int j = max(0, issued - kNB); j < issued; ++j)   // the last tile of each buffer
-      mbar_wait(bar(BKFULL0 + j % kNB), uint32_t(j / kNB) & 1u, p.fault);
+    if (nq > 0) mbar_wait(bar(BQ), uint32_t(nq - 1) & 1u, p.fault);
+    for (int t = max(0, issued - kNB); t < issued; ++t)   // the last tile of each buffer
+      mbar_wait(bar(BKFULL0 + t % kNB), uint32_t(t / kNB) & 1u, p.fault);
   } else if (warp == kCtrlWarp) {
     // ------------------------------------------------------------- control warp
     // The whole warp waits; one elected lane issues.  (A wait on the issuing thread
-    // alone stalls the MMAs it has queued far longer.)
-    bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BQREADY), 0, p.fault));
-    tc_fence_after();
+    // alone stalls the MMAs it has queued far longer.)  Order: S(g) = Q K(g)^T, then
+    // O += P(g-1) V(g-1); across an item boundary S of the next item is issued
+    // before the last PV of the previous one, except at a query switch.
     const uint32_t id_qk = idesc_e4m3(128, kTokM, false);
     const uint32_t id_pv = idesc_e4m3(128, kDvHalf, true);
     // Base descriptors, built once; operand steps add offsets (>> 4) to the
@@ -315,52 +357,77 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     const uint64_t qld = smem_desc(smem_u32(sm + kOffQLo), 16, 512);
     // V (MN-major): 64-column atoms one box apart, 8-token groups 512 bytes apart
     const uint64_t vd = smem_desc(smem_u32(sm + kOffK + 4 * half * kBoxBytes), kBoxBytes, 512);
-    for (int i = 0; ok && i <= n_tiles; ++i) {
-      if (i < n_tiles) {  // S(i) = Q K(i)^T into S buffer i % 2
-        const int buf = i % kNB;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(BKFULL0 + buf), uint32_t(i / kNB) & 1u, p.fault));
-        if (ok && i == n_tiles - 1 && tail < kTokM)
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(BTAIL), 0, p.fault));
+    bool ok = true;
+    int g = 0, nq = 0, cur_q = -1, mi = 0;
+    int pend = -1, pend_mi = 0;  // tile whose PV is still to issue, and its item ordinal
+    bool pend_first = false;     // ... which is the first tile of that item
+    auto issue_pv = [&]() -> bool {
+      const int t = pend, buf = t % kNB;
+      bool r = __all_sync(0xffffffffu, mbar_wait(bar(BPFULL0 + (t & 1)), uint32_t(t >> 1) & 1u, p.fault));
+      if (r && pend_first && pend_mi > 0)  // the previous item's O has been read out
+        r = __all_sync(0xffffffffu, mbar_wait(bar(BORDY), uint32_t(pend_mi - 1) & 1u, p.fault));
+      if (!r) return false;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t a_p = tmem + kColS + 64 * (t & 1);   // P (hi | lo) over S buffer t % 2
+        const uint64_t vb = vd + ((buf * kTileBytes) >> 4);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {  // tokens 32 k .. 32 k + 31
+          const uint64_t vbk = vb + ((k * 32 * 64) >> 4);
+          mma_ts(tmem + kColO, a_p + 8 * k, vbk, id_pv, (pend_first && k == 0) ? 0u : 1u);
+          mma_ts(tmem + kColO, a_p + 16 + 8 * k, vbk, id_pv, 1u);
+        }
+        umma_commit(bar(BKEMPTY0 + buf));
+      }
+      __syncwarp();
+      pend = -1;
+      return true;
+    };
+    for (int m = begin; m < end && ok; ++m) {
+      const psd_work_item it = p.items[m];
+      const int nt = (it.n_tokens + kTokM - 1) / kTokM;
+      if (nt <= 0) continue;  // (the planner emits no empty items)
+      if (it.q_index != cur_q) {
+        // the split of the next query waits for every PV issued so far
+        if (pend >= 0) ok = issue_pv();
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(BQREADY), uint32_t(nq) & 1u, p.fault));
+        if (!ok) break;
+        tc_fence_after();
+        cur_q = it.q_index;
+        ++nq;
+      }
+#pragma unroll 1
+      for (int j = 0; j < nt; ++j) {
+        const int buf = g % kNB;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(BKFULL0 + buf), uint32_t(g / kNB) & 1u, p.fault));
         if (!ok) break;
         tc_fence_after();
         if (elect_one()) {
-          const uint32_t d_s = tmem + kColS + 64 * (i & 1);
+          const uint32_t d_s = tmem + kColS + 64 * (g & 1);
           const uint64_t kb = kd + ((buf * kTileBytes) >> 4);
 #pragma unroll
           for (int b = 0; b < kBoxes; ++b) {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const uint64_t kbj = kb + ((b * kBoxBytes + j * 32) >> 4);
+            for (int h = 0; h < 2; ++h) {
+              const uint64_t kbh = kb + ((b * kBoxBytes + h * 32) >> 4);
               if (b < kBoxes - 1)
-                mma_ts(d_s, tmem + kColQ + 16 * b + 8 * j, kbj, id_qk, (b | j) != 0);
+                mma_ts(d_s, tmem + kColQ + 16 * b + 8 * h, kbh, id_qk, (b | h) != 0);
               else
-                mma_ss(d_s, qhd + ((j * 32) >> 4), kbj, id_qk, 1u);
-              mma_ss(d_s, qld + ((b * kQBoxBytes + j * 32) >> 4), kbj, id_qk, 1u);
+                mma_ss(d_s, qhd + ((h * 32) >> 4), kbh, id_qk, 1u);
+              mma_ss(d_s, qld + ((b * kQBoxBytes + h * 32) >> 4), kbh, id_qk, 1u);
             }
           }
-          umma_commit(bar(BSFULL0 + (i & 1)));
+          umma_commit(bar(BSFULL0 + (g & 1)));
         }
         __syncwarp();
+        if (pend >= 0 && !(ok = issue_pv())) break;
+        pend = g++;
+        pend_first = j == 0;
+        pend_mi = mi;
       }
-      if (i > 0) {  // O += P(i-1) V(i-1), P (hi | lo) in S buffer (i-1) % 2
-        const int j = i - 1, buf = j % kNB;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(BPFULL0 + (j & 1)), uint32_t(j >> 1) & 1u, p.fault));
-        if (!ok) break;
-        tc_fence_after();
-        if (elect_one()) {
-          const uint32_t a_p = tmem + kColS + 64 * (j & 1);
-          const uint64_t vb = vd + ((buf * kTileBytes) >> 4);
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {  // tokens 32 k .. 32 k + 31
-            const uint64_t vbk = vb + ((k * 32 * 64) >> 4);
-            mma_ts(tmem + kColO, a_p + 8 * k, vbk, id_pv, (j | k) != 0);
-            mma_ts(tmem + kColO, a_p + 16 + 8 * k, vbk, id_pv, 1u);
-          }
-          umma_commit(bar(BKEMPTY0 + buf));
-        }
-        __syncwarp();
-      }
+      ++mi;
     }
+    if (ok && pend >= 0) issue_pv();
     // every MMA this warp issued has completed before TMEM is released
     if (elect_one()) umma_commit(bar(BDRAIN));
     __syncwarp();
@@ -369,152 +436,176 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // ------------------------------------------------------------------ row warps
     const int row = tid;                          // head = TMEM lane
     const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-    // Query split.  Pass 1 moves the bf16 row from the landing boxes to TMEM
-    // columns 0..287 (free until the first PV) and takes its largest magnitude;
-    // pass 2 scales the row by 2^k (largest element to [128, 256)) and writes
-    // hi = e4m3(x), lo = e4m3(x - hi): Q_hi[0:512] to TMEM, the rest to shared memory.
-    bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BQ), 0, p.fault));
-    float amax = 0.f;
-    if (ok) {
+    bool ok = true;
+    int g = 0, nq = 0, cur_q = -1, mi = 0;
+    float qs = 0.f;  // score scale of this row for the current query
+    for (int m = begin; m < end && ok; ++m) {
+      const psd_work_item it = p.items[m];
+      const int nt = (it.n_tokens + kTokM - 1) / kTokM;
+      if (nt <= 0) continue;  // (the planner emits no empty items)
+      if (it.q_index != cur_q) {
+        // Query split.  Pass 1 moves the bf16 row from the landing boxes to TMEM
+        // columns 0..287 (free between items) and takes its largest magnitude;
+        // pass 2 scales the row by 2^k (largest element to [128, 256)) and writes
+        // hi = e4m3(x), lo = e4m3(x - hi): Q_hi[0:512] to TMEM, the rest to shared
+        // memory over the landing boxes, once every row warp has read them.
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(BQ), uint32_t(nq) & 1u, p.fault));
+        if (!ok) break;
+        float amax = 0.f;
 #pragma unroll 1
-      for (int b = 0; b < kBoxes; ++b) {
-        uint32_t w[32];
+        for (int b = 0; b < kBoxes; ++b) {
+          uint32_t w[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(sm + q_land(b) + row * 128 + ((c ^ (row & 7)) << 4));
-          w[4 * c] = v.x;
-          w[4 * c + 1] = v.y;
-          w[4 * c + 2] = v.z;
-          w[4 * c + 3] = v.w;
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(sm + q_land_at(b, g) + row * 128 + ((c ^ (row & 7)) << 4));
+            w[4 * c] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
+          }
+#pragma unroll
+          for (int c = 0; c < 32; ++c) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[c])), fabsf(bf16_hi(w[c]))));
+          PSD_TMEM_ST32(lane_base + 32 * b, w);
         }
-#pragma unroll
-        for (int c = 0; c < 32; ++c) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[c])), fabsf(bf16_hi(w[c]))));
-        PSD_TMEM_ST32(lane_base + 32 * b, w);
-      }
-      tmem_st_wait();
-    }
-    row_warps_sync();  // every landing row is read before pass 2 overwrites the Q area
-    // power of two: amax * 2^k in [128, 256); zero and subnormal rows keep k = 0
-    const int ex = int((__float_as_uint(amax) >> 23) & 0xffu) - 127;
-    const int kq = ex > -127 ? max(-120, min(120, 7 - ex)) : 0;
-    const float qmul = __uint_as_float(uint32_t(127 + kq) << 23);
-    const float qs = p.q_scale * __uint_as_float(uint32_t(127 - kq) << 23);  // score scale of this row
-    if (ok) {
+        tmem_st_wait();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BQSEEN));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(BQSEEN), uint32_t(nq) & 1u, p.fault));
+        if (!ok) break;
+        // power of two: amax * 2^k in [128, 256); zero and subnormal rows keep k = 0
+        const int ex = int((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+        const int kq = ex > -127 ? max(-120, min(120, 7 - ex)) : 0;
+        const float qmul = __uint_as_float(uint32_t(127 + kq) << 23);
+        qs = p.q_scale * __uint_as_float(uint32_t(127 - kq) << 23);
 #pragma unroll 1
-      for (int b = 0; b < kBoxes; ++b) {
-        uint32_t w[32], hi[16], lo[16];
-        PSD_TMEM_LD32(lane_base + 32 * b, w);
-        tmem_ld_wait();
+        for (int b = 0; b < kBoxes; ++b) {
+          uint32_t w[32], hi[16], lo[16];
+          PSD_TMEM_LD32(lane_base + 32 * b, w);
+          tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          split4(bf16_lo(w[2 * c]) * qmul, bf16_hi(w[2 * c]) * qmul, bf16_lo(w[2 * c + 1]) * qmul,
-                 bf16_hi(w[2 * c + 1]) * qmul, hi[c], lo[c]);
-        if (b < kBoxes - 1) {
-          PSD_TMEM_ST16(lane_base + kColQ + 16 * b, hi);
-        } else {
+          for (int c = 0; c < 16; ++c)
+            split4(bf16_lo(w[2 * c]) * qmul, bf16_hi(w[2 * c]) * qmul, bf16_lo(w[2 * c + 1]) * qmul,
+                   bf16_hi(w[2 * c + 1]) * qmul, hi[c], lo[c]);
+          if (b < kBoxes - 1) {
+            PSD_TMEM_ST16(lane_base + kColQ + 16 * b, hi);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4 *>(sm + kOffQHiTail + sw64(row, c)) =
+                  make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+          }
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4 *>(sm + kOffQHiTail + sw64(row, c)) =
-                make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+            *reinterpret_cast<uint4 *>(sm + kOffQLo + b * kQBoxBytes + sw64(row, c)) =
+                make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4 *>(sm + kOffQLo + b * kQBoxBytes + sw64(row, c)) =
-              make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+        tmem_st_wait();
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BQREADY));
+        cur_q = it.q_index;
+        ++nq;
       }
-      tmem_st_wait();
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar(BQREADY));
 
-    float m_ref = neg_inf(), l_sum = 0.f;
-    const bool qpos = qs >= 0.f;
-    for (int i = 0; i < n_tiles && ok; ++i) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(BSFULL0 + (i & 1)), uint32_t(i >> 1) & 1u, p.fault));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t s_col = lane_base + kColS + 64 * (i & 1);
-      uint32_t r0[32], r1[32];
-      PSD_TMEM_LD32(s_col, r0);
-      PSD_TMEM_LD32(s_col + 32, r1);
-      tmem_ld_wait();
-      const int valid = i == n_tiles - 1 ? tail : kTokM;
-      const bool partial = valid < kTokM;
-      float s[64];  // raw scores (q 2^k) . k_codes
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        s[c] = __uint_as_float(r0[c]);
-        s[c + 32] = __uint_as_float(r1[c]);
-      }
-      // max of the scaled valid scores = qs times the raw max (min if qs < 0)
-      float mr = qpos ? neg_inf() : -neg_inf();
-      if (!partial) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) mr = qpos ? fmaxf(mr, s[c]) : fminf(mr, s[c]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < valid) mr = qpos ? fmaxf(mr, s[c]) : fminf(mr, s[c]);
-      }
-      const float mt = mr * qs;
-      const bool grow = mt > m_ref + kLazyRescale;
-      if (__any_sync(0xffffffffu, grow)) {
-        const float m_new = grow ? mt : m_ref;
-        if (i >= 1) {  // PV(i-1) must be done; then rescale this warp's O rows in TMEM
-          const int j = i - 1;
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(BKEMPTY0 + j % kNB), uint32_t(j / kNB) & 1u, p.fault));
-          if (!ok) break;
-          tc_fence_after();
-          const float alpha = ex2(m_ref - m_new);
+      float m_ref = neg_inf(), l_sum = 0.f;
+      const bool qpos = qs >= 0.f;
+      const int tail = it.n_tokens - (nt - 1) * kTokM;   // valid tokens of the last tile
 #pragma unroll 1
-          for (int cb = 0; cb < kDvHalf / 16; ++cb) {  // 16 columns at a time: 64 scores stay live
-            uint32_t o[16];
-            PSD_TMEM_LD16(lane_base + kColO + cb * 16, o);
-            tmem_ld_wait();
+      for (int j = 0; j < nt; ++j, ++g) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(BSFULL0 + (g & 1)), uint32_t(g >> 1) & 1u, p.fault));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t s_col = lane_base + kColS + 64 * (g & 1);
+        uint32_t r0[32], r1[32];
+        PSD_TMEM_LD32(s_col, r0);
+        PSD_TMEM_LD32(s_col + 32, r1);
+        tmem_ld_wait();
+        const int valid = j == nt - 1 ? tail : kTokM;
+        const bool partial = valid < kTokM;
+        float s[64];  // raw scores (q 2^k) . k_codes
 #pragma unroll
-            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            PSD_TMEM_ST16(lane_base + kColO + cb * 16, o);
+        for (int c = 0; c < 32; ++c) {
+          s[c] = __uint_as_float(r0[c]);
+          s[c + 32] = __uint_as_float(r1[c]);
+        }
+        // max of the scaled valid scores = qs times the raw max (min if qs < 0)
+        float mr = qpos ? neg_inf() : -neg_inf();
+        if (!partial) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) mr = qpos ? fmaxf(mr, s[c]) : fminf(mr, s[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < valid) mr = qpos ? fmaxf(mr, s[c]) : fminf(mr, s[c]);
+        }
+        const float mt = mr * qs;
+        const bool grow = mt > m_ref + kLazyRescale;
+        if (__any_sync(0xffffffffu, grow)) {
+          const float m_new = grow ? mt : m_ref;
+          if (j >= 1) {  // PV(g-1) must be done; then rescale this warp's O rows in TMEM
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault));
+            if (!ok) break;
+            tc_fence_after();
+            const float alpha = ex2(m_ref - m_new);
+#pragma unroll 1
+            for (int cb = 0; cb < kDvHalf / 16; ++cb) {  // 16 columns at a time: 64 scores stay live
+              uint32_t o[16];
+              PSD_TMEM_LD16(lane_base + kColO + cb * 16, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              PSD_TMEM_ST16(lane_base + kColO + cb * 16, o);
+            }
+            l_sum *= alpha;
           }
-          l_sum *= alpha;
+          m_ref = m_new;
         }
-        m_ref = m_new;
-      }
-      // P = 2^(qs s - m_ref + 4) <= 2^8, split into e4m3 hi and lo words (4 tokens
-      // each) and written over the first 32 columns of this S buffer.  l sums the
-      // unsplit P in f32.
-      const float2 qs2 = make_float2(qs, qs), nb2 = make_float2(kPBias - m_ref, kPBias - m_ref);
-      float2 lacc = make_float2(0.f, 0.f);
-      uint32_t pw[32];
+        // P = 2^(qs s - m_ref + 4) <= 2^8, split into e4m3 hi and lo words (4 tokens
+        // each) and written over the first 32 columns of this S buffer.  l sums the
+        // unsplit P in f32.
+        const float2 qs2 = make_float2(qs, qs), nb2 = make_float2(kPBias - m_ref, kPBias - m_ref);
+        float2 lacc = make_float2(0.f, 0.f);
+        uint32_t pw[32];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int t = 4 * c;
-        const float2 x01 = __ffma2_rn(make_float2(s[t], s[t + 1]), qs2, nb2);
-        const float2 x23 = __ffma2_rn(make_float2(s[t + 2], s[t + 3]), qs2, nb2);
-        float a0 = ex2(x01.x), a1 = ex2(x01.y), a2 = ex2(x23.x), a3 = ex2(x23.y);
-        if (partial) {
-          a0 = t < valid ? a0 : 0.f;
-          a1 = t + 1 < valid ? a1 : 0.f;
-          a2 = t + 2 < valid ? a2 : 0.f;
-          a3 = t + 3 < valid ? a3 : 0.f;
+        for (int c = 0; c < 16; ++c) {
+          const int t = 4 * c;
+          const float2 x01 = __ffma2_rn(make_float2(s[t], s[t + 1]), qs2, nb2);
+          const float2 x23 = __ffma2_rn(make_float2(s[t + 2], s[t + 3]), qs2, nb2);
+          float a0 = ex2(x01.x), a1 = ex2(x01.y), a2 = ex2(x23.x), a3 = ex2(x23.y);
+          if (partial) {
+            a0 = t < valid ? a0 : 0.f;
+            a1 = t + 1 < valid ? a1 : 0.f;
+            a2 = t + 2 < valid ? a2 : 0.f;
+            a3 = t + 3 < valid ? a3 : 0.f;
+          }
+          lacc = __fadd2_rn(lacc, __fadd2_rn(make_float2(a0, a1), make_float2(a2, a3)));
+          split4(a0, a1, a2, a3, pw[c], pw[16 + c]);
         }
-        lacc = __fadd2_rn(lacc, __fadd2_rn(make_float2(a0, a1), make_float2(a2, a3)));
-        split4(a0, a1, a2, a3, pw[c], pw[16 + c]);
+        l_sum += lacc.x + lacc.y;
+        PSD_TMEM_ST32(s_col, pw);
+        if (partial) {
+          // Rows past the item's last token (still inside its page) may hold anything:
+          // zero them in this CTA's four V boxes, so that P = 0 never meets a NaN.
+          // S of this tile is complete, so its MMAs no longer read the buffer.
+          uint8_t *vt = sm + kOffK + (g % kNB) * kTileBytes + 4 * half * kBoxBytes;
+          const int n16 = (kTokM - valid) * 4;   // 16-byte chunks per box
+#pragma unroll 1
+          for (int c = row; c < 4 * n16; c += 32 * kRowWarps)
+            *reinterpret_cast<uint4 *>(vt + (c / n16) * kBoxBytes + valid * 64 + (c % n16) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async();
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BPFULL0 + (g & 1)));
       }
-      l_sum += lacc.x + lacc.y;
-      PSD_TMEM_ST32(s_col, pw);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BPFULL0 + (i & 1)));
-    }
-    // epilogue: O / l for this row and V half
-    if (ok && n_tiles > 0) {
-      const int j = n_tiles - 1;
-      ok = mbar_wait(bar(BKEMPTY0 + j % kNB), uint32_t(j / kNB) & 1u, p.fault);
-    }
-    if (__all_sync(0xffffffffu, ok) && n_tiles > 0) {
+      if (!ok) break;
+      // epilogue: O / l for this row and V half, once the item's last PV is done
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault));
+      if (!ok) break;
       tc_fence_after();
       const int64_t orow = int64_t(it.out_row) * p.Hq_req + row;
       float *dst = p.v_out + orow * kDvM + half * kDvHalf;
@@ -525,12 +616,17 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         PSD_TMEM_LD32(lane_base + kColO + cb * 32, o);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; c += 4)
-          *reinterpret_cast<float4 *>(dst + cb * 32 + c) =
-              make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
-                          __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+        for (int c = 0; c < 32; c += 8)
+          st_global_v8(dst + cb * 32 + c, __uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
+                       __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv,
+                       __uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv,
+                       __uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv);
       }
       if (half == 0) p.lse_out[orow] = m_ref - kPBias + log2f(l_sum);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BORDY));   // PV of the next item may overwrite O
+      ++mi;
     }
   }
   tc_fence_before();
@@ -588,7 +684,7 @@ psd_status launch_partial_mla(const PartialLaunch &L, const DeviceInfo &dev, cud
   MLAParams p;
   p.page_indices = L.page_indices;
   p.items = L.items;
-  p.order = L.order;
+  p.num_items = L.num_items;
   p.v_out = L.v_out;
   p.lse_out = L.lse_out;
   p.fault = L.fault;
@@ -600,7 +696,9 @@ psd_status launch_partial_mla(const PartialLaunch &L, const DeviceInfo &dev, cud
   cudaError_t e = cudaFuncSetAttribute(partial_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(kSmemMLA));
   if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-  const dim3 grid(static_cast<unsigned>(L.num_items), 1, 2);
+  // persistent: one CTA pair per two SMs, each pair a token-balanced run of items
+  const int pairs = std::max(1, std::min(L.num_items, dev.num_sms / 2));
+  const dim3 grid(static_cast<unsigned>(pairs), 1, 2);
   partial_mla_kernel<<<grid, kThreadsM, kSmemMLA, s>>>(tmQ, tmK, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "partial (MLA tcgen05) launch: %s", cudaGetErrorString(e));

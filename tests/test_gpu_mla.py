@@ -93,3 +93,25 @@ def test_mla_heads_of_different_magnitude():
     o, lse = Dev(w).decode(enable=0)
     ro, rl = A.decode_attention(A.workload_arrays(w))
     assert_close(o, lse, ro, rl, "fp8_e4m3", "MLA mixed head magnitudes")
+
+
+def test_mla_many_short_requests_switch_queries_inside_a_cta():
+    """300 requests of 1 to 130 tokens, 64-token items: every CTA pair of the
+    persistent launch walks several requests (a query split per switch) and many
+    ragged last tiles."""
+    rng = np.random.default_rng(7)
+    lengths = [int(x) for x in rng.integers(1, 131, size=300)]
+    w = _mla_small(7, lengths, num_pages=1024, tile=64)
+    o, lse = Dev(w).decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "fp8_e4m3", "MLA many short requests")
+
+
+def test_mla_many_items_per_request_keep_the_query():
+    """Three long requests in 256-token items: a CTA pair runs consecutive items of
+    one request on the query it split once; partials checked chunk by chunk."""
+    w = _mla_small(8, [20000, 18001, 9999], num_pages=1024, tile=256)
+    v, l, _, o_indptr = Dev(w).partials()
+    rv, rl, ro = oracle_partials(w)
+    assert o_indptr.tolist() == ro
+    assert_close(v, l, rv, rl, "fp8_e4m3", "MLA partials, many items per request")
