@@ -81,6 +81,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;   // S buffer b at kColS + 64 b
 constexpr float kLazyRescale = 4.f;             // log2 units
 constexpr float kPBias = 4.f;                   // P = 2^(score - m + 4) <= 2^8
+// Run partition costs in tokens of tile work (a 64-token tile takes about 2100
+// cycles): one item's O write-out about 6K cycles, one query split about 25K.
+constexpr int kItemCostTok = 180, kSplitCostTok = 750;
 
 // mbarrier slots (uint64 each) at kOffBar
 enum { BQ = 0, BQSEEN, BQREADY, BORDY, BDRAIN, BSFULL0, BPFULL0 = BSFULL0 + 2, BKFULL0 = BPFULL0 + 2,
@@ -248,14 +251,21 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   // This CTA pair's items: the contiguous run of the (request-major) item list whose
-  // first tokens fall in its 1/gridDim.x share of all tokens.  Items stay whole, and
-  // consecutive items mostly belong to one request and reuse its split query.
+  // first cost units fall in its 1/gridDim.x share of the total cost.  An item costs
+  // its tokens plus the O write-out of one item, plus a query split where the
+  // request changes (in tokens of tile work).  Items stay whole, and consecutive
+  // items mostly belong to one request and reuse its split query.
   {
     const int n = p.num_items;
     const int per = (n + kThreadsM - 1) / kThreadsM;
     const int a0 = min(n, tid * per), a1 = min(n, a0 + per);
+    auto cost = [&](int i) -> long long {
+      const psd_work_item it = p.items[i];
+      const bool first = i == 0 || __ldg(&p.items[i - 1].q_index) != it.q_index;
+      return it.n_tokens > 0 ? it.n_tokens + kItemCostTok + (first ? kSplitCostTok : 0) : 0;
+    };
     long long part = 0;
-    for (int i = a0; i < a1; ++i) part += __ldg(&p.items[i].n_tokens);
+    for (int i = a0; i < a1; ++i) part += cost(i);
     sscan[tid] = part;
     __syncthreads();
     if (tid == 0) {  // exclusive scan of the per-thread sums; the total at the end
@@ -275,7 +285,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     for (int i = a0; i < a1; ++i) {
       c_lo += start < lo_t;
       c_hi += start < hi_t;
-      start += __ldg(&p.items[i].n_tokens);
+      start += cost(i);
     }
     if (c_lo) atomicAdd(srange, c_lo);
     if (c_hi) atomicAdd(srange + 1, c_hi);
