@@ -228,25 +228,43 @@ def merge_algorithmic_bytes(arm: Arm) -> int:
 
 
 def e2e_timing(arm: Arm, steps: int, warmup: int, flush):
-    """Same decode step through the public API with host buffers: the step's query
-    rows and page table are copied from pinned host memory, the outputs read back."""
+    """Same decode step through the public API with host buffers.  The step's query
+    rows and page table travel in one host-to-device copy from a pinned staging
+    buffer (device tensors are views of one allocation); the library uploads the
+    plan; the output rows and LSE come back in one device-to-host copy."""
     psd, w = arm.psd, arm.w
-    q_host = w.q.pin_memory()
-    idx_host = torch.from_numpy(np.ascontiguousarray(w.page_indices, dtype=np.int32)).pin_memory()
-    o_host = torch.empty(arm.o.shape, dtype=torch.float32).pin_memory()
-    l_host = torch.empty(arm.lse.shape, dtype=torch.float32).pin_memory()
+    q_bytes = w.q.numel() * 2
+    idx = np.ascontiguousarray(w.page_indices, dtype=np.int32)
+    off_idx = (q_bytes + 255) // 256 * 256
+    in_bytes = off_idx + idx.nbytes
+    host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    host_in[:q_bytes].copy_(w.q.contiguous().view(torch.uint8).reshape(-1))
+    host_in[off_idx:].copy_(torch.from_numpy(idx).view(torch.uint8))
+    dev_in = torch.empty(in_bytes, dtype=torch.uint8, device="cuda")
+    q_dev = dev_in[:q_bytes].view(torch.bfloat16).view(w.q.shape)
+    idx_dev = dev_in[off_idx:].view(torch.int32)
+    o_elems, l_elems = arm.o.numel(), arm.lse.numel()
+    dev_out = torch.empty(o_elems + l_elems, dtype=torch.float32, device="cuda")
+    host_out = torch.empty(o_elems + l_elems, dtype=torch.float32).pin_memory()
+    o_dev, l_dev = dev_out[:o_elems].view(arm.o.shape), dev_out[o_elems:].view(arm.lse.shape)
+    args = psd.decode_args(q_dev, arm.k, arm.v, idx_dev, num_pages=w.num_pages, page_size=w.page_size,
+                           Hkv=w.Hkv, Dv=w.Dv, sm_scale=w.sm_scale, k_scale=w.k_scale, v_scale=w.v_scale)
 
     def step():
-        arm.q.copy_(q_host, non_blocking=True)
-        arm.indices.copy_(idx_host, non_blocking=True)
-        arm.step()
-        o_host.copy_(arm.o, non_blocking=True)
-        l_host.copy_(arm.lse, non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
+        psd.plan_decode(arm.table, w.tile_tokens, arm.enable, w.min_shared_pages, w.min_members, plan=arm.plan)
+        psd.cascade_decode(arm.ctx, args, arm.plan, o_dev, l_dev, arm.ws)
+        host_out.copy_(dev_out, non_blocking=True)
 
     times = time_steps(step, steps, warmup, flush)
+    torch.cuda.synchronize()
+    arm.step()
+    torch.cuda.synchronize()
+    got = host_out[:o_elems].view(arm.o.shape)
+    assert torch.equal(got, arm.o.cpu()), "end-to-end outputs differ from the device-resident step"
     plan_bytes = (arm.plan.num_items * 16 + (w.batch * 3 + 1) * 4 + 256)
-    h2d = q_host.numel() * 2 + idx_host.numel() * 4 + plan_bytes
-    d2h = o_host.numel() * 4 + l_host.numel() * 4
+    h2d = in_bytes + plan_bytes
+    d2h = (o_elems + l_elems) * 4
     return times, h2d, d2h
 
 
