@@ -291,7 +291,8 @@ psd_status paged_decode_partial(psd_ctx *ctx, const psd_decode_args *args,
  * i in [o_indptr[r], o_indptr[r+1]):  M = max lse_i, w_i = 2^(lse_i - M),
  *   v_out = sum w_i v_i / sum w_i,  lse_out = M + log2(sum w_i).
  * A one-row group copies v and lse bit-exactly; an empty or all -inf group
- * gives 0 and -inf.  v_in device [N, H, D] f32, lse_in device [N, H] f32,
+ * gives 0 and -inf.  A row whose lse is -inf is an empty partial (no tokens): its
+ * weight is zero and its v is not used, whatever it holds.  v_in device [N, H, D] f32, lse_in device [N, H] f32,
  * o_indptr_dev device [num_out + 1] int32 (non-decreasing), v_out device
  * [num_out, H, D] f32, lse_out device [num_out, H] f32 or NULL.  D % 4 == 0,
  * D <= 1024; all pointers 16-byte aligned. */

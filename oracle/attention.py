@@ -189,9 +189,11 @@ def merge_states(v_in: np.ndarray, lse_in: np.ndarray, o_indptr) -> tuple:
     For output row r and head h over rows i in [o_indptr[r], o_indptr[r+1]):
         M = max_i lse_i,  w_i = 2^(lse_i - M),
         out = sum_i w_i v_i / sum_i w_i,  lse_out = M + log2 sum_i w_i.
-    A one-row group gives w = 1, out = v, lse_out = lse.  An empty group, or one
-    whose LSEs are all -inf, gives out = 0 and lse_out = -inf (the pages leave this
-    open; neither plan produces it).
+    A one-row group gives w = 1, out = v, lse_out = lse.  A row whose LSE is -inf is
+    an empty partial (no tokens): its weight 2^(-inf - M) is zero and its v is not
+    used, whatever it holds (the pages define no V for an empty partial).  An empty
+    group, or one whose LSEs are all -inf, gives out = 0 and lse_out = -inf (the
+    pages leave this open).
     """
     v_in = np.asarray(v_in, dtype=np.float64)
     lse_in = np.asarray(lse_in, dtype=np.float64)
@@ -209,7 +211,9 @@ def merge_states(v_in: np.ndarray, lse_in: np.ndarray, o_indptr) -> tuple:
         mx_safe = np.where(ok, mx, 0.0)
         w = np.exp2(l - mx_safe)                              # [n, H]
         sw = w.sum(axis=0)
-        acc = (w[:, :, None] * v_in[lo:hi]).sum(axis=0)
+        live = ~np.isneginf(l)                                # empty rows contribute nothing
+        acc = np.where(live[:, :, None], w[:, :, None] * np.where(live[:, :, None], v_in[lo:hi], 0.0),
+                       0.0).sum(axis=0)
         out[r] = np.where(ok[:, None], acc / np.where(ok, sw, 1.0)[:, None], 0.0)
         lse_out[r] = np.where(ok, mx_safe + np.log2(np.where(ok, sw, 1.0)), -np.inf)
     return out, lse_out

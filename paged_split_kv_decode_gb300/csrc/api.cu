@@ -121,14 +121,28 @@ bool dispatchable(const PartialLaunch &L) {
 // (128 heads, 576/512): the tcgen05 kernel; other fp8 or latent shapes: the
 // 64-row mma.sync kernel (also used for MLA when the context asks for CUDA_CORE,
 // as the legacy-tensor-path reference).
+PartialKind select_partial(const PartialLaunch &L, const DeviceInfo &dev) {
+  if (dev.partial_kernel == PSD_KERNEL_CUDA_CORE && partial_cc_supports(L)) return PartialKind::kCudaCore;
+  if (partial_tcs_supports(L)) return PartialKind::kTensorSmall;
+  if (partial_cc_supports(L)) return PartialKind::kCudaCore;
+  if (partial_mla_supports(L) && dev.partial_kernel != PSD_KERNEL_CUDA_CORE) return PartialKind::kMLA;
+  if (partial_tc_supports(L)) return PartialKind::kTensorLegacy;
+  return PartialKind::kNone;
+}
+
+// Only the MLA kernel accumulates runs of items (PartialLaunch::merge_runs).
+bool writes_empty_rows(const PartialLaunch &L, const DeviceInfo &dev) {
+  return L.merge_runs && select_partial(L, dev) == PartialKind::kMLA;
+}
+
 psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
-  if (dev.partial_kernel == PSD_KERNEL_CUDA_CORE && partial_cc_supports(L))
-    return launch_partial_cc(L, dev, s);
-  if (partial_tcs_supports(L)) return launch_partial_tcs(L, dev, s);
-  if (partial_cc_supports(L)) return launch_partial_cc(L, dev, s);
-  if (partial_mla_supports(L) && dev.partial_kernel != PSD_KERNEL_CUDA_CORE)
-    return launch_partial_mla(L, dev, s);
-  if (partial_tc_supports(L)) return launch_partial_tc(L, dev, s);
+  switch (select_partial(L, dev)) {
+    case PartialKind::kCudaCore: return launch_partial_cc(L, dev, s);
+    case PartialKind::kTensorSmall: return launch_partial_tcs(L, dev, s);
+    case PartialKind::kMLA: return launch_partial_mla(L, dev, s);
+    case PartialKind::kTensorLegacy: return launch_partial_tc(L, dev, s);
+    case PartialKind::kNone: break;
+  }
   return fail(PSD_ERR_UNSUPPORTED, "no kernel for Dqk %d, Dv %d, rows/KV head %d, dtype %d, latent %d",
               L.Dqk, L.Dv, L.G_cta, L.kv_dtype, int(L.latent_v));
 }
@@ -402,6 +416,7 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
     return fail(PSD_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, lay.total);
 
   PartialLaunch L1 = base_launch(args);
+  L1.merge_runs = true;  // the partial rows feed the merge below
   PartialLaunch L0 = L1;
   L0.G_cta = M * L1.Gm;
   if (!dispatchable(L1)) return launch_partial(L1, ctx->dev, nullptr);
@@ -479,7 +494,7 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   time_mark(ctx, 4, s);
   const bool merge_follows_partial = !(M > 0 && !fused) && !ctx->timing;
   st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq,
-                    args->Dv, o, lse, ctx->dev, s, merge_follows_partial);
+                    args->Dv, o, lse, ctx->dev, s, merge_follows_partial, writes_empty_rows(L1, ctx->dev));
   time_mark(ctx, 5, s);
   ctx->tev_used[0] = ctx->timing && M > 0 && !fused;
   ctx->tev_used[1] = ctx->timing;
@@ -563,6 +578,7 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
   if (workspace_bytes < lay.total)
     return fail(PSD_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, lay.total);
   PartialLaunch L1 = base_launch(args);
+  L1.merge_runs = true;  // the partial rows feed the merge below
   if (!dispatchable(L1)) return launch_partial(L1, ctx->dev, nullptr);
   for (int32_t s = 0; s < S; ++s) {
     PartialLaunch L0 = L1;
@@ -653,7 +669,7 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
   }
   time_mark(ctx, 4, s);
   st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq, args->Dv, o,
-                    lse, ctx->dev, s, !joined && !ctx->timing);
+                    lse, ctx->dev, s, !joined && !ctx->timing, writes_empty_rows(L1, ctx->dev));
   time_mark(ctx, 5, s);
   ctx->tev_used[0] = ctx->timing && joined;
   ctx->tev_used[1] = ctx->timing;

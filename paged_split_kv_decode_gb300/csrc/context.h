@@ -60,6 +60,11 @@ psd_status validate_items(const psd_decode_args *a, const psd_work_item *items, 
                           int64_t out_rows, bool stacked, int32_t num_members);
 PartialLaunch base_launch(const psd_decode_args *a);
 bool dispatchable(const PartialLaunch &L);
+enum class PartialKind { kNone, kCudaCore, kTensorSmall, kMLA, kTensorLegacy };
+// The kernel launch_partial runs for L on dev.
+PartialKind select_partial(const PartialLaunch &L, const DeviceInfo &dev);
+// The launch may leave empty partial rows (LSE -inf, v not written) for the merge.
+bool writes_empty_rows(const PartialLaunch &L, const DeviceInfo &dev);
 psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s);
 
 }  // namespace psd

@@ -42,6 +42,10 @@ struct PartialLaunch {
   int32_t kv_dtype = PSD_BF16;
   bool latent_v = false;
   int32_t max_item_tokens = 0;
+  // The partial rows feed this library's merge: a kernel may accumulate a run of
+  // consecutive items of one request into one partial, written to the run's last
+  // row, and mark the other rows empty (LSE -inf, v unused by the merge).
+  bool merge_runs = false;
   float q_scale = 1.f;  // sm_scale * log2(e) * k_scale
   float v_scale = 1.f;
   // Fused cascade launch (16-row-group tensor-core kernel only): `items` starts
@@ -68,8 +72,12 @@ psd_status launch_rope_append(const psd_rope_append_args *a, cudaStream_t s);
 
 // after_partial: the launch directly follows a partial kernel on stream s (no event
 // or copy between them), so it may start early and wait for that grid on the device.
+// skip_empty: many rows are empty (LSE -inf); each row's LSE is read before its v,
+// and an empty row's v is not loaded.  Without it the rows of a batch are loaded
+// with the LSE values (one round trip fewer) and an empty row's v is ignored.
 psd_status launch_merge(const float *v_in, const float *lse_in, const int32_t *o_indptr,
                         int64_t num_out, int32_t H, int32_t D, float *v_out, float *lse_out,
-                        const DeviceInfo &dev, cudaStream_t s, bool after_partial = false);
+                        const DeviceInfo &dev, cudaStream_t s, bool after_partial = false,
+                        bool skip_empty = false);
 
 }  // namespace psd

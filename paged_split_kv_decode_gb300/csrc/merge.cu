@@ -3,12 +3,15 @@
 // o_indptr [M + 1] grouping contiguous rows; a group of one is the identity).
 //
 // HBM-bound stream: each input row of one head is D floats read once, each output
-// row D floats written once.  One warp owns one (output row, head); lanes hold
+// row D floats written once.  A row whose LSE is -inf is an empty partial: weight
+// zero, and its v is not used.  One warp owns one (output row, head); lanes hold
 // float4 slices of D.  The first 16 / NV input rows are loaded together with the
 // first 32 LSE values (the rows do not depend on the maximum), and later rows in
 // batches of the same size, so a group of up to 16 rows costs one round trip to
-// memory after the group bounds.  When the partial kernel before it on the stream
-// allows it, the merge launches early, reads o_indptr, then waits for that grid.
+// memory after the group bounds.  The SKIP form, for partials with many empty rows,
+// reads each batch's LSE values first and loads only the live rows' v.  When the
+// partial kernel before it on the stream allows it, the merge launches early, reads
+// o_indptr, then waits for that grid.
 #include <cuda_runtime.h>
 
 #include "device.cuh"
@@ -23,8 +26,8 @@ constexpr int kMergeWarps = 8;
 // NV: float4 slices per lane (D <= 128 * NV).  WIDE batches 16 / NV rows for grids of
 // about one wave (latency-bound); the narrow form batches half as many rows with
 // fewer registers, so more warps per SM keep loads in flight on large grids.
-template <int NV, bool WIDE>
-__global__ void __launch_bounds__(kMergeWarps * 32, WIDE ? 1 : (NV >= 8 ? 2 : 3))
+template <int NV, bool WIDE, bool SKIP>
+__global__ void __launch_bounds__(kMergeWarps * 32, WIDE ? 1 : (NV >= (SKIP ? 4 : 8) ? 2 : 3))
     merge_states_kernel(const float *__restrict__ v_in, const float *__restrict__ lse_in,
                         const int32_t *__restrict__ o_indptr, int64_t num_out, int H, int D,
                         float *__restrict__ v_out, float *__restrict__ lse_out) {
@@ -42,10 +45,13 @@ __global__ void __launch_bounds__(kMergeWarps * 32, WIDE ? 1 : (NV >= 8 ? 2 : 3)
   float4 *out4 = reinterpret_cast<float4 *>(v_out + (r * H + h) * int64_t(D));
 
   float4 v[U][NV];
-  auto load_rows = [&](int first, int count) {
+  // Rows first .. first + count - 1 (at most U) of the group; lw holds, in lane i,
+  // the LSE of row w0 + i of the current 32-row window, and j0 = first - w0.
+  auto load_rows = [&](int first, int count, float lw, int j0) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const bool ok = u < count;
+      bool ok = u < count;
+      if constexpr (SKIP) ok = __shfl_sync(0xffffffffu, lw, (j0 + u) & 31) != neg_inf() && ok;
       const float4 *src =
           reinterpret_cast<const float4 *>(v_in + (int64_t(lo + first + u) * H + h) * D);
 #pragma unroll
@@ -57,7 +63,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, WIDE ? 1 : (NV >= 8 ? 2 : 3)
   };
 
   const float l_first = lane < n ? __ldg(lse_in + int64_t(lo + lane) * H + h) : neg_inf();
-  load_rows(0, n);
+  load_rows(0, n, l_first, 0);
 
   if (n == 1) {  // identity: w = 1, l = 1, out = v bit for bit
     const float l = __shfl_sync(0xffffffffu, l_first, 0);
@@ -96,10 +102,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32, WIDE ? 1 : (NV >= 8 ? 2 : 3)
     const float w_mine = lane < cnt ? ex2(l - M) : 0.f;
     sw += w_mine;
     for (int j = 0; j < cnt; j += U) {
-      if (i0 + j > 0) load_rows(i0 + j, cnt - j);
+      if (i0 + j > 0) load_rows(i0 + j, cnt - j, l, j);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const float w = j + u < cnt ? __shfl_sync(0xffffffffu, w_mine, (j + u) & 31) : 0.f;
+        if (w == 0.f) continue;  // an empty row (LSE -inf): its v is not used, whatever it holds
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
           acc[k].x = fmaf(w, v[u][k].x, acc[k].x);
@@ -122,8 +129,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32, WIDE ? 1 : (NV >= 8 ? 2 : 3)
   if (lse_out && lane == 0) lse_out[r * H + h] = M + log2f(sw);
 }
 
-template <int NV>
-cudaError_t launch_nv(dim3 grid, bool wide, bool early, cudaStream_t s, const float *v_in, const float *lse_in,
+template <int NV, bool SKIP>
+cudaError_t launch_form(dim3 grid, bool wide, bool early, cudaStream_t s, const float *v_in, const float *lse_in,
                       const int32_t *o_indptr, int64_t num_out, int H, int D, float *v_out,
                       float *lse_out) {
   cudaLaunchConfig_t cfg = {};
@@ -137,17 +144,25 @@ cudaError_t launch_nv(dim3 grid, bool wide, bool early, cudaStream_t s, const fl
   cfg.attrs = attr;
   cfg.numAttrs = early ? 1 : 0;
   if (wide)
-    return cudaLaunchKernelEx(&cfg, merge_states_kernel<NV, true>, v_in, lse_in, o_indptr, num_out,
+    return cudaLaunchKernelEx(&cfg, merge_states_kernel<NV, true, SKIP>, v_in, lse_in, o_indptr, num_out,
                               H, D, v_out, lse_out);
-  return cudaLaunchKernelEx(&cfg, merge_states_kernel<NV, false>, v_in, lse_in, o_indptr, num_out, H,
+  return cudaLaunchKernelEx(&cfg, merge_states_kernel<NV, false, SKIP>, v_in, lse_in, o_indptr, num_out, H,
                             D, v_out, lse_out);
+}
+
+template <int NV>
+cudaError_t launch_nv(dim3 grid, bool wide, bool early, bool skip, cudaStream_t s, const float *v_in,
+                      const float *lse_in, const int32_t *o_indptr, int64_t num_out, int H, int D,
+                      float *v_out, float *lse_out) {
+  return skip ? launch_form<NV, true>(grid, wide, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out)
+              : launch_form<NV, false>(grid, wide, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
 }
 
 }  // namespace
 
 psd_status launch_merge(const float *v_in, const float *lse_in, const int32_t *o_indptr,
                         int64_t num_out, int32_t H, int32_t D, float *v_out, float *lse_out,
-                        const DeviceInfo &dev, cudaStream_t s, bool after_partial) {
+                        const DeviceInfo &dev, cudaStream_t s, bool after_partial, bool skip_empty) {
   if (num_out == 0 || H == 0) return PSD_OK;
   const int64_t warps = num_out * H;
   const int64_t blocks = (warps + kMergeWarps - 1) / kMergeWarps;
@@ -157,13 +172,13 @@ psd_status launch_merge(const float *v_in, const float *lse_in, const int32_t *o
   const bool wide = blocks <= 2LL * dev.num_sms;
   cudaError_t e;
   if (D <= 128)
-    e = launch_nv<1>(grid, wide, after_partial, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
+    e = launch_nv<1>(grid, wide, after_partial, skip_empty, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
   else if (D <= 256)
-    e = launch_nv<2>(grid, wide, after_partial, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
+    e = launch_nv<2>(grid, wide, after_partial, skip_empty, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
   else if (D <= 512)
-    e = launch_nv<4>(grid, wide, after_partial, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
+    e = launch_nv<4>(grid, wide, after_partial, skip_empty, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
   else
-    e = launch_nv<8>(grid, wide, after_partial, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
+    e = launch_nv<8>(grid, wide, after_partial, skip_empty, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "merge_states launch: %s", cudaGetErrorString(e));
   return PSD_OK;

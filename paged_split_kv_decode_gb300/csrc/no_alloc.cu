@@ -109,6 +109,7 @@ extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_arg
                 lay.total, kNoAllocScratchBytes);
 
   PartialLaunch L1 = base_launch(args);
+  L1.merge_runs = true;  // the partial rows feed the merge below
   PartialLaunch L0 = L1;
   L0.G_cta = M * L1.Gm;
   if (!dispatchable(L1)) return launch_partial(L1, ctx->dev, nullptr);
@@ -154,7 +155,7 @@ extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_arg
   L1.fault = fault;
   if ((st = launch_partial(L1, ctx->dev, s)) != PSD_OK) return st;
   st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq,
-                    args->Dv, o, lse, ctx->dev, s, true);
+                    args->Dv, o, lse, ctx->dev, s, true, writes_empty_rows(L1, ctx->dev));
   if (st != PSD_OK) return st;
   if (fault_bits_dev) {
     e = cudaMemcpyAsync(fault_bits_dev, fault, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);

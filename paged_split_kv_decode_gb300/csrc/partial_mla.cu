@@ -31,6 +31,9 @@
 //     ragged last tile.
 //   * Per tile the control warp waits twice (tile landed, P written) and commits
 //     twice (S ready, tile and P consumed).
+//   * When the rows feed this library's merge, consecutive items of one request in
+//     a CTA's run accumulate into one partial (O, max and sum carry over), written
+//     at the last of them; the rows of the others are marked empty (LSE -inf).
 // The k_scale and the query row's power of two fold into the score scale, v_scale
 // into the output.  The two CTAs of an item both compute S; the tile is read from
 // HBM once and from L2 by the second CTA.  Every mbarrier wait is bounded.
@@ -82,7 +85,8 @@ constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;   // S buffer b at kColS
 constexpr float kLazyRescale = 4.f;             // log2 units
 constexpr float kPBias = 4.f;                   // P = 2^(score - m + 4) <= 2^8
 // Run partition costs in tokens of tile work (a 64-token tile takes about 2100
-// cycles): one item's O write-out about 6K cycles, one query split about 25K.
+// cycles): one O write-out about 6K cycles (charged to the items that write one),
+// one query split about 25K.
 constexpr int kItemCostTok = 180, kSplitCostTok = 750;
 
 // mbarrier slots (uint64 each) at kOffBar
@@ -99,8 +103,15 @@ struct MLAParams {
   int32_t *fault;
   int64_t num_pages;
   int Hq_req, page_size;
+  int merge_runs;  // rows feed the merge: accumulate consecutive items of one request
   float q_scale, v_scale;
 };
+
+// Item b continues item a's partial: the next chunk of the same request, whose row
+// follows a's in the request's merge group.
+__device__ __forceinline__ bool continues(const psd_work_item &a, const psd_work_item &b) {
+  return b.q_index == a.q_index && b.out_row == a.out_row + 1 && a.n_tokens > 0 && b.n_tokens > 0;
+}
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   // 64-byte swizzle (layout code 4), descriptor version 1
@@ -262,7 +273,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     auto cost = [&](int i) -> long long {
       const psd_work_item it = p.items[i];
       const bool first = i == 0 || __ldg(&p.items[i - 1].q_index) != it.q_index;
-      return it.n_tokens > 0 ? it.n_tokens + kItemCostTok + (first ? kSplitCostTok : 0) : 0;
+      const bool writes = !p.merge_runs || i + 1 == n || !continues(it, p.items[i + 1]);
+      return it.n_tokens > 0 ? it.n_tokens + (writes ? kItemCostTok : 0) + (first ? kSplitCostTok : 0) : 0;
     };
     long long part = 0;
     for (int i = a0; i < a1; ++i) part += cost(i);
@@ -368,14 +380,18 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // V (MN-major): 64-column atoms one box apart, 8-token groups 512 bytes apart
     const uint64_t vd = smem_desc(smem_u32(sm + kOffK + 4 * half * kBoxBytes), kBoxBytes, 512);
     bool ok = true;
-    int g = 0, nq = 0, cur_q = -1, mi = 0;
-    int pend = -1, pend_mi = 0;  // tile whose PV is still to issue, and its item ordinal
+    int g = 0, nq = 0, cur_q = -1, npart = 0;
+    int pend = -1, pend_po = 0;  // tile whose PV is still to issue, and its partial's ordinal
     bool pend_first = false;     // ... which is the first tile of that item
+    bool pend_cont = false;      // ... which adds to the previous item's O
     auto issue_pv = [&]() -> bool {
       const int t = pend, buf = t % kNB;
       bool r = __all_sync(0xffffffffu, mbar_wait(bar(BPFULL0 + (t & 1)), uint32_t(t >> 1) & 1u, p.fault));
-      if (r && pend_first && pend_mi > 0)  // the previous item's O has been read out
-        r = __all_sync(0xffffffffu, mbar_wait(bar(BORDY), uint32_t(pend_mi - 1) & 1u, p.fault));
+      // The previous partial's O has been read out.  BORDY completes once per read-out
+      // and the row warps read out partial k only after PV of partial k is issued,
+      // so they are never two phases ahead of this wait.
+      if (r && pend_first && !pend_cont && pend_po > 0)
+        r = __all_sync(0xffffffffu, mbar_wait(bar(BORDY), uint32_t(pend_po - 1) & 1u, p.fault));
       if (!r) return false;
       tc_fence_after();
       if (elect_one()) {
@@ -384,7 +400,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 #pragma unroll
         for (int k = 0; k < 2; ++k) {  // tokens 32 k .. 32 k + 31
           const uint64_t vbk = vb + ((k * 32 * 64) >> 4);
-          mma_ts(tmem + kColO, a_p + 8 * k, vbk, id_pv, (pend_first && k == 0) ? 0u : 1u);
+          mma_ts(tmem + kColO, a_p + 8 * k, vbk, id_pv, (pend_first && !pend_cont && k == 0) ? 0u : 1u);
           mma_ts(tmem + kColO, a_p + 16 + 8 * k, vbk, id_pv, 1u);
         }
         umma_commit(bar(BKEMPTY0 + buf));
@@ -397,6 +413,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       const psd_work_item it = p.items[m];
       const int nt = (it.n_tokens + kTokM - 1) / kTokM;
       if (nt <= 0) continue;  // (the planner emits no empty items)
+      const bool cont = p.merge_runs && m > begin && continues(p.items[m - 1], it);
+      if (!cont) ++npart;
       if (it.q_index != cur_q) {
         // the split of the next query waits for every PV issued so far
         if (pend >= 0) ok = issue_pv();
@@ -433,9 +451,9 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         if (pend >= 0 && !(ok = issue_pv())) break;
         pend = g++;
         pend_first = j == 0;
-        pend_mi = mi;
+        pend_cont = cont;
+        pend_po = npart - 1;
       }
-      ++mi;
     }
     if (ok && pend >= 0) issue_pv();
     // every MMA this warp issued has completed before TMEM is released
@@ -447,12 +465,15 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     const int row = tid;                          // head = TMEM lane
     const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
     bool ok = true;
-    int g = 0, nq = 0, cur_q = -1, mi = 0;
+    int g = 0, nq = 0, cur_q = -1;
     float qs = 0.f;  // score scale of this row for the current query
+    float m_ref = neg_inf(), l_sum = 0.f;  // running max (log2, biased P) and sum
     for (int m = begin; m < end && ok; ++m) {
       const psd_work_item it = p.items[m];
       const int nt = (it.n_tokens + kTokM - 1) / kTokM;
       if (nt <= 0) continue;  // (the planner emits no empty items)
+      // A continued item adds to the previous item's O, m_ref and l_sum.
+      const bool cont = p.merge_runs && m > begin && continues(p.items[m - 1], it);
       if (it.q_index != cur_q) {
         // Query split.  Pass 1 moves the bf16 row from the landing boxes to TMEM
         // columns 0..287 (free between items) and takes its largest magnitude;
@@ -518,7 +539,10 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         ++nq;
       }
 
-      float m_ref = neg_inf(), l_sum = 0.f;
+      if (!cont) {
+        m_ref = neg_inf();
+        l_sum = 0.f;
+      }
       const bool qpos = qs >= 0.f;
       const int tail = it.n_tokens - (nt - 1) * kTokM;   // valid tokens of the last tile
 #pragma unroll 1
@@ -553,7 +577,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         const bool grow = mt > m_ref + kLazyRescale;
         if (__any_sync(0xffffffffu, grow)) {
           const float m_new = grow ? mt : m_ref;
-          if (j >= 1) {  // PV(g-1) must be done; then rescale this warp's O rows in TMEM
+          if (j >= 1 || cont) {  // PV(g-1) must be done; then rescale this warp's O rows in TMEM
             ok = __all_sync(0xffffffffu,
                             mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault));
             if (!ok) break;
@@ -613,6 +637,12 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         if (lane == 0) mbar_arrive(bar(BPFULL0 + (g & 1)));
       }
       if (!ok) break;
+      if (p.merge_runs && m + 1 < end && continues(it, p.items[m + 1])) {
+        // The next item continues this partial: this item's row is empty (LSE -inf,
+        // v not written; the merge does not read it), and O is not read out.
+        if (half == 0) p.lse_out[int64_t(it.out_row) * p.Hq_req + row] = neg_inf();
+        continue;
+      }
       // epilogue: O / l for this row and V half, once the item's last PV is done
       ok = __all_sync(0xffffffffu, mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault));
       if (!ok) break;
@@ -635,8 +665,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       if (half == 0) p.lse_out[orow] = m_ref - kPBias + log2f(l_sum);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BORDY));   // PV of the next item may overwrite O
-      ++mi;
+      if (lane == 0) mbar_arrive(bar(BORDY));   // PV of the next partial may overwrite O
     }
   }
   tc_fence_before();
@@ -701,6 +730,7 @@ psd_status launch_partial_mla(const PartialLaunch &L, const DeviceInfo &dev, cud
   p.num_pages = L.num_pages;
   p.Hq_req = L.Hq_req;
   p.page_size = L.page_size;
+  p.merge_runs = L.merge_runs ? 1 : 0;
   p.q_scale = L.q_scale;
   p.v_scale = L.v_scale;
   cudaError_t e = cudaFuncSetAttribute(partial_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -84,6 +84,26 @@ def test_empty_and_neg_inf_groups():
     assert torch.equal(vo[3, 1].cpu(), v_in[2, 1]) and torch.equal(vo[3, 0].cpu(), torch.zeros(8))
 
 
+def test_empty_partials_in_groups_are_ignored():
+    """Rows with LSE -inf inside larger groups (v NaN) contribute nothing, against the
+    oracle (which ignores them too), over groups of 1 to 40 rows."""
+    rng = np.random.default_rng(11)
+    o_indptr = synth.merge_groups(rng, 400, 1, 40)
+    N = int(o_indptr[-1])
+    v_in = torch.from_numpy(rng.standard_normal((N, 8, 64), dtype=np.float32))
+    lse_in = torch.from_numpy(rng.uniform(-5, 20, size=(N, 8)).astype(np.float32))
+    empty = torch.from_numpy(rng.random((N, 8)) < 0.4)
+    for r in range(len(o_indptr) - 1):      # keep one live row per (group, head)
+        empty[int(o_indptr[r])] = False
+    lse_in[empty] = -float("inf")
+    v_in[empty] = float("nan")
+    ro, rl = A.merge_states(v_in.numpy(), lse_in.numpy(), o_indptr)
+    assert np.isfinite(ro).all()
+    vo, lo = _gpu_merge(v_in, lse_in, o_indptr)
+    assert np.abs(vo.cpu().double().numpy() - ro).max() < TOL_O
+    assert np.abs(lo.cpu().double().numpy() - rl).max() < TOL_L
+
+
 def test_lse_out_may_be_null():
     v_in, lse_in, o_indptr = synth.merge_inputs(6, 100)
     ro, _ = A.merge_states(v_in.numpy(), lse_in.numpy(), o_indptr)

@@ -6,9 +6,10 @@ import numpy as np
 import pytest
 import torch
 
+import paged_split_kv_decode_gb300 as psd
 import synth
 from oracle import attention as A
-from _gpu_util import Dev, assert_close, oracle_partials
+from _gpu_util import Dev, assert_close, ctx, oracle_partials
 
 pytestmark = pytest.mark.gpu
 
@@ -115,3 +116,39 @@ def test_mla_many_items_per_request_keep_the_query():
     rv, rl, ro = oracle_partials(w)
     assert o_indptr.tolist() == ro
     assert_close(v, l, rv, rl, "fp8_e4m3", "MLA partials, many items per request")
+
+
+def test_mla_decode_accumulates_runs_of_items():
+    """Decode through the merge: a CTA pair adds consecutive items of one request into
+    one partial and marks the others empty, and the runs of the persistent launch end
+    mid-request.  Against the oracle, and beside merge_states over the per-item
+    partials of the same work list."""
+    w = _mla_small(9, [20000, 18001, 9999, 64, 1, 130, 4097, 2047], num_pages=1024, tile=256)
+    d = Dev(w)
+    o, lse = d.decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "fp8_e4m3", "MLA runs of items")
+    v, l, _, o_indptr = d.partials()
+    vo = torch.empty((w.batch, w.Hq, w.Dv), dtype=torch.float32, device="cuda")
+    lo_ = torch.empty((w.batch, w.Hq), dtype=torch.float32, device="cuda")
+    psd.merge_states(ctx(), torch.from_numpy(v).float().cuda(), torch.from_numpy(l).float().cuda(),
+                     torch.from_numpy(np.asarray(o_indptr, dtype=np.int32)).cuda(), vo, lo_)
+    # Both within the fp8 bounds of the oracle.  They are not bit-equal: a run carries
+    # one running max across items, so P's two e4m3 terms round differently.
+    assert_close(vo.cpu().double().numpy(), lo_.cpu().double().numpy(), ro, rl, "fp8_e4m3",
+                 "MLA per-item partials merged")
+    assert np.abs(vo.cpu().double().numpy() - o).max() < 2e-3
+
+
+def test_mla_cascade_level1_runs():
+    """A shared whole-page prefix: level 0 (stacked rows) on the 64-row kernel, level 1
+    on the persistent kernel with runs of items accumulated, one merge over both."""
+    rng = np.random.default_rng(10)
+    lengths = [4096 + 1500, 4096 + 3000, 4096 + 70, 6000, 2500]
+    w = synth._make("mla_cascade", rng, lengths, Hq=128, Hkv=1, Dqk=576, Dv=512, page_size=64,
+                    num_pages=1024, tile_tokens=512, kv_dtype="fp8_e4m3", latent_v=True,
+                    shared=([0, 1, 2], 4096 // 64), min_shared_pages=16, min_members=2)
+    o, lse, stats, _ = Dev(w).decode(enable=1, with_stats=True)
+    assert stats["path"] == 1 and stats["members"] == 3
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "fp8_e4m3", "MLA cascade")

@@ -80,3 +80,26 @@ def test_two_row_merge_weights_by_powers_of_two():
     v = np.array([[[3.0]], [[6.0]]])
     o, lo = A.merge_states(v, np.array([[0.0], [1.0]]), [0, 2])
     assert abs(o[0, 0, 0] - 5.0) < 1e-15 and abs(lo[0, 0] - np.log2(3.0)) < 1e-15
+
+
+def test_empty_partials_are_ignored_whatever_their_v():
+    """A row with LSE = -inf is an empty partial (a chunk with no tokens): merging a
+    group with such rows (v NaN or huge) equals merging the group without them, and
+    equals attention over the union of the non-empty chunks."""
+    rng = np.random.default_rng(4)
+    q, K, V = _request(rng, L=60)
+    o, lse = A.attend(q, K, V, 0.4)
+    parts = [A.attend(q, K[a:b], V[a:b], 0.4) for a, b in ((0, 25), (25, 60))]
+    H, D = parts[0][0].shape
+    empty_v = np.full((H, D), np.nan)
+    rows_v = [parts[0][0], empty_v, parts[1][0], np.full((H, D), 1e300)]
+    rows_l = [parts[0][1], np.full(H, -np.inf), parts[1][1], np.full(H, -np.inf)]
+    mo, ml = A.merge_states(np.stack(rows_v), np.stack(rows_l), [0, 4])
+    assert np.abs(mo[0] - o).max() < 1e-13 and np.abs(ml[0] - lse).max() < 1e-13
+    # mixed: head 0 of a row empty, the other heads live
+    l2 = np.stack([parts[0][1], parts[1][1]]).copy()
+    v2 = np.stack([parts[0][0], parts[1][0]]).copy()
+    l2[1, 0], v2[1, 0] = -np.inf, np.nan
+    mo2, ml2 = A.merge_states(v2, l2, [0, 2])
+    assert np.array_equal(mo2[0, 0], parts[0][0][0]) and ml2[0, 0] == parts[0][1][0]
+    assert np.abs(mo2[0, 1:] - o[1:]).max() < 1e-13
