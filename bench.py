@@ -39,8 +39,8 @@ NOMINAL_HBM_GBS = 8000.0
 # ncu capture summarised in profiles/partial_tcs_flat_decode.md.  Reported only while
 # the kernel source is the one the counters were taken on.
 TRAFFIC_SOURCE = os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", "partial_tcs.cu")
-TRAFFIC_SHA256 = "bdf00e09fac468e2d0a0a015ca0724da4f4f1508a8fed112c43a4c3c0effa93f"
-TRAFFIC_BYTES = 316077568 + 1174272
+TRAFFIC_SHA256 = "fbb7f543e472180bdc4a17b798fccd72e92fee3a3b9b2a0e6b7c77df25b291ed"
+TRAFFIC_BYTES = 316074240 + 1252608
 
 
 def partial_traffic():

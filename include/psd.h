@@ -145,10 +145,13 @@ typedef struct {
   int32_t prefix_chunks, suffix_chunks;
 } psd_cascade_stats;
 
-/* In-context counters (Task item 5, without a metrics server). */
+/* In-context counters (Task item 5, without a metrics server).  lists_inline /
+ * lists_uploaded count decode calls whose work lists travelled in the kernel
+ * launches' parameters / by one host-to-device copy into the workspace. */
 typedef struct {
   int64_t launches_flat, launches_cascade;
   int64_t cascade_shared_tokens, cascade_member_sequences, cascade_failures;
+  int64_t lists_inline, lists_uploaded;
 } psd_counters;
 
 typedef struct psd_ctx psd_ctx;
@@ -307,7 +310,11 @@ psd_status merge_states(psd_ctx *ctx, const float *v_in, const float *lse_in,
  * level-0 and level-1 rows (and passes a non-member's single chunk group through).
  * o: device [batch, Hq, Dv] f32.  lse: device [batch, Hq] f32 (log2) or NULL.
  * workspace: >= psd_workspace_bytes(batch, plan item total, plan->num_rows, Hq, Dv).
- * stats (host, nullable) receives which path ran. */
+ * stats (host, nullable) receives which path ran.  The work lists reach the GPU in
+ * the launches' parameters when they fit (16 KB of items, order and members, and
+ * batch < 1024) and the bf16 tensor-core partial kernel serves every launch;
+ * otherwise by one copy from pinned staging into the workspace.  Either way the
+ * workspace's fault word is cleared on the stream before the first kernel. */
 psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
                           const psd_cascade_plan *plan, float *o, float *lse,
                           void *workspace, size_t workspace_bytes,

@@ -87,7 +87,8 @@ class CascadeStats(C.Structure):
 
 class Counters(C.Structure):
     _fields_ = [("launches_flat", i64), ("launches_cascade", i64), ("cascade_shared_tokens", i64),
-                ("cascade_member_sequences", i64), ("cascade_failures", i64)]
+                ("cascade_member_sequences", i64), ("cascade_failures", i64),
+                ("lists_inline", i64), ("lists_uploaded", i64)]
 
 
 _LIB = None

@@ -158,6 +158,51 @@ bool dispatch_fused(const PartialLaunch &L0, const PartialLaunch &L1, const Devi
   return partial_tcs_supports(L0) && partial_tcs_supports(L1) && L1.G_cta <= 16;
 }
 
+// Work lists of one call, placed either in the workspace by one H2D copy or, when
+// they fit and every launch of the call reads them from its parameters, in `block`
+// (the items, order, members and row bases; the merge takes o_indptr the same way).
+struct CallLists {
+  bool inl = false;
+  InlineLists block;
+  const uint8_t *base = nullptr;  // device address of the lists' first byte (the items)
+  // Points L's list pointers (device addresses inside the workspace's lists) at the
+  // same offsets of the parameter block.
+  void apply(PartialLaunch &L) const {
+    if (!inl) return;
+    auto off = [&](const void *ptr) -> uint32_t {
+      return ptr ? uint32_t(static_cast<const uint8_t *>(ptr) - base) : 0u;
+    };
+    L.inline_lists = &block;
+    L.inl_items = off(L.items);
+    L.inl_order = off(L.order);
+    L.inl_members = off(L.members);
+    L.inl_row_base = off(L.member_row_base);
+  }
+};
+
+psd_status upload(psd_ctx *ctx, void *dst, const void *src, size_t bytes, cudaStream_t s);
+
+// Inline lists when they fit and every launch takes them; otherwise one upload of the
+// host copy of the workspace's list region.  Either way the fault word at the
+// workspace's start is zero on the stream before the kernels.
+psd_status place_lists(psd_ctx *ctx, CallLists &cl, uint8_t *ws, const WorkspaceLayout &lay,
+                       const std::vector<uint8_t> &host, int32_t batch, bool all_inline_kernels,
+                       cudaStream_t s) {
+  const size_t used = lay.indptr_off - lay.items_off;
+  cl.base = ws + lay.items_off;
+  cl.inl = all_inline_kernels && used <= kInlineListBytes && batch + 1 <= kInlineIndptr;
+  if (!cl.inl) {
+    ctx->counters.lists_uploaded += 1;
+    return upload(ctx, ws, host.data(), host.size(), s);
+  }
+  ctx->counters.lists_inline += 1;
+  cl.block.used = used;
+  std::memcpy(cl.block.bytes, host.data() + lay.items_off, used);
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "fault word clear: %s", cudaGetErrorString(e));
+  return PSD_OK;
+}
+
 // Copies `bytes` of host data into a pinned staging buffer and enqueues one H2D
 // copy to `dst` on `s`.
 psd_status upload(psd_ctx *ctx, void *dst, const void *src, size_t bytes, cudaStream_t s) {
@@ -437,14 +482,17 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   }
   std::memcpy(host.data() + lay.indptr_off, plan->o_indptr, sizeof(int32_t) * (B + 1));
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  st = upload(ctx, ws, host.data(), host.size(), s);
+  const bool fused = M > 0 && dispatch_fused(L0, L1, ctx->dev);
+  const bool tcs_only = select_partial(L1, ctx->dev) == PartialKind::kTensorSmall &&
+                        (M == 0 || fused || select_partial(L0, ctx->dev) == PartialKind::kTensorSmall);
+  CallLists cl;
+  st = place_lists(ctx, cl, ws, lay, host, B, tcs_only, s);
   if (st != PSD_OK) return st;
 
   float *vpart = reinterpret_cast<float *>(ws + lay.vpart_off);
   float *lpart = reinterpret_cast<float *>(ws + lay.lpart_off);
   int32_t *fault = reinterpret_cast<int32_t *>(ws);
   const psd_work_item *ditems = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
-  const bool fused = M > 0 && dispatch_fused(L0, L1, ctx->dev);
   if (fused) {  // both levels in one launch of the 16-row-group tensor-core kernel
     L1.items = ditems;
     L1.order = reinterpret_cast<const int32_t *>(ws + lay.order_off) + n0;
@@ -469,6 +517,7 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->fork, 0);
     if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cascade fork: %s", cudaGetErrorString(e));
     time_mark(ctx, 0, ctx->side);
+    cl.apply(L0);
     st = launch_partial(L0, ctx->dev, ctx->side);
     time_mark(ctx, 1, ctx->side);
     if (st != PSD_OK) return st;
@@ -483,6 +532,7 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   L1.v_out = vpart;
   L1.lse_out = lpart;
   L1.fault = fault;
+  cl.apply(L1);
   time_mark(ctx, 2, s);
   st = launch_partial(L1, ctx->dev, s);
   time_mark(ctx, 3, s);
@@ -494,7 +544,8 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   time_mark(ctx, 4, s);
   const bool merge_follows_partial = !(M > 0 && !fused) && !ctx->timing;
   st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq,
-                    args->Dv, o, lse, ctx->dev, s, merge_follows_partial, writes_empty_rows(L1, ctx->dev));
+                    args->Dv, o, lse, ctx->dev, s, merge_follows_partial, writes_empty_rows(L1, ctx->dev),
+                    cl.inl ? plan->o_indptr : nullptr);
   time_mark(ctx, 5, s);
   ctx->tev_used[0] = ctx->timing && M > 0 && !fused;
   ctx->tev_used[1] = ctx->timing;
@@ -601,15 +652,6 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
   }
   std::memcpy(host.data() + lay.indptr_off, plan->o_indptr, sizeof(int32_t) * (B + 1));
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  st = upload(ctx, ws, host.data(), host.size(), s);
-  if (st != PSD_OK) return st;
-
-  float *vpart = reinterpret_cast<float *>(ws + lay.vpart_off);
-  float *lpart = reinterpret_cast<float *>(ws + lay.lpart_off);
-  int32_t *fault = reinterpret_cast<int32_t *>(ws);
-  const psd_work_item *ditems = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
-  const int32_t *dmembers = reinterpret_cast<const int32_t *>(ws + lay.members_off);
-  const int32_t *drow_base = reinterpret_cast<const int32_t *>(ws + lay.row_base_off);
   // Every segment's level 0 and level 1 in one launch when the 16-row-group
   // tensor-core kernel serves all of them.
   bool fused = S > 0 && S <= PartialLaunch::kMaxFusedSegments;
@@ -618,6 +660,22 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
     L0.G_cta = plan->segments[k].num_members * L1.Gm;
     fused = dispatch_fused(L0, L1, ctx->dev);
   }
+  bool tcs_only = select_partial(L1, ctx->dev) == PartialKind::kTensorSmall;
+  for (int32_t k = 0; tcs_only && !fused && k < S; ++k) {
+    PartialLaunch L0 = L1;
+    L0.G_cta = plan->segments[k].num_members * L1.Gm;
+    tcs_only = select_partial(L0, ctx->dev) == PartialKind::kTensorSmall;
+  }
+  CallLists cl;
+  st = place_lists(ctx, cl, ws, lay, host, B, tcs_only, s);
+  if (st != PSD_OK) return st;
+
+  float *vpart = reinterpret_cast<float *>(ws + lay.vpart_off);
+  float *lpart = reinterpret_cast<float *>(ws + lay.lpart_off);
+  int32_t *fault = reinterpret_cast<int32_t *>(ws);
+  const psd_work_item *ditems = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
+  const int32_t *dmembers = reinterpret_cast<const int32_t *>(ws + lay.members_off);
+  const int32_t *drow_base = reinterpret_cast<const int32_t *>(ws + lay.row_base_off);
   if (fused) {
     L1.fused_segments = S;
     L1.fused_l0_items = n0;
@@ -645,6 +703,7 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
       L0.v_out = vpart;
       L0.lse_out = lpart;
       L0.fault = fault;
+      cl.apply(L0);
       st = launch_partial(L0, ctx->dev, ctx->side);
       if (st != PSD_OK) return st;
     }
@@ -658,6 +717,7 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
   L1.v_out = vpart;
   L1.lse_out = lpart;
   L1.fault = fault;
+  cl.apply(L1);
   time_mark(ctx, 2, s);
   st = launch_partial(L1, ctx->dev, s);
   time_mark(ctx, 3, s);
@@ -669,7 +729,8 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
   }
   time_mark(ctx, 4, s);
   st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq, args->Dv, o,
-                    lse, ctx->dev, s, !joined && !ctx->timing, writes_empty_rows(L1, ctx->dev));
+                    lse, ctx->dev, s, !joined && !ctx->timing, writes_empty_rows(L1, ctx->dev),
+                    cl.inl ? plan->o_indptr : nullptr);
   time_mark(ctx, 5, s);
   ctx->tev_used[0] = ctx->timing && joined;
   ctx->tev_used[1] = ctx->timing;

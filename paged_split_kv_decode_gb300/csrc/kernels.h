@@ -3,6 +3,8 @@
 
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "psd_internal.h"
 
 namespace psd {
@@ -14,6 +16,31 @@ struct DeviceInfo {
   void *encode_tiled = nullptr;  // driver cuTensorMapEncodeTiled
   int partial_kernel = 0;        // psd_partial_kernel preference for G <= 16
 };
+
+// Per-call work lists carried in a launch's parameter space.  A small H2D copy in
+// front of the kernels costs about 5 us of device time on GB300; parameters of up to
+// a few KB arrive with the launch at no measurable cost.  Only kernels whose CTAs read
+// a few warp-uniform entries take them (parameter loads go through the constant cache).
+// A launch carries the smallest of these block sizes that holds its lists (the
+// parameter copy grows with the declared size, about 0.1 us per KB).
+constexpr size_t kInlineListBytes = 16384;
+template <int CAP> struct ListBlock {
+  alignas(16) unsigned char bytes[CAP];
+};
+struct InlineLists {  // host side: `used` bytes of lists
+  size_t used = 0;
+  alignas(16) unsigned char bytes[kInlineListBytes];
+};
+constexpr int kInlineIndptr = 1024;  // o_indptr entries carried by a merge launch
+struct InlineIndptr {
+  int32_t v[kInlineIndptr];
+};
+struct NoInline {  // stands in for the blocks above in launches that do not use them
+  alignas(16) unsigned char bytes[16];
+  int32_t v[4];
+};
+template <int CAP> using ListParam = std::conditional_t<CAP != 0, ListBlock<CAP != 0 ? CAP : 16>, NoInline>;
+template <bool INL> using IndptrParam = std::conditional_t<INL, InlineIndptr, NoInline>;
 
 // One partial-attention launch over a device work list.
 //   Items with q_index >= 0 use query rows q[q_index, kv*Gm + g] (g < Gm) and
@@ -46,6 +73,12 @@ struct PartialLaunch {
   // consecutive items of one request into one partial, written to the run's last
   // row, and mark the other rows empty (LSE -inf, v unused by the merge).
   bool merge_runs = false;
+  // When set, items / order / members / member_row_base are not read from the device
+  // pointers above but from this host block, copied into the launch's parameters, at
+  // the given byte offsets (order may still be NULL: identity).  Honoured by the
+  // 16-row-group tensor-core kernel only.
+  const InlineLists *inline_lists = nullptr;
+  uint32_t inl_items = 0, inl_order = 0, inl_members = 0, inl_row_base = 0;
   float q_scale = 1.f;  // sm_scale * log2(e) * k_scale
   float v_scale = 1.f;
   // Fused cascade launch (16-row-group tensor-core kernel only): `items` starts
@@ -78,6 +111,8 @@ psd_status launch_rope_append(const psd_rope_append_args *a, cudaStream_t s);
 psd_status launch_merge(const float *v_in, const float *lse_in, const int32_t *o_indptr,
                         int64_t num_out, int32_t H, int32_t D, float *v_out, float *lse_out,
                         const DeviceInfo &dev, cudaStream_t s, bool after_partial = false,
-                        bool skip_empty = false);
+                        bool skip_empty = false, const int32_t *o_indptr_host = nullptr);
+// o_indptr_host: when not NULL and num_out + 1 <= kInlineIndptr, the group bounds are
+// taken from this host array, copied into the launch's parameters; o_indptr is unused.
 
 }  // namespace psd

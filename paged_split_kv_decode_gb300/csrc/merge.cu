@@ -14,6 +14,8 @@
 // o_indptr, then waits for that grid.
 #include <cuda_runtime.h>
 
+#include <cstring>
+
 #include "device.cuh"
 #include "kernels.h"
 
@@ -26,11 +28,13 @@ constexpr int kMergeWarps = 8;
 // NV: float4 slices per lane (D <= 128 * NV).  WIDE batches 16 / NV rows for grids of
 // about one wave (latency-bound); the narrow form batches half as many rows with
 // fewer registers, so more warps per SM keep loads in flight on large grids.
-template <int NV, bool WIDE, bool SKIP>
+// INL: the group bounds come in the launch's parameters (`inl`), not from o_indptr.
+template <int NV, bool WIDE, bool SKIP, bool INL>
 __global__ void __launch_bounds__(kMergeWarps * 32, WIDE ? 1 : (NV >= (SKIP ? 4 : 8) ? 2 : 3))
     merge_states_kernel(const float *__restrict__ v_in, const float *__restrict__ lse_in,
                         const int32_t *__restrict__ o_indptr, int64_t num_out, int H, int D,
-                        float *__restrict__ v_out, float *__restrict__ lse_out) {
+                        float *__restrict__ v_out, float *__restrict__ lse_out,
+                        const __grid_constant__ IndptrParam<INL> inl) {
   constexpr int U = WIDE ? (NV >= 8 ? 2 : 16 / NV) : (NV >= 8 ? 1 : 8 / NV);  // rows per batch
   const int lane = threadIdx.x & 31;
   const int64_t gw = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
@@ -38,7 +42,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32, WIDE ? 1 : (NV >= (SKIP ? 4 
   const int64_t r = gw / H;
   const int h = int(gw - r * H);
   // o_indptr is in place before the partial kernel starts; the partials are not.
-  const int lo = __ldg(o_indptr + r), hi = __ldg(o_indptr + r + 1);
+  int lo, hi;
+  if constexpr (INL) {
+    lo = inl.v[r];
+    hi = inl.v[r + 1];
+  } else {
+    lo = __ldg(o_indptr + r);
+    hi = __ldg(o_indptr + r + 1);
+  }
   wait_for_prior_grid();
   const int n = hi - lo;
   const int D4 = D >> 2;
@@ -129,10 +140,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32, WIDE ? 1 : (NV >= (SKIP ? 4 
   if (lse_out && lane == 0) lse_out[r * H + h] = M + log2f(sw);
 }
 
-template <int NV, bool SKIP>
+template <int NV, bool SKIP, bool INL>
 cudaError_t launch_form(dim3 grid, bool wide, bool early, cudaStream_t s, const float *v_in, const float *lse_in,
-                      const int32_t *o_indptr, int64_t num_out, int H, int D, float *v_out,
-                      float *lse_out) {
+                        const int32_t *o_indptr, int64_t num_out, int H, int D, float *v_out,
+                        float *lse_out, const IndptrParam<INL> &inl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kMergeWarps * 32);
@@ -144,26 +155,41 @@ cudaError_t launch_form(dim3 grid, bool wide, bool early, cudaStream_t s, const 
   cfg.attrs = attr;
   cfg.numAttrs = early ? 1 : 0;
   if (wide)
-    return cudaLaunchKernelEx(&cfg, merge_states_kernel<NV, true, SKIP>, v_in, lse_in, o_indptr, num_out,
-                              H, D, v_out, lse_out);
-  return cudaLaunchKernelEx(&cfg, merge_states_kernel<NV, false, SKIP>, v_in, lse_in, o_indptr, num_out, H,
-                            D, v_out, lse_out);
+    return cudaLaunchKernelEx(&cfg, merge_states_kernel<NV, true, SKIP, INL>, v_in, lse_in, o_indptr,
+                              num_out, H, D, v_out, lse_out, inl);
+  return cudaLaunchKernelEx(&cfg, merge_states_kernel<NV, false, SKIP, INL>, v_in, lse_in, o_indptr, num_out,
+                            H, D, v_out, lse_out, inl);
 }
 
 template <int NV>
-cudaError_t launch_nv(dim3 grid, bool wide, bool early, bool skip, cudaStream_t s, const float *v_in,
-                      const float *lse_in, const int32_t *o_indptr, int64_t num_out, int H, int D,
-                      float *v_out, float *lse_out) {
-  return skip ? launch_form<NV, true>(grid, wide, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out)
-              : launch_form<NV, false>(grid, wide, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
+cudaError_t launch_nv(dim3 grid, bool wide, bool early, bool skip, const InlineIndptr *inl, cudaStream_t s,
+                      const float *v_in, const float *lse_in, const int32_t *o_indptr, int64_t num_out, int H,
+                      int D, float *v_out, float *lse_out) {
+  if (inl)
+    return skip ? launch_form<NV, true, true>(grid, wide, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out,
+                                              lse_out, *inl)
+                : launch_form<NV, false, true>(grid, wide, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out,
+                                               lse_out, *inl);
+  const NoInline none{};
+  return skip ? launch_form<NV, true, false>(grid, wide, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out,
+                                             lse_out, none)
+              : launch_form<NV, false, false>(grid, wide, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out,
+                                              lse_out, none);
 }
 
 }  // namespace
 
 psd_status launch_merge(const float *v_in, const float *lse_in, const int32_t *o_indptr,
                         int64_t num_out, int32_t H, int32_t D, float *v_out, float *lse_out,
-                        const DeviceInfo &dev, cudaStream_t s, bool after_partial, bool skip_empty) {
+                        const DeviceInfo &dev, cudaStream_t s, bool after_partial, bool skip_empty,
+                        const int32_t *o_indptr_host) {
   if (num_out == 0 || H == 0) return PSD_OK;
+  InlineIndptr block;
+  const InlineIndptr *inl = nullptr;
+  if (o_indptr_host && num_out + 1 <= kInlineIndptr) {
+    std::memcpy(block.v, o_indptr_host, sizeof(int32_t) * size_t(num_out + 1));
+    inl = &block;
+  }
   const int64_t warps = num_out * H;
   const int64_t blocks = (warps + kMergeWarps - 1) / kMergeWarps;
   if (blocks > 0x7fffffffLL) return fail(PSD_ERR_UNSUPPORTED, "merge_states: grid too large");
@@ -172,13 +198,13 @@ psd_status launch_merge(const float *v_in, const float *lse_in, const int32_t *o
   const bool wide = blocks <= 2LL * dev.num_sms;
   cudaError_t e;
   if (D <= 128)
-    e = launch_nv<1>(grid, wide, after_partial, skip_empty, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
+    e = launch_nv<1>(grid, wide, after_partial, skip_empty, inl, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
   else if (D <= 256)
-    e = launch_nv<2>(grid, wide, after_partial, skip_empty, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
+    e = launch_nv<2>(grid, wide, after_partial, skip_empty, inl, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
   else if (D <= 512)
-    e = launch_nv<4>(grid, wide, after_partial, skip_empty, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
+    e = launch_nv<4>(grid, wide, after_partial, skip_empty, inl, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
   else
-    e = launch_nv<8>(grid, wide, after_partial, skip_empty, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
+    e = launch_nv<8>(grid, wide, after_partial, skip_empty, inl, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "merge_states launch: %s", cudaGetErrorString(e));
   return PSD_OK;

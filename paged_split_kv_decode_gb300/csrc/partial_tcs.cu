@@ -24,6 +24,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "device.cuh"
 #include "kernels.h"
@@ -43,6 +44,8 @@ struct TCSParams {
   const int32_t *order;
   const int32_t *members;
   const int32_t *member_row_base;
+  uint32_t inl_items, inl_order, inl_members, inl_row_base;  // offsets in the inline lists
+  int has_order;
   float *v_out;
   float *lse_out;
   int32_t *fault;
@@ -91,10 +94,14 @@ __device__ __forceinline__ uint32_t sw128(int row, int col8) {
   return uint32_t((col8 >> 3) * (kTileTok * 128) + row * 128 + (((col8 & 7) ^ (row & 7)) << 4));
 }
 
-template <int D>
+// CAP > 0: the work lists come in the launch's parameters (`lists`, CAP bytes), not
+// from global memory.
+template <int D, int CAP>
 __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
     partial_tcs_kernel(const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const TCSParams p) {
+                       const __grid_constant__ CUtensorMap tmV, const TCSParams p,
+                       const __grid_constant__ ListParam<CAP> lists) {
+  constexpr bool INL = CAP != 0;
   constexpr int KSTEPS = D / 16;
   constexpr int NT = D / 8;                       // n8 tiles of the output
   constexpr uint32_t TILE_BYTES = kTileTok * D * 2;
@@ -104,6 +111,19 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
   // 128-byte-swizzled TMA boxes need 1024-byte aligned destinations.
   uint8_t *base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const psd_work_item *items = p.items;
+  const int32_t *order = p.order, *members = p.members, *row_base = p.member_row_base;
+  if constexpr (INL) {
+    items = reinterpret_cast<const psd_work_item *>(lists.bytes + p.inl_items);
+    order = p.has_order ? reinterpret_cast<const int32_t *>(lists.bytes + p.inl_order) : nullptr;
+    members = reinterpret_cast<const int32_t *>(lists.bytes + p.inl_members);
+    row_base = reinterpret_cast<const int32_t *>(lists.bytes + p.inl_row_base);
+  }
+  // list entries: parameter-space loads when inline, read-only global loads otherwise
+  auto ld_list = [](const int32_t *a) -> int32_t {
+    if constexpr (INL) return *a;
+    else return __ldg(a);
+  };
   int item_index, group, G_rows, member0 = 0;
   if (int(blockIdx.x) < p.n_l0_tasks) {
     const int task = int(blockIdx.x);
@@ -117,11 +137,11 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
     member0 = p.seg_member0[sg];
   } else {
     const int j = blockIdx.x - p.n_l0_tasks;
-    item_index = p.l1_base + (p.order ? __ldg(p.order + j) : j);
+    item_index = p.l1_base + (order ? ld_list(order + j) : j);
     group = blockIdx.z;
     G_rows = p.G_cta;
   }
-  const psd_work_item it = p.items[item_index];
+  const psd_work_item it = items[item_index];
   const int kv = blockIdx.y;
   const int row0 = group * 16;  // this CTA's 16-row group of the KV head's rows
   const int rows = min(16, G_rows - row0);
@@ -143,7 +163,7 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
       const int g = row0 + r0 + 8 * h;
       if (g < G_rows) {
         const int m = g / p.Gm;
-        const int qb = it.q_index >= 0 ? it.q_index : __ldg(p.members + member0 + m);
+        const int qb = it.q_index >= 0 ? it.q_index : ld_list(members + member0 + m);
         const int head = kv * p.Gm + (g - m * p.Gm);
         qrow[h] = p.q + (int64_t(qb) * p.Hq_req + head) * p.Dqk;
       }
@@ -373,7 +393,7 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
     const bool live = M != neg_inf();
     const float f = live ? p.v_scale / L : 0.f;
     const int m = g / p.Gm;
-    const int row = it.q_index >= 0 ? it.out_row : __ldg(p.member_row_base + member0 + m) + it.out_row;
+    const int row = it.q_index >= 0 ? it.out_row : ld_list(row_base + member0 + m) + it.out_row;
     const int head = kv * p.Gm + (g - m * p.Gm);
     const int64_t orow = int64_t(row) * p.Hq_req + head;
     *reinterpret_cast<float4 *>(p.v_out + orow * p.Dv + d) = make_float4(O.x * f, O.y * f, O.z * f, O.w * f);
@@ -403,6 +423,10 @@ size_t tcs_smem_bytes() {
   return std::max(ring, red) + 1024 /* base alignment */ + kWarpsS * kStagesS * sizeof(uint64_t);
 }
 
+template <int D, int CAP>
+psd_status run_tcs(dim3 grid, size_t smem, cudaStream_t s, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                   const TCSParams &p, const InlineLists *lists);
+
 template <int D>
 psd_status launch_tcs(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
   CUtensorMap tmK, tmV;
@@ -416,6 +440,11 @@ psd_status launch_tcs(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_
   p.order = L.order;
   p.members = L.members;
   p.member_row_base = L.member_row_base;
+  p.inl_items = L.inl_items;
+  p.inl_order = L.inl_order;
+  p.inl_members = L.inl_members;
+  p.inl_row_base = L.inl_row_base;
+  p.has_order = L.order != nullptr;
   p.v_out = L.v_out;
   p.lse_out = L.lse_out;
   p.fault = L.fault;
@@ -456,13 +485,30 @@ psd_status launch_tcs(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_
     grid_z = 1;  // level-1 items have G_cta <= 16 rows (checked by the caller)
   }
   const size_t smem = tcs_smem_bytes<D>();
-  auto kern = partial_tcs_kernel<D>;
+  const dim3 grid(grid_x, static_cast<unsigned>(L.Hkv), grid_z);
+  if (!L.inline_lists) return run_tcs<D, 0>(grid, smem, s, tmK, tmV, p, nullptr);
+  const size_t used = L.inline_lists->used;
+  if (used <= 4096) return run_tcs<D, 4096>(grid, smem, s, tmK, tmV, p, L.inline_lists);
+  if (used <= 8192) return run_tcs<D, 8192>(grid, smem, s, tmK, tmV, p, L.inline_lists);
+  if (used <= 16384) return run_tcs<D, 16384>(grid, smem, s, tmK, tmV, p, L.inline_lists);
+  return fail(PSD_ERR_INVALID_ARG, "inline lists of %zu bytes", used);
+}
+
+template <int D, int CAP>
+psd_status run_tcs(dim3 grid, size_t smem, cudaStream_t s, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                   const TCSParams &p, const InlineLists *lists) {
+  auto kern = partial_tcs_kernel<D, CAP>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   }
-  const dim3 grid(grid_x, static_cast<unsigned>(L.Hkv), grid_z);
-  kern<<<grid, kWarpsS * 32, smem, s>>>(tmK, tmV, p);
+  if constexpr (CAP == 0) {
+    kern<<<grid, kWarpsS * 32, smem, s>>>(tmK, tmV, p, NoInline{});
+  } else {
+    ListParam<CAP> blk;
+    std::memcpy(blk.bytes, lists->bytes, lists->used);
+    kern<<<grid, kWarpsS * 32, smem, s>>>(tmK, tmV, p, blk);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "partial (small-group tensor cores) launch: %s", cudaGetErrorString(e));
   return PSD_OK;

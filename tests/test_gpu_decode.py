@@ -182,3 +182,46 @@ def test_outputs_ignore_nan_canaries():
     assert torch.isnan(w.k_pool.float()).any()
     o, lse = Dev(w).decode(enable=0)
     assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("tile,inline", [(2048, True), (256, True), (128, False)])
+def test_work_lists_inline_or_uploaded(tile, inline):
+    """80 requests of 512-4096 tokens: at tiles of 2048 and 256 the work lists (about
+    4 KB and 15 KB) travel in the launches' parameters, at 128 (about 29 KB) by one
+    upload into the workspace; outputs match the oracle either way."""
+    rng = np.random.default_rng(12)
+    lengths = synth.lengths_with_partial_last_page(rng, 80, 512, 4096, 16)
+    w = synth._make("flat80", rng, lengths, Hq=32, Hkv=8, Dqk=128, Dv=128, page_size=16,
+                    num_pages=16384, tile_tokens=tile)
+    before = ctx().counters()
+    o, lse = Dev(w).decode(enable=0)
+    after = ctx().counters()
+    assert after["lists_inline"] - before["lists_inline"] == int(inline)
+    assert after["lists_uploaded"] - before["lists_uploaded"] == int(not inline)
+    req = [0, 17, 45, 79]
+    ro, rl = A.decode_attention(A.workload_arrays(w), requests=req)
+    assert_close(o[req], lse[req], ro[req], rl[req], "bf16", f"flat, tile {tile}")
+
+
+def test_fault_word_is_cleared_by_the_next_call():
+    """A call whose page table holds an out-of-range id flags the workspace; the next
+    clean call on the same workspace starts from a cleared fault word (inline lists:
+    the clear is a memset on the stream, not the list upload)."""
+    w = synth.tiny_cascade(seed=0)
+    d = Dev(w)
+    plan = psd.plan_decode(d.table, w.tile_tokens, 1, 4, 2)
+    ws = psd.workspace_for(plan, w.Hq, w.Dv, "cuda")
+    o = torch.empty((w.batch, w.Hq, w.Dv), device="cuda")
+    bad = d.indices.clone()
+    bad[5] = w.num_pages + 3
+    before = ctx().counters()["lists_inline"]
+    psd.cascade_decode(ctx(), d.args(), plan, o, None, ws)          # clean
+    args_bad = psd.decode_args(d.q, d.k, d.v, bad, num_pages=w.num_pages, page_size=w.page_size,
+                               Hkv=w.Hkv, Dv=w.Dv, sm_scale=w.sm_scale)
+    psd.cascade_decode(ctx(), args_bad, plan, o, None, ws)          # flags
+    psd.cascade_decode(ctx(), d.args(), plan, o, None, ws)          # clean again
+    assert ctx().counters()["lists_inline"] - before == 3
+    assert psd.check_device_error(ctx(), ws) == 0
+    psd.cascade_decode(ctx(), args_bad, plan, o, None, ws)
+    with pytest.raises(psd.PsdError):
+        psd.check_device_error(ctx(), ws)
