@@ -39,8 +39,8 @@ NOMINAL_HBM_GBS = 8000.0
 # ncu capture summarised in profiles/partial_tcs_flat_decode.md.  Reported only while
 # the kernel source is the one the counters were taken on.
 TRAFFIC_SOURCE = os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", "partial_tcs.cu")
-TRAFFIC_SHA256 = "fbb7f543e472180bdc4a17b798fccd72e92fee3a3b9b2a0e6b7c77df25b291ed"
-TRAFFIC_BYTES = 316074240 + 1252608
+TRAFFIC_SHA256 = "b4c560570833aa61d0db42194307167437d3e5bbcba9cb48e75b3e0cb8ec9058"
+TRAFFIC_BYTES = 316075008 + 1245696
 
 
 def partial_traffic():
@@ -465,6 +465,42 @@ def host_plan_us(w, reps=200):
             "note": "per call, through the Python binding"}
 
 
+def cascade_comparison(wc, label, args, flush, plan_us=False):
+    """Flat arm vs cascade arm on one batch: step times, per-kernel times and the
+    criterion (T_flat - T_casc) / T_flat >= 0.7 x the fraction of K/V reads removed."""
+    flat_arm, casc_arm = Arm(wc, enable=0), Arm(wc, enable=1)
+    casc_arm.step()
+    casc_arm.check()
+    st = casc_arm.stats
+    tf = statistics.mean(time_steps(flat_arm.step, args.steps, args.warmup, flush))
+    tc = statistics.mean(time_steps(casc_arm.step, args.steps, args.warmup, flush))
+    kf = kernel_timing(flat_arm, args.steps, args.warmup, flush)
+    kc = kernel_timing(casc_arm, args.steps, args.warmup, flush)
+    flat_arm.check()
+    flat_b, uniq_b = flat_kv_bytes(wc), unique_kv_bytes(wc)
+    removed = (flat_b - uniq_b) / flat_b
+    reduction = (tf - tc) / tf
+    out = {
+        "workload": label,
+        "flat_ms": round(tf, 4), "cascade_ms": round(tc, 4),
+        "flat_tokens_per_s": round(wc.batch / (tf * 1e-3), 1),
+        "cascade_tokens_per_s": round(wc.batch / (tc * 1e-3), 1),
+        "flat_kv_bytes": int(flat_b), "unique_kv_bytes": int(uniq_b),
+        "flat_unique_kv_gbs": round(uniq_b / (tf * 1e-3) / 1e9, 1),
+        "cascade_unique_kv_gbs": round(uniq_b / (tc * 1e-3) / 1e9, 1),
+        "flat_arm_algorithmic_gbs": round(flat_b / (kf["partial_ms"] * 1e-3) / 1e9, 1),
+        "removed_read_fraction": round(removed, 4), "wall_time_reduction": round(reduction, 4),
+        "criterion_reduction_ge_0.7x_removed": bool(reduction >= 0.7 * removed),
+        "flat_kernels_ms": {k: round(v, 5) for k, v in kf.items()},
+        "cascade_kernels_ms": {k: round(v, 5) for k, v in kc.items()},
+        "stats": st,
+    }
+    if plan_us:
+        out["host_plan_us"] = host_plan_us(wc)
+    del flat_arm, casc_arm
+    return out
+
+
 def run_ours(args):
     rank, world, local = dist_setup(args.gpus)
     torch.cuda.set_device(local)
@@ -503,33 +539,16 @@ def run_ours(args):
     if not args.quick and args.workload in ("all", "cascade"):
         # cascade workload: flat arm vs cascade arm on the same inputs
         wc = synth.cascade_decode(seed=0, canary=False)
-        flat_arm, casc_arm = Arm(wc, enable=0), Arm(wc, enable=1)
-        casc_arm.step()
-        casc_arm.check()
-        st = casc_arm.stats
-        tf = statistics.mean(time_steps(flat_arm.step, args.steps, args.warmup, flush))
-        tc = statistics.mean(time_steps(casc_arm.step, args.steps, args.warmup, flush))
-        kf = kernel_timing(flat_arm, args.steps, args.warmup, flush)
-        kc = kernel_timing(casc_arm, args.steps, args.warmup, flush)
-        flat_b, uniq_b = flat_kv_bytes(wc), unique_kv_bytes(wc)
-        removed = (flat_b - uniq_b) / flat_b
-        reduction = (tf - tc) / tf
-        extra["flat_vs_cascade"] = {
-            "workload": "cascade decode: 64 requests, 16 share an 8192-token prefix (suffix U[64,1024]), "
-                        "48 independent U[512,4096]; Hq=32, Hkv=8, D=128, page 16, tile 512",
-            "flat_ms": round(tf, 4), "cascade_ms": round(tc, 4),
-            "flat_tokens_per_s": round(wc.batch / (tf * 1e-3), 1),
-            "cascade_tokens_per_s": round(wc.batch / (tc * 1e-3), 1),
-            "flat_unique_kv_gbs": round(uniq_b / (tf * 1e-3) / 1e9, 1),
-            "cascade_unique_kv_gbs": round(uniq_b / (tc * 1e-3) / 1e9, 1),
-            "removed_read_fraction": round(removed, 4), "wall_time_reduction": round(reduction, 4),
-            "criterion_reduction_ge_0.7x_removed": bool(reduction >= 0.7 * removed),
-            "flat_kernels_ms": {k: round(v, 5) for k, v in kf.items()},
-            "cascade_kernels_ms": {k: round(v, 5) for k, v in kc.items()},
-            "stats": st,
-            "host_plan_us": host_plan_us(wc),
-        }
-        del flat_arm, casc_arm
+        extra["flat_vs_cascade"] = cascade_comparison(
+            wc, "cascade decode: 64 requests, 16 share an 8192-token prefix (suffix U[64,1024]), "
+                "48 independent U[512,4096]; Hq=32, Hkv=8, D=128, page 16, tile 512", args, flush, plan_us=True)
+        # The same batch with a 65536-token shared prefix (268 MB of K/V, more than the
+        # 129 MB L2), so the flat arm's re-reads of the prefix go to DRAM.
+        wl = synth.cascade_decode(seed=0, canary=False, shared_tokens=65536)
+        extra["flat_vs_cascade_prefix_beyond_l2"] = cascade_comparison(
+            wl, "cascade decode, prefix larger than L2: 64 requests, 16 share a 65536-token prefix "
+                "(suffix U[64,1024]), 48 independent U[512,4096]; Hq=32, Hkv=8, D=128, page 16, tile 512",
+            args, flush)
     if not args.quick and args.workload in ("all", "mla"):
         wm = synth.mla_decode(seed=0, canary=False, batch=args.mla_batch)
         marm = Arm(wm, enable=1)

@@ -313,8 +313,7 @@ psd_status merge_states(psd_ctx *ctx, const float *v_in, const float *lse_in,
  * stats (host, nullable) receives which path ran.  The work lists reach the GPU in
  * the launches' parameters when they fit (16 KB of items, order and members, and
  * batch < 1024) and the bf16 tensor-core partial kernel serves every launch;
- * otherwise by one copy from pinned staging into the workspace.  Either way the
- * workspace's fault word is cleared on the stream before the first kernel. */
+ * otherwise by one copy from pinned staging into the workspace. */
 psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
                           const psd_cascade_plan *plan, float *o, float *lse,
                           void *workspace, size_t workspace_bytes,
@@ -476,9 +475,12 @@ typedef struct {
 
 psd_status rope_append_kv(psd_ctx *ctx, const psd_rope_append_args *args, psd_stream_t stream);
 
-/* Synchronises `stream` and reads the workspace's fault flag: PSD_OK, or
+/* Synchronises `stream` and reads the workspace's fault word: PSD_OK, or
  * PSD_ERR_DEVICE_FAULT with the PSD_FAULT_* bits in *fault_bits (nullable).
- * Clears the flag. */
+ * The word (the workspace's first 8 bytes) is tagged with the call that wrote it:
+ * only faults of this context's latest decode call on `workspace` are reported, so
+ * nothing has to clear it between calls and a fresh workspace needs no
+ * initialisation.  A reported fault is cleared. */
 psd_status psd_check_device_error(psd_ctx *ctx, void *workspace, psd_stream_t stream,
                                   int32_t *fault_bits);
 

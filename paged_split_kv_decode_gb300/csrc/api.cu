@@ -183,8 +183,7 @@ struct CallLists {
 psd_status upload(psd_ctx *ctx, void *dst, const void *src, size_t bytes, cudaStream_t s);
 
 // Inline lists when they fit and every launch takes them; otherwise one upload of the
-// host copy of the workspace's list region.  Either way the fault word at the
-// workspace's start is zero on the stream before the kernels.
+// host copy of the workspace's list region.
 psd_status place_lists(psd_ctx *ctx, CallLists &cl, uint8_t *ws, const WorkspaceLayout &lay,
                        const std::vector<uint8_t> &host, int32_t batch, bool all_inline_kernels,
                        cudaStream_t s) {
@@ -198,8 +197,6 @@ psd_status place_lists(psd_ctx *ctx, CallLists &cl, uint8_t *ws, const Workspace
   ctx->counters.lists_inline += 1;
   cl.block.used = used;
   std::memcpy(cl.block.bytes, host.data() + lay.items_off, used);
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), s);
-  if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "fault word clear: %s", cudaGetErrorString(e));
   return PSD_OK;
 }
 
@@ -394,7 +391,7 @@ extern "C" psd_status paged_decode_partial(psd_ctx *ctx, const psd_decode_args *
   L.num_items = num_items;
   L.v_out = v_out;
   L.lse_out = lse_out;
-  L.fault = reinterpret_cast<int32_t *>(ws);
+  L.fault = next_fault(ctx, ws);
   ctx->tev_used[0] = false;
   ctx->tev_used[1] = ctx->timing;
   ctx->tev_used[2] = false;
@@ -491,7 +488,7 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
 
   float *vpart = reinterpret_cast<float *>(ws + lay.vpart_off);
   float *lpart = reinterpret_cast<float *>(ws + lay.lpart_off);
-  int32_t *fault = reinterpret_cast<int32_t *>(ws);
+  const FaultRef fault = next_fault(ctx, ws);
   const psd_work_item *ditems = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
   if (fused) {  // both levels in one launch of the 16-row-group tensor-core kernel
     L1.items = ditems;
@@ -672,7 +669,7 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
 
   float *vpart = reinterpret_cast<float *>(ws + lay.vpart_off);
   float *lpart = reinterpret_cast<float *>(ws + lay.lpart_off);
-  int32_t *fault = reinterpret_cast<int32_t *>(ws);
+  const FaultRef fault = next_fault(ctx, ws);
   const psd_work_item *ditems = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
   const int32_t *dmembers = reinterpret_cast<const int32_t *>(ws + lay.members_off);
   const int32_t *drow_base = reinterpret_cast<const int32_t *>(ws + lay.row_base_off);
@@ -794,13 +791,17 @@ extern "C" psd_status psd_check_device_error(psd_ctx *ctx, void *workspace, psd_
   if (!ctx || !workspace) return fail(PSD_ERR_INVALID_ARG, "NULL");
   DeviceGuard g(ctx->dev.device);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  int32_t flag = 0;
-  cudaError_t e = cudaMemcpyAsync(&flag, workspace, sizeof(flag), cudaMemcpyDeviceToHost, s);
+  unsigned long long word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "psd_check_device_error: %s", cudaGetErrorString(e));
+  // only the bits of this context's latest call on the workspace count
+  const auto it = ctx->ws_epoch.find(workspace);
+  const bool latest = it != ctx->ws_epoch.end() && it->second == uint32_t(word >> 32);
+  const int32_t flag = latest ? int32_t(uint32_t(word)) : 0;
   if (fault_bits) *fault_bits = flag;
   if (flag) {
-    e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
+    e = cudaMemsetAsync(workspace, 0, sizeof(word), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     return fail(PSD_ERR_DEVICE_FAULT, "kernel fault flag 0x%x (1 = page id out of range, 2 = wait timeout)", flag);
   }

@@ -5,6 +5,7 @@
 
 #include <array>
 #include <map>
+#include <unordered_map>
 
 #include "kernels.h"
 #include "psd_internal.h"
@@ -32,9 +33,20 @@ struct psd_ctx {
   std::map<std::array<int64_t, 9>, int32_t> tuned;
   void *flush = nullptr;
   size_t flush_bytes = 0;
+  // Fault-word epochs: a counter advanced by every decode call, and the epoch of the
+  // latest call on each workspace (what psd_check_device_error compares against).
+  uint32_t epoch = 0;
+  std::unordered_map<const void *, uint32_t> ws_epoch;
 };
 
 namespace psd {
+// The fault word of a new decode call on workspace `ws`: a fresh epoch, recorded as
+// the workspace's latest.
+inline FaultRef next_fault(psd_ctx *c, void *ws) {
+  if (++c->epoch == 0) c->epoch = 1;
+  c->ws_epoch[ws] = c->epoch;
+  return FaultRef{static_cast<unsigned long long *>(ws), c->epoch};
+}
 // Records timing event `i` (0..5) of the context on stream `s` when timing is on.
 inline void time_mark(psd_ctx *c, int i, cudaStream_t s) {
   if (c->timing && c->tev[i]) cudaEventRecord(c->tev[i], s);

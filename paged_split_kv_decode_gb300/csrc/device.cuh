@@ -10,6 +10,7 @@
 #include <stdint.h>
 
 #include "../../include/psd.h"
+#include "kernels.h"
 
 namespace psd {
 
@@ -53,8 +54,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Flags `bits` in a call's fault word (FaultRef): OR into the word when it carries
+// the call's epoch, replace it otherwise.
+__device__ __forceinline__ void raise_fault(const FaultRef &f, uint32_t bits) {
+  unsigned long long seen = *reinterpret_cast<volatile unsigned long long *>(f.word);
+  for (int tries = 0; tries < 64; ++tries) {
+    const uint32_t mine = uint32_t(seen >> 32) == f.epoch ? uint32_t(seen) : 0u;
+    const unsigned long long want = (static_cast<unsigned long long>(f.epoch) << 32) | (mine | bits);
+    if (want == seen) return;
+    const unsigned long long prev = atomicCAS(f.word, seen, want);
+    if (prev == seen) return;
+    seen = prev;
+  }
+}
+
 // Waits for phase `parity` of the barrier; returns false (and flags the fault
 // word) if it has not completed within kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const FaultRef &fault) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) {
+      raise_fault(fault, PSD_FAULT_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t *fault) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();

@@ -17,6 +17,16 @@ struct DeviceInfo {
   int partial_kernel = 0;        // psd_partial_kernel preference for G <= 16
 };
 
+// The workspace's fault word: 64 bits at its start, (epoch << 32) | fault bits.  The
+// kernels of one call carry that call's epoch; a kernel that flags a fault ORs its
+// bits in when the word holds its epoch and replaces the word otherwise, so the word
+// needs no clearing before a call, and bits left by an earlier call (or whatever a
+// fresh workspace holds) never read as a fault of the current one.
+struct FaultRef {
+  unsigned long long *word = nullptr;
+  uint32_t epoch = 0;
+};
+
 // Per-call work lists carried in a launch's parameter space.  A small H2D copy in
 // front of the kernels costs about 5 us of device time on GB300; parameters of up to
 // a few KB arrive with the launch at no measurable cost.  Only kernels whose CTAs read
@@ -59,7 +69,7 @@ struct PartialLaunch {
   const int32_t *member_row_base = nullptr;  // device, stacked items only
   float *v_out = nullptr;
   float *lse_out = nullptr;
-  int32_t *fault = nullptr;
+  FaultRef fault;
   int64_t num_pages = 0;
   int32_t q_batch = 0;  // requests in q
   int32_t Hq_req = 0;  // query heads per request in q and in the outputs

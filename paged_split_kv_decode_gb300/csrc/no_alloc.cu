@@ -136,7 +136,9 @@ extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_arg
 
   float *vpart = reinterpret_cast<float *>(ws + lay.vpart_off);
   float *lpart = reinterpret_cast<float *>(ws + lay.lpart_off);
-  int32_t *fault = reinterpret_cast<int32_t *>(ws);
+  // The scratch's fault word was cleared above, so its low 32 bits are this call's
+  // fault bits whatever the epoch.
+  const FaultRef fault = next_fault(ctx, ws);
   const psd_work_item *ditems = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
   if (M > 0) {
     L0.items = ditems;
@@ -158,7 +160,7 @@ extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_arg
                     args->Dv, o, lse, ctx->dev, s, true, writes_empty_rows(L1, ctx->dev));
   if (st != PSD_OK) return st;
   if (fault_bits_dev) {
-    e = cudaMemcpyAsync(fault_bits_dev, fault, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+    e = cudaMemcpyAsync(fault_bits_dev, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess)
       return fail(PSD_ERR_CUDA, "cascade_decode_no_alloc: fault word: %s", cudaGetErrorString(e));
   }

@@ -42,7 +42,7 @@ struct CCParams {
   const int32_t *member_row_base;
   float *v_out;
   float *lse_out;
-  int32_t *fault;
+  FaultRef fault;
   int64_t num_pages;
   const int32_t *order;  // CTA -> item (longest items first), or NULL
   int Hq_req, Dqk, Dv, page_size, sub, Gm, G_cta;  // sub = tokens per ring tile
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kWarps * 32, G <= 4 ? 4 : 2)
       const int slot0 = (t - pos * TPP) * SUB;
       const uint32_t bar = smem_u32(&bars[s]);
       if (id < 0 || int64_t(id) >= p.num_pages) {
-        atomicOr(p.fault, PSD_FAULT_PAGE_ID);
+        raise_fault(p.fault, PSD_FAULT_PAGE_ID);
         mbar_arrive(bar);
       } else {
         mbar_arrive_expect_tx(bar, 2 * tile_bytes);

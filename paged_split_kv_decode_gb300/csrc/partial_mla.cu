@@ -100,7 +100,7 @@ struct MLAParams {
   int num_items;
   float *v_out;
   float *lse_out;
-  int32_t *fault;
+  FaultRef fault;
   int64_t num_pages;
   int Hq_req, page_size;
   int merge_runs;  // rows feed the merge: accumulate consecutive items of one request
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         if (lane == 0) {
           int page = __ldg(p.page_indices + it.page_off + tok / P);
           if (page < 0 || int64_t(page) >= p.num_pages) {  // out of range: load the zero fill
-            atomicOr(p.fault, PSD_FAULT_PAGE_ID);
+            raise_fault(p.fault, PSD_FAULT_PAGE_ID);
             page = -1;
           }
           mbar_arrive_expect_tx(bar(BKFULL0 + buf), kTileBytes);

@@ -39,7 +39,7 @@ struct TCParams {
   const int32_t *member_row_base;
   float *v_out;
   float *lse_out;
-  int32_t *fault;
+  FaultRef fault;
   int64_t num_pages;
   int Hq_req, Hkv, page_size, Gm, G_cta;
   float q_scale, v_scale;
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(TCShape<DQK, DV, FP8, LATENT>::THREADS)
                     : p.k_pool + slot * k_tok_stride + int64_t(kv) * DQK * S::ESZ + cc * 16;
           bytes = 16;
         } else {
-          atomicOr(p.fault, PSD_FAULT_PAGE_ID);
+          raise_fault(p.fault, PSD_FAULT_PAGE_ID);
         }
       }
       uint32_t dst;

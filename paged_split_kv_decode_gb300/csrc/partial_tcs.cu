@@ -48,7 +48,7 @@ struct TCSParams {
   int has_order;
   float *v_out;
   float *lse_out;
-  int32_t *fault;
+  FaultRef fault;
   int64_t num_pages;
   int Hq_req, Dqk, Dv, page_size, Gm, G_cta;
   int tpp_log2;  // log2(page_size / 16), or -1
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
       const int slot0 = (t - pos * TPP) * kTileTok;
       const uint32_t bar = smem_u32(&bars[s]);
       if (id < 0 || int64_t(id) >= p.num_pages) {
-        atomicOr(p.fault, PSD_FAULT_PAGE_ID);
+        raise_fault(p.fault, PSD_FAULT_PAGE_ID);
         mbar_arrive(bar);
       } else {
         mbar_arrive_expect_tx(bar, 2 * TILE_BYTES);

@@ -203,10 +203,11 @@ def test_work_lists_inline_or_uploaded(tile, inline):
     assert_close(o[req], lse[req], ro[req], rl[req], "bf16", f"flat, tile {tile}")
 
 
-def test_fault_word_is_cleared_by_the_next_call():
-    """A call whose page table holds an out-of-range id flags the workspace; the next
-    clean call on the same workspace starts from a cleared fault word (inline lists:
-    the clear is a memset on the stream, not the list upload)."""
+def test_fault_word_reports_only_the_latest_call():
+    """A call whose page table holds an out-of-range id flags the workspace's fault
+    word; after a later clean call on the same workspace the check reports nothing
+    (the word carries the epoch of the call that wrote it, and no call clears it), and
+    a fault of the latest call is reported again."""
     w = synth.tiny_cascade(seed=0)
     d = Dev(w)
     plan = psd.plan_decode(d.table, w.tile_tokens, 1, 4, 2)
@@ -225,3 +226,22 @@ def test_fault_word_is_cleared_by_the_next_call():
     psd.cascade_decode(ctx(), args_bad, plan, o, None, ws)
     with pytest.raises(psd.PsdError):
         psd.check_device_error(ctx(), ws)
+
+
+@pytest.mark.slow
+def test_cascade_prefix_beyond_l2_sampled():
+    """The cascade batch with a 65536-token shared prefix (268 MB of K/V, more than
+    L2) that the bench times beside the configured batch: cascade and flat outputs of
+    sampled members and non-members against the oracle, and against each other."""
+    w = synth.cascade_decode(seed=0, shared_tokens=65536)
+    d = Dev(w)
+    o, lse, stats, _ = d.decode(enable=1, with_stats=True)
+    assert stats["path"] == 1 and stats["members"] == 16 and stats["shared_pages"] == 4096
+    of, lf = d.decode(enable=0)
+    members = [int(b) for b in np.where(w.lengths > 65536)[0]]
+    others = [int(b) for b in np.where(w.lengths <= 65536)[0]]
+    req = sorted({members[0], members[-1], others[0], others[-1]})
+    ro, rl = A.decode_attention(A.workload_arrays(w), requests=req)
+    assert_close(o[req], lse[req], ro[req], rl[req], "bf16", "cascade, prefix beyond L2")
+    assert_close(of[req], lf[req], ro[req], rl[req], "bf16", "flat, prefix beyond L2")
+    assert np.abs(o - of).max() < 2e-3 and np.abs(lse - lf).max() < 1e-3

@@ -101,3 +101,17 @@ def test_counters_track_paths():
     assert after["launches_cascade"] == before["launches_cascade"] + 1
     assert after["launches_flat"] == before["launches_flat"] + 1
     assert after["cascade_member_sequences"] == before["cascade_member_sequences"] + 3
+
+
+def test_fresh_workspace_garbage_is_not_a_fault():
+    """A workspace whose first bytes hold garbage (all ones, as a reused allocation
+    might) reads as no fault after a clean call: the fault word's epoch is not the
+    call's."""
+    w = synth.tiny_cascade(seed=0)
+    d = Dev(w)
+    plan = psd.plan_decode(d.table, w.tile_tokens, 1, 4, 2)
+    ws = psd.workspace_for(plan, w.Hq, w.Dv, "cuda")
+    ws.fill_(255)
+    o = torch.empty((w.batch, w.Hq, w.Dv), device="cuda")
+    psd.cascade_decode(ctx(), d.args(), plan, o, None, ws)
+    assert psd.check_device_error(ctx(), ws) == 0
