@@ -24,6 +24,8 @@
  *   - Device work is enqueued asynchronously on the caller's stream (NULL = the
  *     legacy default stream).  Host arrays passed in may be reused as soon as the
  *     call returns.
+ *   - A batch of 0 requests is valid and does no device work; q and the outputs
+ *     may then be NULL.
  *   - Host validation (shapes, page table, page ids < num_pages, alignment) runs
  *     before any launch and returns PSD_ERR_INVALID_ARG.  Kernels re-check page
  *     ids; a bad id or an expired bounded wait sets a flag in the workspace that

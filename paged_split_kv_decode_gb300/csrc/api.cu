@@ -49,7 +49,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 psd_status validate_args(const psd_decode_args *a) {
   if (!a) return fail(PSD_ERR_INVALID_ARG, "args: NULL");
-  if (!a->q || !a->k_pool || !a->v_pool || !a->page_indices_dev)
+  if ((a->batch > 0 && !a->q) || !a->k_pool || !a->v_pool || !a->page_indices_dev)
     return fail(PSD_ERR_INVALID_ARG, "args: NULL device pointer");
   if (!aligned16(a->q) || !aligned16(a->k_pool) || !aligned16(a->v_pool))
     return fail(PSD_ERR_INVALID_ARG, "args: q / k_pool / v_pool must be 16-byte aligned");
@@ -426,7 +426,8 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   if (!ctx) return fail(PSD_ERR_INVALID_ARG, "NULL context");
   psd_status st = validate_args(args);
   if (st != PSD_OK) return st;
-  if (!plan || !o || !workspace) return fail(PSD_ERR_INVALID_ARG, "cascade_decode: NULL plan / o / workspace");
+  if (!plan || (!o && args->batch > 0) || !workspace)
+    return fail(PSD_ERR_INVALID_ARG, "cascade_decode: NULL plan / o / workspace");
   if (!aligned16(workspace) || !aligned16(o))
     return fail(PSD_ERR_INVALID_ARG, "cascade_decode: workspace and o must be 16-byte aligned");
   const int32_t B = args->batch;
@@ -583,9 +584,10 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
                                             void *workspace, size_t workspace_bytes,
                                             psd_cascade_stats *stats, psd_stream_t stream) {
   clear_error();
-  if (!ctx || !plan || !o || !lse || !workspace) return fail(PSD_ERR_INVALID_ARG, "cascade_decode_nested: NULL");
+  if (!ctx || !plan || !workspace) return fail(PSD_ERR_INVALID_ARG, "cascade_decode_nested: NULL");
   psd_status st = validate_args(args);
   if (st != PSD_OK) return st;
+  if (args->batch > 0 && (!o || !lse)) return fail(PSD_ERR_INVALID_ARG, "cascade_decode_nested: NULL o / lse");
   if (!aligned16(workspace)) return fail(PSD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   const int32_t B = plan->batch, S = plan->num_segments, E = plan->num_entries;
   const int32_t n0 = plan->l0_num_items, n1 = plan->l1_num_items;

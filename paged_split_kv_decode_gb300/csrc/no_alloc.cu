@@ -75,7 +75,7 @@ extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_arg
   if (!ctx) return fail(PSD_ERR_INVALID_ARG, "NULL context");
   psd_status st = validate_args(args);
   if (st != PSD_OK) return st;
-  if (!plan || !o) return fail(PSD_ERR_INVALID_ARG, "cascade_decode_no_alloc: NULL plan / o");
+  if (!plan || (!o && args->batch > 0)) return fail(PSD_ERR_INVALID_ARG, "cascade_decode_no_alloc: NULL plan / o");
   if (!aligned16(o)) return fail(PSD_ERR_INVALID_ARG, "cascade_decode_no_alloc: o must be 16-byte aligned");
   const int32_t B = args->batch;
   if (plan->batch != B || plan->page_size != args->page_size)

@@ -245,3 +245,52 @@ def test_cascade_prefix_beyond_l2_sampled():
     assert_close(o[req], lse[req], ro[req], rl[req], "bf16", "cascade, prefix beyond L2")
     assert_close(of[req], lf[req], ro[req], rl[req], "bf16", "flat, prefix beyond L2")
     assert np.abs(o - of).max() < 2e-3 and np.abs(lse - lf).max() < 1e-3
+
+
+def test_empty_batch_is_a_no_op():
+    """A decode step with no requests: planning gives an empty flat plan, and
+    cascade_decode, paged_decode_partial and merge_states return without device work
+    (q and the outputs are empty tensors)."""
+    w = synth.tiny_cascade(seed=0)
+    d = Dev(w)
+    empty = np.zeros(0, dtype=np.int32)
+    t = psd.HostTable(np.zeros(1, dtype=np.int32), empty, empty, w.page_size)
+    plan = psd.plan_decode(t, w.tile_tokens, 1, 4, 2)
+    assert plan.num_members == 0 and plan.num_rows == 0
+    q0 = torch.empty((0, w.Hq, w.Dqk), dtype=torch.bfloat16, device="cuda")
+    args = psd.decode_args(q0, d.k, d.v, d.indices, num_pages=w.num_pages, page_size=w.page_size,
+                           Hkv=w.Hkv, Dv=w.Dv, sm_scale=w.sm_scale)
+    o = torch.empty((0, w.Hq, w.Dv), device="cuda")
+    lse = torch.empty((0, w.Hq), device="cuda")
+    ws = psd.workspace_for(plan, w.Hq, w.Dv, "cuda")
+    stats = psd.cascade_decode(ctx(), args, plan, o, lse, ws)
+    assert stats["path"] == 0 and stats["batch"] == 0
+    assert psd.check_device_error(ctx(), ws) == 0
+    items, o_indptr = psd.split_plan(t, w.tile_tokens)
+    assert len(items) == 0 and list(o_indptr) == [0]
+    psd.paged_decode_partial(ctx(), args, items, o, lse, ws)
+    psd.merge_states(ctx(), torch.empty((0, w.Hq, w.Dv), device="cuda"), torch.empty((0, w.Hq), device="cuda"),
+                     torch.zeros(1, dtype=torch.int32, device="cuda"), o, lse)
+    torch.cuda.synchronize()
+
+
+def test_one_long_request_merges_hundreds_of_chunks():
+    """One 131072-token request split into 256 chunks of 512: one merge group of 256
+    rows (eight 32-row LSE windows), plus a one-token request beside it."""
+    rng = np.random.default_rng(23)
+    w = synth._make("long", rng, [131072, 1], Hq=8, Hkv=2, Dqk=128, Dv=128, page_size=16,
+                    num_pages=8200, tile_tokens=512)
+    o, lse = Dev(w).decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "bf16", "long request")
+
+
+def test_largest_stacked_group_per_kv_head():
+    """256 query rows on one KV head (the most the 16-row-group kernel takes), D=128."""
+    rng = np.random.default_rng(24)
+    lengths = synth.lengths_with_partial_last_page(rng, 3, 100, 1500, 16)
+    w = synth._make("g256", rng, lengths, Hq=256, Hkv=1, Dqk=128, Dv=128, page_size=16,
+                    num_pages=512, tile_tokens=256)
+    o, lse = Dev(w).decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "bf16", "G=256")
