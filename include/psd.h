@@ -311,6 +311,10 @@ psd_status merge_states(psd_ctx *ctx, const float *v_in, const float *lse_in,
  * attends every request's remaining tokens; merge_states combines each member's
  * level-0 and level-1 rows (and passes a non-member's single chunk group through).
  * o: device [batch, Hq, Dv] f32.  lse: device [batch, Hq] f32 (log2) or NULL.
+ * o and lse may instead be pinned host memory (cudaHostAlloc / cudaHostRegister,
+ * same pointer on host and device): the merge kernel then stores the outputs into
+ * host memory over the host link, and they are readable once the stream has
+ * synchronised; no separate device-to-host copy is needed.
  * workspace: >= psd_workspace_bytes(batch, plan item total, plan->num_rows, Hq, Dv).
  * stats (host, nullable) receives which path ran.  The work lists reach the GPU in
  * the launches' parameters when they fit (16 KB of items, order and members, and

@@ -38,6 +38,16 @@ def _dev_ptr(t: torch.Tensor, name: str) -> int:
     return t.data_ptr()
 
 
+def _out_ptr(t: torch.Tensor, name: str) -> int:
+    """Decode outputs may be CUDA tensors or pinned host tensors (the merge kernel then
+    stores into host memory over the host link; the pointer is the same on both sides)."""
+    if isinstance(t, torch.Tensor) and t.device.type == "cpu" and t.is_pinned():
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        return t.data_ptr()
+    return _dev_ptr(t, name)
+
+
 def kv_dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.bfloat16:
         return L.PSD_BF16
@@ -414,8 +424,8 @@ def cascade_decode(ctx: Context, args: L.DecodeArgs, plan: Plan, o: torch.Tensor
     """cascade_decode (flat when the plan has no members); returns the path stats."""
     stats = L.CascadeStats()
     L.check(L.load().cascade_decode(
-        ctx.handle, C.byref(args), C.byref(plan.c), _dev_ptr(o, "o"),
-        None if lse is None else _dev_ptr(lse, "lse"), _dev_ptr(workspace, "workspace"),
+        ctx.handle, C.byref(args), C.byref(plan.c), _out_ptr(o, "o"),
+        None if lse is None else _out_ptr(lse, "lse"), _dev_ptr(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), C.byref(stats), _stream(stream)))
     return {k: getattr(stats, k) for k, _ in L.CascadeStats._fields_}
 

@@ -294,3 +294,23 @@ def test_largest_stacked_group_per_kv_head():
     o, lse = Dev(w).decode(enable=0)
     ro, rl = A.decode_attention(A.workload_arrays(w))
     assert_close(o, lse, ro, rl, "bf16", "G=256")
+
+
+@pytest.mark.parametrize("maker", [synth.tiny_cascade, synth.flat_decode])
+def test_outputs_into_pinned_host_memory(maker):
+    """cascade_decode with o and lse in pinned host memory: the merge kernel stores
+    them over the host link; after a stream sync they equal the device outputs bit
+    for bit."""
+    w = maker(seed=3)
+    d = Dev(w)
+    plan = psd.plan_decode(d.table, w.tile_tokens, 1, w.min_shared_pages, w.min_members)
+    ws = psd.workspace_for(plan, w.Hq, w.Dv, "cuda")
+    o = torch.empty((w.batch, w.Hq, w.Dv), device="cuda")
+    lse = torch.empty((w.batch, w.Hq), device="cuda")
+    psd.cascade_decode(ctx(), d.args(), plan, o, lse, ws)
+    oh = torch.full((w.batch, w.Hq, w.Dv), float("nan")).pin_memory()
+    lh = torch.full((w.batch, w.Hq), float("nan")).pin_memory()
+    psd.cascade_decode(ctx(), d.args(), plan, oh, lh, ws)
+    torch.cuda.synchronize()
+    assert psd.check_device_error(ctx(), ws) == 0
+    assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu())
