@@ -140,6 +140,155 @@ __global__ void __launch_bounds__(kMergeWarps * 32, WIDE ? 1 : (NV >= (SKIP ? 4 
   if (lse_out && lane == 0) lse_out[r * H + h] = M + log2f(sw);
 }
 
+// Large grids with an even head count: one warp merges heads h and h + 1 of one
+// output row.  The group bounds are read once for both, their LSE pairs come in one
+// 8-byte load per row, and both heads' rows are in flight together, which doubles
+// the bytes a warp has outstanding at the cost of running two blocks per SM.
+template <int NV, bool SKIP, bool INL>
+__global__ void __launch_bounds__(kMergeWarps * 32, 2)
+    merge_pair_kernel(const float *__restrict__ v_in, const float *__restrict__ lse_in,
+                      const int32_t *__restrict__ o_indptr, int64_t num_out, int H, int D,
+                      float *__restrict__ v_out, float *__restrict__ lse_out,
+                      const __grid_constant__ IndptrParam<INL> inl) {
+  constexpr int U = NV >= 8 ? 1 : 8 / NV;  // rows per batch and head
+  const int lane = threadIdx.x & 31;
+  const int Hp = H >> 1;
+  const int64_t gw = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  if (gw >= num_out * Hp) return;
+  const int64_t r = gw / Hp;
+  const int h0 = 2 * int(gw - r * Hp);
+  int lo, hi;
+  if constexpr (INL) {
+    lo = inl.v[r];
+    hi = inl.v[r + 1];
+  } else {
+    lo = __ldg(o_indptr + r);
+    hi = __ldg(o_indptr + r + 1);
+  }
+  wait_for_prior_grid();
+  const int n = hi - lo;
+  const int D4 = D >> 2;
+
+  float4 v[2][U][NV];
+  // rows first .. first + count - 1 of both heads; lw[t] holds, in lane i, head t's
+  // LSE of row w0 + i of the current 32-row window, and j0 = first - w0
+  auto load_rows = [&](int first, int count, const float2 lw, int j0) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      bool ok0 = u < count, ok1 = ok0;
+      if constexpr (SKIP) {
+        ok0 = __shfl_sync(0xffffffffu, lw.x, (j0 + u) & 31) != neg_inf() && ok0;
+        ok1 = __shfl_sync(0xffffffffu, lw.y, (j0 + u) & 31) != neg_inf() && ok1;
+      }
+      const float4 *src = reinterpret_cast<const float4 *>(v_in + (int64_t(lo + first + u) * H + h0) * D);
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        const int d4 = lane + 32 * k;
+        v[0][u][k] = (ok0 && d4 < D4) ? __ldcs(src + d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[1][u][k] = (ok1 && d4 < D4) ? __ldcs(src + D4 + d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  };
+  auto lse_pair = [&](int i) -> float2 {  // LSE of heads h0, h0 + 1 for group row i
+    return __ldg(reinterpret_cast<const float2 *>(lse_in + int64_t(lo + i) * H + h0));
+  };
+  const float2 ninf2 = make_float2(neg_inf(), neg_inf());
+  const float2 l_first = lane < n ? lse_pair(lane) : ninf2;
+  load_rows(0, n, l_first, 0);
+  float4 *out4 = reinterpret_cast<float4 *>(v_out + (r * H + h0) * int64_t(D));
+
+  if (n == 1) {  // identity: out = v bit for bit
+    const float l0 = __shfl_sync(0xffffffffu, l_first.x, 0), l1 = __shfl_sync(0xffffffffu, l_first.y, 0);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int d4 = lane + 32 * k;
+      if (d4 < D4) {
+        out4[d4] = l0 != neg_inf() ? v[0][0][k] : make_float4(0.f, 0.f, 0.f, 0.f);
+        out4[D4 + d4] = l1 != neg_inf() ? v[1][0][k] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    if (lse_out && lane == 0) {
+      lse_out[r * H + h0] = l0;
+      lse_out[r * H + h0 + 1] = l1;
+    }
+    return;
+  }
+
+  float M0 = l_first.x, M1 = l_first.y;
+  for (int i = lane + 32; i < n; i += 32) {
+    const float2 l = lse_pair(i);
+    M0 = fmaxf(M0, l.x);
+    M1 = fmaxf(M1, l.y);
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    M0 = fmaxf(M0, __shfl_xor_sync(0xffffffffu, M0, off));
+    M1 = fmaxf(M1, __shfl_xor_sync(0xffffffffu, M1, off));
+  }
+  // an empty or all -inf group gives 0 and -inf (per head)
+  const bool live0 = n > 0 && M0 != neg_inf(), live1 = n > 0 && M1 != neg_inf();
+  const float Ms0 = live0 ? M0 : 0.f, Ms1 = live1 ? M1 : 0.f;
+
+  float4 acc[2][NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) acc[0][k] = acc[1][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float sw0 = 0.f, sw1 = 0.f;
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const int cnt = min(32, n - i0);
+    const float2 l = i0 == 0 ? l_first : (lane < cnt ? lse_pair(i0 + lane) : ninf2);
+    const float w0_mine = lane < cnt ? ex2(l.x - Ms0) : 0.f;
+    const float w1_mine = lane < cnt ? ex2(l.y - Ms1) : 0.f;
+    sw0 += w0_mine;
+    sw1 += w1_mine;
+    for (int j = 0; j < cnt; j += U) {
+      if (i0 + j > 0) load_rows(i0 + j, cnt - j, l, j);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const bool in = j + u < cnt;
+        const float w0 = in ? __shfl_sync(0xffffffffu, w0_mine, (j + u) & 31) : 0.f;
+        const float w1 = in ? __shfl_sync(0xffffffffu, w1_mine, (j + u) & 31) : 0.f;
+        if (w0 != 0.f) {  // an empty row (LSE -inf): its v is not used, whatever it holds
+#pragma unroll
+          for (int k = 0; k < NV; ++k) {
+            acc[0][k].x = fmaf(w0, v[0][u][k].x, acc[0][k].x);
+            acc[0][k].y = fmaf(w0, v[0][u][k].y, acc[0][k].y);
+            acc[0][k].z = fmaf(w0, v[0][u][k].z, acc[0][k].z);
+            acc[0][k].w = fmaf(w0, v[0][u][k].w, acc[0][k].w);
+          }
+        }
+        if (w1 != 0.f) {
+#pragma unroll
+          for (int k = 0; k < NV; ++k) {
+            acc[1][k].x = fmaf(w1, v[1][u][k].x, acc[1][k].x);
+            acc[1][k].y = fmaf(w1, v[1][u][k].y, acc[1][k].y);
+            acc[1][k].z = fmaf(w1, v[1][u][k].z, acc[1][k].z);
+            acc[1][k].w = fmaf(w1, v[1][u][k].w, acc[1][k].w);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    sw0 += __shfl_xor_sync(0xffffffffu, sw0, off);
+    sw1 += __shfl_xor_sync(0xffffffffu, sw1, off);
+  }
+  const float inv0 = live0 ? 1.f / sw0 : 0.f, inv1 = live1 ? 1.f / sw1 : 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int d4 = lane + 32 * k;
+    if (d4 < D4) {
+      __stcs(out4 + d4, make_float4(acc[0][k].x * inv0, acc[0][k].y * inv0, acc[0][k].z * inv0, acc[0][k].w * inv0));
+      __stcs(out4 + D4 + d4,
+             make_float4(acc[1][k].x * inv1, acc[1][k].y * inv1, acc[1][k].z * inv1, acc[1][k].w * inv1));
+    }
+  }
+  if (lse_out && lane == 0) {
+    lse_out[r * H + h0] = live0 ? M0 + log2f(sw0) : neg_inf();
+    lse_out[r * H + h0 + 1] = live1 ? M1 + log2f(sw1) : neg_inf();
+  }
+}
+
 template <int NV, bool SKIP, bool INL>
 cudaError_t launch_form(dim3 grid, bool wide, bool early, cudaStream_t s, const float *v_in, const float *lse_in,
                         const int32_t *o_indptr, int64_t num_out, int H, int D, float *v_out,
@@ -161,10 +310,49 @@ cudaError_t launch_form(dim3 grid, bool wide, bool early, cudaStream_t s, const 
                             H, D, v_out, lse_out, inl);
 }
 
+template <int NV, bool SKIP, bool INL>
+cudaError_t launch_pair_impl(dim3 grid, bool early, cudaStream_t s, const float *v_in, const float *lse_in,
+                        const int32_t *o_indptr, int64_t num_out, int H, int D, float *v_out, float *lse_out,
+                        const IndptrParam<INL> &inl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = early ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, merge_pair_kernel<NV, SKIP, INL>, v_in, lse_in, o_indptr, num_out, H, D, v_out,
+                            lse_out, inl);
+}
+template <int NV, bool SKIP, bool INL>
+cudaError_t launch_pair(dim3 grid, bool early, cudaStream_t s, const float *v_in, const float *lse_in,
+                        const int32_t *o_indptr, int64_t num_out, int H, int D, float *v_out, float *lse_out,
+                        const IndptrParam<INL> &inl) {
+  if constexpr (NV <= 2)
+    return launch_pair_impl<NV, SKIP, INL>(grid, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out, inl);
+  else
+    return cudaErrorInvalidValue;  // (not selected: the launcher takes this form only for NV <= 2)
+}
+
 template <int NV>
 cudaError_t launch_nv(dim3 grid, bool wide, bool early, bool skip, const InlineIndptr *inl, cudaStream_t s,
                       const float *v_in, const float *lse_in, const int32_t *o_indptr, int64_t num_out, int H,
                       int D, float *v_out, float *lse_out) {
+  // Large grids, even H, D <= 256 (two heads' rows fit the registers) and 8-byte
+  // aligned LSE rows: two heads per warp.
+  if (NV <= 2 && !wide && H % 2 == 0 && reinterpret_cast<uintptr_t>(lse_in) % 8 == 0) {
+    const int64_t blocks = (num_out * (H / 2) + kMergeWarps - 1) / kMergeWarps;
+    const dim3 g2(static_cast<unsigned>(blocks));
+    const NoInline none{};
+    if (inl)
+      return skip ? launch_pair<NV, true, true>(g2, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out, *inl)
+                  : launch_pair<NV, false, true>(g2, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out, *inl);
+    return skip ? launch_pair<NV, true, false>(g2, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out, none)
+                : launch_pair<NV, false, false>(g2, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out, none);
+  }
   if (inl)
     return skip ? launch_form<NV, true, true>(grid, wide, early, s, v_in, lse_in, o_indptr, num_out, H, D, v_out,
                                               lse_out, *inl)

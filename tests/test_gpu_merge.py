@@ -130,3 +130,44 @@ def test_merge_sweep_large_sampled(num_out):
     assert np.abs(lo[ridx].cpu().double().numpy() - rl).max() < TOL_L
     del v_in, lse_in, vo, lo
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("H,misaligned", [(6, False), (6, True), (5, False)])
+def test_two_heads_per_warp_and_its_fallbacks(H, misaligned):
+    """Large grids merge two heads per warp when H is even and the LSE rows are 8-byte
+    aligned; odd H, or an LSE buffer that starts one float past an 8-byte boundary,
+    take the one-head form.  Each matches the oracle, with an empty group, a group of
+    one, an all -inf group and empty rows (v NaN) included, and the two forms agree
+    bit for bit."""
+    rng = np.random.default_rng(40 + H)
+    sizes = rng.integers(1, 21, size=900)
+    sizes[3], sizes[4] = 0, 1
+    o_indptr = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    N = int(o_indptr[-1])
+    v_in = torch.from_numpy(rng.standard_normal((N, H, 128), dtype=np.float32))
+    lse_in = torch.from_numpy(rng.uniform(-5, 20, size=(N, H)).astype(np.float32))
+    a, b = int(o_indptr[7]), int(o_indptr[8])
+    lse_in[a:b, 0] = -float("inf")                       # group 7, head 0: all -inf
+    empty = torch.from_numpy(rng.random((N, H)) < 0.2)
+    empty[torch.from_numpy(o_indptr[:-1][sizes > 0].astype(np.int64))] = False
+    lse_in[empty] = -float("inf")
+    v_in[empty] = float("nan")
+    ro, rl = A.merge_states(v_in.numpy(), lse_in.numpy(), o_indptr)
+    if misaligned:
+        store = torch.empty(N * H + 1, device="cuda")
+        dl = store[1:].view(N, H)
+        dl.copy_(lse_in.cuda())
+        assert dl.data_ptr() % 8 == 4
+    else:
+        dl = lse_in
+    vo, lo = _gpu_merge(v_in, dl, o_indptr)
+    assert np.abs(vo.cpu().double().numpy() - ro).max() < TOL_O
+    assert np.array_equal(np.isneginf(lo.cpu().numpy()), np.isneginf(rl))
+    fin = np.isfinite(rl)
+    assert np.abs(lo.cpu().double().numpy()[fin] - rl[fin]).max() < TOL_L
+    if H % 2 == 0 and not misaligned:   # the other form on the same rows
+        store = torch.empty(N * H + 1, device="cuda")
+        dl1 = store[1:].view(N, H)
+        dl1.copy_(lse_in.cuda())
+        vo1, lo1 = _gpu_merge(v_in, dl1, o_indptr)
+        assert torch.equal(vo1, vo) and torch.equal(lo1, lo)
