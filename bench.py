@@ -267,12 +267,12 @@ def e2e_timing(arm: Arm, steps: int, warmup: int, flush):
     return times, h2d, d2h
 
 
-def merge_sweep(ctx, steps: int, warmup: int, flush, hbm: float):
+def merge_sweep(ctx, steps: int, warmup: int, flush, hbm: float, sizes=(1024, 16384, 262144, 1048576)):
     """merge_states alone over the sweep's sizes (H=32, D=128, log2 LSE ~ U(-5,20),
     groups U[1,16] with a group of one), inputs drawn on the device."""
     import paged_split_kv_decode_gb300 as psd
     out = []
-    for M in (1024, 16384, 262144, 1048576):
+    for M in sizes:
         v_in, lse_in, o_indptr = synth.merge_inputs_device(0, M)
         ind = torch.from_numpy(o_indptr).cuda()
         N = int(o_indptr[-1])
@@ -570,7 +570,9 @@ def run_ours(args):
         }
         del marm
     if not args.quick and args.workload in ("all", "merge"):
-        extra["merge_sweep"] = merge_sweep(arm.ctx, args.steps, args.warmup, flush, hbm)
+        sizes = tuple(int(x) for x in args.merge_rows.split(",")) if args.merge_rows else \
+            (1024, 16384, 262144, 1048576)
+        extra["merge_sweep"] = merge_sweep(arm.ctx, args.steps, args.warmup, flush, hbm, sizes)
     if not args.quick and args.workload in ("all", "cascade", "nested"):
         extra["nested"] = nested_timing(args.steps, args.warmup, flush)
     if not args.quick and args.workload in ("all", "tune"):
@@ -682,6 +684,7 @@ def main():
                    default="all",
                    help="which workloads run after the flat headline")
     p.add_argument("--mla-batch", type=int, default=128, help="requests in the MLA workload")
+    p.add_argument("--merge-rows", default="", help="merge sweep sizes, comma-separated (default 1K,16K,256K,1M)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     args = p.parse_args()
     if args.warmup < 3:
