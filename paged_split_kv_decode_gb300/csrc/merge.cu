@@ -74,7 +74,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32, WIDE ? 1 : (NV >= (SKIP ? 4 
   };
 
   const float l_first = lane < n ? __ldg(lse_in + int64_t(lo + lane) * H + h) : neg_inf();
-  load_rows(0, n, l_first, 0);
+  // (SKIP loads only the live rows below; row 0 here serves the identity case)
+  load_rows(0, SKIP ? min(n, 1) : n, l_first, 0);
 
   if (n == 1) {  // identity: w = 1, l = 1, out = v bit for bit
     const float l = __shfl_sync(0xffffffffu, l_first, 0);
@@ -112,6 +113,43 @@ __global__ void __launch_bounds__(kMergeWarps * 32, WIDE ? 1 : (NV >= (SKIP ? 4 
                             : (lane < cnt ? __ldg(lse_in + int64_t(lo + i0 + lane) * H + h) : neg_inf());
     const float w_mine = lane < cnt ? ex2(l - M) : 0.f;
     sw += w_mine;
+    if constexpr (SKIP) {
+      // Only the window's live rows, U at a time in increasing order (the same sum,
+      // in the same order, as visiting every row and skipping zero weights).
+      unsigned live = __ballot_sync(0xffffffffu, lane < cnt && l != neg_inf());
+      while (live) {
+        int idx[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          idx[u] = live ? __ffs(live) - 1 : -1;
+          live &= live - 1u;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float4 *src =
+              reinterpret_cast<const float4 *>(v_in + (int64_t(lo + i0 + max(idx[u], 0)) * H + h) * D);
+#pragma unroll
+          for (int k = 0; k < NV; ++k) {
+            const int d4 = lane + 32 * k;
+            v[u][k] = (idx[u] >= 0 && d4 < D4) ? __ldcs(src + d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (idx[u] < 0) break;  // warp-uniform
+          const float w = __shfl_sync(0xffffffffu, w_mine, idx[u]);
+          if (w == 0.f) continue;
+#pragma unroll
+          for (int k = 0; k < NV; ++k) {
+            acc[k].x = fmaf(w, v[u][k].x, acc[k].x);
+            acc[k].y = fmaf(w, v[u][k].y, acc[k].y);
+            acc[k].z = fmaf(w, v[u][k].z, acc[k].z);
+            acc[k].w = fmaf(w, v[u][k].w, acc[k].w);
+          }
+        }
+      }
+      continue;
+    }
     for (int j = 0; j < cnt; j += U) {
       if (i0 + j > 0) load_rows(i0 + j, cnt - j, l, j);
 #pragma unroll
