@@ -77,7 +77,8 @@ typedef enum {
   PSD_DECLINE_SPAN_BELOW_THRESHOLD = 4 /* includes spans capped below the threshold */
 } psd_decline_reason;
 
-/* Device-fault flag bits written by kernels into the workspace. */
+/* Device-fault flag bits written by kernels into the workspace's fault word (its
+ * first 8 bytes, tagged with the call that wrote them; psd_check_device_error). */
 enum {
   PSD_FAULT_PAGE_ID = 1,      /* a page id outside [0, num_pages) was skipped */
   PSD_FAULT_WAIT_TIMEOUT = 2, /* a bounded barrier wait gave up */

@@ -502,7 +502,7 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
     L1.seg_items[0] = n0;
     L1.seg_rows[0] = L0.G_cta;
     L1.seg_member0[0] = 0;
-  } else if (M > 0) {  // level 0 on the side stream, after the upload
+  } else if (M > 0) {  // level 0 on the side stream, after the lists are placed
     L0.items = ditems;
     L0.order = reinterpret_cast<const int32_t *>(ws + lay.order_off);
     L0.num_items = n0;
@@ -685,7 +685,7 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
     }
     L1.members = dmembers;
     L1.member_row_base = drow_base;
-  } else if (S > 0) {  // every segment's level 0 on the side stream, after the upload
+  } else if (S > 0) {  // every segment's level 0 on the side stream, after the lists are placed
     cudaError_t e = cudaEventRecord(ctx->fork, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->fork, 0);
     if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "nested fork: %s", cudaGetErrorString(e));

@@ -13,15 +13,16 @@
 struct psd_ctx {
   psd::DeviceInfo dev;
   psd_counters counters;
-  // Two pinned staging buffers for the per-call H2D upload of work lists; an
-  // event per buffer tells when its previous copy has finished reading it.
+  // Two pinned staging buffers for the per-call H2D upload of work lists (when they
+  // do not travel in the launch parameters); an event per buffer tells when its
+  // previous copy has finished reading it.
   void *staging[2] = {nullptr, nullptr};
   size_t staging_cap[2] = {0, 0};
   cudaEvent_t staging_done[2] = {nullptr, nullptr};
   bool staging_pending[2] = {false, false};
   int next = 0;
   // Level 0 of a cascade runs on `side`, concurrently with level 1 on the caller's
-  // stream: fork after the upload, join before the merge.
+  // stream: fork once the lists are placed, join before the merge.
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
   // Optional kernel timing: events around level 0, level 1 / flat, and merge.
