@@ -73,3 +73,23 @@ def test_no_segment_is_the_flat_decode():
     assert plan.num_segments == 0 and stats["path"] == 0
     ro, rl = A.decode_attention(A.workload_arrays(w))
     assert_close(o, lse, ro, rl, w.kv_dtype, "flat through the nested entry")
+
+
+def test_more_segments_than_one_launch_holds():
+    """A system prompt for 18 requests and nine two-request tenants with their own
+    sub-prefix: ten segments, more than one fused launch carries, so every
+    segment's level 0 runs on the side stream (its work lists in the launch
+    parameters) before the level-1 launch and the merge."""
+    rng = np.random.default_rng(31)
+    P = 16
+    mem = list(range(18))
+    lengths = [4 * P + 2 * P + int(rng.integers(1, 60)) for _ in mem] + [int(x) for x in rng.integers(20, 200, size=3)]
+    prefixes = [(mem, 4)] + [([2 * k, 2 * k + 1], 2) for k in range(9)]
+    w = synth._make("nested_wide", rng, lengths, Hq=8, Hkv=2, Dqk=64, Dv=64, page_size=P, num_pages=600,
+                    tile_tokens=32, prefixes=prefixes, min_shared_pages=2, min_members=2)
+    before = ctx().counters()["lists_inline"]
+    o, lse, stats, plan = _decode_nested(w, 2, 2, 2)
+    assert plan.num_segments == 10 and stats["path"] == 1
+    assert ctx().counters()["lists_inline"] - before == 1
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, w.kv_dtype, "ten segments")
