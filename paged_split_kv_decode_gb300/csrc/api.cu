@@ -387,6 +387,7 @@ extern "C" psd_status paged_decode_partial(psd_ctx *ctx, const psd_decode_args *
   st = upload(ctx, ws, host.data(), host.size(), s);
   if (st != PSD_OK) return st;
   L.items = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
+  L.items_host = items;
   L.order = reinterpret_cast<const int32_t *>(ws + lay.order_off);
   L.num_items = num_items;
   L.v_out = v_out;
@@ -524,6 +525,7 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   }
   if (!fused) {
     L1.items = ditems + n0;
+    L1.items_host = plan->l1_items;
     L1.order = reinterpret_cast<const int32_t *>(ws + lay.order_off) + n0;
     L1.num_items = n1;
   }
@@ -711,6 +713,7 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
     if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "nested join: %s", cudaGetErrorString(e));
   }
   L1.items = fused ? ditems : ditems + n0;
+  if (!fused) L1.items_host = plan->l1_items;
   L1.order = reinterpret_cast<const int32_t *>(ws + lay.order_off) + n0;
   L1.num_items = n1;
   L1.v_out = vpart;

@@ -63,6 +63,7 @@ struct PartialLaunch {
   const void *v_pool = nullptr;  // == k_pool for a shared latent
   const int32_t *page_indices = nullptr;
   const psd_work_item *items = nullptr;  // device
+  const psd_work_item *items_host = nullptr;  // host copy of `items`, when the caller has one
   const int32_t *order = nullptr;        // device, CTA -> item index (longest first), or NULL
   int32_t num_items = 0;
   const int32_t *members = nullptr;          // device, stacked items only

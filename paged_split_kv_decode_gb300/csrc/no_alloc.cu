@@ -151,6 +151,7 @@ extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_arg
     if ((st = launch_partial(L0, ctx->dev, s)) != PSD_OK) return st;
   }
   L1.items = ditems + n0;
+  L1.items_host = plan->l1_items;
   L1.num_items = n1;
   L1.v_out = vpart;
   L1.lse_out = lpart;

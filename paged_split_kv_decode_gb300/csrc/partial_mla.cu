@@ -42,6 +42,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <vector>
 
 #include "device.cuh"
 #include "kernels.h"
@@ -84,15 +85,18 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;   // S buffer b at kColS + 64 b
 constexpr float kLazyRescale = 4.f;             // log2 units
 constexpr float kPBias = 4.f;                   // P = 2^(score - m + 4) <= 2^8
-// Run partition costs in tokens of tile work (a 64-token tile takes about 2100
-// cycles): one O write-out about 6K cycles (charged to the items that write one),
-// one query split about 25K.
-constexpr int kItemCostTok = 180, kSplitCostTok = 750;
+// Run partition costs in tokens of tile work.  A least-squares fit of per-CTA
+// cycles (clock64 traces, 128-request batch) gives about 2240 cycles per 64-token
+// tile and about 23K per request boundary (an O write-out and a query switch,
+// about 11.5K each), i.e. 330 token-equivalents each.  An item's tokens are counted
+// in whole tiles.
+constexpr int kItemCostTok = 330, kSplitCostTok = 330;
+constexpr int kMaxPairs = 128;  // pairs whose runs the launch parameters carry
 
 // mbarrier slots (uint64 each) at kOffBar
 enum { BQ = 0, BQSEEN, BQREADY, BORDY, BDRAIN, BSFULL0, BPFULL0 = BSFULL0 + 2, BKFULL0 = BPFULL0 + 2,
        BKEMPTY0 = BKFULL0 + kNB, BSLOT = BKEMPTY0 + kNB };
-static_assert(BSLOT * 8 + 12 <= 256, "barrier area");
+static_assert(BSLOT * 8 + 20 <= 256, "barrier area");
 
 struct MLAParams {
   const int32_t *page_indices;
@@ -105,6 +109,13 @@ struct MLAParams {
   int Hq_req, page_size;
   int merge_runs;  // rows feed the merge: accumulate consecutive items of one request
   float q_scale, v_scale;
+  // Runs of the CTA pairs, computed on the host: pair x starts at tile run_tile[x]
+  // of item run_item[x] and ends where pair x + 1 starts.  A run may end inside an
+  // item (when the rows feed the merge and the previous item of the same request is
+  // in the run): its partial then goes to the previous item's row, which the run
+  // left empty.  Without them (has_runs 0) each CTA computes a run of whole items.
+  int has_runs;
+  int32_t run_item[kMaxPairs + 1], run_tile[kMaxPairs + 1];
 };
 
 // Item b continues item a's partial: the next chunk of the same request, whose row
@@ -231,7 +242,9 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + BSLOT);
-  int *srange = reinterpret_cast<int *>(tslot + 1);                // this pair's items [begin, end)
+  // this pair's items [begin, end), the first item from tile srange[2], the last
+  // item up to tile srange[3] (0: to its end)
+  int *srange = reinterpret_cast<int *>(tslot + 1);
   long long *sscan = reinterpret_cast<long long *>(sm + kOffQS);   // scratch until a query lands
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
@@ -254,7 +267,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       mbar_init(bar(BKEMPTY0 + b), 1);
     }
     fence_mbar_init();
-    srange[0] = srange[1] = 0;
+    srange[0] = srange[1] = srange[2] = srange[3] = 0;
   }
   if (warp == kCtrlWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
@@ -266,7 +279,15 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   // its tokens plus the O write-out of one item, plus a query split where the
   // request changes (in tokens of tile work).  Items stay whole, and consecutive
   // items mostly belong to one request and reuse its split query.
-  {
+  if (p.has_runs) {
+    if (tid == 0) {
+      const int x = blockIdx.x;
+      srange[0] = p.run_item[x];
+      srange[1] = p.run_item[x + 1] + (p.run_tile[x + 1] > 0 ? 1 : 0);
+      srange[2] = p.run_tile[x];
+      srange[3] = p.run_tile[x + 1];
+    }
+  } else {
     const int n = p.num_items;
     const int per = (n + kThreadsM - 1) / kThreadsM;
     const int a0 = min(n, tid * per), a1 = min(n, a0 + per);
@@ -274,7 +295,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       const psd_work_item it = p.items[i];
       const bool first = i == 0 || __ldg(&p.items[i - 1].q_index) != it.q_index;
       const bool writes = !p.merge_runs || i + 1 == n || !continues(it, p.items[i + 1]);
-      return it.n_tokens > 0 ? it.n_tokens + (writes ? kItemCostTok : 0) + (first ? kSplitCostTok : 0) : 0;
+      const int tiled = (it.n_tokens + kTokM - 1) / kTokM * kTokM;
+      return it.n_tokens > 0 ? tiled + (writes ? kItemCostTok : 0) + (first ? kSplitCostTok : 0) : 0;
     };
     long long part = 0;
     for (int i = a0; i < a1; ++i) part += cost(i);
@@ -306,7 +328,10 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const int begin = srange[0], end = srange[1];
+  const int begin = srange[0], end = srange[1], first_tile = srange[2], end_tile = srange[3];
+  // tiles [j0, j1) of item m of the run
+  auto tile_lo = [&](int m) { return m == begin ? first_tile : 0; };
+  auto tile_hi = [&](int m, int nt) { return m == end - 1 && end_tile > 0 ? end_tile : nt; };
 
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer warp
@@ -320,6 +345,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       const psd_work_item it = p.items[m];
       const int nt = (it.n_tokens + kTokM - 1) / kTokM;
       if (nt <= 0) continue;  // (the planner emits no empty items)
+      const int j0 = tile_lo(m), j1 = tile_hi(m, nt);
+      if (j1 <= j0) continue;  // (the run planner emits no empty tile range)
       if (it.q_index != cur_q) {
         if (g > 0)
           ok = __all_sync(0xffffffffu, mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault));
@@ -336,7 +363,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         ++nq;
       }
 #pragma unroll 1
-      for (int j = 0; j < nt; ++j) {
+      for (int j = j0; j < j1; ++j) {
         const int buf = g % kNB;
         if (g >= kNB)  // PV(g - 4) has read the buffer
           ok = mbar_wait(bar(BKEMPTY0 + buf), uint32_t(g / kNB - 1) & 1u, p.fault);
@@ -413,6 +440,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       const psd_work_item it = p.items[m];
       const int nt = (it.n_tokens + kTokM - 1) / kTokM;
       if (nt <= 0) continue;  // (the planner emits no empty items)
+      const int j0 = tile_lo(m), j1 = tile_hi(m, nt);
+      if (j1 <= j0) continue;  // (the run planner emits no empty tile range)
       const bool cont = p.merge_runs && m > begin && continues(p.items[m - 1], it);
       if (!cont) ++npart;
       if (it.q_index != cur_q) {
@@ -425,7 +454,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         ++nq;
       }
 #pragma unroll 1
-      for (int j = 0; j < nt; ++j) {
+      for (int j = j0; j < j1; ++j) {
         const int buf = g % kNB;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(BKFULL0 + buf), uint32_t(g / kNB) & 1u, p.fault));
         if (!ok) break;
@@ -450,7 +479,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         __syncwarp();
         if (pend >= 0 && !(ok = issue_pv())) break;
         pend = g++;
-        pend_first = j == 0;
+        pend_first = j == j0;
         pend_cont = cont;
         pend_po = npart - 1;
       }
@@ -472,6 +501,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       const psd_work_item it = p.items[m];
       const int nt = (it.n_tokens + kTokM - 1) / kTokM;
       if (nt <= 0) continue;  // (the planner emits no empty items)
+      const int j0 = tile_lo(m), j1 = tile_hi(m, nt);
+      if (j1 <= j0) continue;  // (the run planner emits no empty tile range)
       // A continued item adds to the previous item's O, m_ref and l_sum.
       const bool cont = p.merge_runs && m > begin && continues(p.items[m - 1], it);
       if (it.q_index != cur_q) {
@@ -546,7 +577,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       const bool qpos = qs >= 0.f;
       const int tail = it.n_tokens - (nt - 1) * kTokM;   // valid tokens of the last tile
 #pragma unroll 1
-      for (int j = 0; j < nt; ++j, ++g) {
+      for (int j = j0; j < j1; ++j, ++g) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(BSFULL0 + (g & 1)), uint32_t(g >> 1) & 1u, p.fault));
         if (!ok) break;
         tc_fence_after();
@@ -577,7 +608,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         const bool grow = mt > m_ref + kLazyRescale;
         if (__any_sync(0xffffffffu, grow)) {
           const float m_new = grow ? mt : m_ref;
-          if (j >= 1 || cont) {  // PV(g-1) must be done; then rescale this warp's O rows in TMEM
+          if (j > j0 || cont) {  // PV(g-1) must be done; then rescale this warp's O rows in TMEM
             ok = __all_sync(0xffffffffu,
                             mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault));
             if (!ok) break;
@@ -647,7 +678,9 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault));
       if (!ok) break;
       tc_fence_after();
-      const int64_t orow = int64_t(it.out_row) * p.Hq_req + row;
+      // a run that ends inside this item writes to the previous item's (empty) row
+      const int out_row = m == end - 1 && end_tile > 0 ? it.out_row - 1 : it.out_row;
+      const int64_t orow = int64_t(out_row) * p.Hq_req + row;
       float *dst = p.v_out + orow * kDvM + half * kDvHalf;
       const float inv = p.v_scale / l_sum;
 #pragma unroll 1
@@ -705,6 +738,81 @@ bool encode_latent_map(CUtensorMap *map, const DeviceInfo &dev, const void *pool
 
 }  // namespace
 
+// The pairs' runs: contiguous stretches of the item list that minimise the largest
+// run cost (binary search on the bound, greedy fill), in the cost units of the
+// in-kernel partition, plus an O write-out for a run that ends inside a request and
+// a query split for one that starts inside it.  When the rows feed the merge, a run
+// may end inside item i at a tile boundary if item i - 1 belongs to the same request
+// and to the run (the run's partial then goes to row i - 1); otherwise runs hold
+// whole items.  The optimum lies in [max(mean, largest item), mean + largest item].
+void plan_runs(const PartialLaunch &L, int pairs, MLAParams &p) {
+  const int n = L.num_items;
+  const psd_work_item *it = L.items_host;
+  std::vector<int64_t> c(static_cast<size_t>(n));
+  std::vector<int32_t> ntl(static_cast<size_t>(n));
+  std::vector<char> first(static_cast<size_t>(n)), writes(static_cast<size_t>(n)), split_ok(static_cast<size_t>(n));
+  int64_t total = 0, cmax = 0;
+  for (int i = 0; i < n; ++i) {
+    const size_t k = size_t(i);
+    ntl[k] = it[i].n_tokens > 0 ? (it[i].n_tokens + kTokM - 1) / kTokM : 0;
+    first[k] = i == 0 || it[i - 1].q_index != it[i].q_index;
+    const bool cont_next = i + 1 < n && it[i + 1].q_index == it[i].q_index &&
+                           it[i + 1].out_row == it[i].out_row + 1 && it[i].n_tokens > 0 && it[i + 1].n_tokens > 0;
+    writes[k] = !L.merge_runs || !cont_next;
+    split_ok[k] = L.merge_runs && i > 0 && ntl[k] >= 2 && it[i - 1].n_tokens > 0 &&
+                  it[i - 1].q_index == it[i].q_index && it[i].out_row == it[i - 1].out_row + 1;
+    c[k] = ntl[k] > 0 ? int64_t(ntl[k]) * kTokM + (writes[k] ? kItemCostTok : 0) + (first[k] ? kSplitCostTok : 0) : 0;
+    total += c[k];
+    cmax = std::max(cmax, c[k]);
+  }
+  // Greedy fill under bound B; returns the number of runs (pairs + 1 when B is too
+  // small) and, when `rec`, the run starts.
+  auto fill = [&](int64_t B, bool rec) {
+    int runs = 1, start = 0;
+    int64_t acc = 0;
+    if (rec) {
+      p.run_item[0] = 0;
+      p.run_tile[0] = 0;
+    }
+    for (int i = 0; i < n; ++i) {
+      const size_t k = size_t(i);
+      if (acc + c[k] <= B || i == start) {
+        acc += c[k];
+        continue;
+      }
+      int tiles = 0;  // tiles of item i that stay in this run
+      if (split_ok[k] && i - 1 >= start) {
+        const int64_t room = B - acc - kItemCostTok - (first[k] ? kSplitCostTok : 0);
+        tiles = room >= kTokM ? int(std::min<int64_t>(room / kTokM, ntl[k] - 1)) : 0;
+      }
+      if (runs == pairs) return pairs + 1;
+      if (rec) {
+        p.run_item[runs] = i;
+        p.run_tile[runs] = tiles;
+      }
+      ++runs;
+      start = i;
+      acc = tiles > 0 ? int64_t(ntl[k] - tiles) * kTokM + (writes[k] ? kItemCostTok : 0) + kSplitCostTok
+                      : c[k] + (first[k] ? 0 : kSplitCostTok);
+    }
+    if (rec)
+      for (int x = runs; x <= pairs; ++x) {
+        p.run_item[x] = n;
+        p.run_tile[x] = 0;
+      }
+    return runs;
+  };
+  const int64_t mean = (total + pairs - 1) / pairs;
+  int64_t lo = std::max(mean, cmax), hi = mean + cmax + kItemCostTok + kSplitCostTok;
+  while (lo < hi) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (fill(mid, false) <= pairs) hi = mid;
+    else lo = mid + 1;
+  }
+  fill(lo, true);
+  p.has_runs = 1;
+}
+
 bool partial_mla_supports(const PartialLaunch &L) {
   return L.latent_v && L.kv_dtype == PSD_FP8_E4M3 && L.Dqk == kDqkM && L.Dv == kDvM &&
          L.G_cta == kRowsM && L.Hq_req == kRowsM && L.Hkv == 1 && L.page_size % kTokM == 0 &&
@@ -738,6 +846,8 @@ psd_status launch_partial_mla(const PartialLaunch &L, const DeviceInfo &dev, cud
   if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   // persistent: one CTA pair per two SMs, each pair a token-balanced run of items
   const int pairs = std::max(1, std::min(L.num_items, dev.num_sms / 2));
+  p.has_runs = 0;
+  if (L.items_host && pairs <= kMaxPairs) plan_runs(L, pairs, p);
   const dim3 grid(static_cast<unsigned>(pairs), 1, 2);
   partial_mla_kernel<<<grid, kThreadsM, kSmemMLA, s>>>(tmQ, tmK, p);
   e = cudaGetLastError();
