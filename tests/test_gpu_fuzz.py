@@ -1,0 +1,50 @@
+"""Seeded random configurations of the decode path on the GPU against the float64
+oracle: batch, head counts, head dims, page size, tile, pool dtype, ragged lengths
+and optional shared prefixes (mlxcel PR #1004, Decomposition, Merge contract and
+Detection sections; ROCm ATOM PR #1701 section 3.2 for the fp8 pool).  Every case
+goes through psd_plan_decode and cascade_decode, flat or cascade as the planner
+decides."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import attention as A
+from _gpu_util import Dev, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    D = int(rng.choice([64, 128, 256]))
+    P = int(rng.choice([16, 32, 64]))
+    tile = P * int(rng.choice([1, 2, 4, 8]))
+    kv_dtype = "fp8_e4m3" if rng.random() < 0.3 else "bf16"
+    if kv_dtype == "fp8_e4m3" and D == 256:  # (fp8 pools with separate K and V take D <= 128)
+        D = 128
+    B = int(rng.integers(1, 13))
+    lengths = [int(x) for x in rng.integers(1, 1500, size=B)]
+    shared = None
+    if B >= 3 and rng.random() < 0.5:
+        members = sorted(int(m) for m in rng.choice(B, size=int(rng.integers(2, B + 1)), replace=False))
+        sp = int(rng.integers(1, 6))
+        for m in members:                       # a member needs a page after the shared span
+            lengths[m] = max(lengths[m], sp * P + int(rng.integers(1, 3 * P)))
+        shared = (members, sp)
+    pages = sum((L + P - 1) // P for L in lengths) + 8
+    w = synth._make(f"fuzz{seed}", rng, lengths, Hq=Hkv * G, Hkv=Hkv, Dqk=D, Dv=D, page_size=P,
+                    num_pages=pages, tile_tokens=tile, kv_dtype=kv_dtype, shared=shared,
+                    min_shared_pages=1, min_members=2)
+    return w
+
+
+@pytest.mark.parametrize("seed", list(range(48)))
+def test_random_decode_configurations(seed):
+    w = _case(seed)
+    o, lse, stats, plan = Dev(w).decode(enable=1, with_stats=True)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, w.kv_dtype,
+                 f"seed {seed}: B={w.batch} Hkv={w.Hkv} G={w.Hq // w.Hkv} D={w.Dqk} P={w.page_size} "
+                 f"tile={w.tile_tokens} {w.kv_dtype} path={stats['path']}")
