@@ -169,8 +169,10 @@ psd_status psd_destroy(psd_ctx *ctx);
  * TENSOR_CORE: the 16-row-group tensor-core kernel (QK^T and PV as m16n8k16
  * MMAs; the stacked level-0 rows are split into groups of 16).  CUDA_CORE: the
  * CUDA-core kernel wherever it applies (G <= 8 rows per KV head; warp-shuffle
- * reductions and f32x2 FMAs).  Both compute the same partials.  fp8 pools and the
- * shared MLA latent always use the 64-row tensor-core kernel. */
+ * reductions and f32x2 FMAs).  Both compute the same partials.  fp8 pools with
+ * separate K and V (head dims 64, 128, 256) use the 64-row mma.sync kernel; the
+ * fp8 MLA latent (128 heads over a 576-wide latent, V its first 512 columns) uses
+ * the tcgen05 kernel, or the 64-row kernel when CUDA_CORE is selected. */
 typedef enum { PSD_KERNEL_AUTO = 0, PSD_KERNEL_CUDA_CORE = 1, PSD_KERNEL_TENSOR_CORE = 2 } psd_partial_kernel;
 psd_status psd_set_partial_kernel(psd_ctx *ctx, int32_t kind);
 /* Kernel timing, for measurement: when enabled, paged_decode_partial and

@@ -371,7 +371,8 @@ psd_status launch_tc(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t
 bool partial_tc_supports(const PartialLaunch &p) {
   const bool fp8 = p.kv_dtype == PSD_FP8_E4M3;
   if (p.latent_v) return p.Dqk == 576 && p.Dv == 512;
-  return p.Dqk == p.Dv && (p.Dqk == 64 || p.Dqk == 128 || (!fp8 && p.Dqk == 256));
+  (void)fp8;
+  return p.Dqk == p.Dv && (p.Dqk == 64 || p.Dqk == 128 || p.Dqk == 256);
 }
 
 psd_status launch_partial_tc(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
@@ -384,7 +385,7 @@ psd_status launch_partial_tc(const PartialLaunch &L, const DeviceInfo &dev, cuda
     switch (L.Dqk) {
       case 64: return fp8 ? launch_tc<64, 64, true, false>(L, dev, s) : launch_tc<64, 64, false, false>(L, dev, s);
       case 128: return fp8 ? launch_tc<128, 128, true, false>(L, dev, s) : launch_tc<128, 128, false, false>(L, dev, s);
-      case 256: if (!fp8) return launch_tc<256, 256, false, false>(L, dev, s); break;
+      case 256: return fp8 ? launch_tc<256, 256, true, false>(L, dev, s) : launch_tc<256, 256, false, false>(L, dev, s);
       default: break;
     }
   }

@@ -22,8 +22,6 @@ def _case(seed):
     P = int(rng.choice([16, 32, 64]))
     tile = P * int(rng.choice([1, 2, 4, 8]))
     kv_dtype = "fp8_e4m3" if rng.random() < 0.3 else "bf16"
-    if kv_dtype == "fp8_e4m3" and D == 256:  # (fp8 pools with separate K and V take D <= 128)
-        D = 128
     B = int(rng.integers(1, 13))
     lengths = [int(x) for x in rng.integers(1, 1500, size=B)]
     shared = None
