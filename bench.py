@@ -464,6 +464,28 @@ def host_plan_us(w, reps=200):
             "note": "per call, through the Python binding"}
 
 
+def large_flat_timing(args, flush, hbm: float):
+    """The flat workload's shapes with four times the requests (128, 1.2 GB of K/V):
+    the partial kernel's rate when a launch's fixed ramp and tail weigh less."""
+    w = synth.flat_decode(seed=0, canary=False, batch=128, num_pages=65536)
+    arm = Arm(w, enable=0)
+    arm.step()
+    arm.check()
+    t = statistics.mean(time_steps(arm.step, args.steps, args.warmup, flush))
+    kt = kernel_timing(arm, args.steps, args.warmup, flush)
+    algo = partial_algorithmic_bytes(arm)
+    uniq = unique_kv_bytes(w)
+    out = {"workload": "flat paged decode, 128 requests (otherwise the flat workload), 65536-page pool",
+           "ms": round(t, 5), "unique_kv_gbs": round(uniq / (t * 1e-3) / 1e9, 1),
+           "frac_of_measured_hbm": round(uniq / (t * 1e-3) / 1e9 / hbm, 4),
+           "partial_ms": round(kt["partial_ms"], 5),
+           "partial_gbs": round(algo / (kt["partial_ms"] * 1e-3) / 1e9, 1),
+           "partial_frac_of_measured_hbm": round(algo / (kt["partial_ms"] * 1e-3) / 1e9 / hbm, 4),
+           "algorithmic_bytes_per_launch": int(algo)}
+    del arm
+    return out
+
+
 def cascade_comparison(wc, label, args, flush, plan_us=False):
     """Flat arm vs cascade arm on one batch: step times, per-kernel times and the
     criterion (T_flat - T_casc) / T_flat >= 0.7 x the fraction of K/V reads removed."""
@@ -575,6 +597,8 @@ def run_ours(args):
         extra["merge_sweep"] = merge_sweep(arm.ctx, args.steps, args.warmup, flush, hbm, sizes)
     if not args.quick and args.workload in ("all", "cascade", "nested"):
         extra["nested"] = nested_timing(args.steps, args.warmup, flush)
+    if not args.quick and args.workload in ("all", "large"):
+        extra["flat_decode_128_requests"] = large_flat_timing(args, flush, hbm)
     if not args.quick and args.workload in ("all", "tune"):
         extra["autotune"] = autotune_report(arm, max(3, args.steps // 4))
     if not args.quick and args.workload in ("all", "append"):
@@ -680,7 +704,7 @@ def main():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--quick", action="store_true", help="flat workload only")
-    p.add_argument("--workload", choices=["all", "cascade", "mla", "merge", "append", "nested", "tune"],
+    p.add_argument("--workload", choices=["all", "cascade", "mla", "merge", "append", "nested", "tune", "large"],
                    default="all",
                    help="which workloads run after the flat headline")
     p.add_argument("--mla-batch", type=int, default=128, help="requests in the MLA workload")

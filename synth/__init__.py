@@ -258,14 +258,14 @@ def tiny_cascade(seed: int = 0, canary: bool = True) -> Workload:
                  canary=canary, min_shared_pages=4, min_members=2)
 
 
-def flat_decode(seed: int = 0, canary: bool = True, batch: int = 32) -> Workload:
+def flat_decode(seed: int = 0, canary: bool = True, batch: int = 32, num_pages: int = 16384) -> Workload:
     """32 requests, Hq=32, Hkv=8, D=128, page 16, lengths U[512,4096] with a partial
     last page, random permutation of a 16384-page pool, tile 512 tokens."""
     rng = np.random.default_rng(seed)
     P = 16
     lengths = lengths_with_partial_last_page(rng, batch, 512, 4096, P)
     return _make("flat_decode", rng, lengths, Hq=32, Hkv=8, Dqk=128, Dv=128, page_size=P,
-                 num_pages=16384, tile_tokens=512, canary=canary)
+                 num_pages=num_pages, tile_tokens=512, canary=canary)
 
 
 def cascade_decode(seed: int = 0, canary: bool = True, members: int = 16,

@@ -314,3 +314,15 @@ def test_outputs_into_pinned_host_memory(maker):
     torch.cuda.synchronize()
     assert psd.check_device_error(ctx(), ws) == 0
     assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu())
+
+
+@pytest.mark.slow
+def test_flat_decode_128_requests_sampled():
+    """The flat workload with 128 requests (the bench's large-batch arm, 1.2 GB of
+    K/V): sampled requests against the oracle, every output finite."""
+    w = synth.flat_decode(seed=0, batch=128, num_pages=65536)
+    o, lse = Dev(w).decode(enable=0)
+    req = [0, 37, 90, 127, int(np.argmax(w.lengths))]
+    ro, rl = A.decode_attention(A.workload_arrays(w), requests=req)
+    assert_close(o[req], lse[req], ro[req], rl[req], "bf16", "flat, 128 requests")
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
