@@ -736,8 +736,6 @@ bool encode_latent_map(CUtensorMap *map, const DeviceInfo &dev, const void *pool
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
 // The pairs' runs: contiguous stretches of the item list that minimise the largest
 // run cost (binary search on the bound, greedy fill), in the cost units of the
 // in-kernel partition, plus an O write-out for a run that ends inside a request and
@@ -812,6 +810,8 @@ void plan_runs(const PartialLaunch &L, int pairs, MLAParams &p) {
   fill(lo, true);
   p.has_runs = 1;
 }
+
+}  // namespace
 
 bool partial_mla_supports(const PartialLaunch &L) {
   return L.latent_v && L.kv_dtype == PSD_FP8_E4M3 && L.Dqk == kDqkM && L.Dv == kDvM &&
