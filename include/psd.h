@@ -489,7 +489,8 @@ psd_status rope_append_kv(psd_ctx *ctx, const psd_rope_append_args *args, psd_st
  * The word (the workspace's first 8 bytes) is tagged with the call that wrote it:
  * only faults of this context's latest decode call on `workspace` are reported, so
  * nothing has to clear it between calls and a fresh workspace needs no
- * initialisation.  A reported fault is cleared. */
+ * initialisation.  The context remembers its 64 most recently used workspaces;
+ * an older one reads as clean.  A reported fault is cleared. */
 psd_status psd_check_device_error(psd_ctx *ctx, void *workspace, psd_stream_t stream,
                                   int32_t *fault_bits);
 

@@ -801,8 +801,8 @@ extern "C" psd_status psd_check_device_error(psd_ctx *ctx, void *workspace, psd_
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "psd_check_device_error: %s", cudaGetErrorString(e));
   // only the bits of this context's latest call on the workspace count
-  const auto it = ctx->ws_epoch.find(workspace);
-  const bool latest = it != ctx->ws_epoch.end() && it->second == uint32_t(word >> 32);
+  const int slot = ctx->epoch_slot(workspace);
+  const bool latest = slot >= 0 && ctx->ws_epoch[slot] == uint32_t(word >> 32);
   const int32_t flag = latest ? int32_t(uint32_t(word)) : 0;
   if (fault_bits) *fault_bits = flag;
   if (flag) {

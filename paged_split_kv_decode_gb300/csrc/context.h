@@ -5,7 +5,6 @@
 
 #include <array>
 #include <map>
-#include <unordered_map>
 
 #include "kernels.h"
 #include "psd_internal.h"
@@ -35,9 +34,19 @@ struct psd_ctx {
   void *flush = nullptr;
   size_t flush_bytes = 0;
   // Fault-word epochs: a counter advanced by every decode call, and the epoch of the
-  // latest call on each workspace (what psd_check_device_error compares against).
+  // latest call on each of the last kEpochSlots workspaces used (what
+  // psd_check_device_error compares against; an older workspace reads as clean).
+  static constexpr int kEpochSlots = 64;
   uint32_t epoch = 0;
-  std::unordered_map<const void *, uint32_t> ws_epoch;
+  const void *ws_ptr[kEpochSlots] = {};
+  uint32_t ws_epoch[kEpochSlots] = {};
+  int ws_next = 0;
+  // the slot of workspace `ws`, or -1
+  int epoch_slot(const void *ws) const {
+    for (int i = 0; i < kEpochSlots; ++i)
+      if (ws_ptr[i] == ws) return i;
+    return -1;
+  }
 };
 
 namespace psd {
@@ -45,7 +54,13 @@ namespace psd {
 // the workspace's latest.
 inline FaultRef next_fault(psd_ctx *c, void *ws) {
   if (++c->epoch == 0) c->epoch = 1;
-  c->ws_epoch[ws] = c->epoch;
+  int i = c->epoch_slot(ws);
+  if (i < 0) {
+    i = c->ws_next;
+    c->ws_next = (c->ws_next + 1) % psd_ctx::kEpochSlots;
+    c->ws_ptr[i] = ws;
+  }
+  c->ws_epoch[i] = c->epoch;
   return FaultRef{static_cast<unsigned long long *>(ws), c->epoch};
 }
 // Records timing event `i` (0..5) of the context on stream `s` when timing is on.
