@@ -46,3 +46,35 @@ def test_random_decode_configurations(seed):
     assert_close(o, lse, ro, rl, w.kv_dtype,
                  f"seed {seed}: B={w.batch} Hkv={w.Hkv} G={w.Hq // w.Hkv} D={w.Dqk} P={w.page_size} "
                  f"tile={w.tile_tokens} {w.kv_dtype} path={stats['path']}")
+
+
+def _mla_case(seed):
+    rng = np.random.default_rng(2000 + seed)
+    P = int(rng.choice([64, 128]))
+    tile = int(rng.choice([64, 128, 256, 512, 2048]))
+    tile = max(tile, P)
+    B = int(rng.integers(1, 13))
+    lengths = [int(x) for x in rng.integers(1, 6000, size=B)]
+    pages = sum((L + P - 1) // P for L in lengths) + 4
+    return synth._make(f"mla_fuzz{seed}", rng, lengths, Hq=128, Hkv=1, Dqk=576, Dv=512, page_size=P,
+                       num_pages=pages, tile_tokens=tile, kv_dtype="fp8_e4m3", latent_v=True)
+
+
+@pytest.mark.parametrize("seed", list(range(12)))
+def test_random_mla_configurations(seed):
+    """MLA decode over random batches, lengths, tiles and page sizes: the persistent
+    kernel's runs are planned on the host and split inside items at tile boundaries
+    (rows feed the merge), so both the merged outputs and the per-chunk partials are
+    checked against the oracle."""
+    from _gpu_util import oracle_partials
+    w = _mla_case(seed)
+    d = Dev(w)
+    o, lse = d.decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "fp8_e4m3",
+                 f"MLA seed {seed}: B={w.batch} P={w.page_size} tile={w.tile_tokens}")
+    if w.batch <= 4:
+        v, l, _, o_indptr = d.partials()
+        rv, rlp, rind = oracle_partials(w)
+        assert o_indptr.tolist() == rind
+        assert_close(v, l, rv, rlp, "fp8_e4m3", f"MLA partials seed {seed}")
