@@ -107,12 +107,19 @@ typedef struct {
   int32_t out_row;
 } psd_work_item;
 
-/* Problem description shared by paged_decode_partial and cascade_decode. */
+/* Problem description shared by paged_decode_partial and cascade_decode.
+ * q and page_indices_dev may also be pinned host memory (cudaHostAlloc or
+ * cudaHostRegister, same pointer on host and device).  The partial kernels then read
+ * the query rows and page ids over the host link as they run.  No separate
+ * host-to-device copy is needed, and a step reads each query row once per work item
+ * and KV head.  The host must not write them until the call's stream work has
+ * finished.  The MLA latent kernel loads q by TMA and takes device q only; with host
+ * q it returns PSD_ERR_UNSUPPORTED before it launches. */
 typedef struct {
-  const void *q;                   /* device [batch, Hq, Dqk] bf16 */
+  const void *q;                   /* [batch, Hq, Dqk] bf16, device or pinned host */
   const void *k_pool;              /* device [num_pages, page_size, Hkv, Dqk] */
   const void *v_pool;              /* device [num_pages, page_size, Hkv, Dv], or k_pool */
-  const int32_t *page_indices_dev; /* device copy of the page table's page_indices */
+  const int32_t *page_indices_dev; /* the page table's page_indices, device or pinned host */
   int64_t num_page_indices;        /* length of page_indices_dev (nnz) */
   int64_t num_pages;
   int32_t batch, Hq, Hkv, Dqk, Dv, page_size;

@@ -38,14 +38,20 @@ def _dev_ptr(t: torch.Tensor, name: str) -> int:
     return t.data_ptr()
 
 
-def _out_ptr(t: torch.Tensor, name: str) -> int:
-    """Decode outputs may be CUDA tensors or pinned host tensors (the merge kernel then
-    stores into host memory over the host link; the pointer is the same on both sides)."""
+def _dev_or_pinned_ptr(t: torch.Tensor, name: str) -> int:
+    """A CUDA tensor, or a pinned host tensor the kernels reach over the host link
+    (the pointer is the same on both sides)."""
     if isinstance(t, torch.Tensor) and t.device.type == "cpu" and t.is_pinned():
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
         return t.data_ptr()
     return _dev_ptr(t, name)
+
+
+def _out_ptr(t: torch.Tensor, name: str) -> int:
+    """Decode outputs may be pinned host tensors: the merge kernel then stores them
+    into host memory directly."""
+    return _dev_or_pinned_ptr(t, name)
 
 
 def kv_dtype_code(t: torch.Tensor) -> int:
@@ -376,14 +382,16 @@ def workspace_bytes(batch: int, num_items: int, num_rows: int, Hq: int, Dv: int)
 def decode_args(q, k_pool, v_pool, page_indices_dev, *, num_pages: int, page_size: int,
                 Hkv: int, Dv: int, sm_scale: float, k_scale: float = 1.0,
                 v_scale: float = 1.0) -> L.DecodeArgs:
-    """psd_decode_args from device tensors (v_pool is k_pool for a shared latent)."""
+    """psd_decode_args from device tensors (v_pool is k_pool for a shared latent).
+    q and page_indices may instead be pinned host tensors, read by the partial kernels
+    over the host link (not by the MLA latent kernel, which takes device q)."""
     a = L.DecodeArgs()
-    a.q = _dev_ptr(q, "q")
+    a.q = _dev_or_pinned_ptr(q, "q")
     a.k_pool = _dev_ptr(k_pool, "k_pool")
     a.v_pool = _dev_ptr(v_pool, "v_pool")
     if page_indices_dev.dtype != torch.int32:
         raise ValueError("page_indices must be int32")
-    a.page_indices_dev = _dev_ptr(page_indices_dev, "page_indices")
+    a.page_indices_dev = _dev_or_pinned_ptr(page_indices_dev, "page_indices")
     a.num_page_indices = int(page_indices_dev.numel())
     a.num_pages = int(num_pages)
     a.batch, a.Hq, a.Dqk = (int(x) for x in q.shape)

@@ -823,6 +823,13 @@ psd_status launch_partial_mla(const PartialLaunch &L, const DeviceInfo &dev, cud
   if (L.num_items == 0) return PSD_OK;
   if (size_t(dev.smem_optin) < kSmemMLA)
     return fail(PSD_ERR_UNSUPPORTED, "MLA tcgen05 partial needs %u bytes of shared memory", kSmemMLA);
+  // The query rows arrive by TMA, which this kernel points at device memory only.
+  cudaPointerAttributes qa;
+  if (cudaPointerGetAttributes(&qa, L.q) != cudaSuccess || (qa.type != cudaMemoryTypeDevice &&
+                                                           qa.type != cudaMemoryTypeManaged)) {
+    (void)cudaGetLastError();
+    return fail(PSD_ERR_UNSUPPORTED, "the MLA tcgen05 partial takes q in device memory only");
+  }
   CUtensorMap tmQ, tmK;
   if (!encode_q_map(&tmQ, dev, L.q, L.q_batch, L.Hq_req))
     return fail(PSD_ERR_CUDA, "cuTensorMapEncodeTiled failed for q");

@@ -316,6 +316,42 @@ def test_outputs_into_pinned_host_memory(maker):
     assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu())
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("maker", [synth.tiny_cascade, synth.flat_decode, synth.cascade_decode])
+def test_inputs_from_pinned_host_memory(maker, kernel):
+    """cascade_decode with q and page_indices in pinned host memory (read by the
+    partial kernels over the host link) and the outputs in pinned host memory: equal
+    bit for bit to the all-device call, on flat and cascade plans."""
+    w = maker(seed=5)
+    d = Dev(w)
+    plan = psd.plan_decode(d.table, w.tile_tokens, 1, w.min_shared_pages, w.min_members)
+    ws = psd.workspace_for(plan, w.Hq, w.Dv, "cuda")
+    o = torch.empty((w.batch, w.Hq, w.Dv), device="cuda")
+    lse = torch.empty((w.batch, w.Hq), device="cuda")
+    qh = w.q.contiguous().pin_memory()
+    ih = d.indices.cpu().pin_memory()
+    args_h = psd.decode_args(qh, d.k, d.v, ih, num_pages=w.num_pages, page_size=w.page_size,
+                             Hkv=w.Hkv, Dv=w.Dv, sm_scale=w.sm_scale, k_scale=w.k_scale,
+                             v_scale=w.v_scale)
+    oh = torch.full((w.batch, w.Hq, w.Dv), float("nan")).pin_memory()
+    lh = torch.full((w.batch, w.Hq), float("nan")).pin_memory()
+    with use_kernel(kernel):
+        psd.cascade_decode(ctx(), d.args(), plan, o, lse, ws)
+        psd.cascade_decode(ctx(), args_h, plan, oh, lh, ws)
+    torch.cuda.synchronize()
+    assert psd.check_device_error(ctx(), ws) == 0
+    assert (plan.num_members > 0) == (maker is not synth.flat_decode)
+    assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu())
+
+
+def test_pageable_host_query_is_rejected_by_the_binding():
+    w = synth.tiny_cascade(seed=0)
+    d = Dev(w)
+    with pytest.raises(ValueError):
+        psd.decode_args(w.q.contiguous(), d.k, d.v, d.indices, num_pages=w.num_pages,
+                        page_size=w.page_size, Hkv=w.Hkv, Dv=w.Dv, sm_scale=w.sm_scale)
+
+
 @pytest.mark.slow
 def test_flat_decode_128_requests_sampled():
     """The flat workload with 128 requests (the bench's large-batch arm, 1.2 GB of

@@ -58,6 +58,31 @@ def _mla_small(seed, lengths, page_size=64, num_pages=512, tile=2048):
                        num_pages=num_pages, tile_tokens=tile, kv_dtype="fp8_e4m3", latent_v=True)
 
 
+def test_mla_takes_device_query_only():
+    """The MLA kernel loads q by TMA: pinned host q is refused with
+    PSD_ERR_UNSUPPORTED before any launch, and the same call with device q and host
+    page ids runs and matches the oracle."""
+    w = _mla_small(12, [300, 2500])
+    d = Dev(w)
+    plan = psd.plan_decode(d.table, w.tile_tokens, 0, w.min_shared_pages, w.min_members)
+    ws = psd.workspace_for(plan, w.Hq, w.Dv, "cuda")
+    o = torch.empty((w.batch, w.Hq, w.Dv), device="cuda")
+    lse = torch.empty((w.batch, w.Hq), device="cuda")
+    ih = d.indices.cpu().pin_memory()
+    mk = lambda q: psd.decode_args(q, d.k, d.v, ih, num_pages=w.num_pages, page_size=w.page_size,
+                                   Hkv=w.Hkv, Dv=w.Dv, sm_scale=w.sm_scale, k_scale=w.k_scale,
+                                   v_scale=w.v_scale)
+    with pytest.raises(psd.PsdError) as e:
+        psd.cascade_decode(ctx(), mk(w.q.contiguous().pin_memory()), plan, o, lse, ws)
+    assert e.value.status == 2 and "device memory" in str(e.value)
+    psd.cascade_decode(ctx(), mk(d.q), plan, o, lse, ws)
+    torch.cuda.synchronize()
+    assert psd.check_device_error(ctx(), ws) == 0
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o.cpu().double().numpy(), lse.cpu().double().numpy(), ro, rl, "fp8_e4m3",
+                 "MLA, host page ids")
+
+
 @pytest.mark.parametrize("page_size", [64, 128])
 def test_mla_ragged_tails_and_short_items(page_size):
     """Items of 1 to 2049 tokens: single-token and one-short tiles, whole pages, an
