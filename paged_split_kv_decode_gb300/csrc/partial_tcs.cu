@@ -11,20 +11,30 @@
 // shuffles and cannot keep up with HBM, while one m16n8k16 MMA covers 16 tokens x
 // 16 dims for all G rows (padded to 16) in one issue slot.
 //
-// GB300 shape: grid = (work items, Hkv, row groups of 16), 4 warps, 3 CTAs per
-// SM (row groups of one item re-read its K/V tiles from L2, not HBM).  Warp w streams
-// 16-token tiles w, w+4, ... of the item through a private 2-stage ring; each
-// stage is 16 slots of one page loaded by TMA in 64-column boxes with the 128-byte
-// swizzle, so ldmatrix reads are bank-conflict free.  Per tile and warp: S = Q K^T
-// (D/16 x 2 MMAs, Q fragments held in registers), online softmax on the
-// accumulator fragments, P re-packed as the A operand, O += P V (D/8 MMAs, V via
-// transposed ldmatrix).  The four warp states merge through shared memory.
+// GB300 shape: grid = (work items, Hkv, blocks of up to 64 rows), 4 warps, 3 CTAs
+// per SM.  Each tile is 16 slots of one page loaded by TMA in 64-column boxes with
+// the 128-byte swizzle, so ldmatrix reads are bank-conflict free.  Per tile and
+// warp: S = Q K^T (D/16 x 2 MMAs, Q fragments held in registers), online softmax on
+// the accumulator fragments, P re-packed as the A operand, O += P V (D/8 MMAs, V
+// via transposed ldmatrix).  Two ways to spread a CTA's work over its warps:
+//   - up to 48 rows (small query groups): one CTA per 16-row group, in which warp
+//     w streams tiles w, w+4, ... through a private 2-stage ring and the four warp
+//     states merge through shared memory;
+//   - more rows (stacked level-0 rows, large groups): one CTA per block of 64 rows,
+//     in which warp w owns rows 16w..16w+15 and every warp consumes every tile of
+//     one CTA-wide 8-stage ring, so a tile crosses from L2 to the SM once for 64
+//     rows, not once per 16.  The last warp to release a stage refills it.  With
+//     only 2 or 3 groups the per-group CTAs win: a block would leave warps idle.
+//     A block's CTA runs four times as long as a group's, so the launch takes the
+//     blocks only when they fill at least one wave of resident CTAs; fewer, longer
+//     CTAs would set the launch's tail.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstring>
+#include <type_traits>
 
 #include "device.cuh"
 #include "kernels.h"
@@ -36,6 +46,7 @@ namespace {
 constexpr int kWarpsS = 4;
 constexpr int kStagesS = 2;
 constexpr int kTileTok = 16;
+constexpr float kLazyRescale = 8.f;  // log2 units
 
 struct TCSParams {
   const __nv_bfloat16 *q;
@@ -58,6 +69,7 @@ struct TCSParams {
   // from seg_member0[s].  The rest take level-1 items l1_base + order[...].  A plain
   // launch has n_l0_tasks = 0 and l1_base = 0.
   int n_l0_tasks, l1_base, nseg;
+  int allow_shared;  // rows > 48 take 64-row blocks (the shared-tile form)
   int seg_task_end[PartialLaunch::kMaxFusedSegments], seg_item0[PartialLaunch::kMaxFusedSegments];
   int seg_rows[PartialLaunch::kMaxFusedSegments], seg_member0[PartialLaunch::kMaxFusedSegments];
   float q_scale, v_scale;
@@ -74,6 +86,29 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
+}
+// The same two loads at a compile-time byte offset from `addr` (folded into the
+// instruction's address).
+template <int OFF>
+__device__ __forceinline__ void ldsm_x4_at(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                           uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4 + %5];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr), "n"(OFF));
+}
+template <int OFF>
+__device__ __forceinline__ void ldsm_x4_t_at(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                             uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4 + %5];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr), "n"(OFF));
+}
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F &&f) {
+  if constexpr (N > 0) {
+    static_for<N - 1>(f);
+    f(std::integral_constant<int, N - 1>{});
+  }
 }
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -92,6 +127,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // of 16 rows x 128 bytes with the 128-byte swizzle (16-byte chunk index XOR row%8).
 __device__ __forceinline__ uint32_t sw128(int row, int col8) {
   return uint32_t((col8 >> 3) * (kTileTok * 128) + row * 128 + (((col8 & 7) ^ (row & 7)) << 4));
+}
+
+// CTAs per (item, KV head) for `rows` query rows: one per 16-row group (the
+// private form), or, where the launch allows it and there are more than 3 groups,
+// one per block of up to 4 groups (the shared-tile form).
+__host__ __device__ __forceinline__ bool tcs_shared_tiles(int rows, bool allow) { return allow && rows > 48; }
+__host__ __device__ __forceinline__ int tcs_blocks(int rows, bool allow) {
+  const int groups = (rows + 15) >> 4;
+  return tcs_shared_tiles(rows, allow) ? (groups + kWarpsS - 1) / kWarpsS : groups;
 }
 
 // CAP > 0: the work lists come in the launch's parameters (`lists`, CAP bytes), not
@@ -124,34 +168,50 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
     if constexpr (INL) return *a;
     else return __ldg(a);
   };
-  int item_index, group, G_rows, member0 = 0;
+  int item_index, block, G_rows, member0 = 0;
   if (int(blockIdx.x) < p.n_l0_tasks) {
     const int task = int(blockIdx.x);
     int sg = 0;
     while (sg + 1 < p.nseg && task >= p.seg_task_end[sg]) ++sg;
     const int local = task - (sg ? p.seg_task_end[sg - 1] : 0);
-    const int rg = (p.seg_rows[sg] + 15) >> 4;
-    item_index = p.seg_item0[sg] + local / rg;
-    group = local - (local / rg) * rg;
+    const int cpi = tcs_blocks(p.seg_rows[sg], p.allow_shared);
+    item_index = p.seg_item0[sg] + local / cpi;
+    block = local - (local / cpi) * cpi;
     G_rows = p.seg_rows[sg];
     member0 = p.seg_member0[sg];
   } else {
     const int j = blockIdx.x - p.n_l0_tasks;
     item_index = p.l1_base + (order ? ld_list(order + j) : j);
-    group = blockIdx.z;
+    block = blockIdx.z;
     G_rows = p.G_cta;
   }
   const psd_work_item it = items[item_index];
   const int kv = blockIdx.y;
-  const int row0 = group * 16;  // this CTA's 16-row group of the KV head's rows
+  // Shared-tile form: warp w owns rows row0 .. row0 + 15 of the block's 64; warps
+  // past the last row group only take part in the barrier set-up.
+  const bool shared_tiles = tcs_shared_tiles(G_rows, p.allow_shared);
+  const int row0 = shared_tiles ? block * 16 * kWarpsS + 16 * warp : block * 16;
   const int rows = min(16, G_rows - row0);
+  const int n_active = shared_tiles ? min(kWarpsS, ((G_rows + 15) >> 4) - block * kWarpsS) : kWarpsS;
   const int P = p.page_size;
   const int TPP = P / kTileTok;
   const size_t ring_total = size_t(kWarpsS) * kStagesS * 2 * TILE_BYTES;
   const size_t red_total = size_t(kWarpsS) * 16 * (D + 2) * sizeof(float);
-  uint8_t *ring = base + size_t(warp) * kStagesS * 2 * TILE_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(base + (ring_total > red_total ? ring_total : red_total)) +
-                   warp * kStagesS;
+  uint64_t *bars_all = reinterpret_cast<uint64_t *>(base + (ring_total > red_total ? ring_total : red_total));
+  uint32_t *released = reinterpret_cast<uint32_t *>(bars_all + kWarpsS * kStagesS);  // shared form
+  uint8_t *ring = shared_tiles ? base : base + size_t(warp) * kStagesS * 2 * TILE_BYTES;
+  uint64_t *bars = shared_tiles ? bars_all : bars_all + warp * kStagesS;
+  if (shared_tiles) {
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < kWarpsS * kStagesS; ++s) {
+        mbar_init(smem_u32(&bars_all[s]), 1);
+        released[s] = 0u;
+      }
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp >= n_active) return;
+  }
 
   // ---- Q fragments (rows >= G_cta are zero), pre-scaling is applied to S
   uint32_t qa[KSTEPS][4];
@@ -179,7 +239,8 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
   }
 
   const int n_tiles = (it.n_tokens + kTileTok - 1) / kTileTok;
-  const int my_tiles = n_tiles > warp ? (n_tiles - warp + kWarpsS - 1) / kWarpsS : 0;
+  const int my_tiles = shared_tiles ? n_tiles
+                                    : (n_tiles > warp ? (n_tiles - warp + kWarpsS - 1) / kWarpsS : 0);
   const int n_item_pages = (it.n_tokens + P - 1) / P;
   const uint64_t pol = l2_evict_first_policy();
   auto tile_pos = [&](int t) { return p.tpp_log2 >= 0 ? t >> p.tpp_log2 : t / TPP; };
@@ -197,16 +258,21 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
     return __shfl_sync(0xffffffffu, pid, pos - win);
   };
 
-  if (lane == 0) {
+  if (!shared_tiles) {
+    if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < kStagesS; ++s) mbar_init(smem_u32(&bars[s]), 1);
-    fence_mbar_init();
+      for (int s = 0; s < kStagesS; ++s) mbar_init(smem_u32(&bars[s]), 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
   }
-  __syncwarp();
+  // stages of the ring this warp reads, and the tile of the item its i-th use holds
+  const int n_stages = shared_tiles ? kWarpsS * kStagesS : kStagesS;
+  auto tile_of = [&](int i) { return shared_tiles ? i : warp + i * kWarpsS; };
 
   auto issue = [&](int i) {  // all lanes call; lane 0 issues
-    const int s = i % kStagesS;
-    const int t = warp + i * kWarpsS;
+    const int s = i % n_stages;
+    const int t = tile_of(i);
     const int pos = tile_pos(t);
     const int id = page_id(pos, win_i, pid_i);
     if (lane == 0) {
@@ -227,8 +293,8 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
       }
     }
   };
-  {
-    const int pre = my_tiles < kStagesS ? my_tiles : kStagesS;
+  if (!shared_tiles || warp == 0) {
+    const int pre = my_tiles < n_stages ? my_tiles : n_stages;
     for (int i = 0; i < pre; ++i) issue(i);
   }
 
@@ -243,18 +309,29 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
   const int kb_c8 = (lane >> 3) & 1;
   const int vb_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
   const int vb_c8 = lane >> 4;
+  // 16-byte chunk 2j + c of a box row sits at chunk (2j + c) ^ (row % 8), i.e. at
+  // the byte offset of chunk c XOR 32 j (the row starts 128-byte aligned): one
+  // per-lane offset for j = 0; later boxes add 2 KB (immediates).
+  const uint32_t ko0 = uint32_t(kb_tok * 128 + ((kb_c8 ^ (kb_tok & 7)) << 4));
+  const uint32_t vo0 = uint32_t(vb_tok * 128 + ((vb_c8 ^ (vb_tok & 7)) << 4));
 
+  // V fragment masks of a tail tile in the shared form (tokens tk, tk+1 and tk+8,
+  // tk+9 of the transposed ldmatrix); the private form zeroes the rows in its stage.
+  const int tk = (lane & 3) * 2;
   for (int i = 0; i < my_tiles; ++i) {
-    const int s = i % kStagesS;
-    const int t = warp + i * kWarpsS;
+    const int s = i % n_stages;
+    const int t = tile_of(i);
     const int id = page_id(tile_pos(t), win_c, pid_c);
     const bool page_ok = id >= 0 && int64_t(id) < p.num_pages;
     const int valid = page_ok ? min(kTileTok, it.n_tokens - t * kTileTok) : 0;
-    const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / kStagesS) & 1u, p.fault);
+    const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / n_stages) & 1u, p.fault);
     if (!__all_sync(0xffffffffu, ok)) break;
     if (valid > 0) {
       uint8_t *stage = ring + size_t(s) * 2 * TILE_BYTES;
-      if (valid < kTileTok) {
+      const bool vmask = shared_tiles && valid < kTileTok;
+      const uint32_t m_lo = (tk < valid ? 0x0000FFFFu : 0u) | (tk + 1 < valid ? 0xFFFF0000u : 0u);
+      const uint32_t m_hi = (tk + 8 < valid ? 0x0000FFFFu : 0u) | (tk + 9 < valid ? 0xFFFF0000u : 0u);
+      if (!shared_tiles && valid < kTileTok) {
         // Tail tile: V rows past the last token hold other slots (or NaN canaries);
         // P is 0 there, so make them 0 too before the MMA multiplies them.
         constexpr int CH = (D / 64) * 8;  // 16-byte chunks per row
@@ -268,35 +345,49 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
       }
       const uint32_t kbase = smem_u32(stage);
       const uint32_t vbase = kbase + TILE_BYTES;
-      // S = Q K^T over this warp's 16 tokens
+      // S = Q K^T over the tile's 16 tokens: even and odd k-steps accumulate apart
+      // (two shorter MMA chains), then add
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk) {
+      float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const uint32_t kq = kbase + ko0;
+      static_for<KSTEPS>([&](auto kc) {
+        constexpr int kk = decltype(kc)::value;
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + sw128(kb_tok, kk * 2 + kb_c8), b0, b1, b2, b3);
-        mma16816(sc[0], qa[kk], b0, b1);
-        mma16816(sc[1], qa[kk], b2, b3);
-      }
-      // scale, mask, online softmax (rows lane/4 and lane/4 + 8)
-      const int tok0 = (lane & 3) * 2;
+        ldsm_x4_at<(kk >> 2) * kTileTok * 128>(kq ^ uint32_t(32 * (kk & 3)), b0, b1, b2, b3);
+        float(&acc)[2][4] = (kk & 1) ? sd : sc;
+        mma16816(acc[0], qa[kk], b0, b1);
+        mma16816(acc[1], qa[kk], b2, b3);
+      });
+      // scale, mask (tail tiles only), online softmax (rows lane/4 and lane/4 + 8)
       float tmax[2] = {neg_inf(), neg_inf()};
 #pragma unroll
       for (int n = 0; n < 2; ++n)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const bool live = n * 8 + tok0 + (j & 1) < valid;
-          sc[n][j] = live ? sc[n][j] * p.q_scale : neg_inf();
-          tmax[j >> 1] = fmaxf(tmax[j >> 1], sc[n][j]);
-        }
-      float m_new[2];
+        for (int j = 0; j < 4; ++j) sc[n][j] = (sc[n][j] + sd[n][j]) * p.q_scale;
+      if (valid < kTileTok) {
+        const int tok0 = (lane & 3) * 2;
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (n * 8 + tok0 + (j & 1) >= valid) sc[n][j] = neg_inf();
+      }
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tmax[j >> 1] = fmaxf(tmax[j >> 1], sc[n][j]);
+      // Lazy rescale: the running max moves only when a row's tile max exceeds it by
+      // more than 2^8 (P <= 2^8 otherwise, far inside f32 and bf16 range).
+      bool grow[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 1));
         tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 2));
-        m_new[h] = fmaxf(m_run[h], tmax[h]);
+        grow[h] = tmax[h] > m_run[h] + kLazyRescale;
       }
-      if (!__all_sync(0xffffffffu, m_new[0] == m_run[0] && m_new[1] == m_run[1])) {
-        const float a0 = ex2(m_run[0] - m_new[0]), a1 = ex2(m_run[1] - m_new[1]);
+      if (__any_sync(0xffffffffu, grow[0] || grow[1])) {
+        const float a0 = grow[0] ? ex2(m_run[0] - tmax[0]) : 1.f;
+        const float a1 = grow[1] ? ex2(m_run[1] - tmax[1]) : 1.f;
         l_run[0] *= a0;
         l_run[1] *= a1;
 #pragma unroll
@@ -306,8 +397,8 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
           o[n][2] *= a1;
           o[n][3] *= a1;
         }
-        m_run[0] = m_new[0];
-        m_run[1] = m_new[1];
+        if (grow[0]) m_run[0] = tmax[0];
+        if (grow[1]) m_run[1] = tmax[1];
       }
 #pragma unroll
       for (int n = 0; n < 2; ++n)
@@ -326,19 +417,71 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
         pa[k] = pack_bf16x2(x0, x1);
         pl[k] = pack_bf16x2(x0 - bf16_lo(pa[k]), x1 - bf16_hi(pa[k]));
       }
-      // O += P V
-#pragma unroll
-      for (int n = 0; n < NT; n += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vbase + sw128(vb_tok, n + vb_c8), b0, b1, b2, b3);
-        mma16816(o[n], pa, b0, b1);
-        mma16816(o[n + 1], pa, b2, b3);
-        mma16816(o[n], pl, b0, b1);
-        mma16816(o[n + 1], pl, b2, b3);
-      }
+      // O += P V (in the shared form, V of a tail tile's dead tokens is zeroed in
+      // the fragments)
+      const uint32_t vq = vbase + vo0;
+      auto pv = [&](auto masked) {
+        static_for<NT / 2>([&](auto nc) {
+          constexpr int n = 2 * decltype(nc)::value;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t_at<(n >> 3) * kTileTok * 128>(vq ^ uint32_t(32 * ((n >> 1) & 3)), b0, b1, b2, b3);
+          if constexpr (decltype(masked)::value) {
+            b0 &= m_lo;
+            b1 &= m_hi;
+            b2 &= m_lo;
+            b3 &= m_hi;
+          }
+          mma16816(o[n], pa, b0, b1);
+          mma16816(o[n + 1], pa, b2, b3);
+          mma16816(o[n], pl, b0, b1);
+          mma16816(o[n + 1], pl, b2, b3);
+        });
+      };
+      if (vmask) pv(std::true_type{});
+      else pv(std::false_type{});
     }
     __syncwarp();
-    if (i + kStagesS < my_tiles) issue(i + kStagesS);
+    if (!shared_tiles) {
+      if (i + kStagesS < my_tiles) issue(i + kStagesS);
+    } else {
+      // Release the stage; the warp whose release completes this use refills it.
+      // The counter only grows: use u of a stage is complete at (u + 1) * n_active.
+      uint32_t last = 0;
+      if (lane == 0) {
+        __threadfence_block();
+        last = atomicAdd(&released[s], 1u) == uint32_t(i / n_stages + 1) * uint32_t(n_active) - 1u;
+      }
+      if (__shfl_sync(0xffffffffu, last, 0) && i + n_stages < my_tiles) {
+        __threadfence_block();
+        issue(i + n_stages);
+      }
+    }
+  }
+
+  if (shared_tiles) {  // this warp's rows are complete: write them
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = (lane >> 2) + 8 * h;
+      if (r >= rows) continue;
+      const int g = row0 + r;
+      const bool live = m_run[h] != neg_inf();
+      const float f = live ? p.v_scale / l_run[h] : 0.f;
+      const int m = g / p.Gm;
+      const int row = it.q_index >= 0 ? it.out_row : ld_list(row_base + member0 + m) + it.out_row;
+      const int head = kv * p.Gm + (g - m * p.Gm);
+      const int64_t orow = int64_t(row) * p.Hq_req + head;
+      float *dst = p.v_out + orow * p.Dv + (lane & 3) * 2;
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+        *reinterpret_cast<float2 *>(dst + n * 8) = make_float2(o[n][2 * h] * f, o[n][2 * h + 1] * f);
+      if ((lane & 3) == 0) p.lse_out[orow] = live ? m_run[h] + log2f(l_run[h]) : neg_inf();
+    }
+    return;
   }
 
   // ---- merge the four warps through shared memory (rings no longer used).  Only
@@ -420,7 +563,8 @@ template <int D>
 size_t tcs_smem_bytes() {
   const size_t ring = size_t(kWarpsS) * kStagesS * 2 * kTileTok * D * 2;
   const size_t red = size_t(kWarpsS) * 16 * (D + 2) * sizeof(float);
-  return std::max(ring, red) + 1024 /* base alignment */ + kWarpsS * kStagesS * sizeof(uint64_t);
+  return std::max(ring, red) + 1024 /* base alignment */ +
+         kWarpsS * kStagesS * (sizeof(uint64_t) + sizeof(uint32_t)) /* barriers, release counters */;
 }
 
 template <int D, int CAP>
@@ -462,7 +606,20 @@ psd_status launch_tcs(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_
   p.n_l0_tasks = 0;
   p.l1_base = 0;
   p.nseg = 0;
-  unsigned grid_x = static_cast<unsigned>(L.num_items), grid_z = static_cast<unsigned>((L.G_cta + 15) / 16);
+  // The shared-tile form only where its CTAs fill a wave (3 resident per SM).
+  const int64_t wave = int64_t(dev.num_sms > 0 ? dev.num_sms : 1) * 3;
+  if (L.fused_segments > 0) {
+    int64_t blocks = 0;
+    for (int sg = 0; sg < L.fused_segments && sg < PartialLaunch::kMaxFusedSegments; ++sg)
+      if (tcs_shared_tiles(L.seg_rows[sg], true))
+        blocks += int64_t(L.seg_items[sg]) * tcs_blocks(L.seg_rows[sg], true) * L.Hkv;
+    p.allow_shared = blocks >= wave;
+  } else {
+    p.allow_shared = tcs_shared_tiles(L.G_cta, true) &&
+                     int64_t(L.num_items) * tcs_blocks(L.G_cta, true) * L.Hkv >= wave;
+  }
+  unsigned grid_x = static_cast<unsigned>(L.num_items),
+           grid_z = static_cast<unsigned>(tcs_blocks(L.G_cta, p.allow_shared));
   if (L.fused_segments > 0) {  // level-0 items of every segment precede L.items' level-1 items
     if (L.fused_segments > PartialLaunch::kMaxFusedSegments)
       return fail(PSD_ERR_UNSUPPORTED, "fused cascade launch: %d segments > %d", L.fused_segments,
@@ -470,7 +627,7 @@ psd_status launch_tcs(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_
     int64_t tasks = 0;
     int item0 = 0;
     for (int sg = 0; sg < L.fused_segments; ++sg) {
-      tasks += int64_t(L.seg_items[sg]) * ((L.seg_rows[sg] + 15) / 16);
+      tasks += int64_t(L.seg_items[sg]) * tcs_blocks(L.seg_rows[sg], p.allow_shared);
       if (tasks > 0x7fffffffLL) return fail(PSD_ERR_UNSUPPORTED, "fused cascade launch: too many tasks");
       p.seg_task_end[sg] = int(tasks);
       p.seg_item0[sg] = item0;

@@ -344,6 +344,96 @@ def test_inputs_from_pinned_host_memory(maker, kernel):
     assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu())
 
 
+@pytest.mark.parametrize("G,D", [(20, 128), (24, 64), (40, 128), (64, 128), (80, 64), (132, 128)])
+def test_large_query_groups_share_each_tile(G, D):
+    """More than 16 query rows per KV head.  Up to 48 rows (20, 24, 40 here) take a
+    CTA per 16-row group; more rows (64, 80, 132) take blocks of 64 rows whose warps
+    own a group each and read every tile from one shared ring, with a partly filled
+    last warp and blocks with idle warps.  Ragged lengths with single-token and tail
+    tiles, NaN canaries in every unused slot, against the oracle."""
+    rng = np.random.default_rng(G + D)
+    lengths = [1, 15, 16, 17, 300, 515, 1024, 1300]
+    w = synth._make(f"gqa{G}", rng, lengths, Hq=2 * G, Hkv=2, Dqk=D, Dv=D, page_size=16,
+                    num_pages=sum((n + 15) // 16 for n in lengths) + 8, tile_tokens=256)
+    o, lse = Dev(w).decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "bf16", f"G={G}, D={D}")
+
+
+@pytest.mark.parametrize("members", [5, 9, 17, 33])
+def test_cascade_stacked_rows_in_shared_tile_blocks(members):
+    """Level-0 stacks members x G rows per KV head (20, 36, 68, 132 here): CTAs per
+    16-row group below 49 rows, blocks of 64 rows with partly filled and idle warps
+    above, through the fused launch, against the oracle and the flat arm."""
+    rng = np.random.default_rng(70 + members)
+    B = members + 3
+    P, sp = 16, 40
+    lengths = [int(x) for x in rng.integers(1, 900, size=B)]
+    mem = sorted(int(m) for m in rng.choice(B, size=members, replace=False))
+    for m in mem:
+        lengths[m] = sp * P + int(rng.integers(1, 200))
+    w = synth._make(f"casc{members}", rng, lengths, Hq=8, Hkv=2, Dqk=128, Dv=128, page_size=P,
+                    num_pages=sum((n + P - 1) // P for n in lengths) + 8, tile_tokens=128,
+                    shared=(mem, sp), min_shared_pages=1, min_members=2)
+    d = Dev(w)
+    o, lse, stats, plan = d.decode(enable=1, with_stats=True)
+    assert stats["path"] == 1 and stats["members"] == members
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "bf16", f"cascade, {members} members")
+    fo, fl = d.decode(enable=0)
+    assert np.abs(o - fo).max() < 2e-3
+
+
+def _wave():
+    """Resident CTAs of the tensor-core partial kernel per wave (three per SM)."""
+    return 3 * torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("G", [64, 80])
+def test_large_groups_in_shared_tile_blocks(G):
+    """64-row blocks take the shared-tile form once they fill a wave of resident
+    CTAs.  This batch has enough work items for 1.25 waves of blocks (80 rows: a
+    full block and one with a single live warp per item).  Ragged lengths, NaN
+    canaries in every unused slot, every output against the oracle."""
+    rng = np.random.default_rng(300 + G)
+    Hkv, D, P, tile = 8, 128, 16, 64
+    need = -(-_wave() * 5 // 4 // (Hkv * ((G + 63) // 64)))
+    lengths = []
+    while sum(-(-n // tile) for n in lengths) < need:
+        lengths.append(int(rng.integers(1, 700)))
+    lengths[0] = 1
+    w = synth._make(f"gqa{G}_blocks", rng, lengths, Hq=Hkv * G, Hkv=Hkv, Dqk=D, Dv=D, page_size=P,
+                    num_pages=sum((n + P - 1) // P for n in lengths) + 8, tile_tokens=tile)
+    o, lse = Dev(w).decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "bf16", f"G={G}, shared-tile blocks")
+
+
+def test_cascade_level0_in_shared_tile_blocks():
+    """16 members x 4 rows = 64 stacked rows per KV head, with enough prefix chunks
+    (tile 64) for 1.25 waves of level-0 blocks, so the fused launch takes the
+    shared-tile form for level 0: every output against the oracle and the flat arm."""
+    rng = np.random.default_rng(77)
+    Hkv, P, tile, members = 8, 16, 64, 16
+    chunks = -(-_wave() * 5 // 4 // Hkv)
+    sp = chunks * tile // P
+    B = members + 4
+    lengths = [int(x) for x in rng.integers(1, 900, size=B)]
+    mem = sorted(int(m) for m in rng.choice(B, size=members, replace=False))
+    for m in mem:
+        lengths[m] = sp * P + int(rng.integers(1, 300))
+    w = synth._make("casc_blocks", rng, lengths, Hq=4 * Hkv, Hkv=Hkv, Dqk=128, Dv=128, page_size=P,
+                    num_pages=sum((n + P - 1) // P for n in lengths) + 8, tile_tokens=tile,
+                    shared=(mem, sp), min_shared_pages=1, min_members=2)
+    d = Dev(w)
+    o, lse, stats, plan = d.decode(enable=1, with_stats=True)
+    assert stats["path"] == 1 and stats["members"] == members and stats["prefix_chunks"] >= chunks
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "bf16", "cascade, level-0 blocks")
+    fo, fl = d.decode(enable=0)
+    assert np.abs(o - fo).max() < 2e-3
+
+
 def test_pageable_host_query_is_rejected_by_the_binding():
     w = synth.tiny_cascade(seed=0)
     d = Dev(w)
