@@ -39,8 +39,8 @@ NOMINAL_HBM_GBS = 8000.0
 # ncu capture summarised in profiles/partial_tcs_flat_decode.md.  Reported only while
 # the kernel source is the one the counters were taken on.
 TRAFFIC_SOURCE = os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", "partial_tcs.cu")
-TRAFFIC_SHA256 = "b4c560570833aa61d0db42194307167437d3e5bbcba9cb48e75b3e0cb8ec9058"
-TRAFFIC_BYTES = 316075008 + 1245696
+TRAFFIC_SHA256 = "e0ef72ba0b83ba58f600d071d0e2a7a2c57727886b3ae2c44e678afe193ced34"
+TRAFFIC_BYTES = 316086272 + 1172224
 
 
 def partial_traffic():
