@@ -174,7 +174,8 @@ psd_status psd_create(psd_ctx **ctx, int device);
 psd_status psd_destroy(psd_ctx *ctx);
 /* Which kernel computes partials on bf16 pools with separate K and V.  AUTO and
  * TENSOR_CORE: the 16-row-group tensor-core kernel (QK^T and PV as m16n8k16
- * MMAs; the stacked level-0 rows are split into groups of 16).  CUDA_CORE: the
+ * MMAs; the stacked level-0 rows are split into groups of 16, or into 64-row
+ * blocks that read each K/V tile once when those blocks fill a wave of the GPU).  CUDA_CORE: the
  * CUDA-core kernel wherever it applies (G <= 8 rows per KV head; warp-shuffle
  * reductions and f32x2 FMAs).  Both compute the same partials.  fp8 pools with
  * separate K and V (head dims 64, 128, 256) use the 64-row mma.sync kernel; the
