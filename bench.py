@@ -9,7 +9,11 @@ the metric is unique KV bytes per second.  The cascade workload (64 requests, 16
 sharing an 8192-token prefix) is timed as a flat arm and a cascade arm on the same
 inputs, and the MLA workload (128 heads over an fp8 576-wide latent) is timed too.
 
-L2 is flushed (a 256 MB write) before every timed step, outside the timed events.
+L2 is flushed (a 512 MB write) before every timed step, outside the timed events.
+The flush also keeps the device busy while the host plans and enqueues the step, so
+the events time the device path rather than the host's enqueue latency; the JSON
+line reports both durations ("flush_us", "host_enqueue_us") so that this can be read
+off each run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -32,7 +36,7 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-L2_FLUSH_BYTES = 256 << 20
+L2_FLUSH_BYTES = 512 << 20
 NOMINAL_HBM_GBS = 8000.0
 
 # DRAM bytes (read + write) of one flat-decode launch of the partial kernel, from the
@@ -173,8 +177,10 @@ class Arm:
         assert self.psd.check_device_error(self.ctx, self.ws) == 0
 
 
-def time_steps(fn, steps: int, warmup: int, flush: torch.Tensor):
-    """Per-step CUDA-event times (ms) with an L2 flush before each step."""
+def time_steps(fn, steps: int, warmup: int, flush: torch.Tensor, host_us: list | None = None):
+    """Per-step CUDA-event times (ms) with an L2 flush before each step.  When
+    `host_us` is given, the host time from the start event's record to the end
+    event's record (planning, marshalling and launches) is appended to it per step."""
     s = torch.cuda.current_stream()
     for _ in range(warmup):
         flush.zero_()
@@ -186,11 +192,28 @@ def time_steps(fn, steps: int, warmup: int, flush: torch.Tensor):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(s)
+        t0 = time.perf_counter()
         fn()
         e1.record(s)
+        if host_us is not None:
+            host_us.append((time.perf_counter() - t0) * 1e6)
         times.append((e0, e1))
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in times]
+
+
+def flush_us(flush: torch.Tensor, reps: int = 5) -> float:
+    """Device time of one L2 flush (µs), CUDA events on the current stream."""
+    s = torch.cuda.current_stream()
+    flush.zero_()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(reps):
+        flush.zero_()
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
 
 
 def kernel_timing(arm: Arm, steps: int, warmup: int, flush, kind: str = "auto"):
@@ -535,7 +558,8 @@ def run_ours(args):
     barrier(world)
     with ClockSampler(local) as clk:
         t_wall0 = time.perf_counter()
-        times = time_steps(arm.step, args.steps, args.warmup, flush)
+        host_us = []
+        times = time_steps(arm.step, args.steps, args.warmup, flush, host_us)
         barrier(world)
         t_wall = time.perf_counter() - t_wall0
         kt = kernel_timing(arm, args.steps, args.warmup, flush)
@@ -620,7 +644,9 @@ def run_ours(args):
                                    "lengths U[512,4096] partial last page, 16384-page pool, tile 512, "
                                    "then merge_states",
                        "batch": w.batch, "unique_kv_bytes": kv_bytes,
-                       "l2": "flushed (256 MB write) before every timed step",
+                       "l2": "flushed (512 MB write) before every timed step",
+                       "flush_us": round(flush_us(flush), 1),
+                       "host_enqueue_us": round(statistics.mean(host_us), 1),
                        "parallelism": f"replicas x{world}"},
             "decode_tokens_per_s": round(world * w.batch / (ms_max * 1e-3), 1),
             "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
