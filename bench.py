@@ -9,8 +9,9 @@ the metric is unique KV bytes per second.  The cascade workload (64 requests, 16
 sharing an 8192-token prefix) is timed as a flat arm and a cascade arm on the same
 inputs, and the MLA workload (128 heads over an fp8 576-wide latent) is timed too.
 
-L2 is flushed (a 512 MB write) before every timed step, outside the timed events.
-The flush also keeps the device busy while the host plans and enqueues the step, so
+L2 is flushed before every timed step, outside the timed events: a 512 MB write,
+then a 256 MB read of another buffer, so the step starts with a clean L2 holding none
+of its inputs (see L2Flush; --l2-flush write keeps the write alone).  The flush also keeps the device busy while the host plans and enqueues the step, so
 the events time the device path rather than the host's enqueue latency; the JSON
 line reports both durations ("flush_us", "host_enqueue_us") so that this can be read
 off each run.
@@ -37,6 +38,7 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 L2_FLUSH_BYTES = 512 << 20
+L2_FLUSH_READ_BYTES = 256 << 20
 NOMINAL_HBM_GBS = 8000.0
 
 # DRAM bytes (read + write) of one flat-decode launch of the partial kernel, from the
@@ -177,18 +179,45 @@ class Arm:
         assert self.psd.check_device_error(self.ctx, self.ws) == 0
 
 
-def time_steps(fn, steps: int, warmup: int, flush: torch.Tensor, host_us: list | None = None):
+class L2Flush:
+    """Evicts the decode's inputs from L2 before a timed step, outside the events.
+
+    'write' writes a 512 MB buffer (about 4x the 129 MB L2).  That leaves L2 full of
+    dirty lines, and the next kernel's reads must first write them back to HBM, so a
+    read-bound kernel timed right after it pays for the flush's write-backs too.
+    'write+read' (the default) then reads a separate 256 MB buffer, which moves those
+    write-backs before the timed region and leaves L2 holding only clean lines that the
+    step never touches.  Either way the step starts with none of its inputs in L2."""
+
+    def __init__(self, mode: str = "write+read"):
+        self.mode = mode
+        self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.rbuf = torch.ones(L2_FLUSH_READ_BYTES // 4, dtype=torch.float32, device="cuda") \
+            if mode == "write+read" else None
+        self.sink = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.buf.zero_()
+        if self.rbuf is not None:
+            torch.sum(self.rbuf, dim=0, out=self.sink)
+
+    def describe(self) -> str:
+        return ("512 MB write, then a 256 MB read of another buffer" if self.rbuf is not None
+                else "512 MB write") + ", before every timed step"
+
+
+def time_steps(fn, steps: int, warmup: int, flush: L2Flush, host_us: list | None = None):
     """Per-step CUDA-event times (ms) with an L2 flush before each step.  When
     `host_us` is given, the host time from the start event's record to the end
     event's record (planning, marshalling and launches) is appended to it per step."""
     s = torch.cuda.current_stream()
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         fn()
     torch.cuda.synchronize()
     times = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(s)
@@ -202,15 +231,15 @@ def time_steps(fn, steps: int, warmup: int, flush: torch.Tensor, host_us: list |
     return [a.elapsed_time(b) for a, b in times]
 
 
-def flush_us(flush: torch.Tensor, reps: int = 5) -> float:
+def flush_us(flush: L2Flush, reps: int = 5) -> float:
     """Device time of one L2 flush (µs), CUDA events on the current stream."""
     s = torch.cuda.current_stream()
-    flush.zero_()
+    flush()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(s)
     for _ in range(reps):
-        flush.zero_()
+        flush()
     e1.record(s)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) * 1e3 / reps
@@ -223,12 +252,12 @@ def kernel_timing(arm: Arm, steps: int, warmup: int, flush, kind: str = "auto"):
     arm.ctx.set_partial_kernel(kind)
     arm.ctx.set_timing(True)
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         arm.step()
     torch.cuda.synchronize()
     out = {"level0_ms": [], "partial_ms": [], "merge_ms": []}
     for _ in range(steps):
-        flush.zero_()
+        flush()
         arm.step()
         for k, v in arm.ctx.kernel_times().items():
             out[k].append(v)
@@ -547,7 +576,7 @@ def run_ours(args):
     rank, world, local = dist_setup(args.gpus)
     torch.cuda.set_device(local)
     hbm, bf16, bf16s, peak_src = measured_peaks()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush(args.l2_flush)
 
     w = synth.flat_decode(seed=0, canary=False)
     arm = Arm(w, enable=1)
@@ -644,7 +673,7 @@ def run_ours(args):
                                    "lengths U[512,4096] partial last page, 16384-page pool, tile 512, "
                                    "then merge_states",
                        "batch": w.batch, "unique_kv_bytes": kv_bytes,
-                       "l2": "flushed (512 MB write) before every timed step",
+                       "l2": "flushed: " + flush.describe(),
                        "flush_us": round(flush_us(flush), 1),
                        "host_enqueue_us": round(statistics.mean(host_us), 1),
                        "parallelism": f"replicas x{world}"},
@@ -659,7 +688,9 @@ def run_ours(args):
                          "launch_ms": round(k_ms, 5)},
             "merge_kernel": {"kernel": "merge_states_kernel<1>", "achieved": round(merge_gbs, 1),
                              "unit": "GB/s", "frac": round(merge_gbs / hbm, 4),
-                             "launch_ms": round(kt["merge_ms"], 5), "algorithmic_bytes": merge_bytes},
+                             "launch_ms": round(kt["merge_ms"], 5), "algorithmic_bytes": merge_bytes,
+                             "note": "3.3 MB per launch on this batch, so latency sets its time; "
+                                     "merge_sweep measures its bandwidth"},
             "partial_cuda_core": {"kernel": "partial_cc_kernel<128,4> (split-KV partial, CUDA cores)",
                                   "achieved": round(achieved_cc, 1), "unit": "GB/s",
                                   "frac": round(achieved_cc / hbm, 4), "launch_ms": round(k_ms_cc, 5)},
@@ -735,6 +766,8 @@ def main():
     p.add_argument("--mla-batch", type=int, default=128, help="requests in the MLA workload")
     p.add_argument("--merge-rows", default="", help="merge sweep sizes, comma-separated (default 1K,16K,256K,1M)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--l2-flush", choices=["write+read", "write"], default="write+read",
+                   help="L2 flush before each timed step (see L2Flush)")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3
