@@ -419,7 +419,7 @@ def autotune_report(arm, reps):
     best, ms = arm.ctx.autotune_tile(arm.args, arm.table, tiles, arm.o, arm.lse, ws, 1, w.min_shared_pages,
                                      w.min_members, reps=reps)
     return {"tiles": tiles, "step_ms": [round(x, 5) for x in ms], "best_tile": best,
-            "method": "psd_autotune_tile: cascade_decode per tile, 256 MB flush before each timed call"}
+            "method": "psd_autotune_tile: cascade_decode per tile, cold clean L2 before each timed call (256 MB write, then 256 MB read of another region)"}
 
 
 def nested_timing(steps, warmup, flush):

@@ -425,9 +425,10 @@ psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args *args,
  * cold-L2 benchmark methodology is not wired to either cascade geometry; both plans
  * use the heuristic chunk size.  psd_autotune_tile times cascade_decode for each
  * candidate tile_tokens on the caller's batch (psd_plan_decode with `enable` and the
- * thresholds): one untimed call, then `reps` timed calls, each preceded by a write
- * of a 256 MB device buffer the context allocates once (cold L2), timed with CUDA
- * events on `stream`; the call is synchronous.  The candidate with the lowest mean
+ * thresholds): one untimed call, then `reps` timed calls, each preceded by a cold-L2
+ * flush (a 256 MB write, then a 256 MB read of another region, so that L2 holds no
+ * input and no dirty line; the context allocates the 512 MB buffer once), timed with
+ * CUDA events on `stream`; the call is synchronous.  The candidate with the lowest mean
  * is recorded under the batch's shape bucket: (Hq, Hkv, Dqk, Dv, kv_dtype,
  * page_size, batch and total tokens each rounded up to a power of two, whether the
  * plan cascades).  Candidates must be positive multiples of page_size; o, lse and
