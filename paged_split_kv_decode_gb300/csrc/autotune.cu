@@ -24,7 +24,7 @@ constexpr size_t kFlushBytes = size_t(256) << 20;
 __global__ void l2_read_flush(const uint4 *__restrict__ src, size_t n16, uint32_t key, uint32_t *keep) {
   uint32_t acc = 0;
   for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += size_t(gridDim.x) * blockDim.x) {
-    const uint4 v = __ldcs(src + i);
+    const uint4 v = src[i];  // default L2 policy: evict-first loads would not displace the dirty lines
     acc ^= v.x ^ v.y ^ v.z ^ v.w;
   }
   if (acc == key) *keep = acc;
