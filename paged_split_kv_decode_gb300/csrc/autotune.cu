@@ -19,8 +19,9 @@ namespace {
 // starts from a clean L2 that holds none of its inputs.
 constexpr size_t kFlushBytes = size_t(256) << 20;
 
-// Reads n16 16-byte words; stores one word to `keep` only when the XOR of all of
-// them equals `key`, which keeps the loads live (the buffer is scratch either way).
+// Reads n16 16-byte words, grid-stride; a thread stores one word to `keep` only when
+// the XOR of the words it read equals `key`, which keeps the loads live (`keep` is
+// scratch, so such a store is harmless).
 __global__ void l2_read_flush(const uint4 *__restrict__ src, size_t n16, uint32_t key, uint32_t *keep) {
   uint32_t acc = 0;
   for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += size_t(gridDim.x) * blockDim.x) {
