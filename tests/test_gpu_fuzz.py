@@ -78,3 +78,43 @@ def test_random_mla_configurations(seed):
         rv, rlp, rind = oracle_partials(w)
         assert o_indptr.tolist() == rind
         assert_close(v, l, rv, rlp, "fp8_e4m3", f"MLA partials seed {seed}")
+
+
+def _distinct_scales_case(seed, latent, shared):
+    import dataclasses
+    rng = np.random.default_rng(3000 + seed)
+    if latent:
+        Hq, Hkv, Dqk, Dv, P, tile = 128, 1, 576, 512, 64, 256
+        lengths = [int(x) for x in rng.integers(1, 3000, size=5)]
+    else:
+        Hq, Hkv, Dqk, Dv, P, tile = 16, 2, 128, 128, 16, 64
+        lengths = [int(x) for x in rng.integers(1, 1500, size=6)]
+    sh = None
+    if shared:
+        members, sp = [0, 2, 3], 3
+        for m in members:
+            lengths[m] = max(lengths[m], sp * P + int(rng.integers(1, 2 * P)))
+        sh = (members, sp)
+    pages = sum((L + P - 1) // P for L in lengths) + 4
+    w = synth._make(f"scales{seed}", rng, lengths, Hq=Hq, Hkv=Hkv, Dqk=Dqk, Dv=Dv, page_size=P,
+                    num_pages=pages, tile_tokens=tile, kv_dtype="fp8_e4m3", latent_v=latent, shared=sh,
+                    min_shared_pages=1, min_members=2)
+    # the same codes with K's and V's scales far apart (V dequantises with v_scale only)
+    return dataclasses.replace(w, k_scale=w.k_scale * 0.5, v_scale=w.k_scale * 4.0)
+
+
+@pytest.mark.parametrize("latent", [False, True], ids=["separate_kv", "latent"])
+@pytest.mark.parametrize("shared", [False, True], ids=["flat", "cascade"])
+def test_fp8_distinct_k_and_v_scales(latent, shared):
+    """fp8 pools whose K and V scales differ by 8x (ROCm ATOM PR #1701, 3.2: each
+    tensor dequantises with its own scale), flat and cascade, against the oracle.  The
+    oracle with V dequantised by K's scale misses by far more than the tolerance, so
+    a kernel that swapped the scales would fail here."""
+    w = _distinct_scales_case(int(latent) * 2 + int(shared), latent, shared)
+    a = A.workload_arrays(w)
+    ro, rl = A.decode_attention(a)
+    slip, _ = A.decode_attention(dict(a, v_scale=a["k_scale"]))
+    assert np.abs(slip - ro).max() > 0.1
+    o, lse, stats, _ = Dev(w).decode(enable=1, with_stats=True)
+    assert stats["path"] == int(shared)
+    assert_close(o, lse, ro, rl, "fp8_e4m3", f"distinct scales latent={latent} shared={shared}")

@@ -164,3 +164,111 @@ def test_fp8_pool_dequant_uses_scale_and_latent_v():
         rows = deq[indices[indptr[b] + j // P], j % P]                # [L, 1, Dqk]
         oo, ll = A.attend(q[b].double().numpy(), rows, rows[..., :Dv], 0.3)
         assert np.abs(o[b] - oo).max() < 1e-12 and np.abs(lse[b] - ll).max() < 1e-12
+
+
+# ------------------------------------------------------------------------------
+# workload_arrays and separate K / V scales, pinned against torch computing the same
+# attention straight from a synth.Workload's own tensors: pages gathered by torch
+# indexing, fp8 codes decoded by torch's float8_e4m3fn cast and scaled by their own
+# tensor's scale (ROCm ATOM PR #1701, 3.2: value = code * scale), request lengths
+# taken from the generator's lengths (not last_page_len), softmax by torch SDPA.
+
+def _torch_decode(w, k_scale=None, v_scale=None):
+    """o [B, Hq, Dv], lse2 [B, Hq] by torch in float64 from the Workload's tensors."""
+    ks = w.k_scale if k_scale is None else k_scale
+    vs = w.v_scale if v_scale is None else v_scale
+    G = w.Hq // w.Hkv
+
+    def dq(raw, scale):
+        if w.kv_dtype == "bf16":
+            return raw.double()
+        return raw.view(torch.float8_e4m3fn).to(torch.float32).double() * scale
+
+    o = torch.empty((w.batch, w.Hq, w.Dv), dtype=torch.float64)
+    lse = torch.empty((w.batch, w.Hq), dtype=torch.float64)
+    for b in range(w.batch):
+        pages = torch.as_tensor(w.page_indices[w.page_indptr[b]:w.page_indptr[b + 1]].astype(np.int64))
+        L = int(w.lengths[b])
+        kraw = w.k_pool[pages].reshape(-1, w.Hkv, w.Dqk)[:L]
+        k = dq(kraw, ks)
+        if w.v_pool is None:
+            v = dq(kraw[..., :w.Dv].contiguous(), vs)
+        else:
+            v = dq(w.v_pool[pages].reshape(-1, w.Hkv, w.Dv)[:L], vs)
+        kt = k.permute(1, 0, 2).repeat_interleave(G, dim=0)     # [Hq, L, Dqk]
+        vt = v.permute(1, 0, 2).repeat_interleave(G, dim=0)
+        qb = w.q[b].double()[:, None, :]
+        o[b] = torch.nn.functional.scaled_dot_product_attention(qb, kt, vt, scale=w.sm_scale)[:, 0]
+        s = torch.einsum("hd,hld->hl", w.q[b].double(), kt) * w.sm_scale
+        lse[b] = torch.logsumexp(s, dim=1) / math.log(2.0)
+    return o.numpy(), lse.numpy()
+
+
+def _small_fp8_kv(seed, kv_scale_ratio=None):
+    import synth
+    rng = np.random.default_rng(seed)
+    lengths = [int(x) for x in rng.integers(1, 120, size=4)]
+    w = synth._make("fp8_kv_small", rng, lengths, Hq=8, Hkv=2, Dqk=64, Dv=64, page_size=16,
+                    num_pages=40, tile_tokens=32, kv_dtype="fp8_e4m3")
+    if kv_scale_ratio is not None:          # same codes, V's scale far from K's
+        import dataclasses
+        w = dataclasses.replace(w, v_scale=w.k_scale * kv_scale_ratio)
+    return w
+
+
+def _small_fp8_latent(seed):
+    import synth
+    rng = np.random.default_rng(seed)
+    lengths = [int(x) for x in rng.integers(1, 300, size=3)]
+    return synth._make("fp8_latent_small", rng, lengths, Hq=16, Hkv=1, Dqk=576, Dv=512, page_size=64,
+                       num_pages=20, tile_tokens=128, kv_dtype="fp8_e4m3", latent_v=True)
+
+
+def _synth_case(kind):
+    import synth
+    if kind == "bf16_tiny_cascade":
+        return synth.tiny_cascade(seed=1)
+    if kind == "fp8_separate_kv":
+        return _small_fp8_kv(21)
+    if kind == "fp8_latent":
+        return _small_fp8_latent(22)
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("kind", ["bf16_tiny_cascade", "fp8_separate_kv", "fp8_latent"])
+def test_workload_arrays_decode_matches_torch_on_synth_workloads(kind):
+    """The adapter every GPU parity test uses (bit views, scales, Dv, sm_scale, a
+    latent's missing V pool) feeds decode_attention the same attention torch computes
+    from the Workload directly."""
+    w = _synth_case(kind)
+    o, lse = A.decode_attention(A.workload_arrays(w))
+    ro, rl = _torch_decode(w)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert np.abs(o - ro).max() < 1e-10
+    assert np.abs(lse - rl).max() < 1e-10
+
+
+def test_fp8_separate_k_and_v_scales_are_applied_independently():
+    """fp8 pool with separate K and V and v_scale = 4 * k_scale: K dequantises with
+    k_scale and V with v_scale.  gather_kv matches torch's cast times each tensor's
+    own scale; decode_attention matches torch; and the slip of dequantising V with
+    k_scale (planted in the inputs, on the CPU) misses torch by far more than the
+    fp8 tolerance."""
+    w = _small_fp8_kv(23, kv_scale_ratio=4.0)
+    a = A.workload_arrays(w)
+    assert a["v_scale"] == 4.0 * a["k_scale"]
+    for b in range(w.batch):
+        K, V = A.gather_kv(a, b)
+        pages = torch.as_tensor(w.page_indices[w.page_indptr[b]:w.page_indptr[b + 1]].astype(np.int64))
+        L = int(w.lengths[b])
+        kt = w.k_pool[pages].reshape(-1, w.Hkv, w.Dqk)[:L].view(torch.float8_e4m3fn).double() * w.k_scale
+        vt = w.v_pool[pages].reshape(-1, w.Hkv, w.Dv)[:L].view(torch.float8_e4m3fn).double() * w.v_scale
+        assert np.array_equal(K, kt.numpy()) and np.array_equal(V, vt.numpy())
+    o, lse = A.decode_attention(a)
+    ro, rl = _torch_decode(w)
+    assert np.abs(o - ro).max() < 1e-10 and np.abs(lse - rl).max() < 1e-10
+    slip, _ = A.decode_attention(dict(a, v_scale=a["k_scale"]))
+    assert np.abs(slip - ro).max() > 10 * 1e-2
+    # and K's scale moves the scores: the same slip on K (k_scale := v_scale) fails too
+    slip_k, slip_kl = A.decode_attention(dict(a, k_scale=a["v_scale"]))
+    assert np.abs(slip_kl - rl).max() > 10 * 1e-3
