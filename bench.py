@@ -20,10 +20,17 @@ off each run.
 """
 from __future__ import annotations
 
+import os
+
+# The oracle's CPU baseline runs one process per core on (request, KV head) tasks whose
+# matmuls are small; a multi-threaded BLAS in each process would oversubscribe the
+# cores (measured 30x slower), so numpy's BLAS keeps one thread per process.  Set
+# before numpy is first imported.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+
 import argparse
 import json
 import math
-import os
 import statistics
 import subprocess
 import sys
@@ -37,13 +44,14 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
+METRIC = "unique KV GB/s (flat paged decode; cascade and MLA arms alongside)"
 L2_FLUSH_BYTES = 512 << 20
 L2_FLUSH_READ_BYTES = 256 << 20
 NOMINAL_HBM_GBS = 8000.0
 
 # DRAM bytes (read + write) of one flat-decode launch of the partial kernel, from the
-# ncu capture summarised in profiles/partial_tcs_flat_decode.md.  Reported only while
-# the kernel source is the one the counters were taken on.
+# ncu capture of the flat partial.  Reported only while the kernel source is the one
+# the counters were taken on.
 TRAFFIC_SOURCE = os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", "partial_tcs.cu")
 TRAFFIC_SHA256 = "e0ef72ba0b83ba58f600d071d0e2a7a2c57727886b3ae2c44e678afe193ced34"
 TRAFFIC_BYTES = 316086272 + 1172224
@@ -79,6 +87,16 @@ def unique_kv_bytes(w) -> int:
             seen.add(key)
             tokens += valid
     return tokens * w.kv_bytes_per_token()
+
+
+def flat_config(w, kv_bytes: int, l2_mode: str) -> dict:
+    """The headline workload, as both arms of the bench name it."""
+    return {"workload": "flat paged decode: B=32, Hq=32, Hkv=8, D=128, page 16, L~U[512,4096], "
+                        "16384-page pool, tile 512, merge",
+            "batch": w.batch, "unique_kv_bytes": int(kv_bytes),
+            "l2": "flushed before every timed step: " + ("512 MB write, then 256 MB read of another buffer"
+                                                         if l2_mode == "write+read" else "512 MB write"),
+            "parallelism": "replicas"}
 
 
 def flat_kv_bytes(w) -> int:
@@ -231,6 +249,17 @@ def time_steps(fn, steps: int, warmup: int, flush: L2Flush, host_us: list | None
     return [a.elapsed_time(b) for a, b in times]
 
 
+def rep_stats(times, reps: int = 5) -> dict:
+    """The K per-step times split into `reps` consecutive reps (fewer when K < reps):
+    each rep's median step time, then the median, minimum and maximum over reps, in
+    ms (the per-arm median/min/max over reps of the mlxcel PR #1004 bench harness,
+    How to run the benchmarks section)."""
+    n = max(1, min(reps, len(times)))
+    per = [statistics.median(times[i * len(times) // n:(i + 1) * len(times) // n]) for i in range(n)]
+    return {"reps": n, "steps_per_rep": len(times) // n, "median_ms": round(statistics.median(per), 5),
+            "min_ms": round(min(per), 5), "max_ms": round(max(per), 5)}
+
+
 def flush_us(flush: L2Flush, reps: int = 5) -> float:
     """Device time of one L2 flush (µs), CUDA events on the current stream."""
     s = torch.cuda.current_stream()
@@ -306,6 +335,17 @@ def e2e_timing(arm: Arm, steps: int, warmup: int, flush):
         psd.cascade_decode(arm.ctx, args, arm.plan, o_host, l_host, arm.ws)
 
     times = time_steps(step, steps, warmup, flush)
+    # Host-observed latency of the same step: from the call's start, with the device
+    # idle and L2 flushed, until the host holds the outputs (stream synchronize).
+    wall = []
+    s = torch.cuda.current_stream()
+    for _ in range(steps):
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        step()
+        s.synchronize()
+        wall.append((time.perf_counter() - t0) * 1e3)
     torch.cuda.synchronize()
     arm.step()
     torch.cuda.synchronize()
@@ -314,7 +354,43 @@ def e2e_timing(arm: Arm, steps: int, warmup: int, flush):
     plan_bytes = (arm.plan.num_items * 16 + (w.batch * 3 + 1) * 4 + 256)
     h2d = in_bytes + plan_bytes
     d2h = (o_elems + l_elems) * 4
-    return times, h2d, d2h
+    return times, h2d, d2h, wall
+
+
+def no_sharing_gate(arm, steps: int, warmup: int, flush) -> dict:
+    """The flat workload (no two requests share a page) with and without shared-prefix
+    detection in front of the flat launch: the no-sharing overhead gate of the mlxcel
+    PR #1004 bench harness (How to run the benchmarks).  Host time per planning call
+    with detection (psd_plan_decode enable=1: the scan runs and declines) and without
+    it (enable=0: the split work list alone), and the device time of the step each way
+    (CUDA events, medians over steps)."""
+    psd, w = arm.psd, arm.w
+
+    def plan(enable):
+        psd.plan_decode(arm.table, w.tile_tokens, enable, w.min_shared_pages, w.min_members, plan=arm.plan)
+
+    def host_us(enable, reps=400):
+        plan(enable)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            plan(enable)
+        return (time.perf_counter() - t0) / reps * 1e6
+
+    def step(enable):
+        plan(enable)
+        psd.cascade_decode(arm.ctx, arm.args, arm.plan, arm.o, arm.lse, arm.ws)
+
+    h_det, h_flat = host_us(1), host_us(0)
+    assert arm.plan.num_members == 0
+    d_det = statistics.median(time_steps(lambda: step(1), steps, warmup, flush))
+    d_flat = statistics.median(time_steps(lambda: step(0), steps, warmup, flush))
+    return {"workload": "the flat workload (nothing shared)",
+            "host_plan_us_with_detection": round(h_det, 2), "host_plan_us_without_detection": round(h_flat, 2),
+            "detection_host_us": round(h_det - h_flat, 2),
+            "device_step_ms_with_detection": round(d_det, 5),
+            "device_step_ms_without_detection": round(d_flat, 5),
+            "note": "host time per call through the Python binding; the device step is timed after an L2 "
+                    "flush that outlasts the host's planning, so detection shows up in host time only"}
 
 
 def merge_sweep(ctx, steps: int, warmup: int, flush, hbm: float, sizes=(1024, 16384, 262144, 1048576)):
@@ -342,32 +418,75 @@ def merge_sweep(ctx, steps: int, warmup: int, flush, hbm: float, sizes=(1024, 16
 
 
 # ----------------------------------------------------------------------- oracle
-def oracle_baseline(w, budget_s: float = 12.0):
-    """The float64 oracle (as it stands) on the host: gather + softmax attention per
-    request.  Requests are processed in order, cycling over the batch, until the
-    time budget is spent."""
+# The float64 oracle, as it stands, timed on the host cores: one task is one
+# (request, KV head) pair (the oracle's gather over that head's slice of the pools,
+# then its softmax attention for the head's G query rows).  The tasks run on every
+# core the process may use, through a pool of forked workers that inherit the
+# workload's arrays; the pool is forked before this process touches CUDA (a process
+# forked after CUDA is initialised must not use it, and these never do).
+_ORACLE = {}
+
+
+def _oracle_task(task) -> int:
     from oracle import attention as A
-    a = A.workload_arrays(w)
-    q = A.bf16_bits_to_f64(a["q_raw"])
-    t0 = time.perf_counter()
-    done_tokens = 0
-    done = 0
-    while True:
-        for b in range(w.batch):
-            K, V = A.gather_kv(a, b)
-            A.attend(q[b], K, V, a["sm_scale"])
-            done_tokens += int(w.lengths[b])
-            done += 1
-            if time.perf_counter() - t0 > budget_s:
-                break
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
-    gbs = done_tokens * w.kv_bytes_per_token() / dt / 1e9
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} requests ({done_tokens} tokens) of the {w.name} batch in {dt:.1f} s, "
-                      "float64 numpy gather + softmax attention"}
+    a, q, G = _ORACLE["a"], _ORACLE["q"], _ORACLE["G"]
+    b, kv = task
+    head = dict(a, k_raw=a["k_raw"][:, :, kv:kv + 1],
+                v_raw=None if a["v_raw"] is None else a["v_raw"][:, :, kv:kv + 1])
+    K, V = A.gather_kv(head, b)
+    A.attend(q[b, kv * G:(kv + 1) * G], K, V, a["sm_scale"])
+    return K.shape[0]
+
+
+class OraclePool:
+    """The oracle over (request, KV head) tasks of one workload, on all host cores
+    (a forked process pool) or on one (this process)."""
+
+    def __init__(self, w):
+        import multiprocessing as mp
+        from oracle import attention as A
+        a = A.workload_arrays(w)
+        _ORACLE.update(a=a, q=A.bf16_bits_to_f64(a["q_raw"]), G=w.Hq // w.Hkv)
+        self.w = w
+        self.tasks = [(b, kv) for b in range(w.batch) for kv in range(w.Hkv)]
+        self.head_bytes = w.kv_bytes_per_token() // w.Hkv
+        self.cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        self.pool = mp.get_context("fork").Pool(self.cores)
+
+    def pass_all_cores(self) -> int:
+        """One pass over every task on all cores; returns the K/V bytes attended."""
+        return sum(self.pool.imap_unordered(_oracle_task, self.tasks, chunksize=2)) * self.head_bytes
+
+    def pass_one_core(self, tasks) -> int:
+        return sum(_oracle_task(t) for t in tasks) * self.head_bytes
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def oracle_baseline(w, budget_all_s: float = 8.0, budget_one_s: float = 6.0):
+    """cpu_baseline: the oracle on all host cores (whole passes over the batch for about
+    budget_all_s) and on one core (tasks in batch order for about budget_one_s)."""
+    op = OraclePool(w)
+    try:
+        op.pass_all_cores()                                   # warm the workers
+        t0, nbytes, passes = time.perf_counter(), 0, 0
+        while passes == 0 or time.perf_counter() - t0 < budget_all_s:
+            nbytes += op.pass_all_cores()
+            passes += 1
+        all_gbs = nbytes / (time.perf_counter() - t0) / 1e9
+    finally:
+        op.close()
+    t0, nbytes1, ntask = time.perf_counter(), 0, 0
+    while ntask == 0 or time.perf_counter() - t0 < budget_one_s:
+        nbytes1 += op.pass_one_core([op.tasks[ntask % len(op.tasks)]])
+        ntask += 1
+    one_gbs = nbytes1 / (time.perf_counter() - t0) / 1e9
+    return {"value": round(all_gbs, 4), "unit": "GB/s", "cores": op.cores, "kind": "oracle",
+            "value_all_cores": round(all_gbs, 4), "cores_all": op.cores, "value_1_core": round(one_gbs, 4),
+            "sample": f"all cores: {passes} whole passes over the {w.name} batch ({len(op.tasks)} "
+                      f"(request, KV head) tasks each); 1 core: {ntask} tasks; float64 numpy oracle"}
 
 
 # ------------------------------------------------------------------- main paths
@@ -543,8 +662,9 @@ def cascade_comparison(wc, label, args, flush, plan_us=False):
     casc_arm.step()
     casc_arm.check()
     st = casc_arm.stats
-    tf = statistics.mean(time_steps(flat_arm.step, args.steps, args.warmup, flush))
-    tc = statistics.mean(time_steps(casc_arm.step, args.steps, args.warmup, flush))
+    tfs = time_steps(flat_arm.step, args.steps, args.warmup, flush)
+    tcs = time_steps(casc_arm.step, args.steps, args.warmup, flush)
+    tf, tc = statistics.mean(tfs), statistics.mean(tcs)
     kf = kernel_timing(flat_arm, args.steps, args.warmup, flush)
     kc = kernel_timing(casc_arm, args.steps, args.warmup, flush)
     flat_arm.check()
@@ -554,6 +674,7 @@ def cascade_comparison(wc, label, args, flush, plan_us=False):
     out = {
         "workload": label,
         "flat_ms": round(tf, 4), "cascade_ms": round(tc, 4),
+        "flat_rep_stats": rep_stats(tfs), "cascade_rep_stats": rep_stats(tcs),
         "flat_tokens_per_s": round(wc.batch / (tf * 1e-3), 1),
         "cascade_tokens_per_s": round(wc.batch / (tc * 1e-3), 1),
         "flat_kv_bytes": int(flat_b), "unique_kv_bytes": int(uniq_b),
@@ -572,13 +693,40 @@ def cascade_comparison(wc, label, args, flush, plan_us=False):
     return out
 
 
+def headline_summary(line: dict) -> dict:
+    """The figures a reader checks first, repeated compactly at the end of the line."""
+    out = {"flat_step_ms": line["rep_stats"], "flat_partial_frac": line["roofline"]["frac"],
+           "e2e_gbs": line["e2e"]["value"], "e2e_wall_ms": line["e2e"]["wall_ms_median"],
+           "detection_host_us": line["no_sharing_gate"]["detection_host_us"]}
+    for key, short in (("flat_vs_cascade", "cascade"), ("flat_vs_cascade_prefix_beyond_l2", "beyond_l2")):
+        c = line.get(key)
+        if c:
+            out[short] = {"flat_ms": c["flat_rep_stats"]["median_ms"], "cascade_ms": c["cascade_rep_stats"]["median_ms"],
+                          "cascade_partial_ms": c["cascade_kernels_ms"]["partial_ms"],
+                          "reduction": c["wall_time_reduction"], "removed": c["removed_read_fraction"],
+                          "criterion": c["criterion_reduction_ge_0.7x_removed"]}
+            if "criterion_on_dram_bytes" in c:
+                out[short]["criterion_dram"] = c["criterion_on_dram_bytes"]
+    m = line.get("mla")
+    if m:
+        out["mla"] = {"ms": m["rep_stats"], "partial_tflops": m["partial_kernel_tflops"],
+                      "partial_frac_bf16_burst": m["partial_kernel_frac_of_burst_bf16"]}
+    c = line.get("cpu_baseline")
+    if c:
+        out["cpu"] = {"all_cores_gbs": c["value_all_cores"], "cores": c["cores_all"], "one_core_gbs": c["value_1_core"]}
+    return out
+
+
 def run_ours(args):
     rank, world, local = dist_setup(args.gpus)
+    w = synth.flat_decode(seed=0, canary=False)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_baseline(w)          # its worker pool forks before CUDA is initialised
     torch.cuda.set_device(local)
     hbm, bf16, bf16s, peak_src = measured_peaks()
     flush = L2Flush(args.l2_flush)
 
-    w = synth.flat_decode(seed=0, canary=False)
     arm = Arm(w, enable=1)
     arm.step()
     arm.check()
@@ -604,8 +752,9 @@ def run_ours(args):
     achieved_cc = algo / (k_ms_cc * 1e-3) / 1e9
     merge_gbs = merge_bytes / (kt["merge_ms"] * 1e-3) / 1e9
 
-    et, h2d, d2h = e2e_timing(arm, args.steps, args.warmup, flush)
+    et, h2d, d2h, wall = e2e_timing(arm, args.steps, args.warmup, flush)
     e2e_ms = dist_max(statistics.mean(et), world)
+    gate = no_sharing_gate(arm, args.steps, args.warmup, flush)
 
     extra = {}
     if not args.quick and args.workload in ("all", "cascade"):
@@ -626,14 +775,15 @@ def run_ours(args):
         marm = Arm(wm, enable=1)
         marm.step()
         marm.check()
-        tm = statistics.mean(time_steps(marm.step, max(3, args.steps // 2), args.warmup, flush))
+        tms = time_steps(marm.step, max(5, args.steps // 2), args.warmup, flush)
+        tm = statistics.mean(tms)
         km = kernel_timing(marm, max(3, args.steps // 2), 1, flush)
         mb = unique_kv_bytes(wm)
         flops = float(np.sum(wm.lengths)) * wm.Hq * (wm.Dqk + wm.Dv) * 2
         extra["mla"] = {
             "workload": f"MLA decode: {wm.batch} requests U[4096,32768], 128 heads, latent 576 fp8-e4m3 "
                         "(V = first 512), page 64, tile 2048",
-            "ms": round(tm, 4), "tokens_per_s": round(wm.batch / (tm * 1e-3), 1),
+            "ms": round(tm, 4), "rep_stats": rep_stats(tms), "tokens_per_s": round(wm.batch / (tm * 1e-3), 1),
             "unique_kv_gbs": round(mb / (tm * 1e-3) / 1e9, 1),
             "tflops": round(flops / (tm * 1e-3) / 1e12, 1),
             "tensor_frac_of_sustained_bf16": round(flops / (tm * 1e-3) / 1e12 / bf16s, 4) if bf16s else None,
@@ -657,7 +807,7 @@ def run_ours(args):
 
     if rank == 0:
         line = {
-            "metric": "unique KV GB/s (flat paged decode; cascade and MLA arms alongside)",
+            "metric": METRIC,
             "value": round(value, 2),
             "unit": "GB/s",
             "n_gpus": world,
@@ -669,14 +819,12 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": "flat paged decode: batch 32, Hq=32, Hkv=8, D=128, page 16, "
-                                   "lengths U[512,4096] partial last page, 16384-page pool, tile 512, "
-                                   "then merge_states",
-                       "batch": w.batch, "unique_kv_bytes": kv_bytes,
-                       "l2": "flushed: " + flush.describe(),
-                       "flush_us": round(flush_us(flush), 1),
-                       "host_enqueue_us": round(statistics.mean(host_us), 1),
-                       "parallelism": f"replicas x{world}"},
+            "config": flat_config(w, kv_bytes, args.l2_flush),
+            "rep_stats": rep_stats(times),
+            "timing_notes": {"flush_us": round(flush_us(flush), 1),
+                             "host_enqueue_us": round(statistics.mean(host_us), 1),
+                             "replicas": world,
+                             "lengths": "L~U[512,4096] with a partial last page (no multiple of 16)"},
             "decode_tokens_per_s": round(world * w.batch / (ms_max * 1e-3), 1),
             "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
             "pct_of_measured_hbm": round(100 * value / world / hbm, 2),
@@ -697,6 +845,8 @@ def run_ours(args):
             "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h),
+                    "wall_ms_median": round(statistics.median(wall), 5),
+                    "wall_gbs": round(world * kv_bytes / (statistics.median(wall) * 1e-3) / 1e9, 1),
                     "transfers": "inputs: query rows and page ids read by the partial kernel from "
                                  "pinned host memory (no staging copy); plan: launch parameters; "
                                  "outputs: merge-kernel stores into pinned host memory"},
@@ -704,9 +854,11 @@ def run_ours(args):
             "wall_s": round(t_wall, 3),
             "clocks": clk.summary(),
         }
+        line["no_sharing_gate"] = gate
         line.update(extra)
-        if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = oracle_baseline(w)
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        line["summary"] = headline_summary(line)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -714,41 +866,37 @@ def run_ours(args):
 
 
 def run_reference(args):
-    """The oracle timed on the host cores, on the flat workload (rank 0 only)."""
+    """The oracle timed on the host cores on the flat workload (rank 0 only): each step
+    is one pass over the whole batch, its (request, KV head) tasks spread over every
+    core this process may use."""
     rank = int(os.environ.get("RANK", 0))
     if rank != 0:
         return
     w = synth.flat_decode(seed=0, canary=False)
     kv_bytes = unique_kv_bytes(w)
-    from oracle import attention as A
-    a = A.workload_arrays(w)
-    q = A.bf16_bits_to_f64(a["q_raw"])
-    reqs = list(range(min(8, w.batch)))           # bounded sample per step
-    sample_bytes = int(np.sum(w.lengths[reqs])) * w.kv_bytes_per_token()
-
-    def step():
-        for b in reqs:
-            K, V = A.gather_kv(a, b)
-            A.attend(q[b], K, V, a["sm_scale"])
-
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = (time.perf_counter() - t0) / args.steps
-    value = sample_bytes / dt / 1e9
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    op = OraclePool(w)
+    try:
+        for _ in range(args.warmup):
+            op.pass_all_cores()
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            nbytes = op.pass_all_cores()
+            times.append((time.perf_counter() - t0) * 1e3)
+    finally:
+        op.close()
+    dt = statistics.mean(times)
+    value = nbytes / (dt * 1e-3) / 1e9
     print(json.dumps({
-        "impl": "reference", "metric": "unique KV GB/s (flat paged decode; cascade and MLA arms alongside)",
-        "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "flat paged decode: batch 32, Hq=32, Hkv=8, D=128, page 16, "
-                               "lengths U[512,4096] partial last page, 16384-page pool, tile 512",
-                   "sample": f"requests {reqs[0]}..{reqs[-1]} per step", "unique_kv_bytes": kv_bytes},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{len(reqs)} of {w.batch} requests per step, float64 numpy"},
+        "config": flat_config(w, kv_bytes, args.l2_flush),
+        "rep_stats": rep_stats(times),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": op.cores, "kind": "oracle",
+                         "sample": f"whole {w.name} batch per step: {len(op.tasks)} (request, KV head) "
+                                   "tasks of the float64 numpy oracle on all cores; no GPU, so the "
+                                   "L2 flush of the config does not apply"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

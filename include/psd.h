@@ -19,8 +19,11 @@
  *     On failure psd_last_error() returns a thread-local message.
  *   - "device" pointers are CUDA global memory on the context's device; "host"
  *     pointers are ordinary CPU memory.  All buffers are owned by the caller.  The
- *     library allocates no device memory on any call: scratch lives in a
- *     caller-provided workspace sized by psd_workspace_bytes().
+ *     decode, merge, planning and append entry points allocate no device memory:
+ *     scratch lives in a caller-provided workspace sized by psd_workspace_bytes()
+ *     (or, for cascade_decode_no_alloc, in the library's own fixed array).  The one
+ *     exception is psd_autotune_tile, which allocates its L2-flush buffer once per
+ *     context (freed by psd_destroy).
  *   - Device work is enqueued asynchronously on the caller's stream (NULL = the
  *     legacy default stream).  Host arrays passed in may be reused as soon as the
  *     call returns.
@@ -191,6 +194,18 @@ psd_status psd_set_partial_kernel(psd_ctx *ctx, int32_t kind);
  * launch; any pointer may be NULL).  Enabling creates the events (host-side CUDA
  * objects, no device memory). */
 psd_status psd_set_timing(psd_ctx *ctx, int32_t enable);
+/* Testing aid for the kernels' bounded waits (no counterpart on the pages).  With
+ * from_tile >= 0, the 16-row-group tensor-core and CUDA-core partial kernels launched
+ * through this context issue no loads for any item's tiles at index from_tile and
+ * later (16-token tiles of the tensor-core kernel, the CUDA-core kernel's own ring
+ * tiles), so their waits for those tiles run out after wait_limit_cycles (1e5 to
+ * 2e9 SM cycles); each timed-out warp stops consuming tiles, the kernel completes,
+ * and the call's fault word carries PSD_FAULT_WAIT_TIMEOUT for
+ * psd_check_device_error.  Tiles before from_tile are waited for before any
+ * withheld one, so no copy is in flight when a wait gives up.  Outputs of such a
+ * call are meaningless.  from_tile < 0 switches the aid off (the default; the
+ * other kernels ignore it).  PSD_ERR_INVALID_ARG for a limit outside the range. */
+psd_status psd_test_withhold_loads(psd_ctx *ctx, int32_t from_tile, int64_t wait_limit_cycles);
 psd_status psd_get_kernel_times(psd_ctx *ctx, float *level0_ms, float *partial_ms, float *merge_ms);
 /* Thread-local message describing the last failure on this thread. */
 const char *psd_last_error(void);
@@ -243,7 +258,7 @@ psd_status psd_plan_capacity(const psd_page_table *host, int32_t *batch_capacity
                              int32_t *item_capacity);
 
 /* Plan cache (mlxcel PR #1004, Left out / unsure: detection re-runs per layer and
- * per step; a CascadePlan slot in the plan cache is the named follow-up).  The key
+ * per step; a cascade-plan entry in the plan cache is the named follow-up).  The key
  * is everything psd_plan_decode reads: the resolved enable switch, both thresholds,
  * tile_tokens, page_size, batch and the full contents of page_indptr, page_indices
  * and last_page_len, since a split-KV plan depends on KV lengths as well as on the
@@ -349,10 +364,19 @@ psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
  *     rejected with PSD_ERR_WORKSPACE_TOO_SMALL and a message naming both sizes.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: do not reset the device (cudaDeviceReset) while using this entry
+ *     point.
  *   - Every call on a device shares the one array, which keeps the last call's
  *     contents; each call clears the fault word itself.  Calls whose device work
  *     overlaps (other streams, unordered host threads) race on the array.
+ *   - The work lists are laid out and ordered as cascade_decode lays them out
+ *     (longest items first, both levels in one launch where one kernel serves
+ *     them).  When the 16-row-group tensor-core kernel runs every launch and the
+ *     lists fit in its launch parameters (up to about 800 items and 1023
+ *     requests), they travel there and the call makes no host-to-device copy;
+ *     otherwise one cudaMemcpyAsync from pageable host memory places them in the
+ *     array.
  *   - fault_bits_dev (device int32, nullable) receives the call's PSD_FAULT_* bits.
  * Results equal cascade_decode's on the same plan. */
 psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_args *args,
@@ -361,9 +385,10 @@ psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_args *args,
                                    psd_stream_t stream);
 
 /* ------------------------------------------------- several and nested shared spans
- * An extension the pages scope out (mlxcel PR #1004, Task item 1: "One shared level
- * only, as scoped"; Left out / unsure: nested sharing, a common system prompt plus a
- * per-tenant sub-prefix, "would need a third level").  Planning rules:
+ * An extension the pages scope out (mlxcel PR #1004: Task item 1 keeps to a single
+ * shared level; Left out / unsure lists nested sharing, a system prompt common to
+ * all plus a per-tenant sub-prefix, as not attempted because it needs another
+ * level).  Planning rules:
  *   every first-page group that passes the thresholds becomes a segment (not only
  *   the one with the most saved reads); inside a segment [start, start + span) its
  *   members are grouped again by their page at start + span and each group gets the

@@ -9,9 +9,10 @@ Source: mlxcel PR #1004, "compute shared prompt prefixes once per decode batch".
   * Detection section: a CSR page table; one block id is one physical pool row.
 ROCm ATOM PR #1701, section 3.2: fp8 latent KV is dequantised as value * k_scale.
 
-The method reaches exactly the dense attention result (Decomposition: "the merge is
-exact up to f32 rounding"), so the oracle is that definition: gather a request's
-pages into contiguous K/V, then plain softmax attention in float64.
+The Decomposition section states that the two key ranges of the cascade are
+disjoint, so its merge reproduces dense attention apart from f32 rounding.  The
+oracle is therefore that definition: gather a request's pages into contiguous K/V,
+then plain softmax attention in float64.
 """
 from __future__ import annotations
 
@@ -103,8 +104,8 @@ def attend(q_b: np.ndarray, K: np.ndarray, V: np.ndarray, sm_scale: float):
     """Softmax attention of one request's query heads over its keys (float64).
 
     q_b [Hq, Dqk], K [L, Hkv, Dqk], V [L, Hkv, Dv].  Query head h reads KV head
-    h // G with G = Hq / Hkv (Decomposition section: "maps query head h to KV head
-    h / NRep").  Returns o [Hq, Dv] and the log-sum-exp in log2 units
+    h // G with G = Hq / Hkv (the head mapping of the Decomposition section, whose
+    NRep is this G).  Returns o [Hq, Dv] and the log-sum-exp in log2 units
         lse2 = log2 sum_j 2^(s_j * log2 e) = (ln sum_j e^(s_j)) / ln 2,
     i.e. the partial kernel's m + log2(l) with m taken on log2-scaled scores
     (Merge contract section).  An empty key set gives o = 0, lse2 = -inf.

@@ -199,10 +199,10 @@ def env_switch(value, default: bool) -> bool:
 
 
 # ------------------------------------------------ several and nested shared spans
-# An extension the pages scope out (Task item 1: "One shared level only, as scoped";
-# Left out / unsure: "Not attempted: nested sharing.  A common system prompt plus a
-# per-tenant sub-prefix would need a third level").  Readings, each pinned by a
-# hand-made case:
+# An extension the pages scope out (Task item 1 keeps to a single shared level; Left
+# out / unsure names nested sharing, a system prompt common to all plus a per-tenant
+# sub-prefix, as not attempted, since it needs one more level).  Readings, each
+# pinned by a hand-made case:
 #   N1  every first-page group that passes the thresholds becomes a segment (the
 #       groups are disjoint), not only the one with the most saved reads;
 #   N2  inside a segment [start, start + span), the members are grouped again by

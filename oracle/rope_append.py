@@ -1,10 +1,10 @@
 """RoPE + KV append into the paged pool (oracle; test infrastructure only).
 
 Source: ROCm ATOM PR #1701.
-  * Section 1 and 3.3 ("Fixed fused kernel + compute_all_q_rope"): one fused kernel
-    applies RoPE to every query and to the new token's rope part of K, concatenates
-    the non-rope latent with the roped part ("concat"), and writes the row into the
-    KV cache only for the slots this rank owns.
+  * Sections 1 and 3.3 (the fused RoPE kernel that also ropes every query): one
+    fused kernel applies RoPE to every query and to the new token's rope part of K,
+    joins the non-rope latent with the roped part, and writes the row into the KV
+    cache only for the slots this rank owns.
   * Section 3.2: fp8 KV is stored as codes that dequantise as code * k_scale.
 mlxcel PR #1004, Left out / unsure: fused RoPE + KV-append decode kernels (#905) are
 the step before this path.

@@ -82,6 +82,11 @@ class Context:
                 "tensor_core": L.PSD_KERNEL_TENSOR_CORE}[kind]
         L.check(L.load().psd_set_partial_kernel(self._h, code))
 
+    def test_withhold_loads(self, from_tile: int, wait_limit_cycles: int = 0):
+        """psd_test_withhold_loads: a testing aid that makes the partial kernels' waits
+        for tiles from `from_tile` on run out (from_tile < 0 switches it off)."""
+        L.check(L.load().psd_test_withhold_loads(self._h, int(from_tile), int(wait_limit_cycles)))
+
     def set_timing(self, enable: bool = True):
         """psd_set_timing: CUDA events around every kernel the library launches."""
         L.check(L.load().psd_set_timing(self._h, int(bool(enable))))
@@ -459,7 +464,9 @@ def check_device_error(ctx: Context, workspace: torch.Tensor, stream=None) -> in
     st = L.load().psd_check_device_error(ctx.handle, _dev_ptr(workspace, "workspace"), _stream(stream),
                                          C.byref(bits))
     if st != L.PSD_OK:
-        raise L.PsdError(st, L.load().psd_last_error().decode(errors="replace"))
+        err = L.PsdError(st, L.load().psd_last_error().decode(errors="replace"))
+        err.fault_bits = int(bits.value)
+        raise err
     return int(bits.value)
 
 

@@ -44,6 +44,8 @@ using namespace psd;
 namespace psd {
 
 static const float kLog2e = 1.4426950408889634f;
+// Longest wait a test may set (about 1 s at 2 GHz): below the default limit.
+static const long long kMaxTestWaitCycles = 2000000000LL;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -149,7 +151,7 @@ psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStr
 
 }  // namespace psd
 
-namespace {
+namespace psd {
 
 // Both cascade levels can share one launch when the 16-row-group tensor-core
 // kernel serves both and level 1 fits one row group.
@@ -157,6 +159,10 @@ bool dispatch_fused(const PartialLaunch &L0, const PartialLaunch &L1, const Devi
   if (dev.partial_kernel == PSD_KERNEL_CUDA_CORE) return false;
   return partial_tcs_supports(L0) && partial_tcs_supports(L1) && L1.G_cta <= 16;
 }
+
+}  // namespace psd
+
+namespace {
 
 // Work lists of one call, placed either in the workspace by one H2D copy or, when
 // they fit and every launch of the call reads them from its parameters, in `block`
@@ -308,6 +314,17 @@ extern "C" psd_status psd_set_partial_kernel(psd_ctx *c, int32_t kind) {
   if (kind != PSD_KERNEL_AUTO && kind != PSD_KERNEL_CUDA_CORE && kind != PSD_KERNEL_TENSOR_CORE)
     return fail(PSD_ERR_INVALID_ARG, "partial kernel kind %d", kind);
   c->dev.partial_kernel = kind;
+  return PSD_OK;
+}
+
+extern "C" psd_status psd_test_withhold_loads(psd_ctx *c, int32_t from_tile, int64_t wait_limit_cycles) {
+  clear_error();
+  if (!c) return fail(PSD_ERR_INVALID_ARG, "NULL context");
+  if (from_tile >= 0 && (wait_limit_cycles < 100000 || wait_limit_cycles > kMaxTestWaitCycles))
+    return fail(PSD_ERR_INVALID_ARG, "psd_test_withhold_loads: wait limit %lld outside [1e5, %lld] cycles",
+                (long long)wait_limit_cycles, (long long)kMaxTestWaitCycles);
+  c->dev.test_withhold_from = from_tile >= 0 ? from_tile : -1;
+  c->dev.test_wait_limit = from_tile >= 0 ? wait_limit_cycles : 0;
   return PSD_OK;
 }
 

@@ -94,5 +94,7 @@ PartialKind select_partial(const PartialLaunch &L, const DeviceInfo &dev);
 // The launch may leave empty partial rows (LSE -inf, v not written) for the merge.
 bool writes_empty_rows(const PartialLaunch &L, const DeviceInfo &dev);
 psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s);
+// Both cascade levels can share one launch of the 16-row-group tensor-core kernel.
+bool dispatch_fused(const PartialLaunch &L0, const PartialLaunch &L1, const DeviceInfo &dev);
 
 }  // namespace psd

@@ -69,12 +69,14 @@ __device__ __forceinline__ void raise_fault(const FaultRef &f, uint32_t bits) {
 }
 
 // Waits for phase `parity` of the barrier; returns false (and flags the fault
-// word) if it has not completed within kWaitLimitCycles.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const FaultRef &fault) {
+// word) if it has not completed within `limit` cycles (kWaitLimitCycles unless a
+// launch was given a shorter limit for testing).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const FaultRef &fault,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       raise_fault(fault, PSD_FAULT_WAIT_TIMEOUT);
       return false;
     }

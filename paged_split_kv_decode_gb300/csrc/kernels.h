@@ -15,6 +15,12 @@ struct DeviceInfo {
   int smem_optin = 0;
   void *encode_tiled = nullptr;  // driver cuTensorMapEncodeTiled
   int partial_kernel = 0;        // psd_partial_kernel preference for G <= 16
+  // Testing aid for the bounded waits (psd_test_withhold_loads): the 16-row-group
+  // tensor-core and CUDA-core partial kernels issue no loads for tiles at index
+  // test_withhold_from and later of any item (-1: off), and give up a wait after
+  // test_wait_limit cycles (0: the default limit).
+  int32_t test_withhold_from = -1;
+  int64_t test_wait_limit = 0;
 };
 
 // The workspace's fault word: 64 bits at its start, (epoch << 32) | fault bits.  The

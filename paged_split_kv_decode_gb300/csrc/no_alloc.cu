@@ -18,6 +18,7 @@
 
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "context.h"
 
@@ -38,7 +39,8 @@ void *g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  The first call on a
 // device looks it up with cudaGetSymbolAddress (host code only sees a host-side
-// stand-in under the array's name, never a usable device address).
+// stand-in under the array's name, never a usable device address) and keeps it for
+// the life of the process; a cudaDeviceReset would invalidate the kept address.
 psd_status scratch_address(int device, uint8_t **out) {
   if (device < 0 || device >= kMaxDevices)
     return psd::fail(PSD_ERR_UNSUPPORTED, "cascade_decode_no_alloc: device %d out of range", device);
@@ -52,14 +54,6 @@ psd_status scratch_address(int device, uint8_t **out) {
     g_scratch_addr[device] = p;
   }
   *out = static_cast<uint8_t *>(g_scratch_addr[device]);
-  return PSD_OK;
-}
-
-psd_status copy_in(void *dst, const void *src, size_t bytes, cudaStream_t s) {
-  if (!bytes) return PSD_OK;
-  cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess)
-    return psd::fail(PSD_ERR_CUDA, "cascade_decode_no_alloc: upload: %s", cudaGetErrorString(e));
   return PSD_OK;
 }
 
@@ -121,18 +115,53 @@ extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_arg
   if (st != PSD_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  // Work lists straight from the caller's host plan; the fault word starts at 0.
-  cudaError_t e = cudaMemsetAsync(ws, 0, 256, s);
+  // The lists as cascade_decode lays them out: items (level 0, then level 1), the
+  // longest-first CTA order of each level, members, member row bases, o_indptr.
+  std::vector<uint8_t> host(lay.lists_bytes, 0);  // the header (fault word) stays 0
+  psd_work_item *hi = reinterpret_cast<psd_work_item *>(host.data() + lay.items_off);
+  if (n0) std::memcpy(hi, plan->l0_items, sizeof(psd_work_item) * n0);
+  if (n1) std::memcpy(hi + n0, plan->l1_items, sizeof(psd_work_item) * n1);
+  int32_t *ho = reinterpret_cast<int32_t *>(host.data() + lay.order_off);
+  longest_first(plan->l0_items, n0, ho);
+  longest_first(plan->l1_items, n1, ho + n0);
+  if (M) {
+    std::memcpy(host.data() + lay.members_off, plan->members, sizeof(int32_t) * M);
+    std::memcpy(host.data() + lay.row_base_off, plan->member_row_base, sizeof(int32_t) * M);
+  }
+  std::memcpy(host.data() + lay.indptr_off, plan->o_indptr, sizeof(int32_t) * (B + 1));
+
+  // Both levels in one launch where the 16-row-group tensor-core kernel serves them;
+  // the lists then travel in the launch parameters when they fit, and only the fault
+  // word is cleared on the device.  Otherwise one copy from this host buffer (the
+  // runtime stages pageable memory before the call returns) places the lists and the
+  // cleared header in the scratch.
+  const bool fused = M > 0 && dispatch_fused(L0, L1, ctx->dev);
+  const bool tcs_only = select_partial(L1, ctx->dev) == PartialKind::kTensorSmall &&
+                        (M == 0 || fused || select_partial(L0, ctx->dev) == PartialKind::kTensorSmall);
+  const size_t used = lay.indptr_off - lay.items_off;
+  const bool inl = tcs_only && used <= kInlineListBytes && B + 1 <= kInlineIndptr;
+  InlineLists block;
+  cudaError_t e;
+  if (inl) {
+    block.used = used;
+    std::memcpy(block.bytes, host.data() + lay.items_off, used);
+    e = cudaMemsetAsync(ws, 0, sizeof(unsigned long long), s);
+  } else {
+    e = cudaMemcpyAsync(ws, host.data(), host.size(), cudaMemcpyHostToDevice, s);
+  }
   if (e != cudaSuccess)
-    return fail(PSD_ERR_CUDA, "cascade_decode_no_alloc: clear: %s", cudaGetErrorString(e));
-  const size_t isz = sizeof(psd_work_item);
-  if ((st = copy_in(ws + lay.items_off, plan->l0_items, isz * n0, s)) != PSD_OK) return st;
-  if ((st = copy_in(ws + lay.items_off + isz * n0, plan->l1_items, isz * n1, s)) != PSD_OK) return st;
-  if ((st = copy_in(ws + lay.members_off, plan->members, sizeof(int32_t) * M, s)) != PSD_OK) return st;
-  if ((st = copy_in(ws + lay.row_base_off, plan->member_row_base, sizeof(int32_t) * M, s)) != PSD_OK)
-    return st;
-  if ((st = copy_in(ws + lay.indptr_off, plan->o_indptr, sizeof(int32_t) * (B + 1), s)) != PSD_OK)
-    return st;
+    return fail(PSD_ERR_CUDA, "cascade_decode_no_alloc: lists: %s", cudaGetErrorString(e));
+  auto place = [&](PartialLaunch &L) {  // list pointers into the parameter block
+    if (!inl) return;
+    auto off = [&](const void *ptr) -> uint32_t {
+      return ptr ? uint32_t(static_cast<const uint8_t *>(ptr) - (ws + lay.items_off)) : 0u;
+    };
+    L.inline_lists = &block;
+    L.inl_items = off(L.items);
+    L.inl_order = off(L.order);
+    L.inl_members = off(L.members);
+    L.inl_row_base = off(L.member_row_base);
+  };
 
   float *vpart = reinterpret_cast<float *>(ws + lay.vpart_off);
   float *lpart = reinterpret_cast<float *>(ws + lay.lpart_off);
@@ -140,25 +169,44 @@ extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_arg
   // fault bits whatever the epoch.
   const FaultRef fault = next_fault(ctx, ws);
   const psd_work_item *ditems = reinterpret_cast<const psd_work_item *>(ws + lay.items_off);
-  if (M > 0) {
-    L0.items = ditems;
-    L0.num_items = n0;
-    L0.members = reinterpret_cast<const int32_t *>(ws + lay.members_off);
-    L0.member_row_base = reinterpret_cast<const int32_t *>(ws + lay.row_base_off);
-    L0.v_out = vpart;
-    L0.lse_out = lpart;
-    L0.fault = fault;
-    if ((st = launch_partial(L0, ctx->dev, s)) != PSD_OK) return st;
+  const int32_t *dorder = reinterpret_cast<const int32_t *>(ws + lay.order_off);
+  const int32_t *dmembers = reinterpret_cast<const int32_t *>(ws + lay.members_off);
+  const int32_t *drow_base = reinterpret_cast<const int32_t *>(ws + lay.row_base_off);
+  if (fused) {
+    L1.items = ditems;
+    L1.members = dmembers;
+    L1.member_row_base = drow_base;
+    L1.fused_segments = 1;
+    L1.fused_l0_items = n0;
+    L1.seg_items[0] = n0;
+    L1.seg_rows[0] = L0.G_cta;
+    L1.seg_member0[0] = 0;
+  } else {
+    if (M > 0) {  // level 0 first, on the same stream
+      L0.items = ditems;
+      L0.order = dorder;
+      L0.num_items = n0;
+      L0.members = dmembers;
+      L0.member_row_base = drow_base;
+      L0.v_out = vpart;
+      L0.lse_out = lpart;
+      L0.fault = fault;
+      place(L0);
+      if ((st = launch_partial(L0, ctx->dev, s)) != PSD_OK) return st;
+    }
+    L1.items = ditems + n0;
+    L1.items_host = plan->l1_items;
   }
-  L1.items = ditems + n0;
-  L1.items_host = plan->l1_items;
+  L1.order = dorder + n0;
   L1.num_items = n1;
   L1.v_out = vpart;
   L1.lse_out = lpart;
   L1.fault = fault;
+  place(L1);
   if ((st = launch_partial(L1, ctx->dev, s)) != PSD_OK) return st;
   st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq,
-                    args->Dv, o, lse, ctx->dev, s, true, writes_empty_rows(L1, ctx->dev));
+                    args->Dv, o, lse, ctx->dev, s, true, writes_empty_rows(L1, ctx->dev),
+                    inl ? plan->o_indptr : nullptr);
   if (st != PSD_OK) return st;
   if (fault_bits_dev) {
     e = cudaMemcpyAsync(fault_bits_dev, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);

@@ -48,6 +48,10 @@ struct CCParams {
   int Hq_req, Dqk, Dv, page_size, sub, Gm, G_cta;  // sub = tokens per ring tile
   int tpp_log2;  // log2(page_size / sub), or -1 if not a power of two
   float q_scale, v_scale;
+  // Testing aid: tiles at this index and later get no loads (INT_MAX: all do), and a
+  // wait gives up after wait_limit cycles.
+  int withhold_from;
+  long long wait_limit;
 };
 
 // Sums G per-lane values over the LPT lanes of a token slot, halving the number
@@ -164,7 +168,11 @@ __global__ void __launch_bounds__(kWarps * 32, G <= 4 ? 4 : 2)
     if (lane == 0) {
       const int slot0 = (t - pos * TPP) * SUB;
       const uint32_t bar = smem_u32(&bars[s]);
-      if (id < 0 || int64_t(id) >= p.num_pages) {
+      if (t >= p.withhold_from) {
+        // testing aid: no load and no arrival, so the wait for this tile runs out.
+        // Every later tile is withheld as well, and the tiles before it were waited
+        // for first, so no copy is in flight when that wait gives up.
+      } else if (id < 0 || int64_t(id) >= p.num_pages) {
         raise_fault(p.fault, PSD_FAULT_PAGE_ID);
         mbar_arrive(bar);
       } else {
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(kWarps * 32, G <= 4 ? 4 : 2)
     const int id = page_id(tile_pos(t), win_c, pid_c);
     const bool page_ok = id >= 0 && int64_t(id) < p.num_pages;
     const int valid = page_ok ? min(SUB, it.n_tokens - t * SUB) : 0;
-    const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / kStages) & 1u, p.fault);
+    const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / kStages) & 1u, p.fault, p.wait_limit);
     if (!__all_sync(0xffffffffu, ok)) break;
     const uint8_t *kb = ring + size_t(s) * 2 * tile_bytes;
     const uint8_t *vb = kb + tile_bytes;
@@ -398,6 +406,8 @@ psd_status launch_cc(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t
   p.G_cta = L.G_cta;
   p.q_scale = L.q_scale;
   p.v_scale = L.v_scale;
+  p.withhold_from = dev.test_withhold_from >= 0 ? dev.test_withhold_from : 0x7fffffff;
+  p.wait_limit = dev.test_wait_limit > 0 ? dev.test_wait_limit : kWaitLimitCycles;
   const size_t smem = cc_smem_bytes<D, G>(sub);
   if (smem > size_t(dev.smem_optin))
     return fail(PSD_ERR_UNSUPPORTED, "page_size %d needs %zu bytes of shared memory", L.page_size, smem);

@@ -73,6 +73,10 @@ struct TCSParams {
   int seg_task_end[PartialLaunch::kMaxFusedSegments], seg_item0[PartialLaunch::kMaxFusedSegments];
   int seg_rows[PartialLaunch::kMaxFusedSegments], seg_member0[PartialLaunch::kMaxFusedSegments];
   float q_scale, v_scale;
+  // Testing aid: tiles at this index and later get no loads (INT_MAX: all do), and a
+  // wait gives up after wait_limit cycles.
+  int withhold_from;
+  long long wait_limit;
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
@@ -278,7 +282,11 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
     if (lane == 0) {
       const int slot0 = (t - pos * TPP) * kTileTok;
       const uint32_t bar = smem_u32(&bars[s]);
-      if (id < 0 || int64_t(id) >= p.num_pages) {
+      if (t >= p.withhold_from) {
+        // testing aid: no load and no arrival, so the wait for this tile runs out.
+        // Every later tile is withheld as well, and the tiles before it were waited
+        // for first, so no copy is in flight when that wait gives up.
+      } else if (id < 0 || int64_t(id) >= p.num_pages) {
         raise_fault(p.fault, PSD_FAULT_PAGE_ID);
         mbar_arrive(bar);
       } else {
@@ -324,7 +332,7 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
     const int id = page_id(tile_pos(t), win_c, pid_c);
     const bool page_ok = id >= 0 && int64_t(id) < p.num_pages;
     const int valid = page_ok ? min(kTileTok, it.n_tokens - t * kTileTok) : 0;
-    const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / n_stages) & 1u, p.fault);
+    const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / n_stages) & 1u, p.fault, p.wait_limit);
     if (!__all_sync(0xffffffffu, ok)) break;
     if (valid > 0) {
       uint8_t *stage = ring + size_t(s) * 2 * TILE_BYTES;
@@ -603,6 +611,8 @@ psd_status launch_tcs(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_
   p.tpp_log2 = (tpp & (tpp - 1)) == 0 ? __builtin_ctz(unsigned(tpp)) : -1;
   p.q_scale = L.q_scale;
   p.v_scale = L.v_scale;
+  p.withhold_from = dev.test_withhold_from >= 0 ? dev.test_withhold_from : 0x7fffffff;
+  p.wait_limit = dev.test_wait_limit > 0 ? dev.test_wait_limit : kWaitLimitCycles;
   p.n_l0_tasks = 0;
   p.l1_base = 0;
   p.nseg = 0;

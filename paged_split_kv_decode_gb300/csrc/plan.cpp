@@ -281,9 +281,9 @@ extern "C" psd_status psd_plan_capacity(const psd_page_table *host, int32_t *bat
 }
 
 // ------------------------------------------------ several and nested shared spans
-// (An extension the pages scope out: mlxcel PR #1004, Task item 1 "One shared level
-// only, as scoped"; Left out / unsure, nested sharing of a system prompt plus a
-// per-tenant sub-prefix.)  Every first-page group passing the thresholds becomes a
+// (An extension the pages scope out: mlxcel PR #1004, Task item 1 keeps to a single
+// shared level; Left out / unsure lists nested sharing of a system prompt plus a
+// per-tenant sub-prefix as not attempted.)  Every first-page group passing the thresholds becomes a
 // segment; inside a segment the members regroup by their page at its end and the
 // same rules apply from there, up to max_levels; segments depth first, groups in
 // order of their lowest batch index.

@@ -1,8 +1,8 @@
 // Decode-plan cache: detection and cascade planning memoised across layers and steps.
 //
 // The pages leave this as a follow-up: the plan cache holds the page table, but the
-// detection scan re-runs per layer per step (mlxcel PR #1004, Left out / unsure: "a
-// CascadePlan slot in the existing plan cache").  Another page reports a bug in
+// detection scan re-runs per layer per step (mlxcel PR #1004, Left out / unsure names
+// a cascade-plan entry in that cache as the follow-up).  Another page reports a bug in
 // exactly such a cache: it was keyed by rows, although split-KV also depends on the
 // KV length (FreeToken issue #750, Layer-major prefill for offloaded MoE, Attention
 // batching section).  So the key here is everything psd_plan_decode reads: the

@@ -115,3 +115,55 @@ def test_fresh_workspace_garbage_is_not_a_fault():
     o = torch.empty((w.batch, w.Hq, w.Dv), device="cuda")
     psd.cascade_decode(ctx(), d.args(), plan, o, None, ws)
     assert psd.check_device_error(ctx(), ws) == 0
+
+
+PSD_FAULT_WAIT_TIMEOUT = 2
+
+
+def _wide_level0_cascade():
+    """16 members sharing an 8192-token prefix split into 128-token chunks: 64 chunks x
+    8 KV heads of 64 stacked rows, enough 64-row blocks to fill a wave, so level 0 runs
+    in the shared-tile form."""
+    import dataclasses
+    w = synth.cascade_decode(seed=4, members=16, others=4, shared_tokens=8192)
+    return dataclasses.replace(w, tile_tokens=128)
+
+
+@pytest.mark.parametrize("case", ["cuda_core_flat", "tensor_core_cascade", "tensor_core_shared_tiles"])
+def test_bounded_wait_runs_out_and_is_reported(case):
+    """A wait that nothing completes gives up after its limit: the partial kernels are
+    told to withhold the loads of every tile from index 1 on, so the waits for those
+    tiles run out (about 1 ms limit), every warp stops, the call completes, and
+    psd_check_device_error reports PSD_FAULT_WAIT_TIMEOUT.  The next decode on the
+    same context is clean and matches the oracle."""
+    from oracle import attention as A
+    from _gpu_util import assert_close, use_kernel
+    w = _wide_level0_cascade() if case == "tensor_core_shared_tiles" else synth.tiny_cascade(seed=2)
+    d = Dev(w)
+    enable = 0 if case == "cuda_core_flat" else 1
+    kind = "cuda_core" if case == "cuda_core_flat" else "auto"
+    with use_kernel(kind):
+        plan = psd.plan_decode(d.table, w.tile_tokens, enable, w.min_shared_pages, w.min_members)
+        assert (plan.num_members > 0) == bool(enable)
+        o = torch.empty((w.batch, w.Hq, w.Dv), device="cuda")
+        lse = torch.empty((w.batch, w.Hq), device="cuda")
+        ws = psd.workspace_for(plan, w.Hq, w.Dv, "cuda")
+        ctx().test_withhold_loads(1, 2_000_000)
+        try:
+            psd.cascade_decode(ctx(), d.args(), plan, o, lse, ws)
+            with pytest.raises(psd.PsdError) as e:
+                psd.check_device_error(ctx(), ws)
+        finally:
+            ctx().test_withhold_loads(-1)
+        assert e.value.status == 4 and e.value.fault_bits == PSD_FAULT_WAIT_TIMEOUT
+        psd.cascade_decode(ctx(), d.args(), plan, o, lse, ws)
+        assert psd.check_device_error(ctx(), ws) == 0
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o.cpu().double().numpy(), lse.cpu().double().numpy(), ro, rl, "bf16", case)
+
+
+def test_withhold_loads_rejects_a_limit_outside_its_range():
+    for bad in (10, 5_000_000_000):
+        with pytest.raises(psd.PsdError):
+            ctx().test_withhold_loads(1, bad)
+    ctx().test_withhold_loads(-1)

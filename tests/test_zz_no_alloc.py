@@ -59,3 +59,53 @@ def test_no_alloc_rejects_plans_beyond_its_scratch():
     with pytest.raises(psd.PsdError) as e:
         psd.cascade_decode_no_alloc(ctx(), d.args(), plan, o)
     assert e.value.status == 5 and "static scratch holds 16777216 bytes" in str(e.value)
+
+
+def test_no_alloc_smaller_plan_after_larger_plan_against_oracle():
+    """A large cascade plan and then the tiny one on the same array: stale partial rows
+    or LSE values the first call left behind must not reach the second call's
+    outputs.  Both are checked against the float64 oracle."""
+    from oracle import attention as A
+    from _gpu_util import assert_close
+    for w in (synth.cascade_decode(seed=1), synth.tiny_cascade(seed=1)):
+        d = Dev(w)
+        plan = psd.plan_decode(d.table, w.tile_tokens, 1, w.min_shared_pages, w.min_members)
+        assert plan.num_members > 0
+        o, lse, _ = _no_alloc(d, plan)
+        ro, rl = A.decode_attention(A.workload_arrays(w))
+        assert_close(o, lse, ro, rl, w.kv_dtype, f"no_alloc {w.name}")
+
+
+def _small_fp8(latent):
+    rng = np.random.default_rng(77 + int(latent))
+    if latent:
+        lengths = [int(x) for x in rng.integers(1, 4000, size=3)]
+        return synth._make("mla_small", rng, lengths, Hq=128, Hkv=1, Dqk=576, Dv=512, page_size=64,
+                           num_pages=sum((L + 63) // 64 for L in lengths) + 2, tile_tokens=2048,
+                           kv_dtype="fp8_e4m3", latent_v=True)
+    lengths = [int(x) for x in rng.integers(1, 1500, size=6)]
+    for m in (0, 1, 4):
+        lengths[m] = max(lengths[m], 4 * 16 + 5)
+    return synth._make("fp8_small", rng, lengths, Hq=16, Hkv=2, Dqk=128, Dv=128, page_size=16,
+                       num_pages=sum((L + 15) // 16 for L in lengths) + 2, tile_tokens=128,
+                       kv_dtype="fp8_e4m3", shared=([0, 1, 4], 4), min_shared_pages=1, min_members=2)
+
+
+@pytest.mark.parametrize("latent", [False, True], ids=["fp8_separate_kv_cascade", "fp8_mla_latent"])
+def test_no_alloc_fp8_and_mla_plans(latent):
+    """fp8 pools: separate K and V with a shared prefix (the 64-row kernel for both
+    levels, lists copied into the array), and the MLA latent (the tcgen05 kernel with
+    runs of items and the merge that skips empty rows).  Against the oracle, and
+    equal within tolerance to cascade_decode with a workspace, twice in a row."""
+    from oracle import attention as A
+    from _gpu_util import assert_close
+    w = _small_fp8(latent)
+    d = Dev(w)
+    plan = psd.plan_decode(d.table, w.tile_tokens, 1, w.min_shared_pages, w.min_members)
+    assert (plan.num_members > 0) == (not latent)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    wo, wl = _with_workspace(d, plan)
+    for _ in range(2):
+        o, lse, _ = _no_alloc(d, plan)
+        assert_close(o, lse, ro, rl, "fp8_e4m3", f"no_alloc {w.name}")
+        assert np.abs(o - wo).max() <= OUT_TOL["fp8_e4m3"] and np.abs(lse - wl).max() <= LSE_TOL
