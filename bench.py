@@ -667,6 +667,17 @@ def cascade_comparison(wc, label, args, flush, plan_us=False):
     tf, tc = statistics.mean(tfs), statistics.mean(tcs)
     kf = kernel_timing(flat_arm, args.steps, args.warmup, flush)
     kc = kernel_timing(casc_arm, args.steps, args.warmup, flush)
+    # each level-0 kernel forced on the same batch (the default picks one by the size
+    # of level 0)
+    level0 = {}
+    for kind in ("mma_sync", "tcgen05"):
+        casc_arm.ctx.set_level0_kernel(kind)
+        tk = time_steps(casc_arm.step, args.steps, args.warmup, flush)
+        kk = kernel_timing(casc_arm, args.steps, args.warmup, flush)
+        level0[kind] = {"rep_stats": rep_stats(tk), "kernels_ms": {k: round(v, 5) for k, v in kk.items()}}
+    casc_arm.ctx.set_level0_kernel("auto")
+    casc_arm.step()
+    casc_arm.check()
     flat_arm.check()
     flat_b, uniq_b = flat_kv_bytes(wc), unique_kv_bytes(wc)
     removed = (flat_b - uniq_b) / flat_b
@@ -685,6 +696,10 @@ def cascade_comparison(wc, label, args, flush, plan_us=False):
         "criterion_reduction_ge_0.7x_removed": bool(reduction >= 0.7 * removed),
         "flat_kernels_ms": {k: round(v, 5) for k, v in kf.items()},
         "cascade_kernels_ms": {k: round(v, 5) for k, v in kc.items()},
+        "level0_kernels": dict(level0, note="mma_sync: level 0 in 16-row groups (or 64-row blocks) of the "
+                                               "mma.sync kernel, in one launch with level 1; tcgen05: the persistent "
+                                               "tcgen05 kernel over (chunk, KV head) tasks, on a second stream; the "
+                                               "headline arm takes the default choice"),
         "stats": st,
     }
     if plan_us:
@@ -702,7 +717,10 @@ def headline_summary(line: dict) -> dict:
         c = line.get(key)
         if c:
             out[short] = {"flat_ms": c["flat_rep_stats"]["median_ms"], "cascade_ms": c["cascade_rep_stats"]["median_ms"],
+                          "cascade_level0_ms": c["cascade_kernels_ms"]["level0_ms"],
                           "cascade_partial_ms": c["cascade_kernels_ms"]["partial_ms"],
+                          "cascade_ms_level0_mma_sync": c["level0_kernels"]["mma_sync"]["rep_stats"]["median_ms"],
+                          "cascade_ms_level0_tcgen05": c["level0_kernels"]["tcgen05"]["rep_stats"]["median_ms"],
                           "reduction": c["wall_time_reduction"], "removed": c["removed_read_fraction"],
                           "criterion": c["criterion_reduction_ge_0.7x_removed"]}
             if "criterion_on_dram_bytes" in c:

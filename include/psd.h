@@ -186,6 +186,19 @@ psd_status psd_destroy(psd_ctx *ctx);
  * the tcgen05 kernel, or the 64-row kernel when CUDA_CORE is selected. */
 typedef enum { PSD_KERNEL_AUTO = 0, PSD_KERNEL_CUDA_CORE = 1, PSD_KERNEL_TENSOR_CORE = 2 } psd_partial_kernel;
 psd_status psd_set_partial_kernel(psd_ctx *ctx, int32_t kind);
+/* Which kernel computes the stacked level-0 rows of a cascade (mlxcel PR #1004,
+ * Decomposition: the M members' G query heads of one KV head, KV-head major) on bf16
+ * pools with separate K and V.  TCGEN05: a persistent kernel on the 5th-generation
+ * tensor cores, one CTA per SM over (level-0 chunk, KV head, block of up to 128
+ * stacked rows) tasks (head dims 64 and 128, page sizes that are multiples of 16, a
+ * positive softmax scale), launched before level 1 on a second
+ * stream.  MMA_SYNC: the 16-row-group tensor-core kernel, sharing one launch with
+ * level 1.  AUTO (the default): TCGEN05 from 32 stacked rows per KV head where it
+ * applies and level 0 holds at least two (chunk, KV head, 128-row) tasks per SM,
+ * unless the CUDA-core partial kernel is selected.  Both compute the same
+ * partials. */
+typedef enum { PSD_LEVEL0_AUTO = 0, PSD_LEVEL0_MMA_SYNC = 1, PSD_LEVEL0_TCGEN05 = 2 } psd_level0_kernel;
+psd_status psd_set_level0_kernel(psd_ctx *ctx, int32_t kind);
 /* Kernel timing, for measurement: when enabled, paged_decode_partial and
  * cascade_decode record CUDA events around each kernel they launch, on the
  * stream that kernel runs on.  psd_get_kernel_times waits for the most recent

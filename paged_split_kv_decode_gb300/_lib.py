@@ -19,7 +19,7 @@ PSD_KERNEL_AUTO, PSD_KERNEL_CUDA_CORE, PSD_KERNEL_TENSOR_CORE = 0, 1, 2
 # Every symbol include/psd.h declares.
 EXPORTS = [
     "psd_create", "psd_destroy", "psd_last_error", "psd_get_counters", "psd_cascade_env_enabled",
-    "psd_set_partial_kernel", "psd_set_timing", "psd_get_kernel_times", "psd_test_withhold_loads",
+    "psd_set_partial_kernel", "psd_set_level0_kernel", "psd_set_timing", "psd_get_kernel_times", "psd_test_withhold_loads",
     "psd_split_plan", "detect_shared_prefix", "build_cascade_plan", "psd_plan_decode",
     "psd_plan_capacity", "psd_workspace_bytes", "paged_decode_partial", "merge_states",
     "cascade_decode", "psd_check_device_error", "cascade_decode_no_alloc",
@@ -109,6 +109,7 @@ def _sig(lib):
     lib.psd_last_error.argtypes = []
     lib.psd_get_counters.argtypes = [V, C.POINTER(Counters)]
     lib.psd_set_partial_kernel.argtypes = [V, i32]
+    lib.psd_set_level0_kernel.argtypes = [V, i32]
     lib.psd_set_timing.argtypes = [V, i32]
     lib.psd_test_withhold_loads.argtypes = [V, i32, C.c_int64]
     lib.psd_get_kernel_times.argtypes = [V, C.POINTER(C.c_float), C.POINTER(C.c_float),

@@ -82,6 +82,12 @@ class Context:
                 "tensor_core": L.PSD_KERNEL_TENSOR_CORE}[kind]
         L.check(L.load().psd_set_partial_kernel(self._h, code))
 
+    def set_level0_kernel(self, kind: str):
+        """psd_set_level0_kernel: 'auto', 'mma_sync' or 'tcgen05' for the stacked
+        level-0 rows of a cascade."""
+        code = {"auto": 0, "mma_sync": 1, "tcgen05": 2}[kind]
+        L.check(L.load().psd_set_level0_kernel(self._h, code))
+
     def test_withhold_loads(self, from_tile: int, wait_limit_cycles: int = 0):
         """psd_test_withhold_loads: a testing aid that makes the partial kernels' waits
         for tiles from `from_tile` on run out (from_tile < 0 switches it off)."""

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpsd.so")
 
-CU_SOURCES = ["api.cu", "merge.cu", "partial_cc.cu", "partial_tcs.cu", "partial_tc.cu", "partial_mla.cu",
+CU_SOURCES = ["api.cu", "merge.cu", "partial_cc.cu", "partial_tcs.cu", "partial_tc.cu", "partial_mla.cu", "partial_l0.cu",
               "no_alloc.cu", "rope_append.cu", "autotune.cu"]
 CPP_SOURCES = ["plan.cpp", "plan_cache.cpp"]
 HEADERS = ["psd_internal.h", "kernels.h", "device.cuh", "context.h"]

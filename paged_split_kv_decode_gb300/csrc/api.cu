@@ -44,6 +44,7 @@ using namespace psd;
 namespace psd {
 
 static const float kLog2e = 1.4426950408889634f;
+static const int kLevel0Tcgen05MinRows = 32;
 // Longest wait a test may set (about 1 s at 2 GHz): below the default limit.
 static const long long kMaxTestWaitCycles = 2000000000LL;
 
@@ -115,7 +116,22 @@ PartialLaunch base_launch(const psd_decode_args *a) {
 
 bool dispatchable(const PartialLaunch &L) {
   return partial_tcs_supports(L) || partial_cc_supports(L) || partial_mla_supports(L) ||
-         partial_tc_supports(L);
+         partial_tc_supports(L) || (L.stacked && partial_l0_supports(L));
+}
+
+// Stacked level-0 rows take the tcgen05 kernel (persistent, one CTA per SM over
+// (chunk, KV head, 128-row block) tasks) when it applies and the context allows it.
+// By default: from 32 rows per KV head, where the 16-row-group form reads every tile
+// two or more times, and when level 0 has at least two tasks per SM.  With fewer,
+// the single launch that runs level 0 beside level 1 is faster (cascade batch with
+// an 8192-token prefix, 128 tasks: 0.097 ms against 0.105 ms a step), because the
+// tcgen05 kernel holds whole SMs that level 1 could share.
+static bool use_level0_tcgen05(const PartialLaunch &L, const DeviceInfo &dev) {
+  if (!L.stacked || !partial_l0_supports(L) || dev.level0_kernel == PSD_LEVEL0_MMA_SYNC) return false;
+  if (dev.level0_kernel == PSD_LEVEL0_TCGEN05) return true;
+  const int64_t tasks = int64_t(L.num_items) * L.Hkv * ((L.G_cta + 127) / 128);
+  return dev.partial_kernel != PSD_KERNEL_CUDA_CORE && L.G_cta >= kLevel0Tcgen05MinRows &&
+         tasks >= 2 * int64_t(dev.num_sms > 0 ? dev.num_sms : 1);
 }
 
 // bf16 pools with separate K and V: the 16-row-group tensor-core kernel (or, for
@@ -124,6 +140,7 @@ bool dispatchable(const PartialLaunch &L) {
 // 64-row mma.sync kernel (also used for MLA when the context asks for CUDA_CORE,
 // as the legacy-tensor-path reference).
 PartialKind select_partial(const PartialLaunch &L, const DeviceInfo &dev) {
+  if (use_level0_tcgen05(L, dev)) return PartialKind::kTensorL0;
   if (dev.partial_kernel == PSD_KERNEL_CUDA_CORE && partial_cc_supports(L)) return PartialKind::kCudaCore;
   if (partial_tcs_supports(L)) return PartialKind::kTensorSmall;
   if (partial_cc_supports(L)) return PartialKind::kCudaCore;
@@ -143,6 +160,7 @@ psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStr
     case PartialKind::kTensorSmall: return launch_partial_tcs(L, dev, s);
     case PartialKind::kMLA: return launch_partial_mla(L, dev, s);
     case PartialKind::kTensorLegacy: return launch_partial_tc(L, dev, s);
+    case PartialKind::kTensorL0: return launch_partial_l0(L, dev, s);
     case PartialKind::kNone: break;
   }
   return fail(PSD_ERR_UNSUPPORTED, "no kernel for Dqk %d, Dv %d, rows/KV head %d, dtype %d, latent %d",
@@ -156,9 +174,12 @@ namespace psd {
 // Both cascade levels can share one launch when the 16-row-group tensor-core
 // kernel serves both and level 1 fits one row group.
 bool dispatch_fused(const PartialLaunch &L0, const PartialLaunch &L1, const DeviceInfo &dev) {
-  if (dev.partial_kernel == PSD_KERNEL_CUDA_CORE) return false;
+  if (dev.partial_kernel == PSD_KERNEL_CUDA_CORE || select_partial(L0, dev) == PartialKind::kTensorL0) return false;
   return partial_tcs_supports(L0) && partial_tcs_supports(L1) && L1.G_cta <= 16;
 }
+
+// Kernels that take their work lists from the launch parameters.
+bool inline_lists_kernel(PartialKind k) { return k == PartialKind::kTensorSmall || k == PartialKind::kTensorL0; }
 
 }  // namespace psd
 
@@ -314,6 +335,15 @@ extern "C" psd_status psd_set_partial_kernel(psd_ctx *c, int32_t kind) {
   if (kind != PSD_KERNEL_AUTO && kind != PSD_KERNEL_CUDA_CORE && kind != PSD_KERNEL_TENSOR_CORE)
     return fail(PSD_ERR_INVALID_ARG, "partial kernel kind %d", kind);
   c->dev.partial_kernel = kind;
+  return PSD_OK;
+}
+
+extern "C" psd_status psd_set_level0_kernel(psd_ctx *c, int32_t kind) {
+  clear_error();
+  if (!c) return fail(PSD_ERR_INVALID_ARG, "NULL context");
+  if (kind != PSD_LEVEL0_AUTO && kind != PSD_LEVEL0_MMA_SYNC && kind != PSD_LEVEL0_TCGEN05)
+    return fail(PSD_ERR_INVALID_ARG, "level-0 kernel kind %d", kind);
+  c->dev.level0_kernel = kind;
   return PSD_OK;
 }
 
@@ -480,6 +510,8 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   L1.merge_runs = true;  // the partial rows feed the merge below
   PartialLaunch L0 = L1;
   L0.G_cta = M * L1.Gm;
+  L0.stacked = true;
+  L0.num_items = n0;
   if (!dispatchable(L1)) return launch_partial(L1, ctx->dev, nullptr);
   if (M > 0 && !dispatchable(L0)) return launch_partial(L0, ctx->dev, nullptr);
 
@@ -500,7 +532,7 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   const bool fused = M > 0 && dispatch_fused(L0, L1, ctx->dev);
   const bool tcs_only = select_partial(L1, ctx->dev) == PartialKind::kTensorSmall &&
-                        (M == 0 || fused || select_partial(L0, ctx->dev) == PartialKind::kTensorSmall);
+                        (M == 0 || fused || inline_lists_kernel(select_partial(L0, ctx->dev)));
   CallLists cl;
   st = place_lists(ctx, cl, ws, lay, host, B, tcs_only, s);
   if (st != PSD_OK) return st;
@@ -652,6 +684,8 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
   for (int32_t s = 0; s < S; ++s) {
     PartialLaunch L0 = L1;
     L0.G_cta = plan->segments[s].num_members * L1.Gm;
+    L0.stacked = true;
+    L0.num_items = plan->segments[s].num_items;
     if (!dispatchable(L0)) return launch_partial(L0, ctx->dev, nullptr);
   }
 
@@ -676,13 +710,17 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
   for (int32_t k = 0; fused && k < S; ++k) {
     PartialLaunch L0 = L1;
     L0.G_cta = plan->segments[k].num_members * L1.Gm;
+    L0.stacked = true;
+    L0.num_items = plan->segments[k].num_items;
     fused = dispatch_fused(L0, L1, ctx->dev);
   }
   bool tcs_only = select_partial(L1, ctx->dev) == PartialKind::kTensorSmall;
   for (int32_t k = 0; tcs_only && !fused && k < S; ++k) {
     PartialLaunch L0 = L1;
     L0.G_cta = plan->segments[k].num_members * L1.Gm;
-    tcs_only = select_partial(L0, ctx->dev) == PartialKind::kTensorSmall;
+    L0.stacked = true;
+    L0.num_items = plan->segments[k].num_items;
+    tcs_only = inline_lists_kernel(select_partial(L0, ctx->dev));
   }
   CallLists cl;
   st = place_lists(ctx, cl, ws, lay, host, B, tcs_only, s);
@@ -713,6 +751,7 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
       const psd_segment &gk = plan->segments[k];
       PartialLaunch L0 = L1;
       L0.G_cta = gk.num_members * L1.Gm;
+      L0.stacked = true;
       L0.items = ditems + gk.first_item;
       L0.order = nullptr;
       L0.num_items = gk.num_items;

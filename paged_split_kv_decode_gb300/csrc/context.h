@@ -88,7 +88,7 @@ psd_status validate_items(const psd_decode_args *a, const psd_work_item *items, 
                           int64_t out_rows, bool stacked, int32_t num_members);
 PartialLaunch base_launch(const psd_decode_args *a);
 bool dispatchable(const PartialLaunch &L);
-enum class PartialKind { kNone, kCudaCore, kTensorSmall, kMLA, kTensorLegacy };
+enum class PartialKind { kNone, kCudaCore, kTensorSmall, kMLA, kTensorLegacy, kTensorL0 };
 // The kernel launch_partial runs for L on dev.
 PartialKind select_partial(const PartialLaunch &L, const DeviceInfo &dev);
 // The launch may leave empty partial rows (LSE -inf, v not written) for the merge.
@@ -96,5 +96,7 @@ bool writes_empty_rows(const PartialLaunch &L, const DeviceInfo &dev);
 psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s);
 // Both cascade levels can share one launch of the 16-row-group tensor-core kernel.
 bool dispatch_fused(const PartialLaunch &L0, const PartialLaunch &L1, const DeviceInfo &dev);
+// Kernels of this kind take their work lists from the launch parameters.
+bool inline_lists_kernel(PartialKind k);
 
 }  // namespace psd

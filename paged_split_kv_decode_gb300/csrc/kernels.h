@@ -15,6 +15,7 @@ struct DeviceInfo {
   int smem_optin = 0;
   void *encode_tiled = nullptr;  // driver cuTensorMapEncodeTiled
   int partial_kernel = 0;        // psd_partial_kernel preference for G <= 16
+  int level0_kernel = 0;         // psd_level0_kernel preference for stacked level-0 rows
   // Testing aid for the bounded waits (psd_test_withhold_loads): the 16-row-group
   // tensor-core and CUDA-core partial kernels issue no loads for tiles at index
   // test_withhold_from and later of any item (-1: off), and give up a wait after
@@ -85,6 +86,7 @@ struct PartialLaunch {
   int32_t G_cta = 0;   // query rows per CTA (Gm, or M*Gm when stacked)
   int32_t kv_dtype = PSD_BF16;
   bool latent_v = false;
+  bool stacked = false;  // a stacked level-0 launch (items with q_index < 0)
   int32_t max_item_tokens = 0;
   // The partial rows feed this library's merge: a kernel may accumulate a run of
   // consecutive items of one request into one partial, written to the run's last
@@ -117,6 +119,8 @@ bool partial_mla_supports(const PartialLaunch &p);
 psd_status launch_partial_mla(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
 bool partial_tc_supports(const PartialLaunch &p);
 psd_status launch_partial_tc(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
+bool partial_l0_supports(const PartialLaunch &p);
+psd_status launch_partial_l0(const PartialLaunch &p, const DeviceInfo &dev, cudaStream_t s);
 
 psd_status launch_rope_append(const psd_rope_append_args *a, cudaStream_t s);
 

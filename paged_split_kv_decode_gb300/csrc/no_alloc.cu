@@ -106,6 +106,8 @@ extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_arg
   L1.merge_runs = true;  // the partial rows feed the merge below
   PartialLaunch L0 = L1;
   L0.G_cta = M * L1.Gm;
+  L0.stacked = true;
+  L0.num_items = n0;
   if (!dispatchable(L1)) return launch_partial(L1, ctx->dev, nullptr);
   if (M > 0 && !dispatchable(L0)) return launch_partial(L0, ctx->dev, nullptr);
 
@@ -137,7 +139,7 @@ extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_arg
   // cleared header in the scratch.
   const bool fused = M > 0 && dispatch_fused(L0, L1, ctx->dev);
   const bool tcs_only = select_partial(L1, ctx->dev) == PartialKind::kTensorSmall &&
-                        (M == 0 || fused || select_partial(L0, ctx->dev) == PartialKind::kTensorSmall);
+                        (M == 0 || fused || inline_lists_kernel(select_partial(L0, ctx->dev)));
   const size_t used = lay.indptr_off - lay.items_off;
   const bool inl = tcs_only && used <= kInlineListBytes && B + 1 <= kInlineIndptr;
   InlineLists block;

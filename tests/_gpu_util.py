@@ -37,6 +37,22 @@ class use_kernel:
         return False
 
 
+class use_level0:
+    """Selects the kernel for the stacked level-0 rows of a cascade ('auto',
+    'mma_sync' = the 16-row-group tensor-core kernel in the fused launch, 'tcgen05' =
+    one CTA per chunk, KV head and 128 rows on the 5th-generation tensor cores)."""
+
+    def __init__(self, kind):
+        self.kind = kind
+
+    def __enter__(self):
+        ctx().set_level0_kernel(self.kind)
+
+    def __exit__(self, *exc):
+        ctx().set_level0_kernel("auto")
+        return False
+
+
 class Dev:
     """Device copies of a synth.Workload."""
 

@@ -10,7 +10,7 @@ import synth
 from oracle import attention as A
 from oracle import cascade as OC
 from oracle import planner as PL
-from _gpu_util import Dev, assert_close, ctx, oracle_partials, use_kernel
+from _gpu_util import Dev, assert_close, ctx, oracle_partials, use_kernel, use_level0
 
 pytestmark = pytest.mark.gpu
 
@@ -62,14 +62,16 @@ def test_tiny_cascade_declines_at_default_thresholds():
     assert_close(o, lse, ro, rl, w.kv_dtype, "declined")
 
 
+@pytest.mark.parametrize("level0", ["mma_sync", "tcgen05"])
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("seed", [0, 1])
-def test_cascade_config_full_size(seed, kernel):
+def test_cascade_config_full_size(seed, kernel, level0):
     """Cascade config at full size: 64 requests, 16 members share 8192 tokens; the
-    cascade arm, the flat arm and the oracle agree."""
+    cascade arm, the flat arm and the oracle agree, with level 0 (64 stacked rows per
+    KV head) in either kernel."""
     w = synth.cascade_decode(seed=seed)
     d = Dev(w)
-    with use_kernel(kernel):
+    with use_kernel(kernel), use_level0(level0):
         o, lse, stats, plan = d.decode(enable=1, with_stats=True)
     assert stats["path"] == 1 and stats["members"] == 16 and stats["shared_pages"] == 512
     ro, rl = A.decode_attention(A.workload_arrays(w))
@@ -360,11 +362,14 @@ def test_large_query_groups_share_each_tile(G, D):
     assert_close(o, lse, ro, rl, "bf16", f"G={G}, D={D}")
 
 
+@pytest.mark.parametrize("level0", ["mma_sync", "tcgen05"])
 @pytest.mark.parametrize("members", [5, 9, 17, 33])
-def test_cascade_stacked_rows_in_shared_tile_blocks(members):
-    """Level-0 stacks members x G rows per KV head (20, 36, 68, 132 here): CTAs per
-    16-row group below 49 rows, blocks of 64 rows with partly filled and idle warps
-    above, through the fused launch, against the oracle and the flat arm."""
+def test_cascade_stacked_rows_in_shared_tile_blocks(members, level0):
+    """Level-0 stacks members x G rows per KV head (20, 36, 68, 132 here).  mma_sync:
+    CTAs per 16-row group below 49 rows, blocks of 64 rows with partly filled and idle
+    warps above, through the fused launch.  tcgen05: one CTA per 128 rows (two row
+    blocks at 132, the second with 4 live rows).  Against the oracle and the flat
+    arm."""
     rng = np.random.default_rng(70 + members)
     B = members + 3
     P, sp = 16, 40
@@ -376,10 +381,11 @@ def test_cascade_stacked_rows_in_shared_tile_blocks(members):
                     num_pages=sum((n + P - 1) // P for n in lengths) + 8, tile_tokens=128,
                     shared=(mem, sp), min_shared_pages=1, min_members=2)
     d = Dev(w)
-    o, lse, stats, plan = d.decode(enable=1, with_stats=True)
+    with use_level0(level0):
+        o, lse, stats, plan = d.decode(enable=1, with_stats=True)
     assert stats["path"] == 1 and stats["members"] == members
     ro, rl = A.decode_attention(A.workload_arrays(w))
-    assert_close(o, lse, ro, rl, "bf16", f"cascade, {members} members")
+    assert_close(o, lse, ro, rl, "bf16", f"cascade, {members} members, level 0 {level0}")
     fo, fl = d.decode(enable=0)
     assert np.abs(o - fo).max() < 2e-3
 
@@ -412,7 +418,8 @@ def test_large_groups_in_shared_tile_blocks(G):
 def test_cascade_level0_in_shared_tile_blocks():
     """16 members x 4 rows = 64 stacked rows per KV head, with enough prefix chunks
     (tile 64) for 1.25 waves of level-0 blocks, so the fused launch takes the
-    shared-tile form for level 0: every output against the oracle and the flat arm."""
+    shared-tile form for level 0 (the mma_sync level-0 kernel): every output against
+    the oracle and the flat arm."""
     rng = np.random.default_rng(77)
     Hkv, P, tile, members = 8, 16, 64, 16
     chunks = -(-_wave() * 5 // 4 // Hkv)
@@ -426,7 +433,8 @@ def test_cascade_level0_in_shared_tile_blocks():
                     num_pages=sum((n + P - 1) // P for n in lengths) + 8, tile_tokens=tile,
                     shared=(mem, sp), min_shared_pages=1, min_members=2)
     d = Dev(w)
-    o, lse, stats, plan = d.decode(enable=1, with_stats=True)
+    with use_level0("mma_sync"):
+        o, lse, stats, plan = d.decode(enable=1, with_stats=True)
     assert stats["path"] == 1 and stats["members"] == members and stats["prefix_chunks"] >= chunks
     ro, rl = A.decode_attention(A.workload_arrays(w))
     assert_close(o, lse, ro, rl, "bf16", "cascade, level-0 blocks")
