@@ -53,14 +53,43 @@ NOMINAL_HBM_GBS = 8000.0
 # ncu capture of the flat partial.  Reported only while the kernel source is the one
 # the counters were taken on.
 TRAFFIC_SOURCE = os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", "partial_tcs.cu")
-TRAFFIC_SHA256 = "e0ef72ba0b83ba58f600d071d0e2a7a2c57727886b3ae2c44e678afe193ced34"
-TRAFFIC_BYTES = 316086272 + 1172224
+TRAFFIC_SHA256 = "9cc955b4b183ab5debe9ebc71c3a8a5a086aa6ba5ca6eb0a516ee92a46b43fce"
+TRAFFIC_BYTES = 316086016 + 1213184
+
+# DRAM bytes read per step by the partial kernels of each arm of the two cascade
+# workloads (median over launches of a single-pass ncu capture of dram__bytes_read.sum,
+# `bench.py --workload cascade`).  They let the criterion be read on the reads each arm
+# makes from DRAM as well as on algorithmic reads.  Valid while the partial kernels'
+# sources are unchanged.
+CASCADE_DRAM_SOURCES = [os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", f)
+                        for f in ("partial_tcs.cu", "partial_l0.cu")]
+CASCADE_DRAM_SHA256 = "4d21e24c970e036ddacf69e9e9cf79536ca6ef447f94c2035d80eba01f7db5ce"
+CASCADE_DRAM_READ = {
+    # 8192-token prefix: the flat arm's prefix re-reads hit the 129 MB L2
+    "flat_vs_cascade": {"flat": 533344512, "cascade": 533302912,
+                        "kernels": "flat: partial_tcs 523x8 CTAs; cascade: one partial_tcs launch, both levels"},
+    # 65536-token prefix (268 MB): the flat arm re-reads part of the prefix from DRAM
+    "flat_vs_cascade_prefix_beyond_l2": {"flat": 930637312, "cascade": 268660608 + 499736192,
+                                         "kernels": "flat: partial_tcs 2315x8 CTAs; cascade: partial_l0 (level 0) "
+                                                    "+ partial_tcs 267x8 (level 1)"},
+}
 
 
 def partial_traffic():
     import hashlib
     with open(TRAFFIC_SOURCE, "rb") as f:
         return TRAFFIC_BYTES if hashlib.sha256(f.read()).hexdigest() == TRAFFIC_SHA256 else None
+
+
+def cascade_dram_reads(key):
+    """The stored DRAM reads of both arms of a cascade workload, or None once the
+    partial kernels' sources differ from those the counters were taken on."""
+    import hashlib
+    h = hashlib.sha256()
+    for path in CASCADE_DRAM_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return CASCADE_DRAM_READ.get(key) if h.hexdigest() == CASCADE_DRAM_SHA256 else None
 
 
 def measured_peaks():
@@ -655,7 +684,7 @@ def large_flat_timing(args, flush, hbm: float):
     return out
 
 
-def cascade_comparison(wc, label, args, flush, plan_us=False):
+def cascade_comparison(wc, label, args, flush, plan_us=False, key=None):
     """Flat arm vs cascade arm on one batch: step times, per-kernel times and the
     criterion (T_flat - T_casc) / T_flat >= 0.7 x the fraction of K/V reads removed."""
     flat_arm, casc_arm = Arm(wc, enable=0), Arm(wc, enable=1)
@@ -694,6 +723,7 @@ def cascade_comparison(wc, label, args, flush, plan_us=False):
         "flat_arm_algorithmic_gbs": round(flat_b / (kf["partial_ms"] * 1e-3) / 1e9, 1),
         "removed_read_fraction": round(removed, 4), "wall_time_reduction": round(reduction, 4),
         "criterion_reduction_ge_0.7x_removed": bool(reduction >= 0.7 * removed),
+        "criterion_on_dram_bytes": None,
         "flat_kernels_ms": {k: round(v, 5) for k, v in kf.items()},
         "cascade_kernels_ms": {k: round(v, 5) for k, v in kc.items()},
         "level0_kernels": dict(level0, note="mma_sync: level 0 in 16-row groups (or 64-row blocks) of the "
@@ -702,6 +732,14 @@ def cascade_comparison(wc, label, args, flush, plan_us=False):
                                                "headline arm takes the default choice"),
         "stats": st,
     }
+    dram = cascade_dram_reads(key)
+    if dram is not None:
+        removed_dram = (dram["flat"] - dram["cascade"]) / dram["flat"]
+        out["criterion_on_dram_bytes"] = {
+            "flat_arm_dram_read": dram["flat"], "cascade_arm_dram_read": dram["cascade"],
+            "removed_dram_fraction": round(removed_dram, 4),
+            "met": bool(reduction >= 0.7 * removed_dram), "kernels": dram["kernels"],
+            "source": "ncu dram__bytes_read.sum per launch (single pass), median over launches"}
     if plan_us:
         out["host_plan_us"] = host_plan_us(wc)
     del flat_arm, casc_arm
@@ -723,8 +761,8 @@ def headline_summary(line: dict) -> dict:
                           "cascade_ms_level0_tcgen05": c["level0_kernels"]["tcgen05"]["rep_stats"]["median_ms"],
                           "reduction": c["wall_time_reduction"], "removed": c["removed_read_fraction"],
                           "criterion": c["criterion_reduction_ge_0.7x_removed"]}
-            if "criterion_on_dram_bytes" in c:
-                out[short]["criterion_dram"] = c["criterion_on_dram_bytes"]
+            if c.get("criterion_on_dram_bytes"):
+                out[short]["criterion_dram"] = {k: c["criterion_on_dram_bytes"][k] for k in ("removed_dram_fraction", "met")}
     m = line.get("mla")
     if m:
         out["mla"] = {"ms": m["rep_stats"], "partial_tflops": m["partial_kernel_tflops"],
@@ -780,14 +818,16 @@ def run_ours(args):
         wc = synth.cascade_decode(seed=0, canary=False)
         extra["flat_vs_cascade"] = cascade_comparison(
             wc, "cascade decode: 64 requests, 16 share an 8192-token prefix (suffix U[64,1024]), "
-                "48 independent U[512,4096]; Hq=32, Hkv=8, D=128, page 16, tile 512", args, flush, plan_us=True)
+                "48 independent U[512,4096]; Hq=32, Hkv=8, D=128, page 16, tile 512", args, flush, plan_us=True,
+            key="flat_vs_cascade")
+    if not args.quick and args.workload in ("all", "cascade", "cascade_l2"):
         # The same batch with a 65536-token shared prefix (268 MB of K/V, more than the
         # 129 MB L2), so the flat arm's re-reads of the prefix go to DRAM.
         wl = synth.cascade_decode(seed=0, canary=False, shared_tokens=65536)
         extra["flat_vs_cascade_prefix_beyond_l2"] = cascade_comparison(
             wl, "cascade decode, prefix larger than L2: 64 requests, 16 share a 65536-token prefix "
                 "(suffix U[64,1024]), 48 independent U[512,4096]; Hq=32, Hkv=8, D=128, page 16, tile 512",
-            args, flush)
+            args, flush, key="flat_vs_cascade_prefix_beyond_l2")
     if not args.quick and args.workload in ("all", "mla"):
         wm = synth.mla_decode(seed=0, canary=False, batch=args.mla_batch)
         marm = Arm(wm, enable=1)
@@ -926,7 +966,8 @@ def main():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--quick", action="store_true", help="flat workload only")
-    p.add_argument("--workload", choices=["all", "cascade", "mla", "merge", "append", "nested", "tune", "large"],
+    p.add_argument("--workload", choices=["all", "cascade", "cascade_l2", "mla", "merge", "append", "nested", "tune",
+                                          "large"],
                    default="all",
                    help="which workloads run after the flat headline")
     p.add_argument("--mla-batch", type=int, default=128, help="requests in the MLA workload")
