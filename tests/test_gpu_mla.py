@@ -2,6 +2,8 @@
 first 512 columns) on the tensor-core partial kernel, against the float64 oracle
 (ROCm ATOM PR #1701 section 3.2 for the fp8 latent; mlxcel PR #1004 Merge contract
 for the split-KV merge)."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -177,3 +179,71 @@ def test_mla_cascade_level1_runs():
     assert stats["path"] == 1 and stats["members"] == 3
     ro, rl = A.decode_attention(A.workload_arrays(w))
     assert_close(o, lse, ro, rl, "fp8_e4m3", "MLA cascade")
+
+
+# ---------------------------------------------------------------------------------
+# Precision of the two-term e4m3 query split inside a row.  The kernel scales each
+# query row by a power of two (its largest element to [128, 256)) and splits it into
+# hi = e4m3(x) and lo = e4m3(x - hi): exact down to about 2^-10 of the row's largest
+# element; below that each element carries an absolute error of up to about 2^-17 of
+# it (e4m3's subnormal step), so a score's absolute error grows with the row's
+# largest element.  These rows spread their magnitudes over 2^20.
+#   * Scores with a spread of a few log2 units (every token weighs in): the bf16
+#     level of accuracy, 2e-3 on outputs and 1e-3 on LSE.
+#   * The default scale 1/sqrt(576) on these rows gives scores of several hundred
+#     log2 units, a softmax that is nearly one-hot: the score errors (about 1e-5 of
+#     the scores) move near-tied weights, and outputs stay within the 1e-2 bound of an
+#     fp8 pool (measured up to 7.8e-3), and the LSE within the bound the split gives:
+#     a score's error is at most sm_scale * log2(e) * 576 * 2^-17 * max|q_row| *
+#     max|K| (measured 1.3e-2 with scores up to about 1500).
+BF16_LEVEL_OUT = 2e-3
+
+
+def _wide_range_rows(w, seed, kind):
+    rng = np.random.default_rng(seed)
+    B, H, D = w.q.shape
+    if kind == "log_uniform":          # |q| log-uniform over [2^-10, 2^10], random signs
+        q = 2.0 ** rng.uniform(-10, 10, size=(B, H, D)) * rng.choice([-1.0, 1.0], size=(B, H, D))
+    elif kind == "spike":              # N(0,1) * 2^-10 with one element per row at +-2^10
+        q = rng.standard_normal((B, H, D)) * 2.0 ** -10
+        col = rng.integers(0, D, size=(B, H))
+        np.put_along_axis(q, col[..., None], rng.choice([-1.0, 1.0], size=(B, H, 1)) * 2.0 ** 10, axis=2)
+    elif kind == "rope_heavy":         # the 64 rope columns 2^8 larger than the 512 latent ones
+        q = rng.standard_normal((B, H, D)) * 2.0 ** -6
+        q[..., 512:] *= 2.0 ** 14
+    else:
+        raise ValueError(kind)
+    return torch.from_numpy(q.astype(np.float32)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("kind", ["log_uniform", "spike", "rope_heavy"])
+@pytest.mark.parametrize("scores", ["normalised", "default"])
+def test_mla_query_rows_spanning_2_to_the_20(kind, scores):
+    """Rows whose elements span 2^20 in magnitude, with the softmax scale either set so
+    the log2 scores have a spread of about 2 (every token matters: the bf16 level of
+    accuracy) or left at 1/sqrt(576) (a nearly one-hot softmax over scores of several
+    hundred: the fp8-pool output bound, the LSE relative to its magnitude)."""
+    import dataclasses
+    w = _mla_small(31 + len(kind), [1100, 2049, 300, 64])
+    q = _wide_range_rows(w, 40 + len(kind), kind)
+    w = dataclasses.replace(w, q=q)
+    if scores == "normalised":
+        a = A.workload_arrays(w)
+        K, _ = A.gather_kv(a, 0)
+        s = A.bf16_bits_to_f64(a["q_raw"])[0] @ K[:, 0, :].T          # raw scores of request 0
+        w = dataclasses.replace(w, sm_scale=float(2.0 / math.log2(math.e) / s.std()))
+    o, lse = Dev(w).decode(enable=0)
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    eo = np.abs(o - ro).max()
+    el = np.abs(lse - rl).max()
+    print(f"{kind} {scores}: out {eo:.3g} lse {el:.3g} (|lse| up to {np.abs(rl).max():.4g})")
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    if scores == "normalised":
+        assert eo <= BF16_LEVEL_OUT and el <= 1e-3, (kind, scores, eo, el)
+    else:
+        assert eo <= 1e-2, (kind, scores, eo)
+        a = A.workload_arrays(w)
+        qmax = np.abs(A.bf16_bits_to_f64(a["q_raw"])).max(axis=2)                 # [B, Hq]
+        kmax = np.array([np.abs(A.gather_kv(a, b)[0]).max() for b in range(w.batch)])
+        bound = w.sm_scale * math.log2(math.e) * 576 * 2.0 ** -17 * qmax * kmax[:, None]
+        assert (np.abs(lse - rl) <= np.maximum(1e-3, bound)).all(), (kind, scores, el)
