@@ -149,9 +149,11 @@ PartialKind select_partial(const PartialLaunch &L, const DeviceInfo &dev) {
   return PartialKind::kNone;
 }
 
-// Only the MLA kernel accumulates runs of items (PartialLaunch::merge_runs).
+// The MLA kernel and the tcgen05 level-0 kernel accumulate runs of items
+// (PartialLaunch::merge_runs) and leave the other rows of a run empty.
 bool writes_empty_rows(const PartialLaunch &L, const DeviceInfo &dev) {
-  return L.merge_runs && select_partial(L, dev) == PartialKind::kMLA;
+  const PartialKind k = select_partial(L, dev);
+  return L.merge_runs && (k == PartialKind::kMLA || k == PartialKind::kTensorL0);
 }
 
 psd_status launch_partial(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t s) {
@@ -592,8 +594,9 @@ extern "C" psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
   }
   time_mark(ctx, 4, s);
   const bool merge_follows_partial = !(M > 0 && !fused) && !ctx->timing;
+  const bool empty_rows = writes_empty_rows(L1, ctx->dev) || (M > 0 && !fused && writes_empty_rows(L0, ctx->dev));
   st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq,
-                    args->Dv, o, lse, ctx->dev, s, merge_follows_partial, writes_empty_rows(L1, ctx->dev),
+                    args->Dv, o, lse, ctx->dev, s, merge_follows_partial, empty_rows,
                     cl.inl ? plan->o_indptr : nullptr);
   time_mark(ctx, 5, s);
   ctx->tev_used[0] = ctx->timing && M > 0 && !fused;
@@ -786,9 +789,16 @@ extern "C" psd_status cascade_decode_nested(psd_ctx *ctx, const psd_decode_args 
     if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "nested join: %s", cudaGetErrorString(e));
   }
   time_mark(ctx, 4, s);
+  bool empty_rows = writes_empty_rows(L1, ctx->dev);
+  for (int32_t k = 0; !fused && k < S; ++k) {
+    PartialLaunch L0 = L1;
+    L0.G_cta = plan->segments[k].num_members * L1.Gm;
+    L0.stacked = true;
+    L0.num_items = plan->segments[k].num_items;
+    empty_rows = empty_rows || writes_empty_rows(L0, ctx->dev);
+  }
   st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq, args->Dv, o,
-                    lse, ctx->dev, s, !joined && !ctx->timing, writes_empty_rows(L1, ctx->dev),
-                    cl.inl ? plan->o_indptr : nullptr);
+                    lse, ctx->dev, s, !joined && !ctx->timing, empty_rows, cl.inl ? plan->o_indptr : nullptr);
   time_mark(ctx, 5, s);
   ctx->tev_used[0] = ctx->timing && joined;
   ctx->tev_used[1] = ctx->timing;

@@ -206,9 +206,9 @@ extern "C" psd_status cascade_decode_no_alloc(psd_ctx *ctx, const psd_decode_arg
   L1.fault = fault;
   place(L1);
   if ((st = launch_partial(L1, ctx->dev, s)) != PSD_OK) return st;
+  const bool empty_rows = writes_empty_rows(L1, ctx->dev) || (M > 0 && !fused && writes_empty_rows(L0, ctx->dev));
   st = launch_merge(vpart, lpart, reinterpret_cast<const int32_t *>(ws + lay.indptr_off), B, args->Hq,
-                    args->Dv, o, lse, ctx->dev, s, true, writes_empty_rows(L1, ctx->dev),
-                    inl ? plan->o_indptr : nullptr);
+                    args->Dv, o, lse, ctx->dev, s, true, empty_rows, inl ? plan->o_indptr : nullptr);
   if (st != PSD_OK) return st;
   if (fault_bits_dev) {
     e = cudaMemcpyAsync(fault_bits_dev, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);

@@ -10,8 +10,13 @@
 // their own denominator, LSE = m + log2 l in log2 units.
 //
 // GB300 design.
-//   * Persistent: one CTA per SM takes tasks t = blockIdx.x, + gridDim.x, ...; the
-//     loads run ahead across task boundaries, so a task pays no pipeline ramp.
+//   * Persistent: one CTA per SM takes a contiguous range of tasks ordered (KV head,
+//     row block, chunk); the loads run ahead across task boundaries, so a task pays no
+//     pipeline ramp.  When the rows feed the merge, a CTA's consecutive chunks of one
+//     KV head and row block form a run: O, max and sum carry over, one partial per run
+//     is written and the run's other chunk rows are marked empty, so the merge reads a
+//     few live rows per member instead of one per chunk (128 with a 65536-token
+//     prefix, where the merge took 26 us).
 //   * Tiles of 64 tokens, loaded by TMA in [16 tokens x 64 columns] boxes with the
 //     128-byte swizzle (one box per page segment and 64 columns) into a ring of 5
 //     stages of 32 KB (D = 128).  Two producer warps take alternate tiles, one copy
@@ -26,14 +31,14 @@
 //     the row warps over the S buffer they came from (TMEM A operand); V straight
 //     from the ring, read MN-major.  8 MMAs of N = D per tile.  The two terms keep
 //     about 16 bits of P; a single bf16 P would cost up to 2^-9 |v|.
-//   * TMEM (512 columns at D = 128): two O buffers [128 x D] f32 (a task's O is read
-//     out while the next task accumulates) and three S buffers [128 x 64].
+//   * TMEM (512 columns at D = 128): two O buffers [128 x D] f32 (a run's O is read
+//     out while the next run accumulates) and three S buffers [128 x 64].
 //   * Roles: row warps 0-3 (thread = stacked row = TMEM lane) run a lazily rescaled
 //     online softmax (O is rescaled in TMEM only when a row's running max grows by
 //     more than 2^8, so P <= 2^8) and zero the V rows past the last token of a
 //     ragged tile; control warp 4 issues the MMAs (converged warp, one elected
 //     lane); producer warps 5-6 issue the TMA loads; epilogue warps 7-10 gather the
-//     members' query rows two tasks ahead and read out each finished task's O / l
+//     members' query rows two runs ahead and read out each finished run's O / l
 //     and LSE.  Clock traces put the row warps on the critical path: a task boundary
 //     cost them about 9000 cycles (read-out, query gather) before the epilogue warps
 //     took that work.
@@ -121,7 +126,8 @@ struct L0Params {
   FaultRef fault;
   int64_t num_pages;
   int num_tasks;      // items x Hkv x row blocks
-  int Hkv, n_rb;      // KV heads, row blocks per (item, KV head)
+  int n_items, Hkv, n_rb;  // level-0 items, KV heads, row blocks per (item, KV head)
+  int runs;           // the rows feed this library's merge: accumulate runs of chunks
   int Hq_req, page_size, Gm, G_rows;
   float q_scale, v_scale;  // q_scale > 0
   long long wait_limit;
@@ -235,21 +241,36 @@ __global__ void __launch_bounds__(kThreads0, 1)
   };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = p.page_size;
-  // This CTA's tasks: t = blockIdx.x + k * gridDim.x, k = 0 .. n_mine - 1.  Task t is
-  // item t / (Hkv * n_rb), KV head (t / n_rb) % Hkv, row block t % n_rb, so the CTAs
-  // at work at one time read the KV heads of the same pages.
-  const int n_mine = p.num_tasks > int(blockIdx.x) ? (p.num_tasks - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
+  // Tasks are numbered t = (kv * n_rb + rb) * n_items + item: the chunks of one KV
+  // head and row block are consecutive.  This CTA takes the contiguous range
+  // [tb, te), k = t - tb.  At one time the CTAs read the same chunk positions of the
+  // different KV heads, so the pages' rows are read together.
+  const int tb = int(int64_t(blockIdx.x) * p.num_tasks / gridDim.x);
+  const int te = int(int64_t(blockIdx.x + 1) * p.num_tasks / gridDim.x);
+  const int n_mine = te - tb;
+  // Runs: maximal ranges of this CTA's tasks with the same KV head and row block (the
+  // same query rows).  When the partial rows feed the merge, a run's chunks accumulate
+  // into one partial (O, running max and sum carry over), written to the row of the
+  // run's last chunk; the rows of its other chunks are empty (LSE -inf), which the
+  // merge reads as no tokens.  Otherwise every task is a run of its own.
+  const int kvrb0 = p.n_items > 0 ? tb / p.n_items : 0;
+  auto new_run = [&](int k) { return k == 0 || !p.runs || (tb + k) % p.n_items == 0; };
+  auto run_of = [&](int k) { return p.runs ? (tb + k) / p.n_items - kvrb0 : k; };
+  auto last_of_run = [&](int k) { return k == n_mine - 1 || new_run(k + 1); };
+  auto run_first = [&](int r) { return p.runs ? max(0, (kvrb0 + r) * p.n_items - tb) : r; };
+  auto run_end = [&](int r) { return p.runs ? min(n_mine, (kvrb0 + r + 1) * p.n_items - tb) : r + 1; };
+  const int n_runs = n_mine > 0 ? run_of(n_mine - 1) + 1 : 0;
   struct Task {
     psd_work_item it;
     int kv, row0, rows, n_tiles;
   };
   auto task = [&](int k) {
-    const int t = int(blockIdx.x) + k * int(gridDim.x);
+    const int t = tb + k;
     Task x;
-    const int per_item = p.Hkv * p.n_rb;
-    x.it = items[t / per_item];
-    x.kv = (t / p.n_rb) % p.Hkv;
-    x.row0 = (t % p.n_rb) * kRows0;
+    const int kvrb = t / p.n_items;
+    x.it = items[t - kvrb * p.n_items];
+    x.kv = kvrb / p.n_rb;
+    x.row0 = (kvrb - x.kv * p.n_rb) * kRows0;
     x.rows = min(kRows0, p.G_rows - x.row0);
     x.n_tiles = (x.it.n_tokens + kTok0 - 1) / kTok0;
     return x;
@@ -365,8 +386,8 @@ __global__ void __launch_bounds__(kThreads0, 1)
     bool ok = true;
     // PVs still to issue, oldest first: PV(g) is issued after S(g + 2)
     struct Pend {
-      int t, k;             // tile, task
-      bool first, last;     // the task's first / last tile
+      int t, k;             // tile, run
+      bool first, last;     // the run's first / last tile
     };
     Pend q0{0, 0, false, false}, q1{0, 0, false, false};   // the queue's two slots
     int pn = 0;
@@ -375,7 +396,7 @@ __global__ void __launch_bounds__(kThreads0, 1)
       const int t = e.t, buf = t % NS;
       bool r = __all_sync(0xffffffffu, mbar_wait(bar(B0_PFULL + t % kSBufs0), uint32_t(t / kSBufs0) & 1u, p.fault,
                                                  p.wait_limit));
-      // the first PV of task k overwrites O buffer k % 2: task k - 2 must have been read out
+      // the first PV of run k overwrites O buffer k % 2: run k - 2 must have been read out
       if (r && e.first && e.k >= 2)
         r = __all_sync(0xffffffffu, mbar_wait(bar(B0_OFREE + (e.k & 1)), uint32_t((e.k - 2) >> 1) & 1u,
                                               p.fault, p.wait_limit));
@@ -400,17 +421,22 @@ __global__ void __launch_bounds__(kThreads0, 1)
       return true;
     };
     int g = 0;
+    uint64_t qk = qd;
     for (int k = 0; k < n_mine && ok; ++k) {
       const Task x = task(k);
-      // Task k's query rows arrive after task k - 2 is read out, which needs its last
-      // PV: issue every pending PV of task k - 2 or earlier first.
-      while (ok && pn > 0 && q0.k <= k - 2) ok = issue_pv();
-      if (!ok) break;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B0_QFULL + (k & 1)), uint32_t(k >> 1) & 1u, p.fault,
-                                             p.wait_limit));
-      if (!ok) break;
-      fence_after();
-      const uint64_t qk = qd + (((k & 1) * Lay::kQBytes) >> 4);
+      const int run = run_of(k);
+      const bool run_ends = last_of_run(k);
+      if (new_run(k)) {
+        // Run r's query rows arrive after run r - 2 is read out, which needs its last
+        // PV: issue every pending PV of run r - 2 or earlier first.
+        while (ok && pn > 0 && q0.k <= run - 2) ok = issue_pv();
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B0_QFULL + (run & 1)), uint32_t(run >> 1) & 1u, p.fault,
+                                               p.wait_limit));
+        if (!ok) break;
+        fence_after();
+        qk = qd + (((run & 1) * Lay::kQBytes) >> 4);
+      }
       for (int j = 0; j < x.n_tiles; ++j, ++g) {
         const int buf = g % NS;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(B0_KFULL + buf), uint32_t(g / NS) & 1u, p.fault,
@@ -427,11 +453,11 @@ __global__ void __launch_bounds__(kThreads0, 1)
                        kk > 0 ? 1u : 0u);
           }
           commit_to(bar(B0_SFULL + g % kSBufs0));
-          if (j == x.n_tiles - 1) commit_to(bar(B0_QFREE + (k & 1)));   // Q tile k % 2 may be refilled
+          if (run_ends && j == x.n_tiles - 1) commit_to(bar(B0_QFREE + (run & 1)));   // Q tile may be refilled
         }
         __syncwarp();
         if (pn == 2 && !(ok = issue_pv())) break;   // PV(g - 2)
-        const Pend e{g, k, j == 0, j == x.n_tiles - 1};
+        const Pend e{g, run, new_run(k) && j == 0, run_ends && j == x.n_tiles - 1};
         if (pn == 0) q0 = e;
         else q1 = e;
         ++pn;
@@ -445,17 +471,17 @@ __global__ void __launch_bounds__(kThreads0, 1)
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue warps
     // Thread = stacked row r = TMEM lane (a warp reaches the lanes of its quadrant,
-    // warp % 4).  Two jobs per task: gather a later task's query rows into its Q
-    // tile, and read out a finished task's O / l with its LSE.
+    // warp % 4).  Two jobs per run: gather a later run's query rows into its Q tile,
+    // and read out a finished run's O / l with its LSE.
     const int r = 32 * (warp & 3) + lane;
     const uint32_t lane_base = tmem + (uint32_t(32 * (warp & 3)) << 16);
-    // Task k's query rows into Q tile k % 2, 128-byte swizzled like a TMA box; rows
-    // past the stacked count are zero.
-    auto load_q = [&](int k) -> bool {
-      if (k >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(B0_QFREE + (k & 1)), uint32_t((k - 2) >> 1) & 1u,
+    // Run u's query rows into Q tile u % 2, 128-byte swizzled like a TMA box; rows past
+    // the stacked count are zero.
+    auto load_q = [&](int u) -> bool {
+      if (u >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(B0_QFREE + (u & 1)), uint32_t((u - 2) >> 1) & 1u,
                                                         p.fault, p.wait_limit)))
         return false;
-      const Task x = task(k);
+      const Task x = task(run_first(u));
       const bool live = r < x.rows;
       const uint4 *src = nullptr;
       if (live) {
@@ -463,7 +489,7 @@ __global__ void __launch_bounds__(kThreads0, 1)
         row_source(x, x.row0 + r, qb, head);
         src = reinterpret_cast<const uint4 *>(p.q + (int64_t(qb) * p.Hq_req + head) * D);
       }
-      uint8_t *qt = sm + Lay::kOffQ + (k & 1) * Lay::kQBytes + r * 128;
+      uint8_t *qt = sm + Lay::kOffQ + (u & 1) * Lay::kQBytes + r * 128;
       uint4 v[D / 8];
 #pragma unroll
       for (int j = 0; j < D / 8; ++j) v[j] = live ? __ldg(src + j) : make_uint4(0u, 0u, 0u, 0u);
@@ -472,35 +498,35 @@ __global__ void __launch_bounds__(kThreads0, 1)
         *reinterpret_cast<uint4 *>(qt + (j >> 3) * Lay::kQBoxBytes + (((j & 7) ^ (r & 7)) << 4)) = v[j];
       fence_proxy_async();  // generic writes, read by the MMAs (async proxy)
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B0_QFULL + (k & 1)));
+      if (lane == 0) mbar_arrive(bar(B0_QFULL + (u & 1)));
       return true;
     };
     bool ok = true;
-    if (n_mine > 0) ok = load_q(0);
-    if (ok && n_mine > 1) ok = load_q(1);
-    for (int k = 0; k < n_mine && ok; ++k) {
-      const Task x = task(k);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B0_OFULL + (k & 1)), uint32_t(k >> 1) & 1u, p.fault,
+    if (n_runs > 0) ok = load_q(0);
+    if (ok && n_runs > 1) ok = load_q(1);
+    for (int u = 0; u < n_runs && ok; ++u) {
+      const int k_last = run_end(u) - 1;
+      const Task x = task(k_last);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(B0_OFULL + (u & 1)), uint32_t(u >> 1) & 1u, p.fault,
                                              p.wait_limit));
       if (ok)
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(B0_LREADY + (k & 1)), uint32_t(k >> 1) & 1u, p.fault,
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B0_LREADY + (u & 1)), uint32_t(u >> 1) & 1u, p.fault,
                                                p.wait_limit));
       if (!ok) break;
       fence_after();
       if (32 * (warp & 3) < x.rows) {
         const bool live = r < x.rows;
         uint32_t lmw[2];
-        tmem_ld2(lane_base + Lay::kColLM + 2 * (k & 1), lmw);
+        tmem_ld2(lane_base + Lay::kColLM + 2 * (u & 1), lmw);
         ld_wait();
         const float l_sum = __uint_as_float(lmw[0]), m_run = __uint_as_float(lmw[1]);
-        int qb, head;
+        int qb, head = 0;
         const int m = live ? row_source(x, x.row0 + r, qb, head) : 0;
-        if (!live) head = 0;
-        const int orow_base = x.it.q_index >= 0 ? x.it.out_row : (live ? ld_list(row_base + m) : 0) + x.it.out_row;
-        const int64_t orow = int64_t(orow_base) * p.Hq_req + head;
+        const int rbase = x.it.q_index >= 0 ? 0 : (live ? ld_list(row_base + m) : 0);
+        const int64_t orow = int64_t(rbase + x.it.out_row) * p.Hq_req + head;
         float *dst = p.v_out + orow * D;
         const float inv = p.v_scale / l_sum;
-        const uint32_t o_col = lane_base + Lay::kColO + D * (k & 1);
+        const uint32_t o_col = lane_base + Lay::kColO + D * (u & 1);
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
           uint32_t o[32];
@@ -517,12 +543,19 @@ __global__ void __launch_bounds__(kThreads0, 1)
             }
           }
         }
-        if (live) p.lse_out[orow] = m_run + log2f(l_sum);
+        if (live) {
+          p.lse_out[orow] = m_run + log2f(l_sum);
+          // the run's other chunks: empty rows (their v is not read by the merge)
+          for (int k = run_first(u); k < k_last; ++k) {
+            const int base = x.it.q_index >= 0 ? 0 : rbase;
+            p.lse_out[int64_t(base + task(k).it.out_row) * p.Hq_req + head] = neg_inf();
+          }
+        }
       }
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B0_OFREE + (k & 1)));   // the first PV of task k + 2 may overwrite O
-      if (k + 2 < n_mine) ok = load_q(k + 2);
+      if (lane == 0) mbar_arrive(bar(B0_OFREE + (u & 1)));   // the first PV of run u + 2 may overwrite O
+      if (u + 2 < n_runs) ok = load_q(u + 2);
     }
   } else {
     // ------------------------------------------------------------------ row warps
@@ -531,13 +564,19 @@ __global__ void __launch_bounds__(kThreads0, 1)
     bool ok = true;
     const float qs = p.q_scale;
     int g = 0;  // tiles consumed so far (all tasks)
+    float m_run = neg_inf(), l_sum = 0.f;  // the run's, m_run in log2 units of the scaled score
     for (int k = 0; k < n_mine && ok; ++k) {
       const Task x = task(k);
+      const int run = run_of(k);
+      const bool first_task = new_run(k);
       const bool warp_live = warp * 32 < x.rows;
       const bool warp_full = warp * 32 + 32 <= x.rows;   // every row of this warp is live
       const int row_valid = r < x.rows ? kTok0 : 0;
-      const uint32_t o_col = lane_base + Lay::kColO + D * (k & 1);
-      float m_run = neg_inf(), l_sum = 0.f;              // m_run in log2 units of the scaled score
+      const uint32_t o_col = lane_base + Lay::kColO + D * (run & 1);
+      if (first_task) {
+        m_run = neg_inf();
+        l_sum = 0.f;
+      }
       for (int j = 0; j < x.n_tiles; ++j, ++g) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(B0_SFULL + g % kSBufs0), uint32_t(g / kSBufs0) & 1u, p.fault,
                                                p.wait_limit));
@@ -570,7 +609,7 @@ __global__ void __launch_bounds__(kThreads0, 1)
           const bool grow = tmax > m_run + kLazy0;
           if (__any_sync(0xffffffffu, grow)) {
             const float m_new = grow ? tmax : m_run;
-            if (j > 0) {  // PV(g - 1) must be done; then rescale this warp's O rows in TMEM
+            if (j > 0 || !first_task) {  // PV(g - 1) of this run must be done; rescale O in TMEM
               ok = __all_sync(0xffffffffu, mbar_wait(bar(B0_KEMPTY + (g - 1) % NS), uint32_t((g - 1) / NS) & 1u,
                                                      p.fault, p.wait_limit));
               if (!ok) break;
@@ -625,20 +664,21 @@ __global__ void __launch_bounds__(kThreads0, 1)
         if (lane == 0) mbar_arrive(bar(B0_PFULL + g % kSBufs0));
       }
       if (!ok) break;
-      // l and m of this task's rows for the epilogue warps; buffer k % 2 was read out
-      // for task k - 2 (normally long done)
-      if (k >= 2)
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(B0_OFREE + (k & 1)), uint32_t((k - 2) >> 1) & 1u, p.fault,
+      if (!last_of_run(k)) continue;
+      // l and m of this run's rows for the epilogue warps; their slot was read out for
+      // run - 2 (normally long done)
+      if (run >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B0_OFREE + (run & 1)), uint32_t((run - 2) >> 1) & 1u, p.fault,
                                                p.wait_limit));
       if (!ok) break;
       {
         const uint32_t lmw[2] = {__float_as_uint(l_sum), __float_as_uint(m_run)};
-        tmem_st2(lane_base + Lay::kColLM + 2 * (k & 1), lmw);
+        tmem_st2(lane_base + Lay::kColLM + 2 * (run & 1), lmw);
         st_wait();
       }
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B0_LREADY + (k & 1)));
+      if (lane == 0) mbar_arrive(bar(B0_LREADY + (run & 1)));
     }
   }
   fence_before();
@@ -705,6 +745,8 @@ psd_status launch_l0(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t
   p.Gm = L.Gm;
   p.G_rows = L.G_cta;
   p.Hkv = L.Hkv;
+  p.n_items = L.num_items;
+  p.runs = L.merge_runs ? 1 : 0;
   p.n_rb = (L.G_cta + kRows0 - 1) / kRows0;
   const int64_t tasks = int64_t(L.num_items) * L.Hkv * p.n_rb;
   if (tasks > 0x7fffffffLL) return fail(PSD_ERR_UNSUPPORTED, "level-0 tcgen05 partial: %lld tasks", (long long)tasks);

@@ -1,10 +1,11 @@
-"""The stacked level-0 rows of the cascade on the tcgen05 kernel (one CTA per level-0
-chunk, KV head and block of 128 stacked rows; mlxcel PR #1004, Decomposition: the M
-members' G query heads of a KV head stacked KV-head major).  Edge cases of its
-64-token tiles against the float64 oracle: spans that end inside a tile (page
-positions past the chunk's pages load as zeros), page sizes from 16 to 128, head
-dims 64 and 128, a page id out of range, lists uploaded or in the launch
-parameters, and the same results as the 16-row-group kernel."""
+"""The stacked level-0 rows of the cascade on the tcgen05 kernel (persistent, one CTA
+per SM over (level-0 chunk, KV head, block of 128 stacked rows) tasks; mlxcel PR
+#1004, Decomposition: the M members' G query heads of a KV head stacked KV-head
+major).  Edge cases of its 64-token tiles against the float64 oracle: spans that end
+inside a tile (page positions past the chunk's pages load as zeros), page sizes from
+16 to 128, head dims 64 and 128, a page id out of range, lists uploaded or in the
+launch parameters, runs of chunks accumulated into one partial, and the same results
+as the 16-row-group kernel."""
 import numpy as np
 import pytest
 import torch
@@ -110,3 +111,21 @@ def test_level0_tcgen05_lists_inline_or_uploaded(tile, inline):
     req = sorted({members[0], members[7], members[-1], others[0], others[-1]})
     ro, rl = A.decode_attention(A.workload_arrays(w), requests=req)
     assert_close(o[req], lse[req], ro[req], rl[req], "bf16", f"cascade, tile {tile}")
+
+
+def test_level0_tcgen05_runs_of_chunks():
+    """400 level-0 tasks (100 chunks x 2 KV heads x 2 row blocks of 160 stacked rows)
+    over one CTA per SM: each CTA takes a contiguous range of about 2.6 tasks, whose
+    chunks of one KV head and row block accumulate into one partial (a run) and leave
+    the run's other chunk rows empty; runs end where the KV head or the row block
+    changes inside a CTA's range.  Against the oracle and the mma.sync form."""
+    w = _cascade(91, 16, 400, 64, 128, 4, 40)
+    d = Dev(w)
+    with use_level0("tcgen05"):
+        o, lse, stats, _ = d.decode(enable=1, with_stats=True)
+    assert stats["path"] == 1 and stats["members"] == 40 and stats["prefix_chunks"] == 100
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o, lse, ro, rl, "bf16", "level 0 tcgen05 runs")
+    with use_level0("mma_sync"):
+        mo, ml = d.decode(enable=1)
+    assert np.abs(o - mo).max() < 2e-3 and np.abs(lse - ml).max() < 1e-3
