@@ -63,13 +63,13 @@ TRAFFIC_BYTES = 316086016 + 1213184
 # sources are unchanged.
 CASCADE_DRAM_SOURCES = [os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", f)
                         for f in ("partial_tcs.cu", "partial_l0.cu")]
-CASCADE_DRAM_SHA256 = "4d21e24c970e036ddacf69e9e9cf79536ca6ef447f94c2035d80eba01f7db5ce"
+CASCADE_DRAM_SHA256 = "75166b25e6ccadd2c49a5bd4e22bca0e0b789af6b87c421c0a18a1888b1bc177"
 CASCADE_DRAM_READ = {
     # 8192-token prefix: the flat arm's prefix re-reads hit the 129 MB L2
-    "flat_vs_cascade": {"flat": 533344512, "cascade": 533302912,
+    "flat_vs_cascade": {"flat": 533343744, "cascade": 533301760,
                         "kernels": "flat: partial_tcs 523x8 CTAs; cascade: one partial_tcs launch, both levels"},
     # 65536-token prefix (268 MB): the flat arm re-reads part of the prefix from DRAM
-    "flat_vs_cascade_prefix_beyond_l2": {"flat": 930637312, "cascade": 268660608 + 499736192,
+    "flat_vs_cascade_prefix_beyond_l2": {"flat": 930633216, "cascade": 268659712 + 499736832,
                                          "kernels": "flat: partial_tcs 2315x8 CTAs; cascade: partial_l0 (level 0) "
                                                     "+ partial_tcs 267x8 (level 1)"},
 }
