@@ -94,6 +94,9 @@ struct L0Layout {
   static constexpr uint32_t kColO = 0, kColS = 2 * D, kColLM = kColS + kSBufs0 * kTok0;
   static constexpr uint32_t kTmemCols = kColLM + 4 <= 256 ? 256 : 512;
   static_assert(kStages <= kMaxStages0, "barrier slots");
+  // The control warp issues S(g + 2) before PV(g), and only PV(g) frees the stage of
+  // tile g: with fewer than three stages tile g + 2 has no stage to land in.
+  static_assert(kStages >= 3, "S runs two tiles ahead of PV");
   static_assert(kSmem <= 227u * 1024u, "shared memory");
   static_assert(kStageBytes % 1024 == 0 && kOffQ % 1024 == 0 && kQBytes % 1024 == 0,
                 "128B-swizzled tiles need 1024-byte alignment");
