@@ -357,7 +357,8 @@ psd_status merge_states(psd_ctx *ctx, const float *v_in, const float *lse_in,
  * workspace: >= psd_workspace_bytes(batch, plan item total, plan->num_rows, Hq, Dv).
  * stats (host, nullable) receives which path ran.  The work lists reach the GPU in
  * the launches' parameters when they fit (16 KB of items, order and members, and
- * batch < 1024) and the bf16 tensor-core partial kernel serves every launch;
+ * batch < 1024) and every launch's kernel takes them there (the bf16 16-row-group
+ * tensor-core kernel, and the tcgen05 kernel for the stacked level-0 rows);
  * otherwise by one copy from pinned staging into the workspace. */
 psd_status cascade_decode(psd_ctx *ctx, const psd_decode_args *args,
                           const psd_cascade_plan *plan, float *o, float *lse,
