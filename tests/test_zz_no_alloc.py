@@ -109,3 +109,31 @@ def test_no_alloc_fp8_and_mla_plans(latent):
         o, lse, _ = _no_alloc(d, plan)
         assert_close(o, lse, ro, rl, "fp8_e4m3", f"no_alloc {w.name}")
         assert np.abs(o - wo).max() <= OUT_TOL["fp8_e4m3"] and np.abs(lse - wl).max() <= LSE_TOL
+
+
+def test_no_alloc_tcgen05_level0_runs_of_chunks():
+    """Level 0 on the tcgen05 kernel with more tasks than SMs (160 chunks x 2 KV heads
+    over one CTA per SM): runs of chunks accumulate into one partial and leave the
+    run's other rows empty (LSE -inf), which the merge must skip.  In the shared
+    array, twice, against the oracle and against cascade_decode with a workspace."""
+    from oracle import attention as A
+    from _gpu_util import assert_close, use_level0
+    rng = np.random.default_rng(7)
+    lengths = [int(x) for x in rng.integers(1, 700, size=11)]
+    mem = sorted(int(m) for m in rng.choice(11, size=8, replace=False))
+    for m in mem:
+        lengths[m] = 640 * 16 + int(rng.integers(1, 48))
+    w = synth._make("no_alloc_l0_runs", rng, lengths, Hq=8, Hkv=2, Dqk=128, Dv=128, page_size=16,
+                    num_pages=sum((n + 15) // 16 for n in lengths) + 8, tile_tokens=64,
+                    shared=(mem, 640), min_shared_pages=1, min_members=2)
+    d = Dev(w)
+    plan = psd.plan_decode(d.table, w.tile_tokens, 1, w.min_shared_pages, w.min_members)
+    assert plan.num_members == 8
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    with use_level0("tcgen05"):
+        wo, wl = _with_workspace(d, plan)
+        for _ in range(2):
+            o, lse, stats = _no_alloc(d, plan)
+            assert stats["path"] == 1 and stats["prefix_chunks"] == 160
+            assert_close(o, lse, ro, rl, "bf16", "no_alloc, tcgen05 level 0 with runs")
+            assert np.abs(o - wo).max() <= OUT_TOL["bf16"] and np.abs(lse - wl).max() <= LSE_TOL
