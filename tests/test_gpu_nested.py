@@ -9,7 +9,7 @@ import torch
 import paged_split_kv_decode_gb300 as psd
 from oracle import attention as A
 import synth
-from _gpu_util import Dev, assert_close, ctx, use_kernel
+from _gpu_util import Dev, assert_close, ctx, use_kernel, use_level0
 
 pytestmark = pytest.mark.gpu
 
@@ -38,11 +38,14 @@ def _decode_nested(w, levels, msp, mm):
     return o.cpu().double().numpy(), lse.cpu().double().numpy(), stats, plan
 
 
+@pytest.mark.parametrize("level0", ["auto", "tcgen05"])
 @pytest.mark.parametrize("kernel", ["auto", "cuda_core"])
 @pytest.mark.parametrize("seed", [0, 1, 2])
-def test_small_nested_matches_dense_attention(seed, kernel):
+def test_small_nested_matches_dense_attention(seed, kernel, level0):
+    """level0 'tcgen05': every segment's stacked rows on the tcgen05 kernel, one
+    launch per segment on the side stream, runs of chunks leaving empty rows."""
     w = _nested_small(seed)
-    with use_kernel(kernel):
+    with use_kernel(kernel), use_level0(level0):
         o, lse, stats, plan = _decode_nested(w, 3, 2, 2)
     assert plan.num_segments == 3 and [s[1] for s in plan.segments] == [8, 4, 4]
     assert stats["path"] == 1 and stats["members"] == 16 and stats["shared_pages"] == 4 + 3 + 2
@@ -93,3 +96,6 @@ def test_more_segments_than_one_launch_holds():
     assert ctx().counters()["lists_inline"] - before == 1
     ro, rl = A.decode_attention(A.workload_arrays(w))
     assert_close(o, lse, ro, rl, w.kv_dtype, "ten segments")
+    with use_level0("tcgen05"):   # ten tcgen05 level-0 launches, lists still inline
+        o, lse, stats, plan = _decode_nested(w, 2, 2, 2)
+    assert_close(o, lse, ro, rl, w.kv_dtype, "ten segments, level 0 on tcgen05")
