@@ -318,12 +318,13 @@ def test_outputs_into_pinned_host_memory(maker):
     assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu())
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kernel,level0", [(k, "auto") for k in KERNELS] + [("auto", "tcgen05")])
 @pytest.mark.parametrize("maker", [synth.tiny_cascade, synth.flat_decode, synth.cascade_decode])
-def test_inputs_from_pinned_host_memory(maker, kernel):
+def test_inputs_from_pinned_host_memory(maker, kernel, level0):
     """cascade_decode with q and page_indices in pinned host memory (read by the
-    partial kernels over the host link) and the outputs in pinned host memory: equal
-    bit for bit to the all-device call, on flat and cascade plans."""
+    partial kernels over the host link, the tcgen05 level-0 kernel included) and the
+    outputs in pinned host memory: equal bit for bit to the all-device call, on flat
+    and cascade plans."""
     w = maker(seed=5)
     d = Dev(w)
     plan = psd.plan_decode(d.table, w.tile_tokens, 1, w.min_shared_pages, w.min_members)
@@ -337,7 +338,7 @@ def test_inputs_from_pinned_host_memory(maker, kernel):
                              v_scale=w.v_scale)
     oh = torch.full((w.batch, w.Hq, w.Dv), float("nan")).pin_memory()
     lh = torch.full((w.batch, w.Hq), float("nan")).pin_memory()
-    with use_kernel(kernel):
+    with use_kernel(kernel), use_level0(level0):
         psd.cascade_decode(ctx(), d.args(), plan, o, lse, ws)
         psd.cascade_decode(ctx(), args_h, plan, oh, lh, ws)
     torch.cuda.synchronize()
