@@ -11,9 +11,11 @@
 // memory after the group bounds.  The SKIP form, for partials with many empty rows,
 // reads each batch's LSE values first and loads only the live rows' v.  When the
 // partial kernel before it on the stream allows it, the merge launches early, reads
-// o_indptr, then waits for that grid.
+// o_indptr, then waits for that grid.  Large merges on their own stream whole input
+// rows through shared memory instead (merge_stream_kernel below).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "device.cuh"
@@ -327,6 +329,219 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2)
   }
 }
 
+// Large merges without a preceding partial kernel (merge_states on its own): three
+// CTAs per SM, each streaming a contiguous range of whole input rows (every head's V,
+// then the row's LSE values) through a ring of four stages in shared memory, each row
+// by two bulk asynchronous copies that a producer warp issues.  The register-held
+// loads of the forms above keep about 128 KB per SM in flight (the register file
+// bounds them), and ncu put that form at 73% of peak DRAM throughput with its warps
+// waiting on loads; the rings keep about 200 KB per SM in flight.  Measured at
+// H = 32, D = 128: 6.82 TB/s at 1M output rows against 6.00, 6.39 against 6.02 at 16K
+// (one CTA per SM with a 13-stage ring: 5.57; two per SM: 6.73).  Consumer thread t
+// owns float4 chunks t + 256 j of a row and, for each chunk's head, a running
+// maximum: a row whose LSE exceeds it rescales that head's sum and weighted V first
+// (online, so the group's maximum is not needed up front).  A one-row group gives
+// weight 1 and sum 1, so out = v and lse_out = lse exactly.  A wait that runs out
+// fills the CTA's unfinished output rows with NaN (there is no fault word here).
+constexpr int kStreamConsumers = 8;                              // warps
+constexpr int kStreamThreads = 32 * (kStreamConsumers + 1);      // + the producer warp
+constexpr int kStreamCtas = 3;                                   // per SM
+constexpr uint32_t kStreamRing = 68 * 1024;                      // per CTA
+constexpr int kStreamMaxStages = 32;
+
+struct StreamParams {
+  const float *v_in;
+  const float *lse_in;
+  const int32_t *o_indptr;
+  int64_t num_out;
+  int H, D, stages;
+  uint32_t row_bytes, lse_bytes, stage_bytes;
+  float *v_out;
+  float *lse_out;
+};
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// A bounded wait with no fault word to report to: false after the limit.
+__device__ __forceinline__ bool stream_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  return true;
+}
+
+template <int C>  // float4 chunks per consumer thread: H * D / 4 = 256 * C
+__global__ void __launch_bounds__(kStreamThreads, kStreamCtas) merge_stream_kernel(const StreamParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(p.stages) * p.stage_bytes);
+  uint64_t *empty = full + p.stages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), kStreamConsumers);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  wait_for_prior_grid();
+  // This CTA's output rows [r0, r1): the group boundaries nearest to its equal share of
+  // the input rows (o_indptr is non-decreasing; lower bound of the share's first row).
+  const int32_t base = __ldg(p.o_indptr), total = __ldg(p.o_indptr + p.num_out) - base;
+  auto first_row = [&](int64_t b) -> int64_t {
+    if (b >= gridDim.x) return p.num_out;
+    const int64_t t = base + int64_t(total) * b / gridDim.x;
+    int64_t lo = 0, hi = p.num_out;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (__ldg(p.o_indptr + mid) < t) lo = mid + 1;
+      else hi = mid;
+    }
+    return lo;
+  };
+  const int64_t r0 = first_row(blockIdx.x), r1 = first_row(int64_t(blockIdx.x) + 1);
+  if (r1 <= r0) return;
+  const int32_t g0 = __ldg(p.o_indptr + r0), g1 = __ldg(p.o_indptr + r1);
+  const int S = p.stages;
+
+  if (warp == kStreamConsumers) {
+    // ------------------------------------------------------------ producer warp
+    if (lane == 0) {
+      bool ok = true;
+      for (int32_t k = 0; k < g1 - g0 && ok; ++k) {
+        const int s = k % S;
+        if (k >= S && !(ok = stream_wait(smem_u32(empty + s), uint32_t(k / S - 1) & 1u))) break;
+        const int64_t row = int64_t(g0) + k;
+        const uint32_t dst = smem_u32(smem + size_t(s) * p.stage_bytes);
+        mbar_arrive_expect_tx(smem_u32(full + s), p.row_bytes + p.lse_bytes);
+        bulk_load(dst, p.v_in + row * p.H * p.D, p.row_bytes, smem_u32(full + s));
+        bulk_load(dst + p.row_bytes, p.lse_in + row * p.H, p.lse_bytes, smem_u32(full + s));
+      }
+      // no copy in flight at exit: the last S rows' barriers complete once they land
+      const int32_t n = g1 - g0;
+      for (int32_t k = n > S ? n - S : 0; ok && k < n; ++k)
+        ok = stream_wait(smem_u32(full + k % S), uint32_t(k / S) & 1u);
+    }
+    return;
+  }
+  // ------------------------------------------------------------- consumer warps
+  const int t = threadIdx.x;
+  const int D4 = p.D >> 2;
+  int head[C];
+#pragma unroll
+  for (int j = 0; j < C; ++j) head[j] = (t + 256 * j) / D4;
+  bool ok = true;
+  for (int64_t r = r0; r < r1 && ok; ++r) {
+    const int32_t lo = __ldg(p.o_indptr + r), n = __ldg(p.o_indptr + r + 1) - lo;
+    float M[C], sw[C];
+    float4 acc[C];
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+      M[j] = neg_inf();
+      sw[j] = 0.f;
+      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int32_t i = 0; i < n; ++i) {
+      const int32_t k = lo + i - g0;
+      const int s = k % S;
+      ok = __all_sync(0xffffffffu, stream_wait(smem_u32(full + s), uint32_t(k / S) & 1u));
+      if (!ok) break;
+      const uint8_t *stage = smem + size_t(s) * p.stage_bytes;
+      const float *lse_row = reinterpret_cast<const float *>(stage + p.row_bytes);
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        const float l = lse_row[head[j]];
+        if (l == neg_inf()) continue;  // an empty partial: its v is not used
+        const float4 v = reinterpret_cast<const float4 *>(stage)[t + 256 * j];
+        if (l > M[j]) {
+          const float a = ex2(M[j] - l);   // 0 while M is -inf
+          acc[j].x *= a;
+          acc[j].y *= a;
+          acc[j].z *= a;
+          acc[j].w *= a;
+          sw[j] *= a;
+          M[j] = l;
+        }
+        const float w = ex2(l - M[j]);
+        acc[j].x = fmaf(w, v.x, acc[j].x);
+        acc[j].y = fmaf(w, v.y, acc[j].y);
+        acc[j].z = fmaf(w, v.z, acc[j].z);
+        acc[j].w = fmaf(w, v.w, acc[j].w);
+        sw[j] += w;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(empty + s));
+    }
+    if (!ok) {  // a wait ran out: this row and the rest of the range read as NaN
+      const float nan = __int_as_float(0x7fc00000);
+      for (int64_t q = r; q < r1; ++q) {
+        float4 *o4 = reinterpret_cast<float4 *>(p.v_out + q * p.H * p.D);
+#pragma unroll
+        for (int j = 0; j < C; ++j) {
+          o4[t + 256 * j] = make_float4(nan, nan, nan, nan);
+          if (p.lse_out && (t + 256 * j) % D4 == 0) p.lse_out[q * p.H + head[j]] = nan;
+        }
+      }
+      break;
+    }
+    float4 *out4 = reinterpret_cast<float4 *>(p.v_out + r * p.H * p.D);
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+      const bool live = M[j] != neg_inf();
+      const float inv = live ? 1.f / sw[j] : 0.f;
+      __stcs(out4 + t + 256 * j, make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv));
+      if (p.lse_out && (t + 256 * j) % D4 == 0) p.lse_out[r * p.H + head[j]] = live ? M[j] + log2f(sw[j]) : neg_inf();
+    }
+  }
+}
+
+template <int C>
+cudaError_t launch_stream_c(const DeviceInfo &dev, cudaStream_t s, const StreamParams &p, size_t smem) {
+  cudaError_t e = cudaFuncSetAttribute(merge_stream_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  merge_stream_kernel<C><<<dim3(static_cast<unsigned>(kStreamCtas * dev.num_sms)), kStreamThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+// The streaming form when it applies: H * D / 4 a multiple of 256 with at most 4
+// chunks per thread (more spill at three CTAs per SM), 16-byte LSE rows, at least 8
+// output rows per CTA (below that the one-wave forms above are faster: 1K rows at
+// H = 32 take 33 us there and 40 us here), and four stages in the ring.  Returns false
+// to fall back.
+bool launch_stream(const DeviceInfo &dev, cudaStream_t s, const float *v_in, const float *lse_in,
+                   const int32_t *o_indptr, int64_t num_out, int H, int D, float *v_out, float *lse_out,
+                   cudaError_t &e) {
+  const int64_t chunks = int64_t(H) * D / 4;
+  if (chunks % 256 != 0 || chunks / 256 > 4 || H % 4 != 0 || num_out < 8LL * kStreamCtas * dev.num_sms) return false;
+  if (reinterpret_cast<uintptr_t>(lse_in) % 16 != 0) return false;
+  StreamParams p;
+  p.v_in = v_in;
+  p.lse_in = lse_in;
+  p.o_indptr = o_indptr;
+  p.num_out = num_out;
+  p.H = H;
+  p.D = D;
+  p.row_bytes = uint32_t(H) * uint32_t(D) * 4u;
+  p.lse_bytes = uint32_t(H) * 4u;
+  p.stage_bytes = p.row_bytes + p.lse_bytes;
+  p.stages = std::min<int>(kStreamMaxStages, int(kStreamRing / p.stage_bytes));
+  p.v_out = v_out;
+  p.lse_out = lse_out;
+  const size_t smem = size_t(p.stages) * p.stage_bytes + 2 * sizeof(uint64_t) * size_t(p.stages);
+  if (p.stages < 4 || smem > size_t(dev.smem_optin)) return false;
+  switch (chunks / 256) {
+    case 1: e = launch_stream_c<1>(dev, s, p, smem); break;
+    case 2: e = launch_stream_c<2>(dev, s, p, smem); break;
+    case 4: e = launch_stream_c<4>(dev, s, p, smem); break;
+    default: return false;
+  }
+  return true;
+}
+
 template <int NV, bool SKIP, bool INL>
 cudaError_t launch_form(dim3 grid, bool wide, bool early, cudaStream_t s, const float *v_in, const float *lse_in,
                         const int32_t *o_indptr, int64_t num_out, int H, int D, float *v_out,
@@ -416,13 +631,17 @@ psd_status launch_merge(const float *v_in, const float *lse_in, const int32_t *o
     std::memcpy(block.v, o_indptr_host, sizeof(int32_t) * size_t(num_out + 1));
     inl = &block;
   }
+  cudaError_t e;
+  if (!after_partial && !inl && launch_stream(dev, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out, e)) {
+    if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "merge_states launch: %s", cudaGetErrorString(e));
+    return PSD_OK;
+  }
   const int64_t warps = num_out * H;
   const int64_t blocks = (warps + kMergeWarps - 1) / kMergeWarps;
   if (blocks > 0x7fffffffLL) return fail(PSD_ERR_UNSUPPORTED, "merge_states: grid too large");
   const dim3 grid(static_cast<unsigned>(blocks));
   // up to two wide blocks per SM cover the grid in one wave
   const bool wide = blocks <= 2LL * dev.num_sms;
-  cudaError_t e;
   if (D <= 128)
     e = launch_nv<1>(grid, wide, after_partial, skip_empty, inl, s, v_in, lse_in, o_indptr, num_out, H, D, v_out, lse_out);
   else if (D <= 256)

@@ -171,3 +171,45 @@ def test_two_heads_per_warp_and_its_fallbacks(H, misaligned):
         dl1.copy_(lse_in.cuda())
         vo1, lo1 = _gpu_merge(v_in, dl1, o_indptr)
         assert torch.equal(vo1, vo) and torch.equal(lo1, lo)
+
+
+@pytest.mark.parametrize("H", [8, 16, 32])
+def test_streaming_form_for_large_merges(H):
+    """Large merges with 16-byte LSE rows and H * D / 4 a multiple of 256 stream whole
+    input rows through shared memory (three CTAs per SM, 1, 2 or 4 float4 chunks per
+    thread here).  Groups of one (bit-exact identity), an empty group, an all -inf
+    group and empty rows whose v is NaN, against the oracle; and against the
+    two-heads-per-warp form on the same rows (an LSE buffer 8 bytes past a 16-byte
+    boundary takes that form), which sums in another order."""
+    rng = np.random.default_rng(70 + H)
+    sizes = rng.integers(1, 17, size=4000)
+    sizes[3], sizes[4], sizes[5] = 0, 1, 1
+    o_indptr = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    N = int(o_indptr[-1])
+    v_in = torch.from_numpy(rng.standard_normal((N, H, 128), dtype=np.float32))
+    lse_in = torch.from_numpy(rng.uniform(-5, 20, size=(N, H)).astype(np.float32))
+    a, b = int(o_indptr[7]), int(o_indptr[8])
+    lse_in[a:b, 0] = -float("inf")                       # group 7, head 0: all -inf
+    empty = torch.from_numpy(rng.random((N, H)) < 0.2)
+    empty[torch.from_numpy(o_indptr[:-1][sizes > 0].astype(np.int64))] = False
+    lse_in[empty] = -float("inf")
+    v_in[empty] = float("nan")
+    ro, rl = A.merge_states(v_in.numpy(), lse_in.numpy(), o_indptr)
+    dl = lse_in.cuda()
+    assert dl.data_ptr() % 16 == 0
+    vo, lo = _gpu_merge(v_in, dl, o_indptr)
+    assert np.abs(vo.cpu().double().numpy() - ro).max() < TOL_O
+    assert np.array_equal(np.isneginf(lo.cpu().numpy()), np.isneginf(rl))
+    fin = np.isfinite(rl)
+    assert np.abs(lo.cpu().double().numpy()[fin] - rl[fin]).max() < TOL_L
+    for g in (4, 5):   # groups of one: v and lse bit for bit
+        row = int(o_indptr[g])
+        assert torch.equal(vo[g].cpu(), v_in[row]) and torch.equal(lo[g].cpu(), lse_in[row])
+    store = torch.empty(N * H + 2, device="cuda")
+    dl2 = store[2:].view(N, H)
+    dl2.copy_(dl)
+    assert dl2.data_ptr() % 16 == 8
+    vo2, lo2 = _gpu_merge(v_in, dl2, o_indptr)
+    assert (vo2 - vo).abs().max().item() < TOL_O
+    both = torch.isfinite(lo2) & torch.isfinite(lo)
+    assert torch.equal(torch.isneginf(lo2), torch.isneginf(lo)) and (lo2[both] - lo[both]).abs().max().item() < TOL_L
