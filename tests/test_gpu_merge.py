@@ -213,3 +213,23 @@ def test_streaming_form_for_large_merges(H):
     assert (vo2 - vo).abs().max().item() < TOL_O
     both = torch.isfinite(lo2) & torch.isfinite(lo)
     assert torch.equal(torch.isneginf(lo2), torch.isneginf(lo)) and (lo2[both] - lo[both]).abs().max().item() < TOL_L
+
+
+def test_streaming_form_offset_indptr_and_trailing_empty_groups():
+    """The streaming form's split of output rows over its CTAs (each the range whose
+    first input row falls in its equal share): o_indptr starting past row 0, one large
+    group, and the last 300 groups empty, every output row against the oracle."""
+    rng = np.random.default_rng(81)
+    sizes = rng.integers(1, 17, size=4000)
+    sizes[-300:] = 0
+    sizes[1000] = 700
+    o_indptr = np.concatenate([[37], 37 + np.cumsum(sizes)]).astype(np.int32)
+    N = int(o_indptr[-1]) + 5
+    v_in = torch.from_numpy(rng.standard_normal((N, 32, 128), dtype=np.float32))
+    lse_in = torch.from_numpy(rng.uniform(-5, 20, size=(N, 32)).astype(np.float32))
+    ro, rl = A.merge_states(v_in.numpy(), lse_in.numpy(), o_indptr)
+    vo, lo = _gpu_merge(v_in, lse_in, o_indptr)
+    assert np.abs(vo.cpu().double().numpy() - ro).max() < TOL_O
+    assert np.array_equal(np.isneginf(lo.cpu().numpy()), np.isneginf(rl))
+    fin = np.isfinite(rl)
+    assert np.abs(lo.cpu().double().numpy()[fin] - rl[fin]).max() < TOL_L
