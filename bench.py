@@ -63,13 +63,13 @@ TRAFFIC_BYTES = 316086016 + 1213184
 # sources are unchanged.
 CASCADE_DRAM_SOURCES = [os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", f)
                         for f in ("partial_tcs.cu", "partial_l0.cu")]
-CASCADE_DRAM_SHA256 = "f3839366da9db814689522e6c97ac87660446ea76a93fd3b1be4f07868f5f7e1"
+CASCADE_DRAM_SHA256 = "e5de381740343d712431c7810b3257bd0f3649b5530ab941676062f04ba9bf2c"
 CASCADE_DRAM_READ = {
     # 8192-token prefix: the flat arm's prefix re-reads hit the 129 MB L2
-    "flat_vs_cascade": {"flat": 533347328, "cascade": 533303808,
+    "flat_vs_cascade": {"flat": 533333504, "cascade": 533295744,
                         "kernels": "flat: partial_tcs 523x8 CTAs; cascade: one partial_tcs launch, both levels"},
     # 65536-token prefix (268 MB): the flat arm re-reads part of the prefix from DRAM
-    "flat_vs_cascade_prefix_beyond_l2": {"flat": 930512256, "cascade": 268659456 + 499737472,
+    "flat_vs_cascade_prefix_beyond_l2": {"flat": 930361216, "cascade": 268659584 + 499737344,
                                          "kernels": "flat: partial_tcs 2315x8 CTAs; cascade: partial_l0 (level 0) "
                                                     "+ partial_tcs 267x8 (level 1)"},
 }

@@ -134,6 +134,7 @@ struct L0Params {
   int Hq_req, page_size, Gm, G_rows;
   float q_scale, v_scale;  // q_scale > 0
   long long wait_limit;
+  int withhold_from;  // testing aid: no loads for an item's tiles from this index on
 };
 
 // Shared-memory matrix descriptor, 128-byte swizzle (layout code 2), version 1.
@@ -324,7 +325,8 @@ __global__ void __launch_bounds__(kThreads0, 1)
     const uint64_t pol = l2_evict_first_policy();
     bool ok = true;
     int g = 0;  // tiles of this CTA so far (all tasks, both producers)
-    for (int k = 0; k < n_mine && ok; ++k) {
+    bool withheld = false;
+    for (int k = 0; k < n_mine && ok && !withheld; ++k) {
       const Task x = task(k);
       const int n_item_pages = (x.it.n_tokens + P - 1) / P;
       // The item's page ids, 32 positions per window, one per lane (a dependent load
@@ -332,6 +334,13 @@ __global__ void __launch_bounds__(kThreads0, 1)
       int win = 0;
       int pid = lane < n_item_pages ? __ldg(p.page_indices + x.it.page_off + lane) : -1;
       for (int j = 0; j < x.n_tiles; ++j, ++g) {
+        if (j >= p.withhold_from) {
+          // testing aid: neither producer loads this tile or any later one (both walk
+          // every tile, so both stop here), so the control warp's wait for it runs out;
+          // every tile before it was loaded, after waits for PVs that were issued.
+          withheld = true;
+          break;
+        }
         if (g % kProducers0 != pw) continue;
         const int buf = g % NS;
         if (g >= NS)  // PV(g - NS) has read the stage
@@ -757,6 +766,7 @@ psd_status launch_l0(const PartialLaunch &L, const DeviceInfo &dev, cudaStream_t
   p.q_scale = L.q_scale;
   p.v_scale = L.v_scale;
   p.wait_limit = dev.test_wait_limit > 0 ? dev.test_wait_limit : kWaitLimitCycles;
+  p.withhold_from = dev.test_withhold_from >= 0 ? dev.test_withhold_from : 0x7fffffff;
   // persistent: one CTA per SM (its shared memory and 512 TMEM columns fill the SM)
   const int sms = dev.num_sms > 0 ? dev.num_sms : 1;
   const dim3 grid(unsigned(tasks < sms ? tasks : sms));

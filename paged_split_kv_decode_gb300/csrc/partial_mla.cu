@@ -116,6 +116,8 @@ struct MLAParams {
   // left empty.  Without them (has_runs 0) each CTA computes a run of whole items.
   int has_runs;
   int32_t run_item[kMaxPairs + 1], run_tile[kMaxPairs + 1];
+  long long wait_limit;  // cycles before a wait gives up
+  int withhold_from;     // testing aid: no loads for an item's tiles from this index on
 };
 
 // Item b continues item a's partial: the next chunk of the same request, whose row
@@ -341,7 +343,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // row warps have split the query.
     bool ok = true;
     int g = 0, issued = 0, nq = 0, cur_q = -1, gate = -kNB;
-    for (int m = begin; m < end && ok; ++m) {
+    bool withheld = false;
+    for (int m = begin; m < end && ok && !withheld; ++m) {
       const psd_work_item it = p.items[m];
       const int nt = (it.n_tokens + kTokM - 1) / kTokM;
       if (nt <= 0) continue;  // (the planner emits no empty items)
@@ -349,7 +352,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       if (j1 <= j0) continue;  // (the run planner emits no empty tile range)
       if (it.q_index != cur_q) {
         if (g > 0)
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault));
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault, p.wait_limit));
         if (!ok) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(BQ), kQBytes);
@@ -364,11 +367,17 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       }
 #pragma unroll 1
       for (int j = j0; j < j1; ++j) {
+        if (j >= p.withhold_from) {
+          // testing aid: this tile and every later one go unloaded, so the control
+          // warp's wait for it runs out; every tile before it was loaded.
+          withheld = true;
+          break;
+        }
         const int buf = g % kNB;
         if (g >= kNB)  // PV(g - 4) has read the buffer
-          ok = mbar_wait(bar(BKEMPTY0 + buf), uint32_t(g / kNB - 1) & 1u, p.fault);
+          ok = mbar_wait(bar(BKEMPTY0 + buf), uint32_t(g / kNB - 1) & 1u, p.fault, p.wait_limit);
         if (ok && g >= gate && g < gate + 2)  // a query landing box sits in this buffer
-          ok = mbar_wait(bar(BQREADY), uint32_t(nq - 1) & 1u, p.fault);
+          ok = mbar_wait(bar(BQREADY), uint32_t(nq - 1) & 1u, p.fault, p.wait_limit);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         const int tok = j * kTokM;
         if (lane == 0) {
@@ -388,9 +397,9 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       }
     }
     // No copy of this CTA may still be in flight when it exits.
-    if (nq > 0) mbar_wait(bar(BQ), uint32_t(nq - 1) & 1u, p.fault);
+    if (nq > 0) mbar_wait(bar(BQ), uint32_t(nq - 1) & 1u, p.fault, p.wait_limit);
     for (int t = max(0, issued - kNB); t < issued; ++t)   // the last tile of each buffer
-      mbar_wait(bar(BKFULL0 + t % kNB), uint32_t(t / kNB) & 1u, p.fault);
+      mbar_wait(bar(BKFULL0 + t % kNB), uint32_t(t / kNB) & 1u, p.fault, p.wait_limit);
   } else if (warp == kCtrlWarp) {
     // ------------------------------------------------------------- control warp
     // The whole warp waits; one elected lane issues.  (A wait on the issuing thread
@@ -413,12 +422,12 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     bool pend_cont = false;      // ... which adds to the previous item's O
     auto issue_pv = [&]() -> bool {
       const int t = pend, buf = t % kNB;
-      bool r = __all_sync(0xffffffffu, mbar_wait(bar(BPFULL0 + (t & 1)), uint32_t(t >> 1) & 1u, p.fault));
+      bool r = __all_sync(0xffffffffu, mbar_wait(bar(BPFULL0 + (t & 1)), uint32_t(t >> 1) & 1u, p.fault, p.wait_limit));
       // The previous partial's O has been read out.  BORDY completes once per read-out
       // and the row warps read out partial k only after PV of partial k is issued,
       // so they are never two phases ahead of this wait.
       if (r && pend_first && !pend_cont && pend_po > 0)
-        r = __all_sync(0xffffffffu, mbar_wait(bar(BORDY), uint32_t(pend_po - 1) & 1u, p.fault));
+        r = __all_sync(0xffffffffu, mbar_wait(bar(BORDY), uint32_t(pend_po - 1) & 1u, p.fault, p.wait_limit));
       if (!r) return false;
       tc_fence_after();
       if (elect_one()) {
@@ -447,7 +456,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       if (it.q_index != cur_q) {
         // the split of the next query waits for every PV issued so far
         if (pend >= 0) ok = issue_pv();
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(BQREADY), uint32_t(nq) & 1u, p.fault));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(BQREADY), uint32_t(nq) & 1u, p.fault, p.wait_limit));
         if (!ok) break;
         tc_fence_after();
         cur_q = it.q_index;
@@ -456,7 +465,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 #pragma unroll 1
       for (int j = j0; j < j1; ++j) {
         const int buf = g % kNB;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(BKFULL0 + buf), uint32_t(g / kNB) & 1u, p.fault));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(BKFULL0 + buf), uint32_t(g / kNB) & 1u, p.fault, p.wait_limit));
         if (!ok) break;
         tc_fence_after();
         if (elect_one()) {
@@ -488,7 +497,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // every MMA this warp issued has completed before TMEM is released
     if (elect_one()) umma_commit(bar(BDRAIN));
     __syncwarp();
-    mbar_wait(bar(BDRAIN), 0, p.fault);
+    mbar_wait(bar(BDRAIN), 0, p.fault, p.wait_limit);
   } else if (warp < kRowWarps) {
     // ------------------------------------------------------------------ row warps
     const int row = tid;                          // head = TMEM lane
@@ -511,7 +520,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         // pass 2 scales the row by 2^k (largest element to [128, 256)) and writes
         // hi = e4m3(x), lo = e4m3(x - hi): Q_hi[0:512] to TMEM, the rest to shared
         // memory over the landing boxes, once every row warp has read them.
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(BQ), uint32_t(nq) & 1u, p.fault));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(BQ), uint32_t(nq) & 1u, p.fault, p.wait_limit));
         if (!ok) break;
         float amax = 0.f;
 #pragma unroll 1
@@ -532,7 +541,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         tmem_st_wait();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BQSEEN));
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(BQSEEN), uint32_t(nq) & 1u, p.fault));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(BQSEEN), uint32_t(nq) & 1u, p.fault, p.wait_limit));
         if (!ok) break;
         // power of two: amax * 2^k in [128, 256); zero and subnormal rows keep k = 0
         const int ex = int((__float_as_uint(amax) >> 23) & 0xffu) - 127;
@@ -578,7 +587,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       const int tail = it.n_tokens - (nt - 1) * kTokM;   // valid tokens of the last tile
 #pragma unroll 1
       for (int j = j0; j < j1; ++j, ++g) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(BSFULL0 + (g & 1)), uint32_t(g >> 1) & 1u, p.fault));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(BSFULL0 + (g & 1)), uint32_t(g >> 1) & 1u, p.fault, p.wait_limit));
         if (!ok) break;
         tc_fence_after();
         const uint32_t s_col = lane_base + kColS + 64 * (g & 1);
@@ -610,7 +619,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
           const float m_new = grow ? mt : m_ref;
           if (j > j0 || cont) {  // PV(g-1) must be done; then rescale this warp's O rows in TMEM
             ok = __all_sync(0xffffffffu,
-                            mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault));
+                            mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault, p.wait_limit));
             if (!ok) break;
             tc_fence_after();
             const float alpha = ex2(m_ref - m_new);
@@ -675,7 +684,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         continue;
       }
       // epilogue: O / l for this row and V half, once the item's last PV is done
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(BKEMPTY0 + (g - 1) % kNB), uint32_t((g - 1) / kNB) & 1u, p.fault, p.wait_limit));
       if (!ok) break;
       tc_fence_after();
       // a run that ends inside this item writes to the previous item's (empty) row
@@ -848,6 +857,8 @@ psd_status launch_partial_mla(const PartialLaunch &L, const DeviceInfo &dev, cud
   p.merge_runs = L.merge_runs ? 1 : 0;
   p.q_scale = L.q_scale;
   p.v_scale = L.v_scale;
+  p.wait_limit = dev.test_wait_limit > 0 ? dev.test_wait_limit : kWaitLimitCycles;
+  p.withhold_from = dev.test_withhold_from >= 0 ? dev.test_withhold_from : 0x7fffffff;
   cudaError_t e = cudaFuncSetAttribute(partial_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(kSmemMLA));
   if (e != cudaSuccess) return fail(PSD_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));

@@ -129,20 +129,25 @@ def _wide_level0_cascade():
     return dataclasses.replace(w, tile_tokens=128)
 
 
-@pytest.mark.parametrize("case", ["cuda_core_flat", "tensor_core_cascade", "tensor_core_shared_tiles"])
+@pytest.mark.parametrize("case", ["cuda_core_flat", "tensor_core_cascade", "tensor_core_shared_tiles",
+                                  "tcgen05_level0_cascade", "tcgen05_level0_wide"])
 def test_bounded_wait_runs_out_and_is_reported(case):
     """A wait that nothing completes gives up after its limit: the partial kernels are
     told to withhold the loads of every tile from index 1 on, so the waits for those
     tiles run out (about 1 ms limit), every warp stops, the call completes, and
     psd_check_device_error reports PSD_FAULT_WAIT_TIMEOUT.  The next decode on the
-    same context is clean and matches the oracle."""
+    same context is clean and matches the oracle.  The tcgen05 level-0 cases give up
+    with a level-0 tile's stage landed and its S MMAs complete, and free their tensor
+    memory after the issued MMAs have drained."""
     from oracle import attention as A
-    from _gpu_util import assert_close, use_kernel
-    w = _wide_level0_cascade() if case == "tensor_core_shared_tiles" else synth.tiny_cascade(seed=2)
+    from _gpu_util import assert_close, use_kernel, use_level0
+    wide = case in ("tensor_core_shared_tiles", "tcgen05_level0_wide")
+    w = _wide_level0_cascade() if wide else synth.tiny_cascade(seed=2)
     d = Dev(w)
     enable = 0 if case == "cuda_core_flat" else 1
     kind = "cuda_core" if case == "cuda_core_flat" else "auto"
-    with use_kernel(kind):
+    level0 = "tcgen05" if case.startswith("tcgen05") else "mma_sync"
+    with use_kernel(kind), use_level0(level0):
         plan = psd.plan_decode(d.table, w.tile_tokens, enable, w.min_shared_pages, w.min_members)
         assert (plan.num_members > 0) == bool(enable)
         o = torch.empty((w.batch, w.Hq, w.Dv), device="cuda")
@@ -167,3 +172,41 @@ def test_withhold_loads_rejects_a_limit_outside_its_range():
         with pytest.raises(psd.PsdError):
             ctx().test_withhold_loads(1, bad)
     ctx().test_withhold_loads(-1)
+
+
+@pytest.mark.parametrize("case,from_tile", [("long_items", 1), ("query_switches", 0)])
+def test_mla_bounded_wait_runs_out_and_is_reported(case, from_tile):
+    """The same aid on the tcgen05 MLA partial.  long_items: four requests in
+    2048-token items, every item's tiles from index 1 on withheld, so the CTAs give up
+    with a tile's S and softmax done and its PV never issued.  query_switches: 300
+    requests of 1 to 130 tokens in 64-token items with no tile loaded, so the
+    producer gives up at its first query switch while the control warp waits for a
+    tile.  Each CTA waits for the copies it issued and for its issued MMAs before
+    freeing its tensor memory; the call reports PSD_FAULT_WAIT_TIMEOUT, and the next
+    decode on the same context is clean and matches the oracle."""
+    from oracle import attention as A
+    from _gpu_util import assert_close
+    if case == "long_items":
+        w = synth.mla_decode(seed=1, batch=4, lo=4096, hi=9000, num_pages=1024)
+    else:
+        rng = np.random.default_rng(7)
+        lengths = [int(x) for x in rng.integers(1, 131, size=300)]
+        w = synth._make("mla_small", rng, lengths, Hq=128, Hkv=1, Dqk=576, Dv=512, page_size=64,
+                        num_pages=1024, tile_tokens=64, kv_dtype="fp8_e4m3", latent_v=True)
+    d = Dev(w)
+    plan = psd.plan_decode(d.table, w.tile_tokens, 0, w.min_shared_pages, w.min_members)
+    o = torch.empty((w.batch, w.Hq, w.Dv), device="cuda")
+    lse = torch.empty((w.batch, w.Hq), device="cuda")
+    ws = psd.workspace_for(plan, w.Hq, w.Dv, "cuda")
+    ctx().test_withhold_loads(from_tile, 2_000_000)
+    try:
+        psd.cascade_decode(ctx(), d.args(), plan, o, lse, ws)
+        with pytest.raises(psd.PsdError) as e:
+            psd.check_device_error(ctx(), ws)
+    finally:
+        ctx().test_withhold_loads(-1)
+    assert e.value.status == 4 and e.value.fault_bits == PSD_FAULT_WAIT_TIMEOUT
+    psd.cascade_decode(ctx(), d.args(), plan, o, lse, ws)
+    assert psd.check_device_error(ctx(), ws) == 0
+    ro, rl = A.decode_attention(A.workload_arrays(w))
+    assert_close(o.cpu().double().numpy(), lse.cpu().double().numpy(), ro, rl, "fp8_e4m3", f"MLA after {case}")
