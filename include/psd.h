@@ -208,17 +208,21 @@ psd_status psd_set_level0_kernel(psd_ctx *ctx, int32_t kind);
  * objects, no device memory). */
 psd_status psd_set_timing(psd_ctx *ctx, int32_t enable);
 /* Testing aid for the kernels' bounded waits (no counterpart on the pages).  With
- * from_tile >= 0, the 16-row-group tensor-core, CUDA-core and tcgen05 level-0
+ * from_tile >= 0, the 16-row-group tensor-core, CUDA-core, tcgen05 level-0 and MLA
  * partial kernels launched through this context issue no loads for any item's tiles
  * at index from_tile and later (16-token tiles of the tensor-core kernel, the
- * CUDA-core kernel's own ring tiles, the level-0 kernel's 64-token tiles), so their
- * waits for those tiles run out after wait_limit_cycles (1e5 to 2e9 SM cycles);
- * each timed-out warp stops consuming tiles, the kernel completes, and the call's
- * fault word carries PSD_FAULT_WAIT_TIMEOUT for psd_check_device_error.  Every copy
- * a kernel did issue is waited for before it exits, and the level-0 kernel frees
- * its tensor memory only after its issued MMAs have completed.  Outputs of such a
- * call are meaningless.  from_tile < 0 switches the aid off (the default; the
- * other kernels ignore it).  PSD_ERR_INVALID_ARG for a limit outside the range. */
+ * CUDA-core kernel's own ring tiles, the 64-token tiles of the tcgen05 kernels), so
+ * their waits for those tiles run out after wait_limit_cycles (1e5 to 2e9 SM
+ * cycles); each timed-out warp stops consuming tiles, the kernel completes, and the
+ * call's fault word carries PSD_FAULT_WAIT_TIMEOUT for psd_check_device_error.
+ * Every copy a kernel did issue is waited for before it exits, and the tcgen05
+ * kernels free their tensor memory only after their issued MMAs have completed.
+ * The streaming form of psd_merge_states copies no input row from index from_tile
+ * of a CTA's range on; its output rows from the first one that needs such a row to
+ * the end of the CTA's range read as NaN (v and LSE: a merge has no fault word).
+ * Outputs of such a call are meaningless.  from_tile < 0 switches the aid off (the
+ * default; the other kernels ignore it).  PSD_ERR_INVALID_ARG for a limit outside
+ * the range. */
 psd_status psd_test_withhold_loads(psd_ctx *ctx, int32_t from_tile, int64_t wait_limit_cycles);
 psd_status psd_get_kernel_times(psd_ctx *ctx, float *level0_ms, float *partial_ms, float *merge_ms);
 /* Thread-local message describing the last failure on this thread. */

@@ -17,9 +17,10 @@ struct DeviceInfo {
   int partial_kernel = 0;        // psd_partial_kernel preference for G <= 16
   int level0_kernel = 0;         // psd_level0_kernel preference for stacked level-0 rows
   // Testing aid for the bounded waits (psd_test_withhold_loads): the 16-row-group
-  // tensor-core, CUDA-core and tcgen05 level-0 partial kernels issue no loads for
-  // tiles at index test_withhold_from and later of any item (-1: off), and give up a
-  // wait after test_wait_limit cycles (0: the default limit).
+  // tensor-core, CUDA-core, tcgen05 level-0 and MLA partial kernels issue no loads
+  // for tiles at index test_withhold_from and later of any item, and the streaming
+  // merge none for input rows from that index of a CTA's range on (-1: off); they
+  // give up a wait after test_wait_limit cycles (0: the default limit).
   int32_t test_withhold_from = -1;
   int64_t test_wait_limit = 0;
 };

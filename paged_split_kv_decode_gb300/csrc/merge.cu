@@ -358,6 +358,8 @@ struct StreamParams {
   uint32_t row_bytes, lse_bytes, stage_bytes;
   float *v_out;
   float *lse_out;
+  long long wait_limit;  // cycles before a wait gives up
+  int withhold_from;     // testing aid: no copies from this input row of a CTA's range on
 };
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
@@ -366,11 +368,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                : "memory");
 }
 // A bounded wait with no fault word to report to: false after the limit.
-__device__ __forceinline__ bool stream_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool stream_wait(uint32_t bar, uint32_t parity, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   return true;
 }
 
@@ -411,20 +413,23 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) merge_stream_kern
   if (warp == kStreamConsumers) {
     // ------------------------------------------------------------ producer warp
     if (lane == 0) {
-      bool ok = true;
-      for (int32_t k = 0; k < g1 - g0 && ok; ++k) {
+      int32_t issued = 0;
+      for (int32_t k = 0; k < g1 - g0; ++k) {
+        if (k >= p.withhold_from) break;  // testing aid: the consumers' wait for row k runs out
         const int s = k % S;
-        if (k >= S && !(ok = stream_wait(smem_u32(empty + s), uint32_t(k / S - 1) & 1u))) break;
+        if (k >= S && !stream_wait(smem_u32(empty + s), uint32_t(k / S - 1) & 1u, p.wait_limit)) break;
         const int64_t row = int64_t(g0) + k;
         const uint32_t dst = smem_u32(smem + size_t(s) * p.stage_bytes);
         mbar_arrive_expect_tx(smem_u32(full + s), p.row_bytes + p.lse_bytes);
         bulk_load(dst, p.v_in + row * p.H * p.D, p.row_bytes, smem_u32(full + s));
         bulk_load(dst + p.row_bytes, p.lse_in + row * p.H, p.lse_bytes, smem_u32(full + s));
+        issued = k + 1;
       }
-      // no copy in flight at exit: the last S rows' barriers complete once they land
-      const int32_t n = g1 - g0;
-      for (int32_t k = n > S ? n - S : 0; ok && k < n; ++k)
-        ok = stream_wait(smem_u32(full + k % S), uint32_t(k / S) & 1u);
+      // No copy in flight at exit, also after a wait ran out: the last S issued rows'
+      // barriers complete once they land (each stage's earlier row was consumed before
+      // its next copy was issued, so every such wait is for the phase in progress).
+      for (int32_t k = issued > S ? issued - S : 0; k < issued; ++k)
+        stream_wait(smem_u32(full + k % S), uint32_t(k / S) & 1u, p.wait_limit);
     }
     return;
   }
@@ -448,7 +453,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtas) merge_stream_kern
     for (int32_t i = 0; i < n; ++i) {
       const int32_t k = lo + i - g0;
       const int s = k % S;
-      ok = __all_sync(0xffffffffu, stream_wait(smem_u32(full + s), uint32_t(k / S) & 1u));
+      ok = __all_sync(0xffffffffu, stream_wait(smem_u32(full + s), uint32_t(k / S) & 1u, p.wait_limit));
       if (!ok) break;
       const uint8_t *stage = smem + size_t(s) * p.stage_bytes;
       const float *lse_row = reinterpret_cast<const float *>(stage + p.row_bytes);
@@ -531,6 +536,8 @@ bool launch_stream(const DeviceInfo &dev, cudaStream_t s, const float *v_in, con
   p.stages = std::min<int>(kStreamMaxStages, int(kStreamRing / p.stage_bytes));
   p.v_out = v_out;
   p.lse_out = lse_out;
+  p.wait_limit = dev.test_wait_limit > 0 ? dev.test_wait_limit : kWaitLimitCycles;
+  p.withhold_from = dev.test_withhold_from >= 0 ? dev.test_withhold_from : 0x7fffffff;
   const size_t smem = size_t(p.stages) * p.stage_bytes + 2 * sizeof(uint64_t) * size_t(p.stages);
   if (p.stages < 4 || smem > size_t(dev.smem_optin)) return false;
   switch (chunks / 256) {

@@ -233,3 +233,58 @@ def test_streaming_form_offset_indptr_and_trailing_empty_groups():
     assert np.array_equal(np.isneginf(lo.cpu().numpy()), np.isneginf(rl))
     fin = np.isfinite(rl)
     assert np.abs(lo.cpu().double().numpy()[fin] - rl[fin]).max() < TOL_L
+
+
+def test_streaming_merge_gives_up_into_nan_rows():
+    """The bounded waits of the streaming form: with the withheld-loads aid its
+    producers copy only the first three input rows of each CTA's range, so the
+    consumers' wait for the fourth runs out (about 1 ms limit).  Each CTA fills the
+    output rows from the first one that needs a withheld input to the end of its range
+    with NaN (v and LSE), every earlier row equals the clean merge bit for bit, and
+    the next merge on the same context is clean.  The expected NaN rows follow from
+    the kernel's partition of the input rows (equal shares of them, each CTA starting
+    at the group that holds its share's first row)."""
+    rng = np.random.default_rng(91)
+    H, D = 32, 128
+    sizes = rng.integers(1, 17, size=4000)
+    o_indptr = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    N, M = int(o_indptr[-1]), 4000
+    v_in = torch.from_numpy(rng.standard_normal((N, H, D), dtype=np.float32)).cuda()
+    lse_in = torch.from_numpy(rng.uniform(-5, 20, size=(N, H)).astype(np.float32)).cuda()
+    assert lse_in.data_ptr() % 16 == 0
+    ind = torch.from_numpy(o_indptr).cuda()
+
+    def run():
+        vo = torch.full((M, H, D), 7.0, device="cuda")
+        lo = torch.full((M, H), 7.0, device="cuda")
+        psd.merge_states(ctx(), v_in, lse_in, ind, vo, lo)
+        torch.cuda.synchronize()
+        return vo, lo
+
+    clean_v, clean_l = run()
+    assert torch.isfinite(clean_v).all() and torch.isfinite(clean_l).all()
+    ctx().test_withhold_loads(3, 2_000_000)
+    try:
+        vo, lo = run()
+    finally:
+        ctx().test_withhold_loads(-1)
+    grid = 3 * torch.cuda.get_device_properties(0).multi_processor_count
+    assert M >= 8 * grid   # the streaming form applies
+    expect_nan = np.zeros(M, dtype=bool)
+    starts = [int(np.searchsorted(o_indptr[:M], N * b // grid, side="left")) for b in range(grid)] + [M]
+    for b in range(grid):
+        r0, r1 = starts[b], starts[b + 1]
+        if r1 <= r0:
+            continue
+        g0 = int(o_indptr[r0])
+        for r in range(r0, r1):
+            expect_nan[r] = int(o_indptr[r + 1]) > g0 + 3
+    nan_v = torch.isnan(vo).all(dim=2).all(dim=1).cpu().numpy()
+    nan_l = torch.isnan(lo).all(dim=1).cpu().numpy()
+    fin = ~expect_nan
+    assert expect_nan.sum() > M // 2 and fin.sum() > 0
+    assert np.array_equal(nan_v, expect_nan) and np.array_equal(nan_l, expect_nan)
+    fin_t = torch.from_numpy(fin).cuda()
+    assert torch.equal(vo[fin_t], clean_v[fin_t]) and torch.equal(lo[fin_t], clean_l[fin_t])
+    again_v, again_l = run()
+    assert torch.equal(again_v, clean_v) and torch.equal(again_l, clean_l)
