@@ -272,6 +272,7 @@ __global__ void __launch_bounds__(kWarps * 32, G <= 4 ? 4 : 2)
   };
 
   const bool exact_steps = steps * TPS == SUB;
+  int failed_at = -1;  // the tile whose wait ran out
   for (int i = 0; i < my_tiles; ++i) {
     const int s = i % kStages;
     const int t = warp + i * kWarps;
@@ -279,7 +280,10 @@ __global__ void __launch_bounds__(kWarps * 32, G <= 4 ? 4 : 2)
     const bool page_ok = id >= 0 && int64_t(id) < p.num_pages;
     const int valid = page_ok ? min(SUB, it.n_tokens - t * SUB) : 0;
     const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / kStages) & 1u, p.fault, p.wait_limit);
-    if (!__all_sync(0xffffffffu, ok)) break;
+    if (!__all_sync(0xffffffffu, ok)) {
+      failed_at = i;
+      break;
+    }
     const uint8_t *kb = ring + size_t(s) * 2 * tile_bytes;
     const uint8_t *vb = kb + tile_bytes;
     if (valid == SUB && exact_steps)
@@ -288,6 +292,16 @@ __global__ void __launch_bounds__(kWarps * 32, G <= 4 ? 4 : 2)
       tile(std::integral_constant<bool, true>(), kb, vb, valid);
     __syncwarp();
     if (i + kStages < my_tiles) issue(i + kStages);
+  }
+  if (failed_at >= 0) {
+    // A wait ran out.  The copies this warp issued for tiles failed_at ..
+    // failed_at + kStages - 1 land before it goes on: it waits for each such tile that
+    // the testing aid did not withhold.  Each stage's previous use is consumed, so every
+    // wait is for the phase in progress; a tile it never loaded only runs out the limit
+    // once more.
+    for (int j = failed_at; j < failed_at + kStages && j < my_tiles; ++j)
+      if (warp + j * kWarps < p.withhold_from)
+        mbar_wait(smem_u32(&bars[j % kStages]), uint32_t(j / kStages) & 1u, p.fault, p.wait_limit);
   }
 
   // Combine the token slots of the warp (all slots share m_run per head).

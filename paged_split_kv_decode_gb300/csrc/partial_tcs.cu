@@ -326,6 +326,7 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
   // V fragment masks of a tail tile in the shared form (tokens tk, tk+1 and tk+8,
   // tk+9 of the transposed ldmatrix); the private form zeroes the rows in its stage.
   const int tk = (lane & 3) * 2;
+  int failed_at = -1;  // the tile whose wait ran out
   for (int i = 0; i < my_tiles; ++i) {
     const int s = i % n_stages;
     const int t = tile_of(i);
@@ -333,7 +334,10 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
     const bool page_ok = id >= 0 && int64_t(id) < p.num_pages;
     const int valid = page_ok ? min(kTileTok, it.n_tokens - t * kTileTok) : 0;
     const bool ok = mbar_wait(smem_u32(&bars[s]), uint32_t(i / n_stages) & 1u, p.fault, p.wait_limit);
-    if (!__all_sync(0xffffffffu, ok)) break;
+    if (!__all_sync(0xffffffffu, ok)) {
+      failed_at = i;
+      break;
+    }
     if (valid > 0) {
       uint8_t *stage = ring + size_t(s) * 2 * TILE_BYTES;
       const bool vmask = shared_tiles && valid < kTileTok;
@@ -464,6 +468,17 @@ __global__ void __launch_bounds__(kWarpsS * 32, D >= 256 ? 1 : 3)
         issue(i + n_stages);
       }
     }
+  }
+
+  if (failed_at >= 0) {
+    // A wait ran out.  Copies issued for tiles failed_at .. failed_at + n_stages - 1
+    // (by this warp, or in the shared form by whichever warp refilled the stage) land
+    // before it goes on: it waits for each such tile that the testing aid did not
+    // withhold.  Each stage's previous use is consumed, so every wait is for the phase
+    // in progress; a tile nobody issued only runs out the limit once more.
+    for (int j = failed_at; j < failed_at + n_stages && j < my_tiles; ++j)
+      if (tile_of(j) < p.withhold_from)
+        mbar_wait(smem_u32(&bars[j % n_stages]), uint32_t(j / n_stages) & 1u, p.fault, p.wait_limit);
   }
 
   if (shared_tiles) {  // this warp's rows are complete: write them
