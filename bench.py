@@ -53,8 +53,8 @@ NOMINAL_HBM_GBS = 8000.0
 # ncu capture of the flat partial.  Reported only while the kernel source is the one
 # the counters were taken on.
 TRAFFIC_SOURCE = os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", "partial_tcs.cu")
-TRAFFIC_SHA256 = "9cc955b4b183ab5debe9ebc71c3a8a5a086aa6ba5ca6eb0a516ee92a46b43fce"
-TRAFFIC_BYTES = 316086016 + 1213184
+TRAFFIC_SHA256 = "65a307d5034b1e9069eaf9efeb0dcda8734670d0a38e66704fd89dfb81b7b1f6"
+TRAFFIC_BYTES = 316089600 + 1150720
 
 # DRAM bytes read per step by the partial kernels of each arm of the two cascade
 # workloads (median over launches of a single-pass ncu capture of dram__bytes_read.sum,
@@ -63,13 +63,13 @@ TRAFFIC_BYTES = 316086016 + 1213184
 # sources are unchanged.
 CASCADE_DRAM_SOURCES = [os.path.join(ROOT, "paged_split_kv_decode_gb300", "csrc", f)
                         for f in ("partial_tcs.cu", "partial_l0.cu")]
-CASCADE_DRAM_SHA256 = "e5de381740343d712431c7810b3257bd0f3649b5530ab941676062f04ba9bf2c"
+CASCADE_DRAM_SHA256 = "601112f6e4e27371b7610a6355e90dc9931e2d3a0dbd4795aefb4a5b7d283b02"
 CASCADE_DRAM_READ = {
     # 8192-token prefix: the flat arm's prefix re-reads hit the 129 MB L2
-    "flat_vs_cascade": {"flat": 533333504, "cascade": 533295744,
+    "flat_vs_cascade": {"flat": 533349504, "cascade": 533303808,
                         "kernels": "flat: partial_tcs 523x8 CTAs; cascade: one partial_tcs launch, both levels"},
     # 65536-token prefix (268 MB): the flat arm re-reads part of the prefix from DRAM
-    "flat_vs_cascade_prefix_beyond_l2": {"flat": 930361216, "cascade": 268659584 + 499737344,
+    "flat_vs_cascade_prefix_beyond_l2": {"flat": 931388288, "cascade": 268661504 + 499737216,
                                          "kernels": "flat: partial_tcs 2315x8 CTAs; cascade: partial_l0 (level 0) "
                                                     "+ partial_tcs 267x8 (level 1)"},
 }
