@@ -60,16 +60,16 @@ def _variants(rng, n):
 def test_lookups_equal_the_oracle_plan_and_hits_follow_lru(api, seed, capacity):
     rng = np.random.default_rng(seed)
     tables = _variants(rng, 8)
-    configs = [(4, 1, 2, 2), (8, 1, 2, 2), (4, 0, 2, 2), (4, 1, 1, 3)]  # (tile, enable, msp, mm)
+    plan_args = [(4, 1, 2, 2), (8, 1, 2, 2), (4, 0, 2, 2), (4, 1, 1, 3)]  # (tile, enable, msp, mm)
     pc = api.PlanCache(capacity)
     model = []  # keys, most recently used last
     hits = misses = 0
     for step in range(60):
         ti = int(rng.integers(0, len(tables)))
-        ci = int(rng.integers(0, len(configs)))
+        ci = int(rng.integers(0, len(plan_args)))
         indptr, indices, last = tables[ti]
-        T, enable, msp, mm = configs[ci]
-        key = (indptr.tobytes(), indices.tobytes(), last.tobytes(), configs[ci])
+        T, enable, msp, mm = plan_args[ci]
+        key = (indptr.tobytes(), indices.tobytes(), last.tobytes(), plan_args[ci])
         expect_hit = key in model
         t = api.HostTable(indptr, indices, last, 4)
         p = pc.lookup(t, T, enable, msp, mm)
