@@ -14,10 +14,14 @@ planner    split-KV work list, shared-prefix detection, cascade plan, head
            stacking index maps (pure Python integers).
 cascade    the two-level cascade evaluated level by level in float64, for
            diagnosis and for the invariants the pages state.
+rope_append  rotary embedding of the new token's query and key rows and their
+           append into the paged pools (bf16 or fp8-e4m3 codes).  The rotation runs
+           in float32, since its roundings decide bit patterns; tests pin it to the
+           exact float64 rotation.
 
 Every numeric function is pinned by ``tests/test_oracle_*.py`` against brute force,
 closed forms, library routines or the pages' invariants.  Parity is pinned for all
 functions here; the planner's tie-break and cap-before-threshold ordering are
 readings of the pages (see the planner docstrings), pinned by hand-made cases.
 """
-from . import attention, planner, cascade  # noqa: F401
+from . import attention, planner, cascade, rope_append  # noqa: F401
