@@ -99,7 +99,8 @@ class Context:
 
     def test_withhold_loads(self, from_tile: int, wait_limit_cycles: int = 0):
         """psd_test_withhold_loads: a testing aid that makes the partial kernels' waits
-        for tiles from `from_tile` on run out (from_tile < 0 switches it off)."""
+        for an item's tiles from `from_tile` on run out, and the streaming merge's waits
+        for a CTA's input rows from that index on (from_tile < 0 switches it off)."""
         L.check(L.load().psd_test_withhold_loads(self._h, int(from_tile), int(wait_limit_cycles)))
 
     def set_timing(self, enable: bool = True):
